@@ -1,0 +1,301 @@
+/*
+ * CPU oracle for the fused residual-add + RMSNorm (TEST INFRASTRUCTURE).
+ *
+ * This file is the plain, slow reference that the CUDA path is checked
+ * against.  Only the tests, the package's smoke check and the bench's CPU
+ * baseline use it; the library's compute path never calls it.  It shares no
+ * code, header, table or constant with the CUDA sources.
+ *
+ * What it computes (blog "CuTeDSL at Perplexity", section "QK norm"): the
+ * regular RMS norm.  The formula printed in that section has lost its
+ * reciprocal square root; the kernel listing that follows it is read
+ * instead: square and sum the elements, divide by the vector length, add EPS,
+ * take the reciprocal square root, multiply the input by it and then by the
+ * weight plus the scalar WEIGHT_BIAS, and cast to the element type.
+ * WEIGHT_BIAS is the "with or without weight bias" knob of section
+ * "Inference at Perplexity"; here it is `weight_offset`.  On top of the norm,
+ * per the fused hot path:
+ *
+ *   per token t, for j in [0, H):
+ *     h_j    = RN_in(x_j + r_j)            (exact sum, rounded once; or x_j)
+ *     ms     = (sum_j h_j^2) / H            (fp64)
+ *     inv    = 1 / sqrt(ms + eps)           (fp64)
+ *     yhat_j = (w_j + weight_offset) * (h_j * inv) + b_j     (fp64)
+ *     out    : RN_out(yhat_j) for f32 / bf16 / f64 outputs, or
+ *              a = max_j |yhat_j|, s = a / 448, scale_t = RN_f32(s),
+ *              q_j = E4M3_RNE_SATFINITE(yhat_j / s)   (q_j = +0 if a == 0)
+ *
+ * The FP8 path (section "Blackwell support": FP8 block scaling with an
+ * absolute-maximum reduction) uses one block per token; 448 is the largest
+ * finite OCP FP8 E4M3 value.  The norm is taken on the ROUNDED residual h,
+ * the value written to residual_out.
+ *
+ * Everything is accumulated in double and rounded once at the end.  The
+ * bfloat16 and E4M3 encoders below are written from the IEEE-754 binary
+ * format rules and the OCP 8-bit floating point specification (E4M3: bias 7,
+ * 3 mantissa bits, no infinities, S.1111.111 is NaN, max 448).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_FP8E4M3 = 2, ORC_F64 = 3 };
+
+/* ------------------------------------------------------------------ */
+/* number formats                                                      */
+
+double oracle_bf16_to_f64(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+static double f32_bits_to_f64(const void *p, int64_t i) {
+    float f;
+    memcpy(&f, (const char *)p + 4 * i, 4);
+    return (double)f;
+}
+
+/* Round |v| to a multiple of 2^q_exp, ties to even.  Scaling by a power of
+ * two is exact, so rint (round-half-even in the default mode) is the only
+ * rounding step. */
+static double round_to_quantum(double a, int q_exp) {
+    return ldexp(rint(ldexp(a, -q_exp)), q_exp);
+}
+
+/* bfloat16: 8 significant bits, exponent range of binary32
+ * (normal >= 2^-126, subnormal quantum 2^-133, max (2 - 2^-7) * 2^127). */
+uint16_t oracle_bf16_from_f64(double v) {
+    if (isnan(v)) return 0x7FC0;
+    int neg = signbit(v) ? 1 : 0;
+    double a = fabs(v);
+    double r;
+    if (isinf(a)) {
+        r = INFINITY;
+    } else if (a == 0.0) {
+        r = 0.0;
+    } else {
+        int e;
+        frexp(a, &e);                 /* a in [2^(e-1), 2^e) */
+        int q = e - 8;                /* 8 significant bits */
+        if (q < -133) q = -133;       /* subnormal quantum */
+        r = round_to_quantum(a, q);
+        const double maxf = ldexp(255.0, 127 - 7);
+        if (r > maxf) r = INFINITY;   /* rounded past the largest finite */
+    }
+    float f = (float)r;               /* exact: r is a bfloat16 value */
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    uint16_t b = (uint16_t)(u >> 16);
+    return (uint16_t)(b | (neg ? 0x8000 : 0));
+}
+
+float oracle_f32_from_f64(double v) { return (float)v; /* IEEE cast: RNE */ }
+
+double oracle_e4m3_to_f64(uint8_t c) {
+    int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp((double)(8 + m), e - 10);
+    return s ? -v : v;
+}
+
+/* OCP E4M3 with round-to-nearest-even and saturation to +-448 for finite
+ * magnitudes above the largest finite value (and for infinities). */
+uint8_t oracle_e4m3_from_f64(double v) {
+    if (isnan(v)) return 0x7F;
+    int neg = signbit(v) ? 1 : 0;
+    double a = fabs(v);
+    double r;
+    if (a == 0.0) {
+        r = 0.0;
+    } else if (isinf(a)) {
+        r = 448.0;
+    } else {
+        int e;
+        frexp(a, &e);                 /* a in [2^(e-1), 2^e) */
+        int q = e - 4;                /* 4 significant bits */
+        if (q < -9) q = -9;           /* subnormal quantum 2^-9 */
+        r = round_to_quantum(a, q);
+        if (r > 448.0) r = 448.0;
+    }
+    uint8_t code;
+    if (r < ldexp(1.0, -6)) {
+        code = (uint8_t)ldexp(r, 9);  /* subnormal: m * 2^-9 */
+    } else {
+        int e;
+        double f = frexp(r, &e);      /* r = f * 2^e, f in [0.5, 1) */
+        int ef = e - 1 + 7;           /* biased exponent of r in [2^(e-1), 2^e) */
+        int m = (int)ldexp(f, 4) - 8; /* 3 mantissa bits */
+        code = (uint8_t)((ef << 3) | m);
+    }
+    return (uint8_t)(code | (neg ? 0x80 : 0));
+}
+
+/* ------------------------------------------------------------------ */
+/* the norm                                                            */
+
+typedef struct {
+    const void *x, *residual, *weight, *bias;
+    void *out, *residual_out;
+    float *out_scale;
+    int64_t n_tokens, hidden;
+    double eps, weight_offset;
+    int in_dtype, out_dtype;
+    int64_t row_begin, row_end;
+    int status;
+} job_t;
+
+static double load_in(const void *p, int dtype, int64_t i) {
+    if (dtype == ORC_F32) return f32_bits_to_f64(p, i);
+    uint16_t b;
+    memcpy(&b, (const char *)p + 2 * i, 2);
+    return oracle_bf16_to_f64(b);
+}
+
+/* RN to the input type; returns the rounded value and stores its bits. */
+static double round_store_in(void *p, int dtype, int64_t i, double v) {
+    if (dtype == ORC_F32) {
+        float f = oracle_f32_from_f64(v);
+        if (p) memcpy((char *)p + 4 * i, &f, 4);
+        return (double)f;
+    }
+    uint16_t b = oracle_bf16_from_f64(v);
+    if (p) memcpy((char *)p + 2 * i, &b, 2);
+    return oracle_bf16_to_f64(b);
+}
+
+static void norm_row(const job_t *J, int64_t t, double *h, double *yhat) {
+    const int64_t H = J->hidden;
+    const int64_t base = t * H;
+    /* residual add, rounded once to the input type */
+    for (int64_t j = 0; j < H; ++j) {
+        double xv = load_in(J->x, J->in_dtype, base + j);
+        if (J->residual) {
+            double rv = load_in(J->residual, J->in_dtype, base + j);
+            h[j] = round_store_in(J->residual_out, J->in_dtype, base + j, xv + rv);
+        } else {
+            h[j] = xv;
+        }
+    }
+    /* mean square over the true hidden size, eps inside the root */
+    double ss = 0.0;
+    for (int64_t j = 0; j < H; ++j) ss += h[j] * h[j];
+    const double ms = ss / (double)H;
+    const double inv = 1.0 / sqrt(ms + J->eps);
+    /* scale */
+    for (int64_t j = 0; j < H; ++j) {
+        double w = J->weight ? load_in(J->weight, J->in_dtype, j) : 1.0;
+        double b = J->bias ? load_in(J->bias, J->in_dtype, j) : 0.0;
+        yhat[j] = (w + J->weight_offset) * (h[j] * inv) + b;
+    }
+    /* output */
+    switch (J->out_dtype) {
+    case ORC_F64:
+        memcpy((double *)J->out + base, yhat, (size_t)H * sizeof(double));
+        break;
+    case ORC_F32:
+        for (int64_t j = 0; j < H; ++j) {
+            float f = oracle_f32_from_f64(yhat[j]);
+            memcpy((char *)J->out + 4 * (base + j), &f, 4);
+        }
+        break;
+    case ORC_BF16:
+        for (int64_t j = 0; j < H; ++j) {
+            uint16_t b = oracle_bf16_from_f64(yhat[j]);
+            memcpy((char *)J->out + 2 * (base + j), &b, 2);
+        }
+        break;
+    case ORC_FP8E4M3: {
+        double a = 0.0;
+        for (int64_t j = 0; j < H; ++j)
+            if (fabs(yhat[j]) > a) a = fabs(yhat[j]);
+        const double s = a / 448.0;
+        J->out_scale[t] = oracle_f32_from_f64(s);
+        uint8_t *q = (uint8_t *)J->out + base;
+        for (int64_t j = 0; j < H; ++j)
+            q[j] = (a == 0.0) ? 0 : oracle_e4m3_from_f64(yhat[j] / s);
+        break;
+    }
+    }
+}
+
+static void *run_job(void *arg) {
+    job_t *J = (job_t *)arg;
+    double *h = (double *)malloc((size_t)J->hidden * sizeof(double));
+    double *yhat = (double *)malloc((size_t)J->hidden * sizeof(double));
+    if (!h || !yhat) {
+        J->status = -2;
+    } else {
+        for (int64_t t = J->row_begin; t < J->row_end; ++t) norm_row(J, t, h, yhat);
+        J->status = 0;
+    }
+    free(h);
+    free(yhat);
+    return NULL;
+}
+
+int oracle_num_cpus(void) {
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n < 1 ? 1 : (int)n;
+}
+
+/*
+ * All pointers are host pointers to contiguous row-major [n_tokens, hidden]
+ * arrays (weight and bias: [hidden]).  residual / weight / bias may be NULL
+ * (no residual add / w = 1 / b = 0).  residual_out is required when residual
+ * is given.  out_scale ([n_tokens] float) is required for ORC_FP8E4M3.
+ * n_threads <= 0 uses every online CPU.  Returns 0, or -1 on a bad
+ * argument, -2 when a buffer could not be allocated.
+ */
+int oracle_rmsnorm(const void *x, const void *residual, const void *weight, const void *bias,
+                   void *out, void *residual_out, float *out_scale, int64_t n_tokens,
+                   int64_t hidden, double eps, double weight_offset, int in_dtype,
+                   int out_dtype, int n_threads) {
+    if (n_tokens < 0 || hidden <= 0) return -1;
+    if (in_dtype != ORC_F32 && in_dtype != ORC_BF16) return -1;
+    if (out_dtype < ORC_F32 || out_dtype > ORC_F64) return -1;
+    if (!x || !out || (residual && !residual_out)) return -1;
+    if (out_dtype == ORC_FP8E4M3 && !out_scale) return -1;
+    if (n_tokens == 0) return 0;
+    if (n_threads <= 0) n_threads = oracle_num_cpus();
+    if (n_threads > n_tokens) n_threads = (int)n_tokens;
+    job_t *jobs = (job_t *)calloc((size_t)n_threads, sizeof(job_t));
+    pthread_t *tids = (pthread_t *)calloc((size_t)n_threads, sizeof(pthread_t));
+    if (!jobs || !tids) {
+        free(jobs);
+        free(tids);
+        return -2;
+    }
+    for (int i = 0; i < n_threads; ++i) {
+        job_t *J = &jobs[i];
+        J->x = x; J->residual = residual; J->weight = weight; J->bias = bias;
+        J->out = out; J->residual_out = residual_out; J->out_scale = out_scale;
+        J->n_tokens = n_tokens; J->hidden = hidden;
+        J->eps = eps; J->weight_offset = weight_offset;
+        J->in_dtype = in_dtype; J->out_dtype = out_dtype;
+        J->row_begin = n_tokens * i / n_threads;
+        J->row_end = n_tokens * (i + 1) / n_threads;
+        J->status = -3;
+    }
+    int status = 0;
+    int started = 0;
+    for (int i = 1; i < n_threads; ++i) {
+        if (pthread_create(&tids[i], NULL, run_job, &jobs[i]) != 0) break;
+        started = i;
+    }
+    run_job(&jobs[0]);
+    for (int i = 1; i <= started; ++i) pthread_join(tids[i], NULL);
+    /* rows of threads that could not be started run here */
+    for (int i = started + 1; i < n_threads; ++i) run_job(&jobs[i]);
+    for (int i = 0; i < n_threads; ++i)
+        if (jobs[i].status != 0) status = jobs[i].status;
+    free(jobs);
+    free(tids);
+    return status;
+}
