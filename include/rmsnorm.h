@@ -1,0 +1,140 @@
+/*
+ * rmsnorm.h -- C ABI of the GB300 (sm_103a) fused residual-add + RMSNorm.
+ *
+ * The operation (blog "CuTeDSL at Perplexity"; section "QK norm" defines the
+ * regular RMS norm, section "Inference at Perplexity" the compile-time
+ * weight-bias / dtype knobs, section "Blackwell support" the FP8 block-scaled
+ * output), per token t of a row-major [n_tokens, hidden] activation:
+ *
+ *   h      = RN_in(x + residual)            (fp32 add, rounded to the input type;
+ *                                            h = x when there is no residual)
+ *   residual_out = h
+ *   inv    = rsqrt(sum(h^2) / hidden + eps) (fp32 accumulation)
+ *   y      = (weight + weight_offset) * (h * inv) + bias
+ *   out    = RN_out(y)                      (f32 or bf16), or for FP8-E4M3:
+ *            a = max|y|, out_scale[t] = a / 448,
+ *            out = E4M3_RN_SATFINITE(y * 448 / a)   (all +0 when a == 0)
+ *
+ * weight_offset is the blog's scalar WEIGHT_BIAS added to every weight; bias is
+ * a per-channel vector added after scaling.  The norm is taken on the ROUNDED
+ * h, the value stored in residual_out.
+ *
+ * Ownership: every buffer belongs to the caller.  The library allocates no
+ * device memory; it keeps a small per-device table of attributes (SM count)
+ * that is filled on the first call on each device.  All calls are asynchronous
+ * on `stream` (NULL = the legacy default stream) and thread-safe.
+ *
+ * Errors: argument errors are returned before anything is launched; a launch
+ * failure returns RMSN_ECUDA (query cudaGetLastError for the cause).
+ */
+#ifndef RMSNORM_GB300_H
+#define RMSNORM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RMSN_OK = 0,
+    RMSN_EINVAL = -1,       /* bad pointer / size / flag combination */
+    RMSN_EALIGN = -2,       /* a pointer is not aligned to its element size */
+    RMSN_EUNSUPPORTED = -3, /* a forced configuration that is not built */
+    RMSN_ECUDA = -4         /* the CUDA runtime reported an error */
+} rmsn_status;
+
+/* flags: input dtype (x, residual, weight, bias, residual_out share it) */
+#define RMSN_IN_F32 0x0u
+#define RMSN_IN_BF16 0x1u
+#define RMSN_IN_MASK 0x3u
+/* output dtype of `out` */
+#define RMSN_OUT_F32 0x0u
+#define RMSN_OUT_BF16 0x4u
+#define RMSN_OUT_FP8E4M3 0x8u
+#define RMSN_OUT_MASK 0xCu
+/* optional operands; each must match a non-NULL pointer */
+#define RMSN_HAS_RESIDUAL 0x10u /* residual and residual_out */
+#define RMSN_HAS_WEIGHT 0x20u   /* weight (else 1) */
+#define RMSN_HAS_BIAS 0x40u     /* bias (else 0) */
+
+/* kernel variants */
+typedef enum {
+    RMSN_VARIANT_WARP_ROWS = 0, /* decode: one warp per row, rows spread over SMs */
+    RMSN_VARIANT_BLOCK_ROW = 1, /* prefill: one block (W warps) per row, register-resident */
+    RMSN_VARIANT_BULK_ROW = 2,  /* prefill: rows streamed to shared memory by bulk async copies */
+    RMSN_VARIANT_GENERIC = 3    /* any hidden size / alignment (element-wise, three passes) */
+} rmsn_variant;
+
+/* One launch configuration. */
+typedef struct {
+    int32_t variant;         /* rmsn_variant */
+    int32_t vec_bytes;       /* bytes per thread per access (32 = 256-bit) */
+    int32_t warps_per_block; /* launched warps per block */
+    int32_t warps_per_row;   /* warps that share one row */
+    int32_t chunks;          /* vectors per thread per row (template) */
+    int32_t max_warps;       /* template block-size bound (register budget) */
+    int32_t stages;          /* shared-memory row buffers (bulk variant) */
+    int32_t grid;            /* blocks launched */
+    int32_t smem_bytes;      /* dynamic shared memory per block */
+    int32_t num_sms;         /* SMs of the device the config was made for */
+} rmsn_config;
+
+/*
+ * Fused residual-add + RMSNorm over x[n_tokens, hidden].
+ *
+ *   x, residual, residual_out : [n_tokens, hidden] of the input dtype
+ *   weight, bias               : [hidden] of the input dtype
+ *   out                        : [n_tokens, hidden] of the output dtype
+ *   out_scale                  : [n_tokens] float32, required iff FP8 output
+ *   eps                        : added to the mean square inside the root
+ *
+ * All pointers are device (or managed / device-accessible) pointers, rows
+ * contiguous (row stride = hidden).  Each pointer must be aligned to its
+ * element size; the 256-bit vector kernels are used when hidden * element
+ * size is a multiple of 32 bytes and every pointer is 32-byte aligned,
+ * otherwise the generic kernel runs.  residual_out may be the same buffer as
+ * residual or x; out may be the same buffer as x or residual when the output
+ * and input dtypes are equal; any other overlap is undefined.  n_tokens == 0
+ * is a no-op.  Returns an rmsn_status.
+ */
+int rmsnorm_fwd(const void* x, const void* residual, const void* weight, const void* bias,
+                void* out, void* residual_out, float* out_scale, int64_t n_tokens,
+                int64_t hidden, float eps, uint32_t flags, cudaStream_t stream);
+
+/*
+ * rmsnorm_fwd with the scalar weight offset (the blog's WEIGHT_BIAS; 0 in
+ * rmsnorm_fwd) and an optional forced configuration (`cfg` NULL = the
+ * selector's choice).  A forced configuration must name a built variant;
+ * its grid is used when > 0 (else the default grid for that variant).
+ */
+int rmsnorm_fwd_ex(const void* x, const void* residual, const void* weight, const void* bias,
+                   void* out, void* residual_out, float* out_scale, int64_t n_tokens,
+                   int64_t hidden, float eps, uint32_t flags, float weight_offset,
+                   const rmsn_config* cfg, cudaStream_t stream);
+
+/*
+ * The configuration rmsnorm_fwd would launch for this shape on the current
+ * device, assuming 32-byte aligned pointers.  Returns an rmsn_status.
+ */
+int rmsnorm_query_config(int64_t n_tokens, int64_t hidden, uint32_t flags, rmsn_config* out);
+
+/*
+ * Every built configuration that can run this shape (for sweeps and tests).
+ * Writes up to `capacity` entries; returns the total number available, or a
+ * negative rmsn_status.
+ */
+int rmsnorm_list_configs(int64_t n_tokens, int64_t hidden, uint32_t flags, rmsn_config* out,
+                         int capacity);
+
+/* Human-readable name of an rmsn_status. */
+const char* rmsnorm_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMSNORM_GB300_H */

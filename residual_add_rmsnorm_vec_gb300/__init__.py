@@ -1,1 +1,21 @@
-"""GB300 (sm_103a) fused residual-add + RMSNorm."""
+"""GB300 (sm_103a) fused residual-add + RMSNorm.
+
+The compute runs in the hand-written CUDA kernels of ``csrc/`` behind the C
+ABI of ``include/rmsnorm.h``; this package only marshals arguments (PyTorch
+provides device memory and streams).  Operation, per token row (blog
+"CuTeDSL at Perplexity", section "QK norm", fused with the residual add and
+the FP8 output of section "Blackwell support"):
+
+    h = RN_in(x + residual);  residual_out = h
+    y = (weight + weight_offset) * h * rsqrt(mean(h^2) + eps) + bias
+    out = RN_out(y)   or   FP8-E4M3 codes of y * 448 / max|y| with scale max|y| / 448
+"""
+from __future__ import annotations
+
+from ._lib import (  # noqa: F401
+    EXPORTED, RMSN_EALIGN, RMSN_ECUDA, RMSN_EINVAL, RMSN_EUNSUPPORTED, RMSN_HAS_BIAS,
+    RMSN_HAS_RESIDUAL, RMSN_HAS_WEIGHT, RMSN_IN_BF16, RMSN_IN_F32, RMSN_OK, RMSN_OUT_BF16,
+    RMSN_OUT_F32, RMSN_OUT_FP8E4M3, VARIANT_BLOCK_ROW, VARIANT_BULK_ROW, VARIANT_GENERIC,
+    VARIANT_NAMES, VARIANT_WARP_ROWS, RmsnConfig, RmsnError, library_path, load,
+    rmsnorm_fwd, rmsnorm_fwd_ex, rmsnorm_list_configs, rmsnorm_query_config, status_string)
+from .api import fused_add_rmsnorm, make_flags  # noqa: F401

@@ -1,0 +1,74 @@
+"""Tensor-level entry point over the C ABI (marshalling only).
+
+``fused_add_rmsnorm`` takes CUDA tensors, allocates the outputs that are not
+given with torch, and calls ``rmsnorm_fwd_ex`` on the current torch stream.
+Nothing here computes: a failed call raises ``RmsnError``.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+_IN = {torch.float32: _lib.RMSN_IN_F32, torch.bfloat16: _lib.RMSN_IN_BF16}
+_OUT = {"f32": (_lib.RMSN_OUT_F32, torch.float32), "bf16": (_lib.RMSN_OUT_BF16, torch.bfloat16),
+        "fp8": (_lib.RMSN_OUT_FP8E4M3, torch.uint8)}
+_DT_NAME = {torch.float32: "f32", torch.bfloat16: "bf16"}
+
+
+def make_flags(in_dtype: str, out_dtype: str, residual: bool, weight: bool, bias: bool) -> int:
+    f = {"f32": _lib.RMSN_IN_F32, "bf16": _lib.RMSN_IN_BF16}[in_dtype]
+    f |= _OUT[out_dtype][0]
+    if residual:
+        f |= _lib.RMSN_HAS_RESIDUAL
+    if weight:
+        f |= _lib.RMSN_HAS_WEIGHT
+    if bias:
+        f |= _lib.RMSN_HAS_BIAS
+    return f
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def fused_add_rmsnorm(x: torch.Tensor, residual: torch.Tensor | None = None,
+                      weight: torch.Tensor | None = None, bias: torch.Tensor | None = None, *,
+                      eps: float, out_dtype: str | None = None, weight_offset: float = 0.0,
+                      out: torch.Tensor | None = None, residual_out: torch.Tensor | None = None,
+                      out_scale: torch.Tensor | None = None, config: _lib.RmsnConfig | None = None,
+                      stream: torch.cuda.Stream | None = None):
+    """Fused residual-add + RMSNorm of x[T, H] on the GPU.
+
+    Returns ``(out, residual_out, out_scale)``; ``residual_out`` is None
+    without a residual, ``out_scale`` is None unless ``out_dtype == "fp8"``
+    (``out`` then holds E4M3 codes as uint8).  Tensors must be contiguous and
+    on the same CUDA device; weight and bias are [H] of x's dtype.
+    """
+    if x.dim() != 2:
+        raise ValueError("x must be [n_tokens, hidden]")
+    if x.dtype not in _IN:
+        raise TypeError(f"unsupported input dtype {x.dtype}")
+    T, H = x.shape
+    in_name = _DT_NAME[x.dtype]
+    out_dtype = out_dtype or in_name
+    out_flag, out_torch = _OUT[out_dtype]
+    for name, t in (("residual", residual), ("weight", weight), ("bias", bias),
+                    ("out", out), ("residual_out", residual_out), ("out_scale", out_scale)):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if out is None:
+        out = torch.empty((T, H), dtype=out_torch, device=x.device)
+    if residual is not None and residual_out is None:
+        residual_out = torch.empty_like(x)
+    if out_dtype == "fp8" and out_scale is None:
+        out_scale = torch.empty((T,), dtype=torch.float32, device=x.device)
+    flags = make_flags(in_name, out_dtype, residual is not None, weight is not None,
+                       bias is not None)
+    s = stream if stream is not None else torch.cuda.current_stream(x.device)
+    st = _lib.rmsnorm_fwd_ex(_ptr(x.contiguous()), _ptr(residual), _ptr(weight), _ptr(bias),
+                             _ptr(out), _ptr(residual_out), _ptr(out_scale), T, H, eps, flags,
+                             weight_offset, config, s.cuda_stream)
+    if st != _lib.RMSN_OK:
+        raise _lib.RmsnError(st, "rmsnorm_fwd_ex")
+    return out, residual_out, (out_scale if out_dtype == "fp8" else None)

@@ -1,0 +1,434 @@
+// Device code of the fused residual-add + RMSNorm for sm_103a.
+//
+// The operation is the regular RMS norm of the blog "CuTeDSL at Perplexity"
+// (section "QK norm": fp32 sum of squares, reciprocal square root of the mean
+// square plus EPS, times the weight plus the scalar WEIGHT_BIAS, cast to the
+// element type), fused with the residual add, an optional per-channel bias
+// and an optional per-token FP8-E4M3 absmax output (section "Blackwell
+// support").  Layout choices follow the same blog, section "Prefill and
+// decode": the per-thread vector is picked for the widest load/store
+// (256-bit on Blackwell), the warp count per block is a compile-time bound so
+// the register allocation is known, decode rows go one warp per block to
+// spread over as many SMs as possible, prefill rows go to multi-warp blocks.
+//
+// Kernels:
+//   rmsn_vec_kernel     one row per warp (WARP_ROWS) or per block; each thread
+//                       holds CH 32-byte vectors of the row in registers
+//                       between the load and the store.
+//   rmsn_generic_kernel any hidden size / alignment; element-wise, re-reads
+//                       the row from the just-written residual_out.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "rmsn_registry.h"
+
+namespace rmsn {
+
+struct F32 {
+    static constexpr int kBytes = 4;
+};
+struct BF16 {
+    static constexpr int kBytes = 2;
+};
+struct FP8 {
+    static constexpr int kBytes = 1;
+};
+
+// 32-byte register vector.
+struct V8 {
+    uint32_t u[8];
+};
+
+// ---------------------------------------------------------------- memory ops
+// Streaming operands (x, residual) are read once: no L1 allocation.  Weight
+// and bias are re-read by every row: default caching so they stay on chip.
+
+__device__ __forceinline__ V8 ld_stream32(const void* p) {
+    V8 v;
+    asm volatile("ld.global.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v.u[0]), "=r"(v.u[1]), "=r"(v.u[2]), "=r"(v.u[3]), "=r"(v.u[4]),
+                   "=r"(v.u[5]), "=r"(v.u[6]), "=r"(v.u[7])
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ V8 ld_keep32(const void* p) {
+    V8 v;
+    asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v.u[0]), "=r"(v.u[1]), "=r"(v.u[2]), "=r"(v.u[3]), "=r"(v.u[4]),
+                   "=r"(v.u[5]), "=r"(v.u[6]), "=r"(v.u[7])
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream32(void* p, const uint32_t* u) {
+    asm volatile("st.global.L1::no_allocate.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p),
+                 "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]),
+                 "r"(u[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_stream16(void* p, const uint32_t* u) {
+    asm volatile("st.global.L1::no_allocate.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(u[0]),
+                 "r"(u[1]), "r"(u[2]), "r"(u[3])
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_stream8(void* p, const uint32_t* u) {
+    asm volatile("st.global.L1::no_allocate.v2.b32 [%0], {%1,%2};" ::"l"(p), "r"(u[0]), "r"(u[1])
+                 : "memory");
+}
+
+// ---------------------------------------------------------------- conversions
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// Round two floats to bf16 (nearest-even) and pack them, `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Round four floats to E4M3 (nearest-even, saturating to +-448), element 0
+// in the lowest byte.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a0, float a1, float a2, float a3) {
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(a1), "f"(a0));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(a3), "f"(a2));
+    return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+// Element k of a 32-byte vector of TI as float.
+template <class TI>
+__device__ __forceinline__ float elem(const V8& v, int k) {
+    if constexpr (TI::kBytes == 2) {
+        return (k & 1) ? bf16_hi(v.u[k >> 1]) : bf16_lo(v.u[k >> 1]);
+    } else {
+        return __uint_as_float(v.u[k]);
+    }
+}
+
+// Make the compiler treat v as redefined here, so values unpacked from it are
+// not hoisted out of the row loop (that would keep 2x the registers live).
+__device__ __forceinline__ void opaque(V8& v) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) asm volatile("" : "+r"(v.u[k]));
+}
+
+template <class TI>
+__device__ __forceinline__ uint32_t ones_word() {
+    return TI::kBytes == 2 ? 0x3F803F80u : 0x3F800000u;
+}
+
+// ---------------------------------------------------------------- reductions
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// Sum (or max) over the warps of a block through shared memory.  `slot` is a
+// [32] float array that alternates between calls so one barrier per call
+// suffices; every thread adds the partials in the same order and so gets the
+// same total.
+template <bool MAX>
+__device__ __forceinline__ float block_allreduce(float v, float* slot) {
+    v = MAX ? warp_max(v) : warp_sum(v);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) slot[warp] = v;
+    __syncthreads();
+    const int nw = blockDim.x >> 5;
+    float t = slot[0];
+    for (int i = 1; i < nw; ++i) t = MAX ? fmaxf(t, slot[i]) : __fadd_rn(t, slot[i]);
+    return t;
+}
+
+__device__ __forceinline__ float inv_rms(float sumsq, int H, float eps) {
+    return __frsqrt_rn(__fadd_rn(__fdiv_rn(sumsq, (float)H), eps));
+}
+
+// y = (w + w_off) * (h * inv) + b, with every rounding explicit so the two
+// FP8 passes recompute identical values.
+template <bool BIAS>
+__device__ __forceinline__ float scale_elem(float h, float inv, float w, float woff, float b) {
+    const float t = __fmul_rn(h, inv);
+    const float wo = __fadd_rn(w, woff);
+    return BIAS ? __fmaf_rn(wo, t, b) : __fmul_rn(wo, t);
+}
+
+// Store the VE outputs of one input vector at element offset `e`.
+template <class TI, class TO>
+__device__ __forceinline__ void store_out(void* out, int64_t e, const float (&y)[32 / TI::kBytes],
+                                          float qmul) {
+    constexpr int VE = 32 / TI::kBytes;
+    if constexpr (TO::kBytes == 4) {
+        uint32_t u[VE];
+#pragma unroll
+        for (int k = 0; k < VE; ++k) u[k] = __float_as_uint(y[k]);
+        float* o = reinterpret_cast<float*>(out) + e;
+#pragma unroll
+        for (int s = 0; s < VE / 8; ++s) st_stream32(o + 8 * s, u + 8 * s);
+    } else if constexpr (TO::kBytes == 2) {
+        uint32_t u[VE / 2];
+#pragma unroll
+        for (int k = 0; k < VE / 2; ++k) u[k] = pack_bf16x2(y[2 * k], y[2 * k + 1]);
+        uint16_t* o = reinterpret_cast<uint16_t*>(out) + e;
+        if constexpr (VE == 16) st_stream32(o, u);
+        else st_stream16(o, u);
+    } else {
+        uint32_t u[VE / 4];
+#pragma unroll
+        for (int k = 0; k < VE / 4; ++k)
+            u[k] = pack_e4m3x4(__fmul_rn(y[4 * k], qmul), __fmul_rn(y[4 * k + 1], qmul),
+                               __fmul_rn(y[4 * k + 2], qmul), __fmul_rn(y[4 * k + 3], qmul));
+        uint8_t* o = reinterpret_cast<uint8_t*>(out) + e;
+        if constexpr (VE == 16) st_stream16(o, u);
+        else st_stream8(o, u);
+    }
+}
+
+// Register budget: blocks of up to WMAX warps; at least 1024 resident threads
+// per SM for CH <= 2 (64 registers / thread), 512 for CH = 4 (128) and 256
+// for CH = 8 (255, one-warp decode rows).
+template <int WMAX, int CH>
+struct Bounds {
+    static constexpr int kThreads = WMAX * 32;
+    static constexpr int kTarget = CH <= 2 ? 1024 : (CH <= 4 ? 512 : 256);
+    static constexpr int kMinBlocks = kTarget / kThreads > 0 ? kTarget / kThreads : 1;
+};
+
+// ---------------------------------------------------------------- vector kernel
+//
+// WARP_ROWS: each warp owns one row (block = WMAX rows); else the block owns
+// one row and has up to WMAX warps.  A thread handles vectors
+// v = c * G + t (c < CH, G = threads per row, t = thread within the row) of
+// VE elements each, so a warp touches 1 KiB of contiguous memory per chunk.
+// Rows are visited grid-stride; weight and bias stay in registers.
+template <class TI, class TO, int CH, int WMAX, bool WARP_ROWS, bool RES, bool BIAS>
+__global__ void __launch_bounds__(Bounds<WMAX, CH>::kThreads, Bounds<WMAX, CH>::kMinBlocks)
+    rmsn_vec_kernel(const RmsnArgs a) {
+    constexpr int VE = 32 / TI::kBytes;  // elements per 32-byte vector
+    constexpr bool FP8OUT = TO::kBytes == 1;
+    __shared__ float red[4][32];
+
+    const int lane = threadIdx.x & 31;
+    const int G = WARP_ROWS ? 32 : (int)blockDim.x;
+    const int t = WARP_ROWS ? lane : (int)threadIdx.x;
+    const int64_t rows_per_step = WARP_ROWS ? (int64_t)gridDim.x * (blockDim.x >> 5) : gridDim.x;
+    int64_t row = WARP_ROWS ? (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)
+                            : (int64_t)blockIdx.x;
+    const int nvec = a.nvec;
+    const int H = a.H;
+
+    V8 wv[CH];
+    V8 bv[BIAS ? CH : 1];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        const int v = c * G + t;
+        if (v < nvec) {
+            if (a.has_w) {
+                wv[c] = ld_keep32(static_cast<const char*>(a.w) + (int64_t)v * 32);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) wv[c].u[k] = ones_word<TI>();
+            }
+            if constexpr (BIAS) bv[c] = ld_keep32(static_cast<const char*>(a.b) + (int64_t)v * 32);
+        }
+    }
+
+    int parity = 0;
+    for (; row < a.T; row += rows_per_step) {
+        const int64_t rbase = row * (int64_t)H;  // element offset of the row
+        V8 hv[CH];
+        V8 rv[RES ? CH : 1];
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int v = c * G + t;
+            if (v < nvec) {
+                const int64_t off = (rbase + (int64_t)v * VE) * TI::kBytes;
+                hv[c] = ld_stream32(static_cast<const char*>(a.x) + off);
+                if constexpr (RES) rv[c] = ld_stream32(static_cast<const char*>(a.r) + off);
+            }
+        }
+        float acc = 0.f;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int v = c * G + t;
+            if (v < nvec) {
+                if constexpr (RES) {
+                    // h = RN_in(x + r); the sum is formed in fp32
+                    if constexpr (TI::kBytes == 2) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const float lo = __fadd_rn(bf16_lo(hv[c].u[k]), bf16_lo(rv[c].u[k]));
+                            const float hi = __fadd_rn(bf16_hi(hv[c].u[k]), bf16_hi(rv[c].u[k]));
+                            hv[c].u[k] = pack_bf16x2(lo, hi);
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            hv[c].u[k] = __float_as_uint(__fadd_rn(__uint_as_float(hv[c].u[k]),
+                                                                   __uint_as_float(rv[c].u[k])));
+                    }
+                    const int64_t off = (rbase + (int64_t)v * VE) * TI::kBytes;
+                    st_stream32(static_cast<char*>(a.res_out) + off, hv[c].u);
+                }
+#pragma unroll
+                for (int k = 0; k < VE; ++k) {
+                    const float h = elem<TI>(hv[c], k);
+                    acc = __fmaf_rn(h, h, acc);
+                }
+            }
+        }
+        float sumsq;
+        if constexpr (WARP_ROWS) {
+            sumsq = warp_sum(acc);
+        } else {
+            sumsq = block_allreduce<false>(acc, red[parity]);
+        }
+        const float inv = inv_rms(sumsq, H, a.eps);
+
+        float qmul = 0.f;
+        if constexpr (FP8OUT) {
+            float amax = 0.f;
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                const int v = c * G + t;
+                if (v < nvec) {
+                    opaque(wv[c]);
+                    if constexpr (BIAS) opaque(bv[BIAS ? c : 0]);
+#pragma unroll
+                    for (int k = 0; k < VE; ++k) {
+                        const float y = scale_elem<BIAS>(elem<TI>(hv[c], k), inv,
+                                                         elem<TI>(wv[c], k), a.woff,
+                                                         BIAS ? elem<TI>(bv[BIAS ? c : 0], k) : 0.f);
+                        amax = fmaxf(amax, fabsf(y));
+                    }
+                }
+            }
+            if constexpr (WARP_ROWS) {
+                amax = warp_max(amax);
+            } else {
+                amax = block_allreduce<true>(amax, red[2 + parity]);
+            }
+            qmul = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
+            if (t == 0) a.scale[row] = __fdiv_rn(amax, 448.f);
+        }
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int v = c * G + t;
+            if (v < nvec) {
+                opaque(wv[c]);
+                if constexpr (BIAS) opaque(bv[BIAS ? c : 0]);
+                float y[VE];
+#pragma unroll
+                for (int k = 0; k < VE; ++k)
+                    y[k] = scale_elem<BIAS>(elem<TI>(hv[c], k), inv, elem<TI>(wv[c], k), a.woff,
+                                            BIAS ? elem<TI>(bv[BIAS ? c : 0], k) : 0.f);
+                store_out<TI, TO>(a.out, rbase + (int64_t)v * VE, y, qmul);
+            }
+        }
+        parity ^= 1;
+    }
+}
+
+// ---------------------------------------------------------------- generic kernel
+//
+// Any hidden size and any pointer aligned to its element size.  One block per
+// row (grid-stride), elements strided by the block: pass 1 forms h, stores
+// residual_out and accumulates the squares; pass 2 re-reads h (from
+// residual_out, written by the same thread) and writes the output; the FP8
+// output takes an extra pass for the row's absmax.
+
+template <class T>
+__device__ __forceinline__ float ld_elem(const void* p, int64_t i) {
+    if constexpr (T::kBytes == 2) {
+        return __uint_as_float((uint32_t)(static_cast<const uint16_t*>(p)[i]) << 16);
+    } else {
+        return static_cast<const float*>(p)[i];
+    }
+}
+
+template <class T>
+__device__ __forceinline__ float round_to(float v) {
+    if constexpr (T::kBytes == 2) {
+        return bf16_lo(pack_bf16x2(v, 0.f));
+    } else {
+        return v;
+    }
+}
+
+template <class T>
+__device__ __forceinline__ void st_elem(void* p, int64_t i, float v) {
+    if constexpr (T::kBytes == 2) {
+        static_cast<uint16_t*>(p)[i] = (uint16_t)(pack_bf16x2(v, 0.f) & 0xFFFFu);
+    } else {
+        static_cast<float*>(p)[i] = v;
+    }
+}
+
+template <class TI>
+__device__ __forceinline__ float generic_y(const RmsnArgs& a, const void* hsrc, int64_t base,
+                                           int j, float inv) {
+    const float h = ld_elem<TI>(hsrc, base + j);
+    const float w = a.has_w ? ld_elem<TI>(a.w, j) : 1.f;
+    if (a.b) return scale_elem<true>(h, inv, w, a.woff, ld_elem<TI>(a.b, j));
+    return scale_elem<false>(h, inv, w, a.woff, 0.f);
+}
+
+template <class TI, class TO, bool RES>
+__global__ void __launch_bounds__(256) rmsn_generic_kernel(const RmsnArgs a) {
+    __shared__ float red[4][32];
+    const int H = a.H;
+    int parity = 0;
+    for (int64_t row = blockIdx.x; row < a.T; row += gridDim.x) {
+        const int64_t base = row * (int64_t)H;
+        float acc = 0.f;
+        for (int j = threadIdx.x; j < H; j += blockDim.x) {
+            float h = ld_elem<TI>(a.x, base + j);
+            if constexpr (RES) {
+                h = round_to<TI>(__fadd_rn(h, ld_elem<TI>(a.r, base + j)));
+                st_elem<TI>(a.res_out, base + j, h);
+            }
+            acc = __fmaf_rn(h, h, acc);
+        }
+        const float inv = inv_rms(block_allreduce<false>(acc, red[parity]), H, a.eps);
+        const void* hsrc = RES ? static_cast<const void*>(a.res_out) : a.x;
+        float qmul = 0.f;
+        if constexpr (TO::kBytes == 1) {
+            float amax = 0.f;
+            for (int j = threadIdx.x; j < H; j += blockDim.x) {
+                amax = fmaxf(amax, fabsf(generic_y<TI>(a, hsrc, base, j, inv)));
+            }
+            amax = block_allreduce<true>(amax, red[2 + parity]);
+            qmul = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
+            if (threadIdx.x == 0) a.scale[row] = __fdiv_rn(amax, 448.f);
+        }
+        for (int j = threadIdx.x; j < H; j += blockDim.x) {
+            const float y = generic_y<TI>(a, hsrc, base, j, inv);
+            if constexpr (TO::kBytes == 1) {
+                uint16_t q;
+                asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+                    : "=h"(q)
+                    : "f"(0.f), "f"(__fmul_rn(y, qmul)));
+                static_cast<uint8_t*>(a.out)[base + j] = (uint8_t)(q & 0xFF);
+            } else {
+                st_elem<TO>(a.out, base + j, y);
+            }
+        }
+        parity ^= 1;
+    }
+}
+
+}  // namespace rmsn

@@ -1,0 +1,44 @@
+// Kernel registry shared by the instantiation units and the C-ABI layer.
+#pragma once
+
+#include <stdint.h>
+
+namespace rmsn {
+
+// Kernel arguments (passed by value).  Pointers are device pointers; `b` is
+// NULL when there is no bias; `nvec` = hidden / elements per 32-byte vector.
+struct RmsnArgs {
+    const void* x;
+    const void* r;
+    const void* w;
+    const void* b;
+    void* out;
+    void* res_out;
+    float* scale;
+    int64_t T;
+    int32_t H;
+    int32_t nvec;
+    float eps;
+    float woff;
+    int32_t has_w;
+};
+
+enum DType : int32_t { kF32 = 0, kBF16 = 1, kFP8 = 2 };
+
+enum Variant : int32_t { kWarpRows = 0, kBlockRow = 1, kBulkRow = 2, kGeneric = 3 };
+
+// One compiled kernel.
+struct KernelEntry {
+    int32_t in_dt, out_dt, variant, chunks, max_warps, stages, res, bias;
+    const void* fn;
+};
+
+// Each instantiation unit returns its table.
+const KernelEntry* kernels_f32_f32(int* n);
+const KernelEntry* kernels_f32_bf16(int* n);
+const KernelEntry* kernels_f32_fp8(int* n);
+const KernelEntry* kernels_bf16_f32(int* n);
+const KernelEntry* kernels_bf16_bf16(int* n);
+const KernelEntry* kernels_bf16_fp8(int* n);
+
+}  // namespace rmsn

@@ -1,0 +1,94 @@
+"""Helpers for GPU-vs-oracle parity: run both sides on the same seeded inputs
+and compare with the tolerances of the fused residual-add + RMSNorm:
+
+* residual_out: bit-exact;
+* bf16 output: at most 1 bf16 ulp (signed-magnitude ordering, +0 == -0);
+* fp32 output: relative error <= 1e-5;
+* FP8-E4M3 output: same code or the adjacent one; per-token scale relative
+  error <= 1e-6.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+BF16_ULP = 1
+F32_RTOL = 1e-5
+FP8_STEPS = 1
+SCALE_RTOL = 1e-6
+
+
+def ordered16(bits: np.ndarray) -> np.ndarray:
+    b = bits.astype(np.int32)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def ordered8(codes: np.ndarray) -> np.ndarray:
+    c = codes.astype(np.int32)
+    mag = c & 0x7F
+    return np.where(c & 0x80, -mag, mag)
+
+
+def bits16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def to_device(inp: dict, dev) -> dict:
+    return {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+
+
+def oracle_run(wl, inp: dict, weight_offset: float = 0.0) -> dict:
+    return oracle.rmsnorm(inp["x"], inp["residual"], inp["weight"], inp["bias"],
+                          eps=float(np.float32(wl.eps)), in_dtype=wl.in_dtype,
+                          out_dtype=wl.out_dtype, weight_offset=weight_offset)
+
+
+def gpu_outputs_to_host(wl, out, res, scale) -> dict:
+    if wl.out_dtype == "bf16":
+        o = bits16(out)
+    elif wl.out_dtype == "fp8":
+        o = out.detach().cpu().numpy()
+    else:
+        o = out.detach().cpu().numpy()
+    r = None
+    if res is not None:
+        r = bits16(res) if wl.in_dtype == "bf16" else res.detach().cpu().numpy()
+    s = None if scale is None else scale.detach().cpu().numpy()
+    return {"out": o, "residual_out": r, "out_scale": s}
+
+
+def compare(wl, got: dict, ref: dict, where: str = "") -> dict:
+    """Assert the tolerances; return statistics."""
+    stats = {}
+    if ref["residual_out"] is not None:
+        g, r = got["residual_out"], ref["residual_out"]
+        if wl.in_dtype == "bf16":
+            bad = np.count_nonzero(g != r)
+        else:
+            bad = np.count_nonzero(g.view(np.uint32) != r.view(np.uint32))
+        assert bad == 0, f"{where}: residual_out differs in {bad} elements"
+    if wl.out_dtype == "bf16":
+        d = np.abs(ordered16(got["out"]) - ordered16(ref["out"]))
+        stats["max_ulp"] = int(d.max()) if d.size else 0
+        stats["exact_frac"] = float((d == 0).mean()) if d.size else 1.0
+        assert stats["max_ulp"] <= BF16_ULP, f"{where}: bf16 output off by {stats['max_ulp']} ulp"
+    elif wl.out_dtype == "f32":
+        g = got["out"].astype(np.float64)
+        r = ref["out"].astype(np.float64)
+        rel = np.abs(g - r) / np.maximum(np.abs(r), np.finfo(np.float32).tiny)
+        stats["max_rel"] = float(rel.max()) if rel.size else 0.0
+        assert stats["max_rel"] <= F32_RTOL, f"{where}: f32 output rel err {stats['max_rel']}"
+    else:
+        d = np.abs(ordered8(got["out"]) - ordered8(ref["out"]))
+        stats["max_steps"] = int(d.max()) if d.size else 0
+        stats["exact_frac"] = float((d == 0).mean()) if d.size else 1.0
+        assert stats["max_steps"] <= FP8_STEPS, f"{where}: fp8 codes {stats['max_steps']} steps apart"
+        gs = got["out_scale"].astype(np.float64)
+        rs = ref["out_scale"].astype(np.float64)
+        rel = np.where(rs == 0, np.abs(gs), np.abs(gs - rs) / np.where(rs == 0, 1, np.abs(rs)))
+        stats["scale_max_rel"] = float(rel.max()) if rel.size else 0.0
+        assert stats["scale_max_rel"] <= SCALE_RTOL, f"{where}: scale rel err {stats['scale_max_rel']}"
+    return stats

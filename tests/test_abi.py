@@ -1,0 +1,118 @@
+"""CPU checks of the C-ABI library: it builds, loads without a GPU, exports
+every function include/rmsnorm.h declares, and rejects bad arguments before
+touching the device."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from residual_add_rmsnorm_vec_gb300 import build
+
+    build.build()
+    import residual_add_rmsnorm_vec_gb300 as pkg
+
+    return pkg
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "rmsnorm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(rmsnorm_\w+)\s*\(", src, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    assert names == sorted(["rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_query_config",
+                            "rmsnorm_list_configs", "rmsnorm_status_string"]), names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import ctypes
+
+    so = ctypes.CDLL(lib.library_path())
+    for name in declared_functions():
+        assert hasattr(so, name), name
+    assert sorted(lib.EXPORTED) == declared_functions()
+
+
+def test_only_abi_symbols_are_exported(lib):
+    import subprocess
+
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    text_syms = [l.split()[-1] for l in out.splitlines() if " T " in l]
+    ours = [s for s in text_syms if not s.startswith("_")]
+    assert sorted(ours) == declared_functions(), ours
+
+
+def test_status_strings(lib):
+    assert lib.status_string(lib.RMSN_OK) == "RMSN_OK"
+    for st in (lib.RMSN_EINVAL, lib.RMSN_EALIGN, lib.RMSN_EUNSUPPORTED, lib.RMSN_ECUDA):
+        assert lib.status_string(st).startswith("RMSN_E")
+    assert lib.status_string(12345) == "unknown rmsn_status"
+
+
+BF16_RES = 0x1 | 0x4 | 0x10 | 0x20  # bf16 in/out, residual, weight
+
+
+@pytest.mark.parametrize("case", [
+    # (x, r, w, b, out, res_out, scale, T, H, eps, flags)
+    ("unknown flag bit", (16, 16, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES | 0x80)),
+    ("bad input dtype", (16, 16, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES | 0x2)),
+    ("bad output dtype", (16, 16, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES | 0xC)),
+    ("residual flag without pointer", (16, None, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES)),
+    ("residual_out missing", (16, 16, 16, None, 16, None, None, 4, 64, 1e-6, BF16_RES)),
+    ("pointer without flag", (16, 16, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES & ~0x20 | 0)),
+    ("bias pointer without flag", (16, 16, 16, 16, 16, 16, None, 4, 64, 1e-6, BF16_RES)),
+    ("fp8 without scale", (16, 16, 16, None, 16, 16, None, 4, 64, 1e-6, 0x1 | 0x8 | 0x10 | 0x20)),
+    ("scale without fp8", (16, 16, 16, None, 16, 16, 16, 4, 64, 1e-6, BF16_RES)),
+    ("hidden zero", (16, 16, 16, None, 16, 16, None, 4, 0, 1e-6, BF16_RES)),
+    ("negative tokens", (16, 16, 16, None, 16, 16, None, -1, 64, 1e-6, BF16_RES)),
+    ("hidden too large", (16, 16, 16, None, 16, 16, None, 1, 1 << 25, 1e-6, BF16_RES)),
+    ("size overflow", (16, 16, 16, None, 16, 16, None, 1 << 40, 1 << 22, 1e-6, BF16_RES)),
+    ("negative eps", (16, 16, 16, None, 16, 16, None, 4, 64, -1.0, BF16_RES)),
+    ("nan eps", (16, 16, 16, None, 16, 16, None, 4, 64, float("nan"), BF16_RES)),
+    ("null x", (None, 16, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES)),
+])
+def test_invalid_arguments_rejected_without_gpu(lib, case):
+    name, (x, r, w, b, o, ro, s, T, H, eps, flags) = case
+    st = lib.rmsnorm_fwd(x, r, w, b, o, ro, s, T, H, eps, flags, None)
+    assert st == lib.RMSN_EINVAL, (name, lib.status_string(st))
+
+
+def test_misaligned_pointer_rejected_without_gpu(lib):
+    # a bf16 pointer at an odd byte address
+    st = lib.rmsnorm_fwd(17, 16, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES, None)
+    assert st == lib.RMSN_EALIGN
+    # an f32 residual at a 2-byte boundary (f32 needs 4); every call here
+    # returns before any launch, so no fake pointer ever reaches a kernel
+    st = lib.rmsnorm_fwd(16, 18, 16, None, 16, 16, None, 4, 64, 1e-6, 0x10 | 0x20, None)
+    assert st == lib.RMSN_EALIGN
+
+
+def test_empty_batch_is_a_no_op_without_gpu(lib):
+    assert lib.rmsnorm_fwd(None, None, None, None, None, None, None, 0, 64, 1e-6, 0x1 | 0x4,
+                           None) == lib.RMSN_OK
+
+
+def test_product_path_has_no_cpu_fallback():
+    # the package must not import the oracle or any CPU implementation
+    pkg_dir = os.path.join(ROOT, "residual_add_rmsnorm_vec_gb300")
+    for fn in os.listdir(pkg_dir):
+        if fn.endswith(".py"):
+            text = open(os.path.join(pkg_dir, fn)).read()
+            assert "import oracle" not in text and "from oracle" not in text, fn
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    import residual_add_rmsnorm_vec_gb300._lib as L
+
+    monkeypatch.setattr(L, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(L, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        L.load()

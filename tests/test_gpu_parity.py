@@ -1,0 +1,284 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs, element by element.  Tolerances are in tests/parity.py:
+residual_out bit-exact, bf16 <= 1 ulp, fp32 relative <= 1e-5, FP8 <= 1 code
+step with per-token scale relative error <= 1e-6.
+
+Workloads are the five hot-path configurations (fp32 plain norm; bf16 decode
+T in {1..256} x H=4096; bf16 prefill 16384 x 8192 with outlier channels;
+FP8 output with bias at H in {5120, 7168}; the tokens x hidden sweep), plus
+ragged, misaligned, aliased and degenerate shapes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import parity
+from residual_add_rmsnorm_vec_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from residual_add_rmsnorm_vec_gb300 import build
+
+    build.build()
+    import residual_add_rmsnorm_vec_gb300 as p
+
+    torch.cuda.set_device(0)
+    return p
+
+
+DEV = "cuda:0"
+
+
+def run_gpu(pkg, wl, inp, config=None, weight_offset=0.0):
+    g = parity.to_device(inp, DEV)
+    out, res, scale = pkg.fused_add_rmsnorm(g["x"], g["residual"], g["weight"], g["bias"],
+                                            eps=wl.eps, out_dtype=wl.out_dtype,
+                                            weight_offset=weight_offset, config=config)
+    torch.cuda.synchronize()
+    return parity.gpu_outputs_to_host(wl, out, res, scale)
+
+
+def check(pkg, wl, rows=None, config=None, weight_offset=0.0, where=""):
+    """Full tensors on the GPU; oracle on all rows or the sampled ``rows``."""
+    inp = synth.make_inputs(wl)
+    got = run_gpu(pkg, wl, inp, config, weight_offset)
+    if rows is not None:
+        sub = synth.make_inputs(wl, rows=rows)
+        ref = parity.oracle_run(wl, sub, weight_offset)
+        got = {k: (None if v is None else v[rows]) for k, v in got.items()}
+    else:
+        ref = parity.oracle_run(wl, inp, weight_offset)
+    return parity.compare(wl, got, ref, where or wl.name)
+
+
+# ---------------------------------------------------------------- the five configs
+
+
+def test_fp32_plain_norm(pkg):
+    st = check(pkg, synth.fp32_workload())
+    assert st["max_rel"] <= 1e-5
+
+
+@pytest.mark.parametrize("T", synth.DECODE_TOKENS)
+def test_decode(pkg, T):
+    check(pkg, synth.decode_workload(T))
+
+
+def test_prefill_full_size(pkg):
+    # every row of the 16384 x 8192 workload, the shape the bench times
+    wl = synth.prefill_workload()
+    st = check(pkg, wl)
+    assert st["exact_frac"] > 0.99
+
+
+@pytest.mark.parametrize("H", synth.FP8_HIDDEN)
+def test_fp8_bias(pkg, H):
+    st = check(pkg, synth.fp8_workload(H))
+    assert st["exact_frac"] > 0.99
+
+
+@pytest.mark.parametrize("H", synth.SWEEP_HIDDEN)
+@pytest.mark.parametrize("T", synth.SWEEP_TOKENS)
+def test_sweep(pkg, T, H):
+    wl = synth.sweep_workload(T, H)
+    rows = None
+    if T * H > 64 * 2**20:
+        rows = synth.sample_rows(T, 1024)
+    check(pkg, wl, rows=rows)
+
+
+# ---------------------------------------------------------------- every built variant
+
+
+FLAG_SETS = [
+    ("bf16", "bf16", True, True, False),
+    ("bf16", "bf16", True, True, True),
+    ("bf16", "bf16", False, False, False),
+    ("bf16", "f32", True, True, True),
+    ("bf16", "fp8", True, True, True),
+    ("bf16", "fp8", False, True, False),
+    ("f32", "f32", False, True, False),
+    ("f32", "f32", True, True, True),
+    ("f32", "bf16", True, True, False),
+    ("f32", "fp8", True, True, True),
+]
+
+
+@pytest.mark.parametrize("fs", FLAG_SETS, ids=lambda f: "-".join(map(str, f)))
+@pytest.mark.parametrize("H", [256, 2048, 5120])
+def test_every_config(pkg, fs, H):
+    in_dt, out_dt, res, w, b = fs
+    T = 37
+    wl = synth.Workload(f"cfg_{in_dt}_{out_dt}", T, H, 77, in_dt, out_dt, 1e-6,
+                        has_residual=res, has_weight=w, has_bias=b)
+    flags = pkg.make_flags(in_dt, out_dt, res, w, b)
+    cfgs = pkg.rmsnorm_list_configs(T, H, flags)
+    assert cfgs, "no configuration for a vector-aligned shape"
+    inp = synth.make_inputs(wl)
+    ref = parity.oracle_run(wl, inp)
+    variants = set()
+    for c in cfgs:
+        got = run_gpu(pkg, wl, inp, config=c)
+        parity.compare(wl, got, ref, f"{wl.name} {c.as_dict()}")
+        variants.add(c.variant)
+        # a small explicit grid exercises the grid-stride row loop
+        c2 = pkg.RmsnConfig.from_dict({**c.as_dict(), "grid": 3})
+        got = run_gpu(pkg, wl, inp, config=c2)
+        parity.compare(wl, got, ref, f"{wl.name} grid=3 {c.as_dict()}")
+    assert pkg.VARIANT_GENERIC in variants and pkg.VARIANT_BLOCK_ROW in variants
+
+
+def test_weight_offset(pkg):
+    wl = synth.Workload("woff", 16, 4096, 5, "bf16", "bf16", 1e-6, has_bias=True)
+    for off in (1.0, -0.5):
+        check(pkg, wl, weight_offset=off)
+
+
+# ---------------------------------------------------------------- edge cases
+
+
+@pytest.mark.parametrize("H", [1, 3, 7, 8, 15, 17, 100, 1000, 4095, 4097, 6000])
+@pytest.mark.parametrize("out_dt", ["bf16", "fp8", "f32"])
+def test_ragged_hidden_generic_path(pkg, H, out_dt):
+    wl = synth.Workload(f"ragged_H{H}", 33, H, 9, "bf16", out_dt, 1e-6, has_bias=True)
+    check(pkg, wl)
+
+
+@pytest.mark.parametrize("H", [1, 5, 8, 1001])
+def test_ragged_hidden_f32(pkg, H):
+    wl = synth.Workload(f"ragged32_H{H}", 19, H, 9, "f32", "f32", 1e-6)
+    check(pkg, wl)
+
+
+def test_empty_batch(pkg):
+    x = torch.empty((0, 4096), dtype=torch.bfloat16, device=DEV)
+    r = torch.empty_like(x)
+    out, res, _ = pkg.fused_add_rmsnorm(x, r, None, None, eps=1e-6)
+    assert out.shape == (0, 4096) and res.shape == (0, 4096)
+
+
+def test_misaligned_pointers_take_generic_path(pkg):
+    # views offset by one bf16 element: 2-byte aligned, not 32-byte aligned
+    wl = synth.Workload("misaligned", 24, 2048, 11, "bf16", "bf16", 1e-6)
+    inp = synth.make_inputs(wl)
+    ref = parity.oracle_run(wl, inp)
+    T, H = wl.n_tokens, wl.hidden
+    bufs = {k: torch.zeros(T * H + 1, dtype=torch.bfloat16, device=DEV) for k in ("x", "r", "o", "ro")}
+    x = bufs["x"][1:].view(T, H)
+    r = bufs["r"][1:].view(T, H)
+    x.copy_(inp["x"])
+    r.copy_(inp["residual"])
+    wbuf = torch.zeros(H + 1, dtype=torch.bfloat16, device=DEV)
+    w = wbuf[1:]
+    w.copy_(inp["weight"])
+    out = bufs["o"][1:].view(T, H)
+    res = bufs["ro"][1:].view(T, H)
+    pkg.fused_add_rmsnorm(x, r, w, None, eps=wl.eps, out=out, residual_out=res)
+    torch.cuda.synchronize()
+    got = parity.gpu_outputs_to_host(wl, out, res, None)
+    parity.compare(wl, got, ref, "misaligned")
+
+
+def test_odd_byte_pointer_rejected(pkg):
+    buf = torch.zeros(2 * 64 * 64 + 2, dtype=torch.uint8, device=DEV)
+    base = buf.data_ptr()
+    st = pkg.rmsnorm_fwd(base + 1, base + 1, None, None, base + 1, base + 1, None, 4, 64, 1e-6,
+                         pkg.make_flags("bf16", "bf16", True, False, False),
+                         torch.cuda.current_stream().cuda_stream)
+    assert st == pkg.RMSN_EALIGN
+
+
+@pytest.mark.parametrize("alias", ["residual_out=residual", "residual_out=x", "out=x",
+                                   "out=residual"])
+def test_in_place_aliasing(pkg, alias):
+    wl = synth.Workload("alias", 40, 4096, 13, "bf16", "bf16", 1e-6)
+    inp = synth.make_inputs(wl)
+    ref = parity.oracle_run(wl, inp)
+    g = parity.to_device(inp, DEV)
+    x, r = g["x"].clone(), g["residual"].clone()
+    out = res = None
+    if alias == "residual_out=residual":
+        res = r
+    elif alias == "residual_out=x":
+        res = x
+    elif alias == "out=x":
+        out = x
+    else:
+        out = r
+    o, ro, _ = pkg.fused_add_rmsnorm(x, r, g["weight"], None, eps=wl.eps, out=out, residual_out=res)
+    torch.cuda.synchronize()
+    got = parity.gpu_outputs_to_host(wl, o, ro, None)
+    parity.compare(wl, got, ref, alias)
+
+
+def test_in_place_no_residual_generic(pkg):
+    wl = synth.Workload("alias_gen", 9, 1000, 14, "bf16", "bf16", 1e-6, has_residual=False)
+    inp = synth.make_inputs(wl)
+    ref = parity.oracle_run(wl, inp)
+    x = inp["x"].to(DEV)
+    o, _, _ = pkg.fused_add_rmsnorm(x, None, inp["weight"].to(DEV), None, eps=wl.eps, out=x)
+    torch.cuda.synchronize()
+    parity.compare(wl, parity.gpu_outputs_to_host(wl, o, None, None), ref, "in-place generic")
+
+
+def test_degenerate_rows(pkg):
+    # zero rows (FP8 scale 0, codes +0), constant rows, huge values, H = 1
+    T, H = 8, 2048
+    x = torch.zeros((T, H), dtype=torch.float32)
+    x[1] = 3.0
+    x[2] = -1e30
+    x[3, ::2] = 1e-30
+    x[4] = torch.linspace(-100, 100, H)
+    xb = x.to(torch.bfloat16)
+    for out_dt in ("bf16", "fp8", "f32"):
+        wl = synth.Workload("degenerate", T, H, 0, "bf16", out_dt, 1e-6, has_residual=False,
+                            has_weight=False)
+        inp = {"x": xb, "residual": None, "weight": None, "bias": None}
+        got = run_gpu(pkg, wl, inp)
+        ref = parity.oracle_run(wl, inp)
+        parity.compare(wl, got, ref, f"degenerate {out_dt}")
+        if out_dt == "fp8":
+            assert got["out_scale"][0] == 0 and not got["out"][0].any()
+            assert np.all(got["out"][1] == 0x7E)
+
+
+def test_forced_unbuilt_config_rejected(pkg):
+    wl = synth.decode_workload(8)
+    inp = parity.to_device(synth.make_inputs(wl), DEV)
+    bad = pkg.RmsnConfig.from_dict({"variant": pkg.VARIANT_BLOCK_ROW, "chunks": 3, "max_warps": 8})
+    with pytest.raises(pkg.RmsnError) as e:
+        pkg.fused_add_rmsnorm(inp["x"], inp["residual"], inp["weight"], None, eps=1e-6, config=bad)
+    assert e.value.status == pkg.RMSN_EUNSUPPORTED
+    # a row wider than one warp's registers cannot take the one-warp shape
+    big = pkg.RmsnConfig.from_dict({"variant": pkg.VARIANT_WARP_ROWS, "chunks": 1, "max_warps": 1})
+    with pytest.raises(pkg.RmsnError):
+        pkg.fused_add_rmsnorm(inp["x"], inp["residual"], inp["weight"], None, eps=1e-6, config=big)
+
+
+def test_selector_decode_vs_prefill(pkg):
+    flags = pkg.make_flags("bf16", "bf16", True, True, False)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    c = pkg.rmsnorm_query_config(8, 4096, flags)
+    assert c.variant == pkg.VARIANT_WARP_ROWS and c.warps_per_block == 1 and c.num_sms == sms
+    c = pkg.rmsnorm_query_config(16384, 8192, flags)
+    assert c.variant in (pkg.VARIANT_BLOCK_ROW, pkg.VARIANT_BULK_ROW)
+    assert c.grid <= 16384
+    c = pkg.rmsnorm_query_config(16, 1000, flags)
+    assert c.variant == pkg.VARIANT_GENERIC
+
+
+def test_streams_are_respected(pkg):
+    wl = synth.decode_workload(128)
+    inp = synth.make_inputs(wl)
+    ref = parity.oracle_run(wl, inp)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g = parity.to_device(inp, DEV)
+        out, res, _ = pkg.fused_add_rmsnorm(g["x"], g["residual"], g["weight"], None, eps=wl.eps)
+    s.synchronize()
+    parity.compare(wl, parity.gpu_outputs_to_host(wl, out, res, None), ref, "side stream")
