@@ -65,7 +65,8 @@ typedef enum {
 typedef enum {
     RMSN_VARIANT_WARP_ROWS = 0, /* decode: one warp per row, rows spread over SMs */
     RMSN_VARIANT_BLOCK_ROW = 1, /* prefill: one block (W warps) per row, register-resident */
-    RMSN_VARIANT_BULK_ROW = 2,  /* prefill: rows streamed to shared memory by bulk async copies */
+    RMSN_VARIANT_BULK_ROW = 2,  /* prefill: persistent blocks; rows streamed into a ring of
+                                   shared-memory buffers by bulk async copies (cp.async.bulk) */
     RMSN_VARIANT_GENERIC = 3    /* any hidden size / alignment (element-wise, three passes) */
 } rmsn_variant;
 
@@ -99,7 +100,8 @@ typedef struct {
  * otherwise the generic kernel runs.  residual_out may be the same buffer as
  * residual or x; out may be the same buffer as x or residual when the output
  * and input dtypes are equal; any other overlap is undefined.  n_tokens == 0
- * is a no-op.  Returns an rmsn_status.
+ * is a no-op once the flags, hidden and eps have been checked (its pointers
+ * may then be NULL).  Returns an rmsn_status.
  */
 int rmsnorm_fwd(const void* x, const void* residual, const void* weight, const void* bias,
                 void* out, void* residual_out, float* out_scale, int64_t n_tokens,
@@ -129,6 +131,16 @@ int rmsnorm_query_config(int64_t n_tokens, int64_t hidden, uint32_t flags, rmsn_
  */
 int rmsnorm_list_configs(int64_t n_tokens, int64_t hidden, uint32_t flags, rmsn_config* out,
                          int capacity);
+
+/*
+ * Status word of the library's kernels on the current device.  Bit 0 is set
+ * when a bounded wait inside a kernel (the bulk-copy variant waits about one
+ * second at most for a row to arrive in shared memory) ran out; that kernel's
+ * outputs are then incomplete.  Reads synchronously (the device's pending
+ * work is not waited for beyond the copy's own ordering); `clear` != 0 resets
+ * the word.  Returns an rmsn_status.
+ */
+int rmsnorm_read_status(uint32_t* status, int clear);
 
 /* Human-readable name of an rmsn_status. */
 const char* rmsnorm_status_string(int status);

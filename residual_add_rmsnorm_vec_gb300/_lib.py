@@ -34,7 +34,7 @@ VARIANT_GENERIC = 3
 VARIANT_NAMES = {0: "warp_rows", 1: "block_row", 2: "bulk_row", 3: "generic"}
 
 EXPORTED = ("rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_query_config", "rmsnorm_list_configs",
-            "rmsnorm_status_string")
+            "rmsnorm_read_status", "rmsnorm_status_string")
 
 
 class RmsnConfig(ctypes.Structure):
@@ -92,6 +92,8 @@ def load() -> ctypes.CDLL:
             lib.rmsnorm_list_configs.restype = ctypes.c_int
             lib.rmsnorm_list_configs.argtypes = [i64, i64, u32, ctypes.POINTER(RmsnConfig),
                                                  ctypes.c_int]
+            lib.rmsnorm_read_status.restype = ctypes.c_int
+            lib.rmsnorm_read_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
             lib.rmsnorm_status_string.restype = ctypes.c_char_p
             lib.rmsnorm_status_string.argtypes = [ctypes.c_int]
             _lib = lib
@@ -137,3 +139,12 @@ def rmsnorm_list_configs(n_tokens: int, hidden: int, flags: int) -> list[RmsnCon
     if m < 0:
         raise RmsnError(m, "rmsnorm_list_configs")
     return [arr[i] for i in range(min(n, m))]
+
+
+def rmsnorm_read_status(clear: bool = False) -> int:
+    """Kernel status word of the current device (0 = no bounded wait ran out)."""
+    v = ctypes.c_uint32(0)
+    st = load().rmsnorm_read_status(ctypes.byref(v), int(bool(clear)))
+    if st != RMSN_OK:
+        raise RmsnError(st, "rmsnorm_read_status")
+    return int(v.value)

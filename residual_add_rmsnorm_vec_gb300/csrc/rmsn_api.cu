@@ -18,6 +18,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "../../include/rmsnorm.h"
@@ -31,26 +32,59 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxHidden = int64_t(1) << 24;
 
+// Status word of the kernels on each device (bit 0: a bounded wait ran out).
+__device__ uint32_t g_status;
+
 struct DeviceInfo {
     std::once_flag once;
     int num_sms = 0;
+    int max_smem = 0;              // opt-in dynamic shared memory per block
+    uint32_t* status = nullptr;    // device address of g_status on this device
     cudaError_t err = cudaSuccess;
+    std::mutex mu;
+    std::vector<std::pair<const void*, int>> smem_set;  // kernel -> raised dynamic smem limit
 };
 
 DeviceInfo g_dev[kMaxDevices];
 
-// SM count of the current device (queried once per device).
-int device_sms(int* dev_out) {
+// Attributes of the current device (queried once per device).
+DeviceInfo* device_info() {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     DeviceInfo& d = g_dev[dev];
     std::call_once(d.once, [&] {
-        int n = 0;
+        int n = 0, sm = 0;
         d.err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (d.err == cudaSuccess)
+            d.err = cudaDeviceGetAttribute(&sm, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (d.err == cudaSuccess) d.err = cudaGetSymbolAddress((void**)&d.status, g_status);
         d.num_sms = n;
+        d.max_smem = sm;
     });
-    if (dev_out) *dev_out = dev;
-    return d.err == cudaSuccess ? d.num_sms : -1;
+    if (d.err != cudaSuccess) return nullptr;
+    return &d;
+}
+
+// Let a bulk kernel use the device's opt-in shared memory, less its static
+// shared memory (once per device and kernel); returns the dynamic limit or 0.
+int enable_smem(DeviceInfo* d, const void* fn) {
+    std::lock_guard<std::mutex> lock(d->mu);
+    for (const auto& f : d->smem_set)
+        if (f.first == fn) return f.second;
+    cudaFuncAttributes attr;
+    if (cudaFuncGetAttributes(&attr, fn) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    const int limit = d->max_smem - (int)attr.sharedSizeBytes;
+    if (limit <= 0 ||
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    d->smem_set.emplace_back(fn, limit);
+    return limit;
 }
 
 const std::vector<KernelEntry>& registry() {
@@ -130,17 +164,26 @@ const KernelEntry* find_kernel(const Problem& p, int variant, int ch, int wmax) 
     return nullptr;
 }
 
-int blocks_per_sm(const void* fn, int threads) {
+int blocks_per_sm(const void* fn, int threads, int smem) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, 0) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess) {
         cudaGetLastError();
-        return 1;
+        return 0;
     }
-    return n > 0 ? n : 1;
+    return n;
 }
 
+// Shared-memory row buffers of the bulk kernel: the requested count, else as
+// many as fit in ~220 KB (one block per SM), at most kMaxStages.
+constexpr int kMaxStages = 8;
+constexpr int kBulkSmemTarget = 220 * 1024;
+
+int bulk_stage_bytes(const Problem& p) { return (int)((p.res ? 2 : 1) * p.H * p.in_bytes); }
+
 // Fill block shape, grid (persistent: at most one resident wave) for an entry.
-bool shape_config(const Problem& p, const KernelEntry& e, int sms, int grid_req, rmsn_config* c) {
+bool shape_config(const Problem& p, const KernelEntry& e, DeviceInfo* d, int grid_req,
+                  int stages_req, rmsn_config* c) {
+    const int sms = d->num_sms;
     memset(c, 0, sizeof(*c));
     c->variant = e.variant;
     c->chunks = e.chunks;
@@ -172,8 +215,21 @@ bool shape_config(const Problem& p, const KernelEntry& e, int sms, int grid_req,
         c->warps_per_row = w;
         threads = w * 32;
         units = p.T;
+        if (e.variant == kBulkRow) {
+            const int sb = bulk_stage_bytes(p);
+            int st = stages_req > 0 ? stages_req : kBulkSmemTarget / sb;
+            if (st > kMaxStages) st = kMaxStages;
+            const int limit = enable_smem(d, e.fn);
+            if (stages_req <= 0)
+                while (st > 2 && (int64_t)st * sb > limit) --st;
+            if (st < 2 || (int64_t)st * sb > limit) return false;
+            c->stages = st;
+            c->smem_bytes = st * sb;
+        }
     }
-    const int64_t resident = (int64_t)sms * blocks_per_sm(e.fn, threads);
+    const int bps = blocks_per_sm(e.fn, threads, c->smem_bytes);
+    if (bps < 1) return false;
+    const int64_t resident = (int64_t)sms * bps;
     int64_t grid = units < resident ? units : resident;
     if (grid_req > 0) grid = grid_req < units ? grid_req : units;
     if (grid < 1) grid = 1;
@@ -183,39 +239,36 @@ bool shape_config(const Problem& p, const KernelEntry& e, int sms, int grid_req,
 
 #include "rmsn_selector_table.inc"
 
-// The selector (see the file comment).
-bool select(const Problem& p, int sms, rmsn_config* c) {
+// The selector (see the file comment): the measured table first, then the
+// decode rule (one warp per block while the whole problem needs no more warps
+// than there are SMs), then the fixed prefill rule (fewest warps with CH <= 2).
+bool select(const Problem& p, DeviceInfo* d, rmsn_config* c) {
     if (!p.vec_ok) {
         const KernelEntry* e = find_kernel(p, kGeneric, 0, 0);
-        return e && shape_config(p, *e, sms, 0, c);
+        return e && shape_config(p, *e, d, 0, 0, c);
+    }
+    int variant = 0, ch = 0, wmax = 0, stages = 0;
+    if (table_lookup(p.in_dt, p.out_dt, p.H, p.T, &variant, &ch, &wmax, &stages)) {
+        const KernelEntry* e = find_kernel(p, variant, ch, wmax);
+        if (e && shape_config(p, *e, d, 0, stages, c)) return true;
     }
     const int64_t warps_needed = (p.T * p.nvec + 31) / 32;
-    if (warps_needed <= sms && p.nvec <= 32 * 8) {
-        // decode: one warp per block, CH = smallest power of two covering the row
-        int ch = 1;
+    if (warps_needed <= d->num_sms && p.nvec <= 32 * 8) {
+        ch = 1;
         while (32 * ch < p.nvec) ch *= 2;
         const KernelEntry* e = find_kernel(p, kWarpRows, ch, 1);
-        if (e && shape_config(p, *e, sms, 0, c)) return true;
+        if (e && shape_config(p, *e, d, 0, 0, c)) return true;
     }
-    // measured table, then the fixed rule: fewest warps with CH <= 2 that fit
-    int ch = 0, wmax = 0;
-    if (!table_lookup(p.in_dt, p.out_dt, p.H, p.T, &ch, &wmax)) {
-        const int cands[][2] = {{2, 4}, {2, 8}, {2, 16}, {2, 32}, {4, 16}};
-        for (auto& cw : cands) {
-            const int w = (int)((p.nvec + 32 * cw[0] - 1) / (32 * cw[0]));
-            if (w <= cw[1]) {
-                ch = cw[0];
-                wmax = cw[1];
-                break;
-            }
-        }
-    }
-    if (ch) {
-        const KernelEntry* e = find_kernel(p, kBlockRow, ch, wmax);
-        if (e && shape_config(p, *e, sms, 0, c)) return true;
+    const int cands[][2] = {{2, 4}, {2, 8}, {2, 16}, {2, 32}, {4, 16}};
+    for (auto& cw : cands) {
+        const int w = (int)((p.nvec + 32 * cw[0] - 1) / (32 * cw[0]));
+        if (w > cw[1]) continue;
+        const KernelEntry* e = find_kernel(p, kBlockRow, cw[0], cw[1]);
+        if (e && shape_config(p, *e, d, 0, 0, c)) return true;
+        break;
     }
     const KernelEntry* e = find_kernel(p, kGeneric, 0, 0);
-    return e && shape_config(p, *e, sms, 0, c);
+    return e && shape_config(p, *e, d, 0, 0, c);
 }
 
 }  // namespace
@@ -243,12 +296,13 @@ RMSN_API int rmsnorm_fwd_ex(const void* x, const void* residual, const void* wei
     if (st != RMSN_OK) return st;
     if ((st = check_shape(n_tokens, hidden, &p)) != RMSN_OK) return st;
     if (!(eps >= 0.f) || !isfinite(eps) || !isfinite(weight_offset)) return RMSN_EINVAL;
+    // an empty batch touches nothing (its buffers may be NULL)
+    if (n_tokens == 0) return RMSN_OK;
     // optional operands must match their flags exactly
     if (p.res != (residual != nullptr) || p.res != (residual_out != nullptr)) return RMSN_EINVAL;
     if (((flags & RMSN_HAS_WEIGHT) != 0) != (weight != nullptr)) return RMSN_EINVAL;
     if (p.bias != (bias != nullptr)) return RMSN_EINVAL;
     if ((p.out_dt == kFP8) != (out_scale != nullptr)) return RMSN_EINVAL;
-    if (n_tokens == 0) return RMSN_OK;
     if (!x || !out) return RMSN_EINVAL;
     const void* ins[] = {x, residual, weight, bias, residual_out};
     for (const void* q : ins)
@@ -257,16 +311,16 @@ RMSN_API int rmsnorm_fwd_ex(const void* x, const void* residual, const void* wei
     p.vec_ok = vector_path_ok(p, ins, 5, out);
     p.nvec = p.vec_ok ? (int)(p.H / p.ve) : 0;
 
-    const int sms = device_sms(nullptr);
-    if (sms <= 0) return RMSN_ECUDA;
+    DeviceInfo* d = device_info();
+    if (!d) return RMSN_ECUDA;
     rmsn_config c;
     const KernelEntry* e = nullptr;
     if (cfg) {
         if (cfg->variant != kGeneric && !p.vec_ok) return RMSN_EUNSUPPORTED;
         e = find_kernel(p, cfg->variant, cfg->chunks, cfg->max_warps);
-        if (!e || !shape_config(p, *e, sms, cfg->grid, &c)) return RMSN_EUNSUPPORTED;
+        if (!e || !shape_config(p, *e, d, cfg->grid, cfg->stages, &c)) return RMSN_EUNSUPPORTED;
     } else {
-        if (!select(p, sms, &c)) return RMSN_EUNSUPPORTED;
+        if (!select(p, d, &c)) return RMSN_EUNSUPPORTED;
         e = find_kernel(p, c.variant, c.chunks, c.max_warps);
         if (!e) return RMSN_EUNSUPPORTED;
     }
@@ -285,6 +339,8 @@ RMSN_API int rmsnorm_fwd_ex(const void* x, const void* residual, const void* wei
     a.eps = eps;
     a.woff = weight_offset;
     a.has_w = weight != nullptr;
+    a.stages = c.stages;
+    a.status = d->status;
     void* args[] = {&a};
     const cudaError_t err = cudaLaunchKernel(e->fn, dim3((unsigned)c.grid),
                                              dim3((unsigned)(c.warps_per_block * 32)), args,
@@ -315,9 +371,9 @@ RMSN_API int rmsnorm_query_config(int64_t n_tokens, int64_t hidden, uint32_t fla
     Problem p{};
     int st = query_problem(n_tokens, hidden, flags, &p);
     if (st != RMSN_OK) return st;
-    const int sms = device_sms(nullptr);
-    if (sms <= 0) return RMSN_ECUDA;
-    return select(p, sms, out) ? RMSN_OK : RMSN_EUNSUPPORTED;
+    DeviceInfo* d = device_info();
+    if (!d) return RMSN_ECUDA;
+    return select(p, d, out) ? RMSN_OK : RMSN_EUNSUPPORTED;
 }
 
 RMSN_API int rmsnorm_list_configs(int64_t n_tokens, int64_t hidden, uint32_t flags,
@@ -326,16 +382,34 @@ RMSN_API int rmsnorm_list_configs(int64_t n_tokens, int64_t hidden, uint32_t fla
     Problem p{};
     int st = query_problem(n_tokens, hidden, flags, &p);
     if (st != RMSN_OK) return st;
-    const int sms = device_sms(nullptr);
-    if (sms <= 0) return RMSN_ECUDA;
+    DeviceInfo* d = device_info();
+    if (!d) return RMSN_ECUDA;
     int count = 0;
     for (const KernelEntry& e : registry()) {
         if (e.in_dt != p.in_dt || e.out_dt != p.out_dt || e.res != (p.res ? 1 : 0)) continue;
         if (e.variant != kGeneric && (e.bias != (p.bias ? 1 : 0) || !p.vec_ok)) continue;
-        rmsn_config c;
-        if (!shape_config(p, e, sms, 0, &c)) continue;
-        if (count < capacity) out[count] = c;
-        ++count;
+        // the bulk kernel is listed once per ring depth
+        const int stage_opts[] = {0, 2, 3, 4, 6, 8};
+        const int n_opts = e.variant == kBulkRow ? 6 : 1;
+        for (int i = 0; i < n_opts; ++i) {
+            if (e.variant == kBulkRow && i == 0) continue;
+            rmsn_config c;
+            if (!shape_config(p, e, d, 0, stage_opts[i], &c)) continue;
+            if (count < capacity) out[count] = c;
+            ++count;
+        }
     }
     return count;
+}
+
+RMSN_API int rmsnorm_read_status(uint32_t* status, int clear) {
+    if (!status) return RMSN_EINVAL;
+    DeviceInfo* d = device_info();
+    if (!d) return RMSN_ECUDA;
+    if (cudaMemcpy(status, d->status, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return RMSN_ECUDA;
+    if (clear && *status) {
+        if (cudaMemset(d->status, 0, sizeof(uint32_t)) != cudaSuccess) return RMSN_ECUDA;
+    }
+    return RMSN_OK;
 }

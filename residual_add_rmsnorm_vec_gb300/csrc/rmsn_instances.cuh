@@ -12,6 +12,12 @@ namespace rmsn {
 #define RMSN_VEC4(CH, WMAX, WR)                                                              \
     RMSN_VEC(CH, WMAX, WR, false, false), RMSN_VEC(CH, WMAX, WR, true, false),               \
         RMSN_VEC(CH, WMAX, WR, false, true), RMSN_VEC(CH, WMAX, WR, true, true)
+#define RMSN_BULK(CH, WMAX, RES, BIAS)                                                       \
+    {RMSN_DTI, RMSN_DTO, kBulkRow, CH, WMAX, 0, RES, BIAS,                                   \
+     (const void*)&rmsn_bulk_kernel<RMSN_TI, RMSN_TO, CH, WMAX, RES, BIAS>}
+#define RMSN_BULK4(CH, WMAX)                                                                 \
+    RMSN_BULK(CH, WMAX, false, false), RMSN_BULK(CH, WMAX, true, false),                     \
+        RMSN_BULK(CH, WMAX, false, true), RMSN_BULK(CH, WMAX, true, true)
 #define RMSN_GEN(RES)                                                                        \
     {RMSN_DTI, RMSN_DTO, kGeneric, 0, 8, 0, RES, -1,                                         \
      (const void*)&rmsn_generic_kernel<RMSN_TI, RMSN_TO, RES>}
@@ -25,6 +31,9 @@ static const KernelEntry kTable[] = {
     RMSN_VEC4(1, 8, false), RMSN_VEC4(2, 8, false), RMSN_VEC4(4, 8, false),
     RMSN_VEC4(1, 16, false), RMSN_VEC4(2, 16, false), RMSN_VEC4(4, 16, false),
     RMSN_VEC4(1, 32, false), RMSN_VEC4(2, 32, false),
+    // prefill: rows streamed through shared memory by bulk async copies
+    RMSN_BULK4(1, 8), RMSN_BULK4(2, 8), RMSN_BULK4(1, 16), RMSN_BULK4(2, 16),
+    RMSN_BULK4(1, 32), RMSN_BULK4(2, 32),
     // any shape
     RMSN_GEN(false), RMSN_GEN(true),
 };

@@ -15,6 +15,8 @@
 //   rmsn_vec_kernel     one row per warp (WARP_ROWS) or per block; each thread
 //                       holds CH 32-byte vectors of the row in registers
 //                       between the load and the store.
+//   rmsn_bulk_kernel    persistent blocks streaming whole rows into a ring of
+//                       shared-memory buffers with bulk async copies.
 //   rmsn_generic_kernel any hidden size / alignment; element-wise, re-reads
 //                       the row from the just-written residual_out.
 #pragma once
@@ -208,18 +210,124 @@ struct Bounds {
     static constexpr int kMinBlocks = kTarget / kThreads > 0 ? kTarget / kThreads : 1;
 };
 
+// ---------------------------------------------------------------- row body
+//
+// Shared by the register-streaming and the bulk-copy kernels.  A thread
+// handles vectors v = c * G + t (c < CH, G = threads per row, t = thread
+// within the row) of VE elements each, so a warp touches 1 KiB of contiguous
+// memory per chunk.  hv holds x on entry (and rv the residual); on exit hv
+// holds h = RN_in(x + r), which was also stored to residual_out.
+
+template <class TI, int CH>
+__device__ __forceinline__ void load_params(const RmsnArgs& a, int G, int t, V8 (&wv)[CH],
+                                            V8* bv, bool bias) {
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        const int v = c * G + t;
+        if (v < a.nvec) {
+            if (a.has_w) {
+                wv[c] = ld_keep32(static_cast<const char*>(a.w) + (int64_t)v * 32);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) wv[c].u[k] = ones_word<TI>();
+            }
+            if (bias) bv[c] = ld_keep32(static_cast<const char*>(a.b) + (int64_t)v * 32);
+        }
+    }
+}
+
+// h = RN_in(x + r) (the sum formed in fp32), stored to residual_out; returns
+// this thread's fp32 sum of h^2.
+template <class TI, int CH, bool RES>
+__device__ __forceinline__ float residual_sumsq(const RmsnArgs& a, int64_t rbase, int G, int t,
+                                                V8 (&hv)[CH], const V8* rv) {
+    constexpr int VE = 32 / TI::kBytes;
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        const int v = c * G + t;
+        if (v < a.nvec) {
+            if constexpr (RES) {
+                if constexpr (TI::kBytes == 2) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const float lo = __fadd_rn(bf16_lo(hv[c].u[k]), bf16_lo(rv[c].u[k]));
+                        const float hi = __fadd_rn(bf16_hi(hv[c].u[k]), bf16_hi(rv[c].u[k]));
+                        hv[c].u[k] = pack_bf16x2(lo, hi);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        hv[c].u[k] = __float_as_uint(__fadd_rn(__uint_as_float(hv[c].u[k]),
+                                                               __uint_as_float(rv[c].u[k])));
+                }
+                const int64_t off = (rbase + (int64_t)v * VE) * TI::kBytes;
+                st_stream32(static_cast<char*>(a.res_out) + off, hv[c].u);
+            }
+#pragma unroll
+            for (int k = 0; k < VE; ++k) {
+                const float h = elem<TI>(hv[c], k);
+                acc = __fmaf_rn(h, h, acc);
+            }
+        }
+    }
+    return acc;
+}
+
+// Scale, (FP8: absmax reduction and per-token scale) and store the row.
+// `reduce_max` is the row-wide max all-reduce (only used for FP8 output).
+template <class TI, class TO, int CH, bool BIAS, class ReduceMax>
+__device__ __forceinline__ void scale_store(const RmsnArgs& a, int64_t row, int64_t rbase, int G,
+                                            int t, float inv, const V8 (&hv)[CH], V8 (&wv)[CH],
+                                            V8* bv, ReduceMax reduce_max) {
+    constexpr int VE = 32 / TI::kBytes;
+    float qmul = 0.f;
+    if constexpr (TO::kBytes == 1) {
+        float amax = 0.f;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int v = c * G + t;
+            if (v < a.nvec) {
+                opaque(wv[c]);
+                if constexpr (BIAS) opaque(bv[c]);
+#pragma unroll
+                for (int k = 0; k < VE; ++k) {
+                    const float y = scale_elem<BIAS>(elem<TI>(hv[c], k), inv, elem<TI>(wv[c], k),
+                                                     a.woff, BIAS ? elem<TI>(bv[c], k) : 0.f);
+                    amax = fmaxf(amax, fabsf(y));
+                }
+            }
+        }
+        amax = reduce_max(amax);
+        qmul = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
+        if (t == 0) a.scale[row] = __fdiv_rn(amax, 448.f);
+    }
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        const int v = c * G + t;
+        if (v < a.nvec) {
+            opaque(wv[c]);
+            if constexpr (BIAS) opaque(bv[c]);
+            float y[VE];
+#pragma unroll
+            for (int k = 0; k < VE; ++k)
+                y[k] = scale_elem<BIAS>(elem<TI>(hv[c], k), inv, elem<TI>(wv[c], k), a.woff,
+                                        BIAS ? elem<TI>(bv[c], k) : 0.f);
+            store_out<TI, TO>(a.out, rbase + (int64_t)v * VE, y, qmul);
+        }
+    }
+}
+
 // ---------------------------------------------------------------- vector kernel
 //
 // WARP_ROWS: each warp owns one row (block = WMAX rows); else the block owns
-// one row and has up to WMAX warps.  A thread handles vectors
-// v = c * G + t (c < CH, G = threads per row, t = thread within the row) of
-// VE elements each, so a warp touches 1 KiB of contiguous memory per chunk.
-// Rows are visited grid-stride; weight and bias stay in registers.
+// one row and has up to WMAX warps.  Each thread loads its CH vectors of x
+// (and the residual) straight into registers; rows are visited grid-stride;
+// weight and bias stay in registers across rows.
 template <class TI, class TO, int CH, int WMAX, bool WARP_ROWS, bool RES, bool BIAS>
 __global__ void __launch_bounds__(Bounds<WMAX, CH>::kThreads, Bounds<WMAX, CH>::kMinBlocks)
     rmsn_vec_kernel(const RmsnArgs a) {
     constexpr int VE = 32 / TI::kBytes;  // elements per 32-byte vector
-    constexpr bool FP8OUT = TO::kBytes == 1;
     __shared__ float red[4][32];
 
     const int lane = threadIdx.x & 31;
@@ -228,118 +336,192 @@ __global__ void __launch_bounds__(Bounds<WMAX, CH>::kThreads, Bounds<WMAX, CH>::
     const int64_t rows_per_step = WARP_ROWS ? (int64_t)gridDim.x * (blockDim.x >> 5) : gridDim.x;
     int64_t row = WARP_ROWS ? (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)
                             : (int64_t)blockIdx.x;
-    const int nvec = a.nvec;
-    const int H = a.H;
 
     V8 wv[CH];
     V8 bv[BIAS ? CH : 1];
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-        const int v = c * G + t;
-        if (v < nvec) {
-            if (a.has_w) {
-                wv[c] = ld_keep32(static_cast<const char*>(a.w) + (int64_t)v * 32);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) wv[c].u[k] = ones_word<TI>();
-            }
-            if constexpr (BIAS) bv[c] = ld_keep32(static_cast<const char*>(a.b) + (int64_t)v * 32);
-        }
-    }
+    load_params<TI, CH>(a, G, t, wv, bv, BIAS);
 
     int parity = 0;
     for (; row < a.T; row += rows_per_step) {
-        const int64_t rbase = row * (int64_t)H;  // element offset of the row
+        const int64_t rbase = row * (int64_t)a.H;  // element offset of the row
         V8 hv[CH];
         V8 rv[RES ? CH : 1];
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
             const int v = c * G + t;
-            if (v < nvec) {
+            if (v < a.nvec) {
                 const int64_t off = (rbase + (int64_t)v * VE) * TI::kBytes;
                 hv[c] = ld_stream32(static_cast<const char*>(a.x) + off);
                 if constexpr (RES) rv[c] = ld_stream32(static_cast<const char*>(a.r) + off);
             }
         }
-        float acc = 0.f;
-#pragma unroll
-        for (int c = 0; c < CH; ++c) {
-            const int v = c * G + t;
-            if (v < nvec) {
-                if constexpr (RES) {
-                    // h = RN_in(x + r); the sum is formed in fp32
-                    if constexpr (TI::kBytes == 2) {
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const float lo = __fadd_rn(bf16_lo(hv[c].u[k]), bf16_lo(rv[c].u[k]));
-                            const float hi = __fadd_rn(bf16_hi(hv[c].u[k]), bf16_hi(rv[c].u[k]));
-                            hv[c].u[k] = pack_bf16x2(lo, hi);
-                        }
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            hv[c].u[k] = __float_as_uint(__fadd_rn(__uint_as_float(hv[c].u[k]),
-                                                                   __uint_as_float(rv[c].u[k])));
-                    }
-                    const int64_t off = (rbase + (int64_t)v * VE) * TI::kBytes;
-                    st_stream32(static_cast<char*>(a.res_out) + off, hv[c].u);
-                }
-#pragma unroll
-                for (int k = 0; k < VE; ++k) {
-                    const float h = elem<TI>(hv[c], k);
-                    acc = __fmaf_rn(h, h, acc);
-                }
-            }
-        }
-        float sumsq;
-        if constexpr (WARP_ROWS) {
-            sumsq = warp_sum(acc);
-        } else {
-            sumsq = block_allreduce<false>(acc, red[parity]);
-        }
-        const float inv = inv_rms(sumsq, H, a.eps);
-
-        float qmul = 0.f;
-        if constexpr (FP8OUT) {
-            float amax = 0.f;
-#pragma unroll
-            for (int c = 0; c < CH; ++c) {
-                const int v = c * G + t;
-                if (v < nvec) {
-                    opaque(wv[c]);
-                    if constexpr (BIAS) opaque(bv[BIAS ? c : 0]);
-#pragma unroll
-                    for (int k = 0; k < VE; ++k) {
-                        const float y = scale_elem<BIAS>(elem<TI>(hv[c], k), inv,
-                                                         elem<TI>(wv[c], k), a.woff,
-                                                         BIAS ? elem<TI>(bv[BIAS ? c : 0], k) : 0.f);
-                        amax = fmaxf(amax, fabsf(y));
-                    }
-                }
-            }
-            if constexpr (WARP_ROWS) {
-                amax = warp_max(amax);
-            } else {
-                amax = block_allreduce<true>(amax, red[2 + parity]);
-            }
-            qmul = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
-            if (t == 0) a.scale[row] = __fdiv_rn(amax, 448.f);
-        }
-#pragma unroll
-        for (int c = 0; c < CH; ++c) {
-            const int v = c * G + t;
-            if (v < nvec) {
-                opaque(wv[c]);
-                if constexpr (BIAS) opaque(bv[BIAS ? c : 0]);
-                float y[VE];
-#pragma unroll
-                for (int k = 0; k < VE; ++k)
-                    y[k] = scale_elem<BIAS>(elem<TI>(hv[c], k), inv, elem<TI>(wv[c], k), a.woff,
-                                            BIAS ? elem<TI>(bv[BIAS ? c : 0], k) : 0.f);
-                store_out<TI, TO>(a.out, rbase + (int64_t)v * VE, y, qmul);
-            }
-        }
+        const float acc = residual_sumsq<TI, CH, RES>(a, rbase, G, t, hv, rv);
+        const float sumsq = WARP_ROWS ? warp_sum(acc) : block_allreduce<false>(acc, red[parity]);
+        const float inv = inv_rms(sumsq, a.H, a.eps);
+        float* slot = red[2 + parity];
+        scale_store<TI, TO, CH, BIAS>(a, row, rbase, G, t, inv, hv, wv, bv, [&](float m) {
+            return WARP_ROWS ? warp_max(m) : block_allreduce<true>(m, slot);
+        });
         parity ^= 1;
+    }
+}
+
+// ---------------------------------------------------------------- bulk-copy kernel
+//
+// Persistent blocks (one row at a time, up to WMAX warps).  Whole rows of x
+// and the residual are moved into a ring of `a.stages` shared-memory buffers
+// by the bulk async-copy engine (cp.async.bulk, completion counted on an
+// mbarrier per buffer), issued by thread 0 up to `stages` rows ahead.  The
+// threads copy their vectors from shared memory into registers, so a buffer
+// is free again after the row's sum-of-squares barrier, where thread 0
+// refills it with the row `stages` ahead.  Bytes in flight per SM are set by
+// the ring size, not by the register file.
+//
+// Every mbarrier wait is bounded (about one second of clock cycles).  A wait
+// that runs out sets bit 0 of *a.status and a shared abort flag; the block
+// still takes part in the row's barrier so no thread is left waiting, then
+// stops, after thread 0 has waited (again bounded) for its copies in flight.
+
+constexpr int kMaxStages = 8;
+constexpr long long kWaitCycles = 2000000000LL;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kWaitCycles) return false;
+    }
+    return true;
+}
+
+// Thread 0: expect `bytes` on `bar`, then copy x (and r) of `row` into `dst`.
+template <bool RES>
+__device__ __forceinline__ void issue_row(const RmsnArgs& a, int64_t row, uint32_t dst,
+                                          uint32_t bar, uint32_t row_bytes) {
+    const uint32_t bytes = RES ? 2 * row_bytes : row_bytes;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+    const char* src = static_cast<const char*>(a.x) + row * (int64_t)row_bytes;
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(row_bytes), "r"(bar)
+        : "memory");
+    if constexpr (RES) {
+        const char* rsrc = static_cast<const char*>(a.r) + row * (int64_t)row_bytes;
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+            "[%3];" ::"r"(dst + row_bytes),
+            "l"(rsrc), "r"(row_bytes), "r"(bar)
+            : "memory");
+    }
+}
+
+__device__ __forceinline__ V8 ld_shared32(uint32_t addr) {
+    V8 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.u[0]), "=r"(v.u[1]), "=r"(v.u[2]), "=r"(v.u[3])
+                 : "r"(addr));
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.u[4]), "=r"(v.u[5]), "=r"(v.u[6]), "=r"(v.u[7])
+                 : "r"(addr + 16));
+    return v;
+}
+
+template <class TI, class TO, int CH, int WMAX, bool RES, bool BIAS>
+__global__ void __launch_bounds__(WMAX * 32, 1) rmsn_bulk_kernel(const RmsnArgs a) {
+    constexpr int VE = 32 / TI::kBytes;
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ __align__(8) uint64_t full[kMaxStages];
+    __shared__ float red[4][32];
+    __shared__ int abort_flag;
+
+    const int G = blockDim.x;
+    const int t = threadIdx.x;
+    const int S = a.stages;
+    const uint32_t row_bytes = (uint32_t)a.H * TI::kBytes;
+    const uint32_t stage_bytes = RES ? 2 * row_bytes : row_bytes;
+    const uint32_t ring0 = smem_u32(ring);
+    // rows of this block: blockIdx.x + k * gridDim.x
+    const int64_t n_my = a.T > blockIdx.x ? (a.T - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+    if (t == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int64_t k = 0; k < S && k < n_my; ++k)
+            issue_row<RES>(a, blockIdx.x + k * gridDim.x, ring0 + (uint32_t)k * stage_bytes,
+                           smem_u32(&full[k]), row_bytes);
+    }
+    __syncthreads();
+
+    V8 wv[CH];
+    V8 bv[BIAS ? CH : 1];
+    load_params<TI, CH>(a, G, t, wv, bv, BIAS);
+
+    int parity = 0;
+    int64_t k_abort = 0;
+    for (int64_t k = 0; k < n_my; ++k) {
+        const int s = (int)(k % S);
+        const uint32_t phase = (uint32_t)((k / S) & 1);
+        k_abort = k;
+        const int64_t row = blockIdx.x + k * gridDim.x;
+        const int64_t rbase = row * (int64_t)a.H;
+        if (!mbar_wait_bounded(smem_u32(&full[s]), phase)) {
+            atomicOr(a.status, 1u);
+            abort_flag = 1;
+        }
+        const uint32_t base = ring0 + (uint32_t)s * stage_bytes;
+        V8 hv[CH];
+        V8 rv[RES ? CH : 1];
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int v = c * G + t;
+            if (v < a.nvec) {
+                hv[c] = ld_shared32(base + (uint32_t)v * 32);
+                if constexpr (RES) rv[c] = ld_shared32(base + row_bytes + (uint32_t)v * 32);
+            }
+        }
+        const float acc = residual_sumsq<TI, CH, RES>(a, rbase, G, t, hv, rv);
+        const float sumsq = block_allreduce<false>(acc, red[parity]);
+        // every thread has read buffer s: refill it with the row S ahead
+        if (abort_flag) break;
+        if (t == 0 && k + S < n_my) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue_row<RES>(a, blockIdx.x + (k + S) * gridDim.x, base, smem_u32(&full[s]),
+                           row_bytes);
+        }
+        const float inv = inv_rms(sumsq, a.H, a.eps);
+        float* slot = red[2 + parity];
+        scale_store<TI, TO, CH, BIAS>(a, row, rbase, G, t, inv, hv, wv, bv,
+                                      [&](float m) { return block_allreduce<true>(m, slot); });
+        parity ^= 1;
+    }
+    if (abort_flag && t == 0) {
+        // drain: rows k_abort .. k_abort + S - 1 may still have copies in
+        // flight; wait (bounded) for each before the block's memory is reused
+        for (int64_t j = k_abort; j < k_abort + S && j < n_my; ++j)
+            mbar_wait_bounded(smem_u32(&full[j % S]), (uint32_t)((j / S) & 1));
     }
 }
 

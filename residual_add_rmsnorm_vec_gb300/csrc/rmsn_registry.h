@@ -21,6 +21,8 @@ struct RmsnArgs {
     float eps;
     float woff;
     int32_t has_w;
+    int32_t stages;      // shared-memory row buffers (bulk kernel)
+    uint32_t* status;    // device status word: bit 0 = a bounded wait ran out
 };
 
 enum DType : int32_t { kF32 = 0, kBF16 = 1, kFP8 = 2 };

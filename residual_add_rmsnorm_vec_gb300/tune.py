@@ -1,0 +1,210 @@
+"""Measure every built launch configuration over a tokens x hidden grid and
+write the selector table (csrc/rmsn_selector_table.inc) from the fastest.
+
+The blog "CuTeDSL at Perplexity" (section "Prefill and decode") picks the warp
+count per block by benchmarking 8/16/32 warps until the bandwidth stops
+improving; this does the same for every variant the library builds (one warp
+per row, one block per row, bulk-copy ring depths, grid shapes) on the
+current GPU.
+
+Timing: CUDA events around each launch on the launching stream, median of
+`reps` launches after warm-up.  When one set of buffers is smaller than
+3 x the L2 size the launches rotate over enough copies to exceed it, so the
+figures are HBM (not L2) bandwidth.
+
+    python -m residual_add_rmsnorm_vec_gb300.tune --out sweep.json --write-table
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import time
+
+L2_BYTES = 129 * 10**6
+TOKENS = (1, 4, 16, 64, 256, 1024, 4096, 16384, 65536)
+HIDDEN = (2048, 4096, 8192, 16384)
+DTYPE_CODES = {"f32": 0, "bf16": 1, "fp8": 2}
+
+
+def _algorithmic_bytes(T, H, in_b, out_b, res, bias, fp8):
+    b = T * H * in_b + T * H * out_b + H * in_b
+    if res:
+        b += 2 * T * H * in_b
+    if bias:
+        b += H * in_b
+    if fp8:
+        b += 4 * T
+    return b
+
+
+def measure(pkg, T, H, in_dt="bf16", out_dt="bf16", res=True, bias=False, reps=30,
+            configs=None):
+    import torch
+
+    dev = torch.device("cuda")
+    tin = torch.bfloat16 if in_dt == "bf16" else torch.float32
+    in_b = 2 if in_dt == "bf16" else 4
+    out_b = {"bf16": 2, "f32": 4, "fp8": 1}[out_dt]
+    tout = {"bf16": torch.bfloat16, "f32": torch.float32, "fp8": torch.uint8}[out_dt]
+    flags = pkg.make_flags(in_dt, out_dt, res, True, bias)
+    set_bytes = T * H * (in_b * (3 if res else 1) + out_b)
+    n_sets = max(1, min(64, -(-3 * L2_BYTES // max(1, set_bytes))))
+    sets = []
+    for _ in range(n_sets):
+        x = torch.randn(T, H, device=dev).to(tin)
+        r = torch.randn(T, H, device=dev).to(tin) if res else None
+        sets.append((x, r, torch.empty(T, H, device=dev, dtype=tout),
+                     torch.empty_like(x) if res else None,
+                     torch.empty(T, device=dev, dtype=torch.float32) if out_dt == "fp8" else None))
+    w = (1 + 0.1 * torch.randn(H, device=dev)).to(tin)
+    b = (0.01 * torch.randn(H, device=dev)).to(tin) if bias else None
+    stream = torch.cuda.current_stream()
+    if configs is None:
+        configs = pkg.rmsnorm_list_configs(T, H, flags)
+    algo = _algorithmic_bytes(T, H, in_b, out_b, res, bias, out_dt == "fp8")
+    results = []
+    for cfg in configs:
+        def launch(i):
+            x, r, o, ro, sc = sets[i % n_sets]
+            st = pkg.rmsnorm_fwd_ex(x.data_ptr(), None if r is None else r.data_ptr(),
+                                    w.data_ptr(), None if b is None else b.data_ptr(),
+                                    o.data_ptr(), None if ro is None else ro.data_ptr(),
+                                    None if sc is None else sc.data_ptr(), T, H, 1e-6, flags,
+                                    0.0, cfg, stream.cuda_stream)
+            if st != pkg.RMSN_OK:
+                raise pkg.RmsnError(st, "rmsnorm_fwd_ex")
+
+        for i in range(5):
+            launch(i)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        torch.cuda.synchronize()
+        for i, (e0, e1) in enumerate(evs):
+            e0.record(stream)
+            launch(i)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = statistics.median(e0.elapsed_time(e1) * 1e3 for e0, e1 in evs)
+        d = cfg.as_dict()
+        d.update(us=round(us, 3), gbs=round(algo / (us * 1e-6) / 1e9, 1))
+        results.append(d)
+    del sets
+    torch.cuda.empty_cache()
+    return results
+
+
+def sweep(pkg, shapes, in_dt, out_dt, res, bias, reps):
+    out = []
+    for T, H in shapes:
+        t0 = time.time()
+        rs = measure(pkg, T, H, in_dt, out_dt, res, bias, reps)
+        best = min(rs, key=lambda d: d["us"])
+        out.append({"T": T, "H": H, "in": in_dt, "out": out_dt, "res": res, "bias": bias,
+                    "best": best, "all": rs})
+        print(f"T={T:6d} H={H:6d} {in_dt}->{out_dt}: best {best['variant_name']} "
+              f"ch{best['chunks']} w{best['warps_per_block']}/{best['max_warps']} "
+              f"st{best['stages']} grid{best['grid']}: {best['us']:.2f} us {best['gbs']:.0f} GB/s"
+              f"  ({len(rs)} configs, {time.time() - t0:.1f} s)", flush=True)
+    return out
+
+
+def write_table(entries, path):
+    """Selector rows from the sweep: per (dtypes, hidden), the best shape from
+    each measured token count upward.  Ties within 1 % prefer fewer warps,
+    then the register kernel, then fewer ring stages."""
+    rows = []
+    for e in entries:
+        best_us = e["best"]["us"]
+        near = [d for d in e["all"] if d["us"] <= best_us * 1.01 and d["variant"] != 3]
+        if not near:
+            continue
+        pick = min(near, key=lambda d: (d["warps_per_block"], d["variant"] != 1, d["stages"],
+                                        d["us"]))
+        rows.append((DTYPE_CODES[e["in"]], DTYPE_CODES[e["out"]], e["H"], e["T"], pick["variant"],
+                     pick["chunks"], pick["max_warps"], pick["stages"], e["res"], e["bias"],
+                     pick["us"], pick["gbs"]))
+    rows.sort()
+    lines = [
+        "// Launch shapes chosen from measured bandwidth on a GB300 by",
+        "// residual_add_rmsnorm_vec_gb300/tune.py (CUDA-event median per launch, inputs",
+        "// rotated past the L2 size).  For one (input dtype, output dtype, hidden) the",
+        "// row with the largest t_min <= n_tokens applies; other shapes fall back to",
+        "// the fixed rule in the selector.",
+        "struct TableRow {",
+        "    int in_dt, out_dt;",
+        "    int64_t hidden, t_min;",
+        "    int variant, chunks, max_warps, stages;",
+        "};",
+        "",
+        "static const TableRow kSelectorTable[] = {",
+    ]
+    seen = set()
+    for r in rows:
+        key = r[:4]
+        if key in seen:
+            continue
+        seen.add(key)
+        lines.append(f"    {{{r[0]}, {r[1]}, {r[2]}, {r[3]}, {r[4]}, {r[5]}, {r[6]}, {r[7]}}},"
+                     f"  // {r[10]:.2f} us, {r[11]:.0f} GB/s")
+    if not seen:
+        lines.append("    {-1, -1, 0, 0, 0, 0, 0, 0},")
+    lines += [
+        "};",
+        "",
+        "bool table_lookup(int in_dt, int out_dt, int64_t hidden, int64_t n_tokens, int* variant,",
+        "                  int* chunks, int* max_warps, int* stages) {",
+        "    const TableRow* best = nullptr;",
+        "    for (const TableRow& r : kSelectorTable) {",
+        "        if (r.in_dt != in_dt || r.out_dt != out_dt || r.hidden != hidden) continue;",
+        "        if (r.t_min <= n_tokens && (!best || r.t_min > best->t_min)) best = &r;",
+        "    }",
+        "    if (!best) return false;",
+        "    *variant = best->variant;",
+        "    *chunks = best->chunks;",
+        "    *max_warps = best->max_warps;",
+        "    *stages = best->stages;",
+        "    return true;",
+        "}",
+    ]
+    with open(path, "w") as f:
+        f.write("\n".join(lines) + "\n")
+
+
+def main():
+    import torch
+
+    import residual_add_rmsnorm_vec_gb300 as pkg
+    from residual_add_rmsnorm_vec_gb300 import build
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--out", default="sweep.json")
+    ap.add_argument("--reps", type=int, default=30)
+    ap.add_argument("--write-table", action="store_true")
+    ap.add_argument("--table-out", default=os.path.join(
+        os.path.dirname(os.path.abspath(__file__)), "csrc", "rmsn_selector_table.inc"))
+    ap.add_argument("--quick", action="store_true", help="a few shapes only")
+    args = ap.parse_args()
+    build.build()
+    torch.cuda.set_device(0)
+    grid = [(T, H) for H in HIDDEN for T in TOKENS]
+    if args.quick:
+        grid = [(1, 4096), (256, 4096), (16384, 8192)]
+    entries = sweep(pkg, grid, "bf16", "bf16", True, False, args.reps)
+    # the other dtype paths of the hot-path workloads
+    entries += sweep(pkg, [(T, H) for H in (5120, 7168) for T in (1, 64, 1024, 4096)],
+                     "bf16", "fp8", True, True, args.reps)
+    entries += sweep(pkg, [(T, 1024) for T in (1, 64, 4096)], "f32", "f32", False, False,
+                     args.reps)
+    meta = {"gpu": torch.cuda.get_device_name(0),
+            "sms": torch.cuda.get_device_properties(0).multi_processor_count,
+            "reps": args.reps}
+    with open(args.out, "w") as f:
+        json.dump({"meta": meta, "entries": entries}, f)
+    if args.write_table:
+        write_table(entries, args.table_out)
+
+
+if __name__ == "__main__":
+    main()

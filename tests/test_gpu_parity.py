@@ -53,7 +53,7 @@ def check(pkg, wl, rows=None, config=None, weight_offset=0.0, where=""):
         got = {k: (None if v is None else v[rows]) for k, v in got.items()}
     else:
         ref = parity.oracle_run(wl, inp, weight_offset)
-    return parity.compare(wl, got, ref, where or wl.name)
+    return parity.compare(wl, got, ref, where or wl.name, bias=inp["bias"])
 
 
 # ---------------------------------------------------------------- the five configs
@@ -74,6 +74,17 @@ def test_prefill_full_size(pkg):
     wl = synth.prefill_workload()
     st = check(pkg, wl)
     assert st["exact_frac"] > 0.99
+
+
+@pytest.mark.parametrize("stages", [2, 3, 6])
+@pytest.mark.parametrize("ch,wmax", [(2, 16), (1, 16), (2, 8)])
+def test_prefill_full_size_bulk_ring(pkg, stages, ch, wmax):
+    # the shared-memory ring variant at every row of the bench workload
+    wl = synth.prefill_workload()
+    cfg = pkg.RmsnConfig.from_dict({"variant": pkg.VARIANT_BULK_ROW, "chunks": ch,
+                                    "max_warps": wmax, "stages": stages})
+    check(pkg, wl, config=cfg)
+    assert pkg.rmsnorm_read_status() == 0
 
 
 @pytest.mark.parametrize("H", synth.FP8_HIDDEN)
@@ -124,13 +135,15 @@ def test_every_config(pkg, fs, H):
     variants = set()
     for c in cfgs:
         got = run_gpu(pkg, wl, inp, config=c)
-        parity.compare(wl, got, ref, f"{wl.name} {c.as_dict()}")
+        parity.compare(wl, got, ref, f"{wl.name} {c.as_dict()}", bias=inp["bias"])
         variants.add(c.variant)
         # a small explicit grid exercises the grid-stride row loop
         c2 = pkg.RmsnConfig.from_dict({**c.as_dict(), "grid": 3})
         got = run_gpu(pkg, wl, inp, config=c2)
-        parity.compare(wl, got, ref, f"{wl.name} grid=3 {c.as_dict()}")
+        parity.compare(wl, got, ref, f"{wl.name} grid=3 {c.as_dict()}", bias=inp["bias"])
     assert pkg.VARIANT_GENERIC in variants and pkg.VARIANT_BLOCK_ROW in variants
+    assert pkg.VARIANT_BULK_ROW in variants
+    assert pkg.rmsnorm_read_status() == 0
 
 
 def test_weight_offset(pkg):
@@ -227,11 +240,13 @@ def test_in_place_no_residual_generic(pkg):
 
 
 def test_degenerate_rows(pkg):
-    # zero rows (FP8 scale 0, codes +0), constant rows, huge values, H = 1
+    # zero rows (FP8 scale 0, codes +0), constant rows, large and tiny values.
+    # The fp32 sum of squares bounds the range: rows need sum(h^2) < FLT_MAX,
+    # i.e. rms(h) < sqrt(FLT_MAX / H) (about 4e17 at H = 2048); 1e15 is inside.
     T, H = 8, 2048
     x = torch.zeros((T, H), dtype=torch.float32)
     x[1] = 3.0
-    x[2] = -1e30
+    x[2] = -1e15
     x[3, ::2] = 1e-30
     x[4] = torch.linspace(-100, 100, H)
     xb = x.to(torch.bfloat16)
@@ -270,6 +285,11 @@ def test_selector_decode_vs_prefill(pkg):
     assert c.grid <= 16384
     c = pkg.rmsnorm_query_config(16, 1000, flags)
     assert c.variant == pkg.VARIANT_GENERIC
+
+
+def test_status_word_clear_after_all_runs(pkg):
+    # no bounded wait in any kernel ran out during the suite
+    assert pkg.rmsnorm_read_status(clear=False) == 0
 
 
 def test_streams_are_respected(pkg):
