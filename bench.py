@@ -196,13 +196,19 @@ def run_ours(args):
     w = host["weight"].to(dev)
     out = torch.empty_like(x)
     res = torch.empty_like(x)
-    cfg = pkg.rmsnorm_query_config(T, H, flags)
+    forced = None
+    if args.config:
+        forced = pkg.RmsnConfig.from_dict(json.loads(args.config))
+    cfg = forced if forced is not None else pkg.rmsnorm_query_config(T, H, flags)
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
     ptrs = (x.data_ptr(), r.data_ptr(), w.data_ptr(), None, out.data_ptr(), res.data_ptr(), None)
 
     def step():
-        st = pkg.rmsnorm_fwd(*ptrs, T, H, wl.eps, flags, sptr)
+        if forced is None:
+            st = pkg.rmsnorm_fwd(*ptrs, T, H, wl.eps, flags, sptr)
+        else:
+            st = pkg.rmsnorm_fwd_ex(*ptrs, T, H, wl.eps, flags, 0.0, forced, sptr)
         if st != pkg.RMSN_OK:
             raise pkg.RmsnError(st, "rmsnorm_fwd")
 
@@ -499,6 +505,9 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--config", default="",
+                    help='force a launch configuration, JSON such as '
+                         '{"variant": 2, "chunks": 2, "max_warps": 32, "stages": 4}')
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

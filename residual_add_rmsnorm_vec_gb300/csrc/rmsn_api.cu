@@ -18,6 +18,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <unordered_map>
 #include <utility>
 #include <vector>
 
@@ -43,7 +44,16 @@ struct DeviceInfo {
     cudaError_t err = cudaSuccess;
     std::mutex mu;
     std::vector<std::pair<const void*, int>> smem_set;  // kernel -> raised dynamic smem limit
+    // occupancy results: (kernel, threads, smem) -> resident blocks per SM
+    std::unordered_map<uint64_t, int> occ_cache;
+    // selector results: (tokens, hidden, flags, vector path) -> configuration
+    std::unordered_map<uint64_t, std::pair<rmsn_config, const KernelEntry*>> sel_cache;
 };
+
+inline uint64_t mix(uint64_t h, uint64_t v) {
+    h ^= v + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+    return h;
+}
 
 DeviceInfo g_dev[kMaxDevices];
 
@@ -164,12 +174,20 @@ const KernelEntry* find_kernel(const Problem& p, int variant, int ch, int wmax) 
     return nullptr;
 }
 
-int blocks_per_sm(const void* fn, int threads, int smem) {
+int blocks_per_sm(DeviceInfo* d, const void* fn, int threads, int smem) {
+    const uint64_t key = mix(mix(reinterpret_cast<uintptr_t>(fn), (uint64_t)threads), (uint64_t)smem);
+    {
+        std::lock_guard<std::mutex> lock(d->mu);
+        auto it = d->occ_cache.find(key);
+        if (it != d->occ_cache.end()) return it->second;
+    }
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
+    std::lock_guard<std::mutex> lock(d->mu);
+    d->occ_cache[key] = n;
     return n;
 }
 
@@ -227,7 +245,7 @@ bool shape_config(const Problem& p, const KernelEntry& e, DeviceInfo* d, int gri
             c->smem_bytes = st * sb;
         }
     }
-    const int bps = blocks_per_sm(e.fn, threads, c->smem_bytes);
+    const int bps = blocks_per_sm(d, e.fn, threads, c->smem_bytes);
     if (bps < 1) return false;
     const int64_t resident = (int64_t)sms * bps;
     int64_t grid = units < resident ? units : resident;
@@ -320,9 +338,25 @@ RMSN_API int rmsnorm_fwd_ex(const void* x, const void* residual, const void* wei
         e = find_kernel(p, cfg->variant, cfg->chunks, cfg->max_warps);
         if (!e || !shape_config(p, *e, d, cfg->grid, cfg->stages, &c)) return RMSN_EUNSUPPORTED;
     } else {
-        if (!select(p, d, &c)) return RMSN_EUNSUPPORTED;
-        e = find_kernel(p, c.variant, c.chunks, c.max_warps);
-        if (!e) return RMSN_EUNSUPPORTED;
+        const uint64_t key = mix(mix(mix((uint64_t)p.T, (uint64_t)p.H), flags), p.vec_ok ? 1 : 0);
+        bool hit = false;
+        {
+            std::lock_guard<std::mutex> lock(d->mu);
+            auto it = d->sel_cache.find(key);
+            if (it != d->sel_cache.end()) {
+                c = it->second.first;
+                e = it->second.second;
+                hit = true;
+            }
+        }
+        if (!hit) {
+            if (!select(p, d, &c)) return RMSN_EUNSUPPORTED;
+            e = find_kernel(p, c.variant, c.chunks, c.max_warps);
+            if (!e) return RMSN_EUNSUPPORTED;
+            std::lock_guard<std::mutex> lock(d->mu);
+            if (d->sel_cache.size() > 4096) d->sel_cache.clear();
+            d->sel_cache[key] = {c, e};
+        }
     }
 
     RmsnArgs a;

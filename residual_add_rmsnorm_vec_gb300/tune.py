@@ -7,10 +7,13 @@ improving; this does the same for every variant the library builds (one warp
 per row, one block per row, bulk-copy ring depths, grid shapes) on the
 current GPU.
 
-Timing: CUDA events around each launch on the launching stream, median of
-`reps` launches after warm-up.  When one set of buffers is smaller than
+Timing: `reps` back-to-back launches are captured in a CUDA graph and the
+graph is replayed; the time per launch is the replay time (CUDA events on
+the replay stream) over the launches, median of several replays, so host
+launch overhead does not enter.  When one set of buffers is smaller than
 3 x the L2 size the launches rotate over enough copies to exceed it, so the
-figures are HBM (not L2) bandwidth.
+figures are HBM (not L2) bandwidth; with --l2-hot one set is reused (the
+decode situation, where the activations of a few tokens stay on chip).
 
     python -m residual_add_rmsnorm_vec_gb300.tune --out sweep.json --write-table
 """
@@ -40,7 +43,7 @@ def _algorithmic_bytes(T, H, in_b, out_b, res, bias, fp8):
 
 
 def measure(pkg, T, H, in_dt="bf16", out_dt="bf16", res=True, bias=False, reps=30,
-            configs=None):
+            configs=None, l2_hot=False, replays=5):
     import torch
 
     dev = torch.device("cuda")
@@ -50,7 +53,7 @@ def measure(pkg, T, H, in_dt="bf16", out_dt="bf16", res=True, bias=False, reps=3
     tout = {"bf16": torch.bfloat16, "f32": torch.float32, "fp8": torch.uint8}[out_dt]
     flags = pkg.make_flags(in_dt, out_dt, res, True, bias)
     set_bytes = T * H * (in_b * (3 if res else 1) + out_b)
-    n_sets = max(1, min(64, -(-3 * L2_BYTES // max(1, set_bytes))))
+    n_sets = 1 if l2_hot else max(1, min(64, -(-3 * L2_BYTES // max(1, set_bytes))))
     sets = []
     for _ in range(n_sets):
         x = torch.randn(T, H, device=dev).to(tin)
@@ -66,27 +69,43 @@ def measure(pkg, T, H, in_dt="bf16", out_dt="bf16", res=True, bias=False, reps=3
     algo = _algorithmic_bytes(T, H, in_b, out_b, res, bias, out_dt == "fp8")
     results = []
     for cfg in configs:
-        def launch(i):
+        def launch_on(i, s):
             x, r, o, ro, sc = sets[i % n_sets]
             st = pkg.rmsnorm_fwd_ex(x.data_ptr(), None if r is None else r.data_ptr(),
                                     w.data_ptr(), None if b is None else b.data_ptr(),
                                     o.data_ptr(), None if ro is None else ro.data_ptr(),
                                     None if sc is None else sc.data_ptr(), T, H, 1e-6, flags,
-                                    0.0, cfg, stream.cuda_stream)
+                                    0.0, cfg, s.cuda_stream)
             if st != pkg.RMSN_OK:
                 raise pkg.RmsnError(st, "rmsnorm_fwd_ex")
 
-        for i in range(5):
+        def launch(i):
+            launch_on(i, stream)
+
+        for i in range(3):
             launch(i)
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(reps)]
         torch.cuda.synchronize()
-        for i, (e0, e1) in enumerate(evs):
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                for i in range(reps):
+                    launch_on(i, cap)
+        stream.wait_stream(cap)
+        g.replay()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(replays):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            launch(i)
+            g.replay()
             e1.record(stream)
-        torch.cuda.synchronize()
-        us = statistics.median(e0.elapsed_time(e1) * 1e3 for e0, e1 in evs)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3 / reps)
+        del g
+        us = statistics.median(times)
         d = cfg.as_dict()
         d.update(us=round(us, 3), gbs=round(algo / (us * 1e-6) / 1e9, 1))
         results.append(d)
@@ -95,11 +114,12 @@ def measure(pkg, T, H, in_dt="bf16", out_dt="bf16", res=True, bias=False, reps=3
     return results
 
 
-def sweep(pkg, shapes, in_dt, out_dt, res, bias, reps):
+def sweep(pkg, shapes, in_dt, out_dt, res, bias, reps, l2_hot_below=0):
+    """``l2_hot_below``: shapes with fewer tokens are timed L2-hot (decode)."""
     out = []
     for T, H in shapes:
         t0 = time.time()
-        rs = measure(pkg, T, H, in_dt, out_dt, res, bias, reps)
+        rs = measure(pkg, T, H, in_dt, out_dt, res, bias, reps, l2_hot=T < l2_hot_below)
         best = min(rs, key=lambda d: d["us"])
         out.append({"T": T, "H": H, "in": in_dt, "out": out_dt, "res": res, "bias": bias,
                     "best": best, "all": rs})
@@ -185,21 +205,24 @@ def main():
     ap.add_argument("--table-out", default=os.path.join(
         os.path.dirname(os.path.abspath(__file__)), "csrc", "rmsn_selector_table.inc"))
     ap.add_argument("--quick", action="store_true", help="a few shapes only")
+    ap.add_argument("--l2-hot-below", type=int, default=512,
+                    help="time shapes with fewer tokens L2-hot (decode sizes)")
     args = ap.parse_args()
     build.build()
     torch.cuda.set_device(0)
     grid = [(T, H) for H in HIDDEN for T in TOKENS]
     if args.quick:
         grid = [(1, 4096), (256, 4096), (16384, 8192)]
-    entries = sweep(pkg, grid, "bf16", "bf16", True, False, args.reps)
+    hot = args.l2_hot_below
+    entries = sweep(pkg, grid, "bf16", "bf16", True, False, args.reps, hot)
     # the other dtype paths of the hot-path workloads
     entries += sweep(pkg, [(T, H) for H in (5120, 7168) for T in (1, 64, 1024, 4096)],
-                     "bf16", "fp8", True, True, args.reps)
+                     "bf16", "fp8", True, True, args.reps, hot)
     entries += sweep(pkg, [(T, 1024) for T in (1, 64, 4096)], "f32", "f32", False, False,
-                     args.reps)
+                     args.reps, hot)
     meta = {"gpu": torch.cuda.get_device_name(0),
             "sms": torch.cuda.get_device_properties(0).multi_processor_count,
-            "reps": args.reps}
+            "reps": args.reps, "l2_hot_below": args.l2_hot_below, "timing": "cuda graph replay"}
     with open(args.out, "w") as f:
         json.dump({"meta": meta, "entries": entries}, f)
     if args.write_table:
