@@ -275,14 +275,25 @@ def test_forced_unbuilt_config_rejected(pkg):
         pkg.fused_add_rmsnorm(inp["x"], inp["residual"], inp["weight"], None, eps=1e-6, config=big)
 
 
+def _same_shape(a, b):
+    keys = ("variant", "chunks", "max_warps", "warps_per_block", "stages")
+    return all(getattr(a, k) == getattr(b, k) for k in keys)
+
+
 def test_selector_decode_vs_prefill(pkg):
     flags = pkg.make_flags("bf16", "bf16", True, True, False)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    c = pkg.rmsnorm_query_config(8, 4096, flags)
+    # a hidden size without measured rows: the decode rule (one warp per block
+    # while the problem needs fewer warps than there are SMs), else multi-warp
+    c = pkg.rmsnorm_query_config(8, 3072, flags)
     assert c.variant == pkg.VARIANT_WARP_ROWS and c.warps_per_block == 1 and c.num_sms == sms
-    c = pkg.rmsnorm_query_config(16384, 8192, flags)
-    assert c.variant in (pkg.VARIANT_BLOCK_ROW, pkg.VARIANT_BULK_ROW)
-    assert c.grid <= 16384
+    c = pkg.rmsnorm_query_config(4096, 3072, flags)
+    assert c.variant == pkg.VARIANT_BLOCK_ROW and c.warps_per_block > 1
+    # measured shapes: whatever the table picked is a valid built configuration
+    for T, H in ((1, 4096), (8, 4096), (256, 4096), (16384, 8192), (4096, 16384)):
+        c = pkg.rmsnorm_query_config(T, H, flags)
+        assert any(_same_shape(c, o) for o in pkg.rmsnorm_list_configs(T, H, flags)), (T, H)
+        assert 1 <= c.grid <= max(T, 1)
     c = pkg.rmsnorm_query_config(16, 1000, flags)
     assert c.variant == pkg.VARIANT_GENERIC
 
