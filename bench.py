@@ -17,9 +17,9 @@ residual_out and y.  Prints ONE JSON line on rank 0:
 --impl reference times the CPU oracle instead (the only reference of this
 method), on a bounded row sample per step.
 
-Multi-GPU: rows are independent, so each rank runs its own full workload
-(weak scaling, no collective on the data path); a barrier and a MAX
-all-reduce of the elapsed time bracket the timed region.
+Multi-GPU: rows are independent, so each rank runs its own full-size slice
+of one seeded global batch (weak scaling, no collective on the data path); a
+barrier and a MAX all-reduce of the elapsed time bracket the timed region.
 """
 from __future__ import annotations
 
@@ -173,6 +173,19 @@ def sum_over_ranks(pg, v: float, device) -> float:
     return float(t.item())
 
 
+def aggregate(pg, elapsed_ms: float, bytes_rank: float, device):
+    """Whole-job throughput: bytes of all ranks over the slowest rank's time.
+    Returns (max elapsed ms, total bytes, GB/s)."""
+    max_ms = max_over_ranks(pg, elapsed_ms, device)
+    total = sum_over_ranks(pg, bytes_rank, device)
+    return max_ms, total, total / (max_ms / 1e3) / 1e9
+
+
+def rank_rows(rank: int, world: int, tokens_per_rank: int) -> range:
+    """Rows of the global batch (world x tokens_per_rank tokens) owned by a rank."""
+    return range(rank * tokens_per_rank, (rank + 1) * tokens_per_rank)
+
+
 # ---------------------------------------------------------------------------- our arm
 
 
@@ -187,10 +200,12 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     build.build()
 
+    # each rank owns a contiguous slice of one seeded global batch (weak scaling)
     wl = synth.prefill_workload(args.tokens, args.hidden)
+    wl_global = synth.prefill_workload(args.tokens * world, args.hidden)
     T, H = wl.n_tokens, wl.hidden
     flags = pkg.make_flags("bf16", "bf16", True, True, False)
-    host = synth.make_inputs(wl)
+    host = synth.make_inputs(wl_global, rows=rank_rows(rank, world, T))
     x = host["x"].to(dev)
     r = host["residual"].to(dev)
     w = host["weight"].to(dev)
@@ -235,12 +250,10 @@ def run_ours(args):
     wall1 = time.time()
     barrier(pg)
     clocks = sampler.stop(wall0, wall1)
-    elapsed_ms = t_start.elapsed_time(t_end)
     kernel_ms = sum(a.elapsed_time(b) for a, b in ev) / K
-    elapsed_ms = max_over_ranks(pg, elapsed_ms, dev)
     bytes_step = wl.algorithmic_bytes()
-    total_bytes = sum_over_ranks(pg, float(bytes_step * K), dev)
-    value = total_bytes / (elapsed_ms / 1e3) / 1e9
+    elapsed_ms, total_bytes, value = aggregate(pg, t_start.elapsed_time(t_end),
+                                               float(bytes_step * K), dev)
 
     # e2e: pinned host buffers, copies inside the timed region, every step
     e2e = run_e2e(pkg, wl, host, dev, stream, flags, max(3, min(K, args.e2e_steps)), pg)

@@ -134,26 +134,38 @@ def _draw_block(dist: str, seed: int, tag: int, block: int, rows: int, cols: int
     raise ValueError(dist)
 
 
-def _draw_rows(dist: str, seed: int, tag: int, n_rows: int, cols: int,
-               rows: np.ndarray | None) -> np.ndarray:
-    """Rows of a [n_rows, cols] float32 draw; all rows, or only ``rows``."""
-    if rows is None:
-        n_blocks = (n_rows + ROW_BLOCK - 1) // ROW_BLOCK
-        out = np.empty((n_rows, cols), dtype=np.float32)
-
-        def fill(k: int) -> None:
-            lo = k * ROW_BLOCK
-            hi = min(n_rows, lo + ROW_BLOCK)
-            out[lo:hi] = _draw_block(dist, seed, tag, k, ROW_BLOCK, cols)[: hi - lo]
-
-        workers = min(n_blocks, os.cpu_count() or 1, 32)
-        if workers > 1:
-            with ThreadPoolExecutor(workers) as ex:
-                list(ex.map(fill, range(n_blocks)))
-        else:
-            for k in range(n_blocks):
-                fill(k)
+def _draw_range(dist: str, seed: int, tag: int, lo: int, hi: int, cols: int) -> np.ndarray:
+    """Rows [lo, hi) of a block-seeded draw, blocks generated in parallel."""
+    out = np.empty((hi - lo, cols), dtype=np.float32)
+    if hi <= lo:
         return out
+
+    def fill(k: int) -> None:
+        b = _draw_block(dist, seed, tag, k, ROW_BLOCK, cols)
+        a, z = max(lo, k * ROW_BLOCK), min(hi, (k + 1) * ROW_BLOCK)
+        out[a - lo:z - lo] = b[a - k * ROW_BLOCK:z - k * ROW_BLOCK]
+
+    blocks = range(lo // ROW_BLOCK, (hi - 1) // ROW_BLOCK + 1)
+    workers = min(len(blocks), os.cpu_count() or 1, 32)
+    if workers > 1:
+        with ThreadPoolExecutor(workers) as ex:
+            list(ex.map(fill, blocks))
+    else:
+        for k in blocks:
+            fill(k)
+    return out
+
+
+def _draw_rows(dist: str, seed: int, tag: int, n_rows: int, cols: int,
+               rows) -> np.ndarray:
+    """Rows of a [n_rows, cols] float32 draw: all rows, a ``range`` of rows,
+    or the rows listed in an index array."""
+    if rows is None:
+        return _draw_range(dist, seed, tag, 0, n_rows, cols)
+    if isinstance(rows, range) and rows.step == 1:
+        if rows.start < 0 or rows.stop > n_rows:
+            raise IndexError("row range out of bounds")
+        return _draw_range(dist, seed, tag, rows.start, rows.stop, cols)
     rows = np.asarray(rows, dtype=np.int64)
     if rows.size and (rows.min() < 0 or rows.max() >= n_rows):
         raise IndexError("row index out of range")
@@ -195,8 +207,9 @@ def to_storage(a: np.ndarray, dtype: str):
 def make_inputs(wl: Workload, rows=None) -> dict:
     """Seeded inputs of ``wl`` as torch CPU tensors in their storage dtype.
 
-    ``rows`` (optional) restricts x and residual to those token indices; the
-    values are the ones the full tensors hold at those rows.
+    ``rows`` (optional: an index array or a ``range``) restricts x and
+    residual to those token indices; the values are the ones the full tensors
+    hold at those rows.
     Returns keys ``x``, ``residual`` (or None), ``weight`` (or None),
     ``bias`` (or None).
     """

@@ -148,10 +148,11 @@ def write_table(entries, path):
     rows.sort()
     lines = [
         "// Launch shapes chosen from measured bandwidth on a GB300 by",
-        "// residual_add_rmsnorm_vec_gb300/tune.py (CUDA-event median per launch, inputs",
-        "// rotated past the L2 size).  For one (input dtype, output dtype, hidden) the",
-        "// row with the largest t_min <= n_tokens applies; other shapes fall back to",
-        "// the fixed rule in the selector.",
+        "// residual_add_rmsnorm_vec_gb300/tune.py (CUDA-graph replay of back-to-back",
+        "// launches; inputs rotated past the L2 size from 512 tokens up, L2-hot below).",
+        "// For one (input dtype, output dtype, hidden) the row with the largest",
+        "// t_min <= n_tokens applies; other shapes fall back to the fixed rule in the",
+        "// selector.",
         "struct TableRow {",
         "    int in_dt, out_dt;",
         "    int64_t hidden, t_min;",
