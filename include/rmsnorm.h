@@ -93,8 +93,9 @@ typedef struct {
  *   out_scale                  : [n_tokens] float32, required iff FP8 output
  *   eps                        : added to the mean square inside the root
  *
- * All pointers are device (or managed / device-accessible) pointers, rows
- * contiguous (row stride = hidden).  Each pointer must be aligned to its
+ * All pointers are device (or device-resident managed) pointers, rows
+ * contiguous (row stride = hidden); for rows in host memory use
+ * rmsnorm_fwd_host.  Each pointer must be aligned to its
  * element size; the 256-bit vector kernels are used when hidden * element
  * size is a multiple of 32 bytes and every pointer is 32-byte aligned,
  * otherwise the generic kernel runs.  residual_out may be the same buffer as
@@ -117,6 +118,28 @@ int rmsnorm_fwd_ex(const void* x, const void* residual, const void* weight, cons
                    void* out, void* residual_out, float* out_scale, int64_t n_tokens,
                    int64_t hidden, float eps, uint32_t flags, float weight_offset,
                    const rmsn_config* cfg, cudaStream_t stream);
+
+/*
+ * rmsnorm_fwd_ex on rows that live in HOST memory: the kernel itself reads x,
+ * residual (and weight, bias) across the CPU-GPU link and writes out,
+ * residual_out and out_scale back to host memory, with no staging buffer and
+ * no allocation (on Grace-Blackwell the link is the coherent NVLink-C2C).
+ *
+ * Each pointer may be device or managed memory, page-locked host memory
+ * (cudaHostAlloc, cudaMallocHost, cudaHostRegister, torch pin_memory), or
+ * ordinary pageable host memory when the device reports pageable-memory
+ * access (cudaDevAttrPageableMemoryAccess); any mix is allowed.  A pointer
+ * the device cannot reach returns RMSN_EINVAL before any launch.  Only the
+ * register-streaming kernels run here (plain loads and stores), shaped for
+ * the link's latency: one block per row, one 32-byte vector per thread where
+ * the row allows it.  The call is asynchronous on `stream`: host outputs are
+ * complete once the stream has been synchronised.  The operation, aliasing
+ * and alignment rules are those of rmsnorm_fwd.  Returns an rmsn_status.
+ */
+int rmsnorm_fwd_host(const void* x, const void* residual, const void* weight, const void* bias,
+                     void* out, void* residual_out, float* out_scale, int64_t n_tokens,
+                     int64_t hidden, float eps, uint32_t flags, float weight_offset,
+                     cudaStream_t stream);
 
 /*
  * The configuration rmsnorm_fwd would launch for this shape on the current

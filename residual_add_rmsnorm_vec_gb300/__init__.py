@@ -17,6 +17,6 @@ from ._lib import (  # noqa: F401
     RMSN_HAS_RESIDUAL, RMSN_HAS_WEIGHT, RMSN_IN_BF16, RMSN_IN_F32, RMSN_OK, RMSN_OUT_BF16,
     RMSN_OUT_F32, RMSN_OUT_FP8E4M3, VARIANT_BLOCK_ROW, VARIANT_BULK_ROW, VARIANT_GENERIC,
     VARIANT_NAMES, VARIANT_WARP_ROWS, RmsnConfig, RmsnError, library_path, load,
-    rmsnorm_fwd, rmsnorm_fwd_ex, rmsnorm_list_configs, rmsnorm_query_config, rmsnorm_read_status,
-    status_string)
-from .api import fused_add_rmsnorm, make_flags  # noqa: F401
+    rmsnorm_fwd, rmsnorm_fwd_ex, rmsnorm_fwd_host, rmsnorm_list_configs, rmsnorm_query_config,
+    rmsnorm_read_status, status_string)
+from .api import fused_add_rmsnorm, fused_add_rmsnorm_host, make_flags  # noqa: F401

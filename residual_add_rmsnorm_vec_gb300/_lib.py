@@ -33,8 +33,8 @@ VARIANT_BULK_ROW = 2
 VARIANT_GENERIC = 3
 VARIANT_NAMES = {0: "warp_rows", 1: "block_row", 2: "bulk_row", 3: "generic"}
 
-EXPORTED = ("rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_query_config", "rmsnorm_list_configs",
-            "rmsnorm_read_status", "rmsnorm_status_string")
+EXPORTED = ("rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_fwd_host", "rmsnorm_query_config",
+            "rmsnorm_list_configs", "rmsnorm_read_status", "rmsnorm_status_string")
 
 
 class RmsnConfig(ctypes.Structure):
@@ -87,6 +87,9 @@ def load() -> ctypes.CDLL:
             lib.rmsnorm_fwd_ex.restype = ctypes.c_int
             lib.rmsnorm_fwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, f32, u32, f32,
                                            ctypes.POINTER(RmsnConfig), vp]
+            lib.rmsnorm_fwd_host.restype = ctypes.c_int
+            lib.rmsnorm_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, f32, u32, f32,
+                                             vp]
             lib.rmsnorm_query_config.restype = ctypes.c_int
             lib.rmsnorm_query_config.argtypes = [i64, i64, u32, ctypes.POINTER(RmsnConfig)]
             lib.rmsnorm_list_configs.restype = ctypes.c_int
@@ -119,6 +122,14 @@ def rmsnorm_fwd_ex(x, residual, weight, bias, out, residual_out, out_scale, n_to
                                      int(n_tokens), int(hidden), float(eps), int(flags),
                                      float(weight_offset),
                                      None if cfg is None else ctypes.byref(cfg), stream))
+
+
+def rmsnorm_fwd_host(x, residual, weight, bias, out, residual_out, out_scale, n_tokens: int,
+                     hidden: int, eps: float, flags: int, weight_offset: float, stream) -> int:
+    """Direct call of ``rmsnorm_fwd_host`` (pointers may be host memory)."""
+    return int(load().rmsnorm_fwd_host(x, residual, weight, bias, out, residual_out, out_scale,
+                                       int(n_tokens), int(hidden), float(eps), int(flags),
+                                       float(weight_offset), stream))
 
 
 def rmsnorm_query_config(n_tokens: int, hidden: int, flags: int) -> RmsnConfig:

@@ -72,3 +72,49 @@ def fused_add_rmsnorm(x: torch.Tensor, residual: torch.Tensor | None = None,
     if st != _lib.RMSN_OK:
         raise _lib.RmsnError(st, "rmsnorm_fwd_ex")
     return out, residual_out, (out_scale if out_dtype == "fp8" else None)
+
+
+def fused_add_rmsnorm_host(x: torch.Tensor, residual: torch.Tensor | None = None,
+                           weight: torch.Tensor | None = None, bias: torch.Tensor | None = None, *,
+                           eps: float, out_dtype: str | None = None, weight_offset: float = 0.0,
+                           out: torch.Tensor | None = None,
+                           residual_out: torch.Tensor | None = None,
+                           out_scale: torch.Tensor | None = None, device: int | None = None,
+                           stream: torch.cuda.Stream | None = None):
+    """Fused residual-add + RMSNorm on tensors in host memory (``rmsnorm_fwd_host``).
+
+    The GPU reads the rows straight from host memory and writes the results
+    back there.  Inputs should be page-locked (``pin_memory()``); outputs
+    that are not given are allocated page-locked.  Returns
+    ``(out, residual_out, out_scale)`` like ``fused_add_rmsnorm``; the call is
+    asynchronous, so synchronise ``stream`` before reading them.
+    """
+    if x.dim() != 2:
+        raise ValueError("x must be [n_tokens, hidden]")
+    if x.dtype not in _IN:
+        raise TypeError(f"unsupported input dtype {x.dtype}")
+    T, H = x.shape
+    in_name = _DT_NAME[x.dtype]
+    out_dtype = out_dtype or in_name
+    _, out_torch = _OUT[out_dtype]
+    for name, t in (("x", x), ("residual", residual), ("weight", weight), ("bias", bias),
+                    ("out", out), ("residual_out", residual_out), ("out_scale", out_scale)):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if out is None:
+        out = torch.empty((T, H), dtype=out_torch, pin_memory=True)
+    if residual is not None and residual_out is None:
+        residual_out = torch.empty((T, H), dtype=x.dtype, pin_memory=True)
+    if out_dtype == "fp8" and out_scale is None:
+        out_scale = torch.empty((T,), dtype=torch.float32, pin_memory=True)
+    flags = make_flags(in_name, out_dtype, residual is not None, weight is not None,
+                       bias is not None)
+    dev = torch.cuda.current_device() if device is None else device
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        st = _lib.rmsnorm_fwd_host(_ptr(x), _ptr(residual), _ptr(weight), _ptr(bias), _ptr(out),
+                                   _ptr(residual_out), _ptr(out_scale), T, H, eps, flags,
+                                   weight_offset, s.cuda_stream)
+    if st != _lib.RMSN_OK:
+        raise _lib.RmsnError(st, "rmsnorm_fwd_host")
+    return out, residual_out, (out_scale if out_dtype == "fp8" else None)

@@ -40,6 +40,7 @@ struct DeviceInfo {
     std::once_flag once;
     int num_sms = 0;
     int max_smem = 0;              // opt-in dynamic shared memory per block
+    int pageable_access = 0;       // device can read and write pageable host memory
     uint32_t* status = nullptr;    // device address of g_status on this device
     cudaError_t err = cudaSuccess;
     std::mutex mu;
@@ -67,6 +68,8 @@ DeviceInfo* device_info() {
         d.err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
         if (d.err == cudaSuccess)
             d.err = cudaDeviceGetAttribute(&sm, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (d.err == cudaSuccess)
+            d.err = cudaDeviceGetAttribute(&d.pageable_access, cudaDevAttrPageableMemoryAccess, dev);
         if (d.err == cudaSuccess) d.err = cudaGetSymbolAddress((void**)&d.status, g_status);
         d.num_sms = n;
         d.max_smem = sm;
@@ -305,29 +308,118 @@ RMSN_API const char* rmsnorm_status_string(int status) {
     }
 }
 
+namespace rmsn {
+namespace {
+
+// Argument checks shared by the entry points.  Fills `p` (including whether
+// the 32-byte vector kernels can run with these pointers).  RMSN_OK with
+// p->T == 0 means "nothing to do".
+int validate(const void* x, const void* residual, const void* weight, const void* bias,
+             const void* out, const void* residual_out, const float* out_scale,
+             int64_t n_tokens, int64_t hidden, float eps, uint32_t flags, float weight_offset,
+             Problem* p) {
+    int st = decode_flags(flags, p);
+    if (st != RMSN_OK) return st;
+    if ((st = check_shape(n_tokens, hidden, p)) != RMSN_OK) return st;
+    if (!(eps >= 0.f) || !isfinite(eps) || !isfinite(weight_offset)) return RMSN_EINVAL;
+    // an empty batch touches nothing (its buffers may be NULL)
+    if (n_tokens == 0) return RMSN_OK;
+    // optional operands must match their flags exactly
+    if (p->res != (residual != nullptr) || p->res != (residual_out != nullptr)) return RMSN_EINVAL;
+    if (((flags & RMSN_HAS_WEIGHT) != 0) != (weight != nullptr)) return RMSN_EINVAL;
+    if (p->bias != (bias != nullptr)) return RMSN_EINVAL;
+    if ((p->out_dt == kFP8) != (out_scale != nullptr)) return RMSN_EINVAL;
+    if (!x || !out) return RMSN_EINVAL;
+    const void* ins[] = {x, residual, weight, bias, residual_out};
+    for (const void* q : ins)
+        if (!aligned(q, (uintptr_t)p->in_bytes)) return RMSN_EALIGN;
+    if (!aligned(out, (uintptr_t)p->out_bytes) || !aligned(out_scale, 4)) return RMSN_EALIGN;
+    p->vec_ok = vector_path_ok(*p, ins, 5, out);
+    p->nvec = p->vec_ok ? (int)(p->H / p->ve) : 0;
+    return RMSN_OK;
+}
+
+int launch(const KernelEntry* e, const rmsn_config& c, DeviceInfo* d, const Problem& p,
+           const void* x, const void* residual, const void* weight, const void* bias, void* out,
+           void* residual_out, float* out_scale, float eps, float weight_offset,
+           cudaStream_t stream) {
+    RmsnArgs a;
+    a.x = x;
+    a.r = residual;
+    a.w = weight;
+    a.b = bias;
+    a.out = out;
+    a.res_out = residual_out;
+    a.scale = out_scale;
+    a.T = p.T;
+    a.H = (int32_t)p.H;
+    a.nvec = p.nvec;
+    a.eps = eps;
+    a.woff = weight_offset;
+    a.has_w = weight != nullptr;
+    a.stages = c.stages;
+    a.status = d->status;
+    void* args[] = {&a};
+    const cudaError_t err = cudaLaunchKernel(e->fn, dim3((unsigned)c.grid),
+                                             dim3((unsigned)(c.warps_per_block * 32)), args,
+                                             (size_t)c.smem_bytes, stream);
+    return err == cudaSuccess ? RMSN_OK : RMSN_ECUDA;
+}
+
+// Device address at which the current device reaches `p`: device and managed
+// memory as is, page-locked host memory through its mapped address, other
+// host memory only where the device can access pageable memory.  Returns
+// false when the device cannot reach `p`.
+bool device_view(DeviceInfo* d, const void* p, const void** dev) {
+    *dev = p;
+    if (!p) return true;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();
+        attr.type = cudaMemoryTypeUnregistered;
+    }
+    switch (attr.type) {
+        case cudaMemoryTypeDevice:
+        case cudaMemoryTypeManaged:
+            return true;
+        case cudaMemoryTypeHost:
+            if (!attr.devicePointer) return false;
+            *dev = attr.devicePointer;
+            return true;
+        default:
+            return d->pageable_access != 0;
+    }
+}
+
+// Launch shape for rows that live in host memory: the register kernels only
+// (plain loads and stores), one block per row with one 32-byte vector per
+// thread where the row allows it, as many blocks as fit on the GPU, so the
+// most requests are in flight across the CPU-GPU link.
+bool select_host(const Problem& p, DeviceInfo* d, rmsn_config* c) {
+    if (p.vec_ok) {
+        const int shapes[][2] = {{1, 4}, {1, 8}, {1, 16}, {1, 32}, {2, 32}, {4, 16}};
+        for (auto& s : shapes) {
+            const int w = (int)((p.nvec + 32 * s[0] - 1) / (32 * s[0]));
+            if (w > s[1]) continue;
+            const KernelEntry* e = find_kernel(p, kBlockRow, s[0], s[1]);
+            if (e && shape_config(p, *e, d, 0, 0, c)) return true;
+        }
+    }
+    const KernelEntry* e = find_kernel(p, kGeneric, 0, 0);
+    return e && shape_config(p, *e, d, 0, 0, c);
+}
+
+}  // namespace
+}  // namespace rmsn
+
 RMSN_API int rmsnorm_fwd_ex(const void* x, const void* residual, const void* weight,
                             const void* bias, void* out, void* residual_out, float* out_scale,
                             int64_t n_tokens, int64_t hidden, float eps, uint32_t flags,
                             float weight_offset, const rmsn_config* cfg, cudaStream_t stream) {
     Problem p{};
-    int st = decode_flags(flags, &p);
-    if (st != RMSN_OK) return st;
-    if ((st = check_shape(n_tokens, hidden, &p)) != RMSN_OK) return st;
-    if (!(eps >= 0.f) || !isfinite(eps) || !isfinite(weight_offset)) return RMSN_EINVAL;
-    // an empty batch touches nothing (its buffers may be NULL)
-    if (n_tokens == 0) return RMSN_OK;
-    // optional operands must match their flags exactly
-    if (p.res != (residual != nullptr) || p.res != (residual_out != nullptr)) return RMSN_EINVAL;
-    if (((flags & RMSN_HAS_WEIGHT) != 0) != (weight != nullptr)) return RMSN_EINVAL;
-    if (p.bias != (bias != nullptr)) return RMSN_EINVAL;
-    if ((p.out_dt == kFP8) != (out_scale != nullptr)) return RMSN_EINVAL;
-    if (!x || !out) return RMSN_EINVAL;
-    const void* ins[] = {x, residual, weight, bias, residual_out};
-    for (const void* q : ins)
-        if (!aligned(q, (uintptr_t)p.in_bytes)) return RMSN_EALIGN;
-    if (!aligned(out, (uintptr_t)p.out_bytes) || !aligned(out_scale, 4)) return RMSN_EALIGN;
-    p.vec_ok = vector_path_ok(p, ins, 5, out);
-    p.nvec = p.vec_ok ? (int)(p.H / p.ve) : 0;
+    int st = validate(x, residual, weight, bias, out, residual_out, out_scale, n_tokens, hidden,
+                      eps, flags, weight_offset, &p);
+    if (st != RMSN_OK || n_tokens == 0) return st;
 
     DeviceInfo* d = device_info();
     if (!d) return RMSN_ECUDA;
@@ -358,28 +450,43 @@ RMSN_API int rmsnorm_fwd_ex(const void* x, const void* residual, const void* wei
             d->sel_cache[key] = {c, e};
         }
     }
+    return launch(e, c, d, p, x, residual, weight, bias, out, residual_out, out_scale, eps,
+                  weight_offset, stream);
+}
 
-    RmsnArgs a;
-    a.x = x;
-    a.r = residual;
-    a.w = weight;
-    a.b = bias;
-    a.out = out;
-    a.res_out = residual_out;
-    a.scale = out_scale;
-    a.T = p.T;
-    a.H = (int32_t)p.H;
-    a.nvec = p.nvec;
-    a.eps = eps;
-    a.woff = weight_offset;
-    a.has_w = weight != nullptr;
-    a.stages = c.stages;
-    a.status = d->status;
-    void* args[] = {&a};
-    const cudaError_t err = cudaLaunchKernel(e->fn, dim3((unsigned)c.grid),
-                                             dim3((unsigned)(c.warps_per_block * 32)), args,
-                                             (size_t)c.smem_bytes, stream);
-    return err == cudaSuccess ? RMSN_OK : RMSN_ECUDA;
+RMSN_API int rmsnorm_fwd_host(const void* x, const void* residual, const void* weight,
+                              const void* bias, void* out, void* residual_out, float* out_scale,
+                              int64_t n_tokens, int64_t hidden, float eps, uint32_t flags,
+                              float weight_offset, cudaStream_t stream) {
+    Problem p{};
+    int st = validate(x, residual, weight, bias, out, residual_out, out_scale, n_tokens, hidden,
+                      eps, flags, weight_offset, &p);
+    if (st != RMSN_OK || n_tokens == 0) return st;
+    DeviceInfo* d = device_info();
+    if (!d) return RMSN_ECUDA;
+    const void* dx;
+    const void* dr;
+    const void* dw;
+    const void* db;
+    const void* dout;
+    const void* dres;
+    const void* dscale;
+    if (!device_view(d, x, &dx) || !device_view(d, residual, &dr) ||
+        !device_view(d, weight, &dw) || !device_view(d, bias, &db) ||
+        !device_view(d, out, &dout) || !device_view(d, residual_out, &dres) ||
+        !device_view(d, out_scale, &dscale))
+        return RMSN_EINVAL;
+    // the mapped addresses decide the vector path
+    const void* ins[] = {dx, dr, dw, db, dres};
+    p.vec_ok = vector_path_ok(p, ins, 5, dout);
+    p.nvec = p.vec_ok ? (int)(p.H / p.ve) : 0;
+    rmsn_config c;
+    if (!select_host(p, d, &c)) return RMSN_EUNSUPPORTED;
+    const KernelEntry* e = find_kernel(p, c.variant, c.chunks, c.max_warps);
+    if (!e) return RMSN_EUNSUPPORTED;
+    return launch(e, c, d, p, dx, dr, dw, db, const_cast<void*>(dout),
+                  const_cast<void*>(dres), static_cast<float*>(const_cast<void*>(dscale)), eps,
+                  weight_offset, stream);
 }
 
 RMSN_API int rmsnorm_fwd(const void* x, const void* residual, const void* weight,
