@@ -11,8 +11,9 @@ residual_out and y.  Prints ONE JSON line on rank 0:
   roofline   the kernel's average launch duration (CUDA events on its stream)
              against the measured HBM copy peak
   decode     us per call at decode sizes (T in {1,8,32,128,256}, H 4096):
-             L2-hot back-to-back and CUDA-graph replay, next to the measured
-             empty-kernel launch time
+             L2-hot back-to-back, CUDA-graph replay, and graph replay of
+             programmatic-dependent launches, next to the measured empty-kernel
+             launch time
   cpu_baseline  the CPU oracle on the host cores (rank 0, N = 1)
 
 --impl reference times the CPU oracle instead (the only reference of this
@@ -437,15 +438,20 @@ def run_decode(pkg, synth, dev, stream):
         ptrs = (x.data_ptr(), r.data_ptr(), w.data_ptr(), None, out.data_ptr(), ro.data_ptr(),
                 None)
 
-        def call():
-            st = pkg.rmsnorm_fwd(*ptrs, T, 4096, wl.eps, flags, torch.cuda.current_stream().cuda_stream)
+        def call(fl=flags):
+            st = pkg.rmsnorm_fwd(*ptrs, T, 4096, wl.eps, fl, torch.cuda.current_stream().cuda_stream)
             if st != pkg.RMSN_OK:
                 raise pkg.RmsnError(st, "rmsnorm_fwd")
 
+        def call_pdl():
+            call(flags | pkg.RMSN_PDL | pkg.RMSN_PDL_EARLY_PARAMS)
+
         us = timeit(call, n)
         gus = graph_time(call)
+        gus_pdl = graph_time(call_pdl)
         cfg = pkg.rmsnorm_query_config(T, 4096, flags)
         per_t[str(T)] = {"us": round(us, 3), "graph_us": round(gus, 3),
+                         "graph_pdl_us": round(gus_pdl, 3),
                          "gbs_l2_hot": round(wl.algorithmic_bytes() / (us * 1e-6) / 1e9, 1),
                          "launch": f"{pkg.VARIANT_NAMES[cfg.variant]} ch{cfg.chunks} "
                                    f"w{cfg.warps_per_block} grid{cfg.grid}"}
@@ -454,6 +460,8 @@ def run_decode(pkg, synth, dev, stream):
     res["within_2x_launch"] = all(v["us"] <= 2 * res["empty_kernel_us"] for v in per_t.values())
     res["within_2x_launch_graph"] = all(v["graph_us"] <= 2 * res["empty_kernel_graph_us"]
                                         for v in per_t.values())
+    res["within_2x_launch_graph_pdl"] = all(v["graph_pdl_us"] <= 2 * res["empty_kernel_graph_us"]
+                                            for v in per_t.values())
     return res
 
 

@@ -60,6 +60,15 @@ typedef enum {
 #define RMSN_HAS_RESIDUAL 0x10u /* residual and residual_out */
 #define RMSN_HAS_WEIGHT 0x20u   /* weight (else 1) */
 #define RMSN_HAS_BIAS 0x40u     /* bias (else 0) */
+/* launch options (blog section "Grid synchronisation": programmatic dependent
+ * launch cuts the launch overhead of chained kernels) */
+#define RMSN_PDL 0x80u /* launch with programmatic stream serialization: the kernel
+                          may start while the preceding kernel in the stream still
+                          runs, and waits for it (and its memory) before reading
+                          any input; it lets its own successor start at once */
+#define RMSN_PDL_EARLY_PARAMS 0x100u /* with RMSN_PDL: weight and bias are not written
+                                        by the preceding kernel and may be read
+                                        before it ends */
 
 /* kernel variants */
 typedef enum {

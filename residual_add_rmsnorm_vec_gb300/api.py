@@ -16,8 +16,13 @@ _OUT = {"f32": (_lib.RMSN_OUT_F32, torch.float32), "bf16": (_lib.RMSN_OUT_BF16, 
 _DT_NAME = {torch.float32: "f32", torch.bfloat16: "bf16"}
 
 
-def make_flags(in_dtype: str, out_dtype: str, residual: bool, weight: bool, bias: bool) -> int:
+def make_flags(in_dtype: str, out_dtype: str, residual: bool, weight: bool, bias: bool,
+               pdl: bool = False, early_params: bool = False) -> int:
     f = {"f32": _lib.RMSN_IN_F32, "bf16": _lib.RMSN_IN_BF16}[in_dtype]
+    if pdl:
+        f |= _lib.RMSN_PDL
+    if early_params:
+        f |= _lib.RMSN_PDL_EARLY_PARAMS
     f |= _OUT[out_dtype][0]
     if residual:
         f |= _lib.RMSN_HAS_RESIDUAL
@@ -37,13 +42,16 @@ def fused_add_rmsnorm(x: torch.Tensor, residual: torch.Tensor | None = None,
                       eps: float, out_dtype: str | None = None, weight_offset: float = 0.0,
                       out: torch.Tensor | None = None, residual_out: torch.Tensor | None = None,
                       out_scale: torch.Tensor | None = None, config: _lib.RmsnConfig | None = None,
-                      stream: torch.cuda.Stream | None = None):
+                      stream: torch.cuda.Stream | None = None, pdl: bool = False,
+                      early_params: bool = False):
     """Fused residual-add + RMSNorm of x[T, H] on the GPU.
 
     Returns ``(out, residual_out, out_scale)``; ``residual_out`` is None
     without a residual, ``out_scale`` is None unless ``out_dtype == "fp8"``
     (``out`` then holds E4M3 codes as uint8).  Tensors must be contiguous and
-    on the same CUDA device; weight and bias are [H] of x's dtype.
+    on the same CUDA device; weight and bias are [H] of x's dtype.  ``pdl``
+    launches with programmatic dependent launch (``early_params``: weight and
+    bias are not written by the preceding kernel).
     """
     if x.dim() != 2:
         raise ValueError("x must be [n_tokens, hidden]")
@@ -64,7 +72,7 @@ def fused_add_rmsnorm(x: torch.Tensor, residual: torch.Tensor | None = None,
     if out_dtype == "fp8" and out_scale is None:
         out_scale = torch.empty((T,), dtype=torch.float32, device=x.device)
     flags = make_flags(in_name, out_dtype, residual is not None, weight is not None,
-                       bias is not None)
+                       bias is not None, pdl, early_params)
     s = stream if stream is not None else torch.cuda.current_stream(x.device)
     st = _lib.rmsnorm_fwd_ex(_ptr(x.contiguous()), _ptr(residual), _ptr(weight), _ptr(bias),
                              _ptr(out), _ptr(residual_out), _ptr(out_scale), T, H, eps, flags,

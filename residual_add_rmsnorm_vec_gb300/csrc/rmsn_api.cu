@@ -119,6 +119,7 @@ struct Problem {
     int64_t T, H;
     int in_dt, out_dt;
     bool res, bias;
+    bool pdl, early_params;  // launch options
     int in_bytes, out_bytes;
     int ve;     // elements per 32-byte vector
     int nvec;   // vectors per row (valid when vec_ok)
@@ -131,7 +132,7 @@ bool aligned(const void* p, uintptr_t a) { return p == nullptr || (reinterpret_c
 
 int decode_flags(uint32_t flags, Problem* p) {
     const uint32_t known = RMSN_IN_MASK | RMSN_OUT_MASK | RMSN_HAS_RESIDUAL | RMSN_HAS_WEIGHT |
-                           RMSN_HAS_BIAS;
+                           RMSN_HAS_BIAS | RMSN_PDL | RMSN_PDL_EARLY_PARAMS;
     if (flags & ~known) return RMSN_EINVAL;
     const uint32_t in = flags & RMSN_IN_MASK, out = flags & RMSN_OUT_MASK;
     if (in == RMSN_IN_F32) p->in_dt = kF32;
@@ -141,6 +142,9 @@ int decode_flags(uint32_t flags, Problem* p) {
     else if (out == RMSN_OUT_BF16) p->out_dt = kBF16;
     else if (out == RMSN_OUT_FP8E4M3) p->out_dt = kFP8;
     else return RMSN_EINVAL;
+    if ((flags & RMSN_PDL_EARLY_PARAMS) && !(flags & RMSN_PDL)) return RMSN_EINVAL;
+    p->pdl = (flags & RMSN_PDL) != 0;
+    p->early_params = (flags & RMSN_PDL_EARLY_PARAMS) != 0;
     p->res = (flags & RMSN_HAS_RESIDUAL) != 0;
     p->bias = (flags & RMSN_HAS_BIAS) != 0;
     p->in_bytes = dtype_bytes(p->in_dt);
@@ -358,11 +362,29 @@ int launch(const KernelEntry* e, const rmsn_config& c, DeviceInfo* d, const Prob
     a.woff = weight_offset;
     a.has_w = weight != nullptr;
     a.stages = c.stages;
+    a.early_params = p.early_params ? 1 : 0;
     a.status = d->status;
     void* args[] = {&a};
-    const cudaError_t err = cudaLaunchKernel(e->fn, dim3((unsigned)c.grid),
-                                             dim3((unsigned)(c.warps_per_block * 32)), args,
-                                             (size_t)c.smem_bytes, stream);
+    cudaError_t err;
+    if (p.pdl) {
+        // programmatic dependent launch: the kernel may start while the
+        // preceding kernel in `stream` runs; it waits for it before reading
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3((unsigned)c.grid);
+        lc.blockDim = dim3((unsigned)(c.warps_per_block * 32));
+        lc.dynamicSmemBytes = (size_t)c.smem_bytes;
+        lc.stream = stream;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        err = cudaLaunchKernelExC(&lc, e->fn, args);
+    } else {
+        err = cudaLaunchKernel(e->fn, dim3((unsigned)c.grid),
+                               dim3((unsigned)(c.warps_per_block * 32)), args,
+                               (size_t)c.smem_bytes, stream);
+    }
     return err == cudaSuccess ? RMSN_OK : RMSN_ECUDA;
 }
 

@@ -63,7 +63,8 @@ BF16_RES = 0x1 | 0x4 | 0x10 | 0x20  # bf16 in/out, residual, weight
 
 @pytest.mark.parametrize("case", [
     # (x, r, w, b, out, res_out, scale, T, H, eps, flags)
-    ("unknown flag bit", (16, 16, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES | 0x80)),
+    ("unknown flag bit", (16, 16, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES | 0x200)),
+    ("early params without pdl", (16, 16, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES | 0x100)),
     ("bad input dtype", (16, 16, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES | 0x2)),
     ("bad output dtype", (16, 16, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES | 0xC)),
     ("residual flag without pointer", (16, None, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES)),

@@ -1,0 +1,86 @@
+"""Programmatic dependent launch (RMSN_PDL): chained calls where each call
+reads what the previous one wrote (y and residual_out feed the next call's
+x and residual, as consecutive norms of a layer stack do).  With PDL the next
+kernel may start before the previous one ends, so a missing wait would read
+stale rows; the chain must be bit-identical to the chain launched without
+PDL (same launch shapes), eagerly and in a CUDA graph, and its first call
+must match the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import parity
+from residual_add_rmsnorm_vec_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from residual_add_rmsnorm_vec_gb300 import build
+
+    build.build()
+    import residual_add_rmsnorm_vec_gb300 as p
+
+    torch.cuda.set_device(0)
+    return p
+
+
+def chain(pkg, inp, eps, n, pdl, early, graph=False):
+    x0 = inp["x"].cuda()
+    r0 = inp["residual"].cuda()
+    w = inp["weight"].cuda()
+    T, H = x0.shape
+    xs = [x0] + [torch.empty_like(x0) for _ in range(n)]
+    rs = [r0] + [torch.empty_like(x0) for _ in range(n)]
+
+    def run():
+        for k in range(n):
+            pkg.fused_add_rmsnorm(xs[k], rs[k], w, None, eps=eps, out=xs[k + 1],
+                                  residual_out=rs[k + 1], pdl=pdl, early_params=early)
+
+    if graph:
+        run()  # warm the launch-shape caches before capture
+        torch.cuda.synchronize()
+        for t in xs[1:] + rs[1:]:
+            t.zero_()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                run()
+        torch.cuda.current_stream().wait_stream(s)
+        g.replay()
+    else:
+        run()
+    torch.cuda.synchronize()
+    return [parity.bits16(t) for t in xs[1:] + rs[1:]]
+
+
+@pytest.mark.parametrize("T,H", [(1, 4096), (8, 4096), (256, 4096), (2048, 8192), (37, 1000)])
+@pytest.mark.parametrize("early", [False, True])
+def test_pdl_chain_matches_plain_chain(pkg, T, H, early):
+    wl = synth.Workload(f"pdl_T{T}_H{H}", T, H, 21, "bf16", "bf16", 1e-6)
+    inp = synth.make_inputs(wl)
+    n = 6
+    ref = chain(pkg, inp, wl.eps, n, pdl=False, early=False)
+    for graph in (False, True):
+        got = chain(pkg, inp, wl.eps, n, pdl=True, early=early, graph=graph)
+        for k, (a, b) in enumerate(zip(got, ref)):
+            assert np.array_equal(a, b), (graph, k)
+    # first link of the chain against the oracle
+    o = parity.oracle_run(wl, inp)
+    got = {"out": ref[0], "residual_out": ref[n], "out_scale": None}
+    parity.compare(wl, got, o, "pdl chain first call")
+    assert pkg.rmsnorm_read_status() == 0
+
+
+def test_early_params_needs_pdl(pkg):
+    x = torch.zeros((4, 64), dtype=torch.bfloat16, device="cuda")
+    flags = pkg.make_flags("bf16", "bf16", False, False, False) | pkg.RMSN_PDL_EARLY_PARAMS
+    st = pkg.rmsnorm_fwd(x.data_ptr(), None, None, None, x.data_ptr(), None, None, 4, 64, 1e-6,
+                         flags, torch.cuda.current_stream().cuda_stream)
+    assert st == pkg.RMSN_EINVAL
