@@ -66,6 +66,9 @@ class Oracle:
         lib.oracle_e4m3_to_f64.restype = ctypes.c_double
         lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
         lib.oracle_num_cpus.restype = ctypes.c_int
+        lib.oracle_qk_norm.restype = ctypes.c_int
+        lib.oracle_qk_norm.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                       ctypes.c_double, ctypes.c_double, ctypes.c_int]
         self.lib = lib
         self.path = path
 
@@ -83,6 +86,29 @@ class Oracle:
 
     def e4m3_to_f64(self, c: int) -> float:
         return float(self.lib.oracle_e4m3_to_f64(int(c)))
+
+    def qk_norm(self, q, k, q_weight=None, k_weight=None, *, n_q_heads: int, n_k_heads: int,
+                head_dim: int, eps: float, dtype: str, weight_offset: float = 0.0):
+        """Per-head norm of q [T, q_stride] and k [T, k_stride] (copies are
+        returned; the inputs are not modified).  Row t of q holds its n_q_heads
+        heads of head_dim elements at the start of the row."""
+        qb = None if q is None else _host_bits(q, dtype).copy()
+        kb = None if k is None else _host_bits(k, dtype).copy()
+        T = (qb if qb is not None else kb).shape[0]
+        qs = qb.shape[1] if qb is not None else 0
+        ks = kb.shape[1] if kb is not None else 0
+        wq = None if q_weight is None else _host_bits(q_weight, dtype)
+        wk = None if k_weight is None else _host_bits(k_weight, dtype)
+
+        def ptr(a):
+            return None if a is None else a.ctypes.data
+
+        st = self.lib.oracle_qk_norm(ptr(qb), ptr(kb), ptr(wq), ptr(wk), T, n_q_heads,
+                                     n_k_heads, head_dim, qs, ks, float(eps),
+                                     float(weight_offset), _DTYPES[dtype])
+        if st != 0:
+            raise RuntimeError(f"oracle_qk_norm failed with status {st}")
+        return qb, kb
 
     def rmsnorm(self, x, residual=None, weight=None, bias=None, *, eps: float,
                 in_dtype: str, out_dtype: str, weight_offset: float = 0.0,
@@ -176,3 +202,8 @@ def _rmsnorm(lib, x, residual=None, weight=None, bias=None, *, eps: float, in_dt
     if st != 0:
         raise RuntimeError(f"oracle_rmsnorm failed with status {st}")
     return {"out": out, "residual_out": res_out, "out_scale": scale}
+
+
+def qk_norm(q, k, q_weight=None, k_weight=None, **kw):
+    """Per-head QK norm on CPU copies; see ``Oracle.qk_norm``."""
+    return default().qk_norm(q, k, q_weight, k_weight, **kw)

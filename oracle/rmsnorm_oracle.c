@@ -299,3 +299,52 @@ int oracle_rmsnorm(const void *x, const void *residual, const void *weight, cons
     free(tids);
     return status;
 }
+
+/* ------------------------------------------------------------------ */
+/* QK norm                                                             */
+/*
+ * Per-head RMS norm of the query and key heads (blog "CuTeDSL at
+ * Perplexity", section "QK norm"): every head vector of length head_dim is
+ * normalised on its own, with the query weight for query heads and the key
+ * weight for key heads, the scalar WEIGHT_BIAS (weight_offset) added to the
+ * weight, and the result cast back to the element type IN PLACE.
+ *
+ * q holds n_tokens rows of n_q_heads * head_dim elements, row t starting at
+ * element t * q_token_stride (likewise k); elements between the heads of a
+ * row and the next row start are not touched.  Weights are [head_dim] or
+ * NULL (1).  Per head, in fp64, rounded once:
+ *   inv = 1 / sqrt(sum_j x_j^2 / head_dim + eps);  x_j <- RN((w_j + off) * (x_j * inv))
+ */
+static void qk_head(void *base, int dtype, int64_t off0, int64_t head_dim, const void *w,
+                    double eps, double woff) {
+    double ss = 0.0;
+    for (int64_t j = 0; j < head_dim; ++j) {
+        double v = load_in(base, dtype, off0 + j);
+        ss += v * v;
+    }
+    const double inv = 1.0 / sqrt(ss / (double)head_dim + eps);
+    for (int64_t j = 0; j < head_dim; ++j) {
+        double v = load_in(base, dtype, off0 + j);
+        double wj = w ? load_in(w, dtype, j) : 1.0;
+        round_store_in(base, dtype, off0 + j, (wj + woff) * (v * inv));
+    }
+}
+
+int oracle_qk_norm(void *q, void *k, const void *q_weight, const void *k_weight,
+                   int64_t n_tokens, int64_t n_q_heads, int64_t n_k_heads, int64_t head_dim,
+                   int64_t q_token_stride, int64_t k_token_stride, double eps,
+                   double weight_offset, int dtype) {
+    if (n_tokens < 0 || n_q_heads < 0 || n_k_heads < 0 || head_dim <= 0) return -1;
+    if (dtype != ORC_F32 && dtype != ORC_BF16) return -1;
+    if (q_token_stride < n_q_heads * head_dim || k_token_stride < n_k_heads * head_dim) return -1;
+    if ((n_q_heads && !q) || (n_k_heads && !k)) return -1;
+    for (int64_t t = 0; t < n_tokens; ++t) {
+        for (int64_t h = 0; h < n_q_heads; ++h)
+            qk_head(q, dtype, t * q_token_stride + h * head_dim, head_dim, q_weight, eps,
+                    weight_offset);
+        for (int64_t h = 0; h < n_k_heads; ++h)
+            qk_head(k, dtype, t * k_token_stride + h * head_dim, head_dim, k_weight, eps,
+                    weight_offset);
+    }
+    return 0;
+}

@@ -394,6 +394,79 @@ def test_threads_do_not_change_results_and_empty_input(oracle_mod):
     assert e["out"].shape == (0, 16)
 
 
+# ---------------------------------------------------------------- QK norm
+
+
+def test_qk_norm_equals_row_norm_of_heads(oracle_mod):
+    # a contiguous [T, heads * D] q is the row norm of its [T * heads, D] view
+    _check_qk_equals_rows(oracle_mod.default())
+
+
+def _check_qk_equals_rows(orc):
+    rng = np.random.default_rng(40)
+    T, Hq, Hk, D = 5, 4, 2, 64
+    q = bf16_tensor(rng.standard_normal((T, Hq * D)))
+    k = bf16_tensor(rng.standard_normal((T, Hk * D)) * 3)
+    wq = bf16_tensor(1 + 0.1 * rng.standard_normal(D))
+    wk = bf16_tensor(1 + 0.2 * rng.standard_normal(D))
+    qo, ko = orc.qk_norm(q, k, wq, wk, n_q_heads=Hq, n_k_heads=Hk, head_dim=D, eps=1e-6,
+                         dtype="bf16", weight_offset=0.5)
+    rq = orc.rmsnorm(q.reshape(T * Hq, D), None, wq, None, eps=1e-6, in_dtype="bf16",
+                     out_dtype="bf16", weight_offset=0.5)["out"]
+    rk = orc.rmsnorm(k.reshape(T * Hk, D), None, wk, None, eps=1e-6, in_dtype="bf16",
+                     out_dtype="bf16", weight_offset=0.5)["out"]
+    assert np.array_equal(qo.reshape(T * Hq, D), rq)
+    assert np.array_equal(ko.reshape(T * Hk, D), rk)
+
+
+def _check_qk_constant_heads(orc):
+    # constant head c: every element becomes (w_j + off) * c / sqrt(c^2 + eps),
+    # with the query weight on query heads and the key weight on key heads
+    D, c, eps, off = 16, 0.25, 0.0625, 0.5
+    wq = bf16_tensor(np.linspace(0.5, 2.0, D))
+    wk = bf16_tensor(np.linspace(-1.0, 1.0, D))
+    q = bf16_tensor(np.full((2, 3 * D), c))
+    k = bf16_tensor(np.full((2, 1 * D), -c))
+    qo, ko = orc.qk_norm(q, k, wq, wk, n_q_heads=3, n_k_heads=1, head_dim=D, eps=eps,
+                         dtype="bf16", weight_offset=off)
+    want_q = torch.from_numpy((wq.double().numpy() + off) * c / math.sqrt(c * c + eps)).to(
+        torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    want_k = torch.from_numpy((wk.double().numpy() + off) * -c / math.sqrt(c * c + eps)).to(
+        torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(qo.reshape(-1, D), np.tile(want_q, (6, 1)))
+    assert np.array_equal(ko.reshape(-1, D), np.tile(want_k, (2, 1)))
+
+
+def _check_qk_strided_fused_qkv(orc):
+    # q and k inside a fused [T, (Hq + 2 Hk) * D + pad] qkv buffer: heads are
+    # normalised like the contiguous case; v and the row padding are untouched
+    rng = np.random.default_rng(41)
+    T, Hq, Hk, D, pad = 3, 2, 1, 32, 16
+    S = (Hq + 2 * Hk) * D + pad
+    qkv = bf16_tensor(rng.standard_normal((T, S)))
+    wq = bf16_tensor(1 + 0.1 * rng.standard_normal(D))
+    wk = bf16_tensor(1 + 0.1 * rng.standard_normal(D))
+    qo, _ = orc.qk_norm(qkv, None, wq, None, n_q_heads=Hq, n_k_heads=0, head_dim=D,
+                        eps=1e-6, dtype="bf16")
+    _, ko = orc.qk_norm(None, qkv[:, Hq * D:].contiguous(), None, wk, n_q_heads=0,
+                        n_k_heads=Hk, head_dim=D, eps=1e-6, dtype="bf16")
+    cq, ck = orc.qk_norm(qkv[:, :Hq * D].contiguous(), qkv[:, Hq * D:(Hq + Hk) * D].contiguous(),
+                         wq, wk, n_q_heads=Hq, n_k_heads=Hk, head_dim=D, eps=1e-6, dtype="bf16")
+    bits = qkv.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(qo[:, :Hq * D], cq)
+    assert np.array_equal(qo[:, Hq * D:], bits[:, Hq * D:])
+    assert np.array_equal(ko[:, :Hk * D], ck)
+    assert np.array_equal(ko[:, Hk * D:], bits[:, (Hq + Hk) * D:])
+
+
+def test_qk_norm_constant_heads(oracle_mod):
+    _check_qk_constant_heads(oracle_mod.default())
+
+
+def test_qk_norm_strided_fused_qkv(oracle_mod):
+    _check_qk_strided_fused_qkv(oracle_mod.default())
+
+
 # ---------------------------------------------------------------- mutants
 
 # Each mutant plants one plausible mistake in the oracle's C source: a dropped
@@ -414,6 +487,9 @@ MUTANTS = {
     "fp8_max_240": ("a / 448.0", "a / 240.0"),
     "bf16_truncates": ("r = round_to_quantum(a, q);\n        const double maxf",
                        "r = ldexp(floor(ldexp(a, -q)), q);\n        const double maxf"),
+    "qk_weights_swapped": ("k_weight, eps,\n                    weight_offset);",
+                           "q_weight, eps,\n                    weight_offset);"),
+    "qk_divisor_off_by_one": ("ss / (double)head_dim + eps", "ss / (double)(head_dim - 1) + eps"),
     "e4m3_ties_up": ("r = round_to_quantum(a, q);\n        if (r > 448.0)",
                      "r = ldexp(floor(ldexp(a, -q) + 0.5), q);\n        if (r > 448.0)"),
 }
@@ -434,6 +510,9 @@ def all_pin_checks(orc):
     for c, eps in ((2.0**-10, 1e-6), (0.75, 0.5), (-3.5, 0.0)):
         checks.append(lambda c=c, eps=eps: test_constant_row_closed_form(orc, c, eps))
     checks.append(lambda: test_brute_force_tiny_rows_exact_rational(orc))
+    checks.append(lambda: _check_qk_equals_rows(orc))
+    checks.append(lambda: _check_qk_constant_heads(orc))
+    checks.append(lambda: _check_qk_strided_fused_qkv(orc))
     failed = 0
     for chk in checks:
         try:
