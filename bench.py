@@ -14,6 +14,8 @@ residual_out and y.  Prints ONE JSON line on rank 0:
              L2-hot back-to-back, CUDA-graph replay, and graph replay of
              programmatic-dependent launches, next to the measured empty-kernel
              launch time
+  qk_norm    per-head QK norm (one launch, fused qkv, in place) against the
+             row norm on the head views (two launches), us per call
   cpu_baseline  the CPU oracle on the host cores (rank 0, N = 1)
 
 --impl reference times the CPU oracle instead (the only reference of this
@@ -261,6 +263,7 @@ def run_ours(args):
     e2e = run_e2e(pkg, wl, host, dev, stream, flags, max(3, min(K, args.e2e_steps)), pg)
 
     decode = None if args.skip_decode else run_decode(pkg, synth, dev, stream)
+    qk = None if args.skip_decode else run_qk(pkg, synth, dev, stream)
 
     peak, peak_src = load_peaks()
     achieved = bytes_step / (kernel_ms / 1e3) / 1e9
@@ -298,6 +301,8 @@ def run_ours(args):
     }
     if decode is not None:
         line["decode"] = decode
+    if qk is not None:
+        line["qk_norm"] = qk
     if rank == 0 and world == 1 and not args.skip_cpu:
         line["cpu_baseline"] = run_cpu_baseline(wl, host, args.cpu_seconds)
     if rank == 0:
@@ -463,6 +468,68 @@ def run_decode(pkg, synth, dev, stream):
     res["within_2x_launch_graph_pdl"] = all(v["graph_pdl_us"] <= 2 * res["empty_kernel_graph_us"]
                                             for v in per_t.values())
     return res
+
+
+def run_qk(pkg, synth, dev, stream):
+    """QK norm (per-head, in place) on Qwen3-8B-like heads (32 query, 8 key,
+    head_dim 128, bf16): one rmsnorm_qk_fwd launch on a fused qkv buffer
+    against the regular row norm applied to the query and key head views
+    (two rmsnorm_fwd launches).  CUDA-graph replay, us per call."""
+    import torch
+
+    Hq, Hk, D = 32, 8, 128
+    out = {"heads": f"{Hq} q + {Hk} k heads x {D}, bf16", "unit": "us/call"}
+    for T in (1, 64, 4096):
+        inp = synth.qk_inputs(T, Hq, Hk, D, "bf16")
+        qkv = inp["qkv"].to(dev)
+        wq, wk = inp["q_weight"].to(dev), inp["k_weight"].to(dev)
+        q = qkv[:, :Hq * D]
+        k = qkv[:, Hq * D:(Hq + Hk) * D]
+        qc = q.contiguous()
+        kc = k.contiguous()
+        fl = pkg.make_flags("bf16", "bf16", False, True, False)
+
+        def qk_call():
+            pkg.qk_norm_(q, k, wq, wk, head_dim=D, eps=1e-6)
+
+        def rows_call():
+            s = torch.cuda.current_stream().cuda_stream
+            for t, w, h in ((qc, wq, Hq), (kc, wk, Hk)):
+                st = pkg.rmsnorm_fwd(t.data_ptr(), None, w.data_ptr(), None, t.data_ptr(), None,
+                                     None, T * h, D, 1e-6, fl, s)
+                if st != pkg.RMSN_OK:
+                    raise pkg.RmsnError(st, "rmsnorm_fwd")
+
+        def graph_us(fn, per_graph=50, replays=10):
+            fn()
+            torch.cuda.synchronize(dev)
+            g = torch.cuda.CUDAGraph()
+            s = torch.cuda.Stream(dev)
+            s.wait_stream(stream)
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s):
+                    for _ in range(per_graph):
+                        fn()
+            stream.wait_stream(s)
+            g.replay()
+            torch.cuda.synchronize(dev)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(replays):
+                g.replay()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            return a.elapsed_time(b) * 1e3 / (replays * per_graph)
+
+        nbytes = 2 * T * (Hq + Hk) * D * 2 + 2 * D * 2
+        us_qk = graph_us(qk_call)
+        us_rows = graph_us(rows_call)
+        out[f"T{T}"] = {"qk_us": round(us_qk, 3), "qk_gbs": round(nbytes / us_qk / 1e3, 1),
+                        "row_norm_us": round(us_rows, 3),
+                        "row_norm_gbs": round(nbytes / us_rows / 1e3, 1),
+                        "speedup": round(us_rows / us_qk, 2)}
+    return out
 
 
 def run_cpu_baseline(wl, host, seconds: float) -> dict:

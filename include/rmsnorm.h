@@ -151,6 +151,30 @@ int rmsnorm_fwd_host(const void* x, const void* residual, const void* weight, co
                      cudaStream_t stream);
 
 /*
+ * QK norm (blog "CuTeDSL at Perplexity", section "QK norm"): per-head RMS
+ * norm of query and key heads, IN PLACE.  Every head of head_dim elements is
+ * normalised on its own:
+ *
+ *   inv = rsqrt(sum(x^2) / head_dim + eps);  x <- RN((w + weight_offset) * (x * inv))
+ *
+ * with w = q_weight[head_dim] for query heads and k_weight[head_dim] for key
+ * heads (NULL = 1).  Token t's query heads start at element t * q_token_stride
+ * of q (n_q_heads heads of head_dim elements, back to back); likewise k.  The
+ * strides let q and k sit inside a fused qkv row; elements outside the heads
+ * are not touched.  The q buffer must span (n_tokens - 1) * q_token_stride +
+ * n_q_heads * head_dim elements (likewise k).  flags: RMSN_IN_F32 or
+ * RMSN_IN_BF16 (q, k and weights share it), optionally RMSN_PDL.  One launch
+ * covers both q and k.  The fast path needs head_dim * element size to be a
+ * multiple of 32 bytes and at most 1024 bytes (head_dim 64, 128, 256 in bf16
+ * and fp32, 512 in bf16), 32-byte aligned pointers and token strides;
+ * otherwise RMSN_EUNSUPPORTED.  Returns an rmsn_status.
+ */
+int rmsnorm_qk_fwd(void* q, void* k, const void* q_weight, const void* k_weight,
+                   int64_t n_tokens, int64_t n_q_heads, int64_t n_k_heads, int64_t head_dim,
+                   int64_t q_token_stride, int64_t k_token_stride, float eps,
+                   float weight_offset, uint32_t flags, cudaStream_t stream);
+
+/*
  * The configuration rmsnorm_fwd would launch for this shape on the current
  * device, assuming 32-byte aligned pointers.  Returns an rmsn_status.
  */

@@ -18,6 +18,7 @@ from ._lib import (  # noqa: F401
     RMSN_PDL, RMSN_PDL_EARLY_PARAMS,
     RMSN_OUT_F32, RMSN_OUT_FP8E4M3, VARIANT_BLOCK_ROW, VARIANT_BULK_ROW, VARIANT_GENERIC,
     VARIANT_NAMES, VARIANT_WARP_ROWS, RmsnConfig, RmsnError, library_path, load,
-    rmsnorm_fwd, rmsnorm_fwd_ex, rmsnorm_fwd_host, rmsnorm_list_configs, rmsnorm_query_config,
+    rmsnorm_fwd, rmsnorm_fwd_ex, rmsnorm_fwd_host, rmsnorm_list_configs, rmsnorm_qk_fwd,
+    rmsnorm_query_config,
     rmsnorm_read_status, status_string)
-from .api import fused_add_rmsnorm, fused_add_rmsnorm_host, make_flags  # noqa: F401
+from .api import fused_add_rmsnorm, fused_add_rmsnorm_host, make_flags, qk_norm_  # noqa: F401

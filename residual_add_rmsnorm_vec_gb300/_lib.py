@@ -35,8 +35,9 @@ VARIANT_BULK_ROW = 2
 VARIANT_GENERIC = 3
 VARIANT_NAMES = {0: "warp_rows", 1: "block_row", 2: "bulk_row", 3: "generic"}
 
-EXPORTED = ("rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_fwd_host", "rmsnorm_query_config",
-            "rmsnorm_list_configs", "rmsnorm_read_status", "rmsnorm_status_string")
+EXPORTED = ("rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_fwd_host", "rmsnorm_qk_fwd",
+            "rmsnorm_query_config", "rmsnorm_list_configs", "rmsnorm_read_status",
+            "rmsnorm_status_string")
 
 
 class RmsnConfig(ctypes.Structure):
@@ -92,6 +93,9 @@ def load() -> ctypes.CDLL:
             lib.rmsnorm_fwd_host.restype = ctypes.c_int
             lib.rmsnorm_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, f32, u32, f32,
                                              vp]
+            lib.rmsnorm_qk_fwd.restype = ctypes.c_int
+            lib.rmsnorm_qk_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, f32,
+                                           u32, vp]
             lib.rmsnorm_query_config.restype = ctypes.c_int
             lib.rmsnorm_query_config.argtypes = [i64, i64, u32, ctypes.POINTER(RmsnConfig)]
             lib.rmsnorm_list_configs.restype = ctypes.c_int
@@ -132,6 +136,16 @@ def rmsnorm_fwd_host(x, residual, weight, bias, out, residual_out, out_scale, n_
     return int(load().rmsnorm_fwd_host(x, residual, weight, bias, out, residual_out, out_scale,
                                        int(n_tokens), int(hidden), float(eps), int(flags),
                                        float(weight_offset), stream))
+
+
+def rmsnorm_qk_fwd(q, k, q_weight, k_weight, n_tokens: int, n_q_heads: int, n_k_heads: int,
+                   head_dim: int, q_token_stride: int, k_token_stride: int, eps: float,
+                   weight_offset: float, flags: int, stream) -> int:
+    """Direct call of ``rmsnorm_qk_fwd`` (in place on q and k)."""
+    return int(load().rmsnorm_qk_fwd(q, k, q_weight, k_weight, int(n_tokens), int(n_q_heads),
+                                     int(n_k_heads), int(head_dim), int(q_token_stride),
+                                     int(k_token_stride), float(eps), float(weight_offset),
+                                     int(flags), stream))
 
 
 def rmsnorm_query_config(n_tokens: int, hidden: int, flags: int) -> RmsnConfig:

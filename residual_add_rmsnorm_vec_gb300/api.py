@@ -126,3 +126,43 @@ def fused_add_rmsnorm_host(x: torch.Tensor, residual: torch.Tensor | None = None
     if st != _lib.RMSN_OK:
         raise _lib.RmsnError(st, "rmsnorm_fwd_host")
     return out, residual_out, (out_scale if out_dtype == "fp8" else None)
+
+
+def qk_norm_(q: torch.Tensor | None, k: torch.Tensor | None, q_weight: torch.Tensor | None = None,
+             k_weight: torch.Tensor | None = None, *, head_dim: int, eps: float,
+             weight_offset: float = 0.0, stream: torch.cuda.Stream | None = None,
+             pdl: bool = False):
+    """Per-head QK norm of q and k IN PLACE (``rmsnorm_qk_fwd``).
+
+    q is [T, Hq * head_dim] or [T, Hq, head_dim], or a column slice of a
+    fused qkv matrix (its row stride is used as the token stride); likewise
+    k.  Either may be None.  Returns (q, k).
+    """
+    def view2d(t):
+        if t is None:
+            return None, 0, 0
+        if t.dim() == 3:
+            t2 = t.reshape(t.shape[0], -1) if t.is_contiguous() else None
+            if t2 is None:
+                raise ValueError("3-D q/k must be contiguous")
+            return t2, t2.shape[1] // head_dim, t2.stride(0)
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError("q/k must be [T, heads*head_dim] with unit column stride")
+        return t, t.shape[1] // head_dim, t.stride(0)
+
+    q2, hq, qs = view2d(q)
+    k2, hk, ks = view2d(k)
+    ref = q2 if q2 is not None else k2
+    if ref is None:
+        return q, k
+    if q2 is not None and k2 is not None and q2.shape[0] != k2.shape[0]:
+        raise ValueError("q and k need the same number of tokens")
+    if ref.dtype not in _IN:
+        raise TypeError(f"unsupported dtype {ref.dtype}")
+    flags = _IN[ref.dtype] | (_lib.RMSN_PDL if pdl else 0)
+    s = stream if stream is not None else torch.cuda.current_stream(ref.device)
+    st = _lib.rmsnorm_qk_fwd(_ptr(q2), _ptr(k2), _ptr(q_weight), _ptr(k_weight), ref.shape[0],
+                             hq, hk, head_dim, qs, ks, eps, weight_offset, flags, s.cuda_stream)
+    if st != _lib.RMSN_OK:
+        raise _lib.RmsnError(st, "rmsnorm_qk_fwd")
+    return q, k

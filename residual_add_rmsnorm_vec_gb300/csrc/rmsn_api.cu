@@ -23,6 +23,7 @@
 #include <vector>
 
 #include "../../include/rmsnorm.h"
+#include "rmsn_qk.h"
 #include "rmsn_registry.h"
 
 #define RMSN_API extern "C" __attribute__((visibility("default")))
@@ -362,6 +363,7 @@ int launch(const KernelEntry* e, const rmsn_config& c, DeviceInfo* d, const Prob
     a.woff = weight_offset;
     a.has_w = weight != nullptr;
     a.stages = c.stages;
+    a.pdl = p.pdl ? 1 : 0;
     a.early_params = p.early_params ? 1 : 0;
     a.status = d->status;
     void* args[] = {&a};
@@ -575,4 +577,85 @@ RMSN_API int rmsnorm_read_status(uint32_t* status, int clear) {
         if (cudaMemset(d->status, 0, sizeof(uint32_t)) != cudaSuccess) return RMSN_ECUDA;
     }
     return RMSN_OK;
+}
+
+RMSN_API int rmsnorm_qk_fwd(void* q, void* k, const void* q_weight, const void* k_weight,
+                            int64_t n_tokens, int64_t n_q_heads, int64_t n_k_heads,
+                            int64_t head_dim, int64_t q_token_stride, int64_t k_token_stride,
+                            float eps, float weight_offset, uint32_t flags, cudaStream_t stream) {
+    if (flags & ~(RMSN_IN_MASK | RMSN_PDL)) return RMSN_EINVAL;
+    const uint32_t in = flags & RMSN_IN_MASK;
+    if (in != RMSN_IN_F32 && in != RMSN_IN_BF16) return RMSN_EINVAL;
+    const int dt = in == RMSN_IN_F32 ? kF32 : kBF16;
+    const int64_t bytes = dt == kF32 ? 4 : 2;
+    if (n_tokens < 0 || n_q_heads < 0 || n_k_heads < 0 || head_dim < 1 || head_dim > 4096)
+        return RMSN_EINVAL;
+    if (n_q_heads > (1 << 20) || n_k_heads > (1 << 20)) return RMSN_EINVAL;
+    if (!(eps >= 0.f) || !isfinite(eps) || !isfinite(weight_offset)) return RMSN_EINVAL;
+    if (n_q_heads && q_token_stride < n_q_heads * head_dim) return RMSN_EINVAL;
+    if (n_k_heads && k_token_stride < n_k_heads * head_dim) return RMSN_EINVAL;
+    const int64_t stride_max = q_token_stride > k_token_stride ? q_token_stride : k_token_stride;
+    if (stride_max > 0 && n_tokens > (INT64_MAX / 8) / stride_max) return RMSN_EINVAL;
+    if (n_tokens == 0 || n_q_heads + n_k_heads == 0) return RMSN_OK;
+    if ((n_q_heads && !q) || (n_k_heads && !k)) return RMSN_EINVAL;
+    const void* ptrs[] = {q, k, q_weight, k_weight};
+    for (const void* p : ptrs)
+        if (!aligned(p, (uintptr_t)bytes)) return RMSN_EALIGN;
+    // every head must start on a 32-byte boundary and be whole 32-byte vectors
+    if ((head_dim * bytes) % 32 != 0 || head_dim * bytes > 32 * 32) return RMSN_EUNSUPPORTED;
+    for (const void* p : ptrs)
+        if (!aligned(p, 32)) return RMSN_EUNSUPPORTED;
+    if ((n_q_heads && (q_token_stride * bytes) % 32) || (n_k_heads && (k_token_stride * bytes) % 32))
+        return RMSN_EUNSUPPORTED;
+
+    DeviceInfo* d = device_info();
+    if (!d) return RMSN_ECUDA;
+    const int nvec = (int)(head_dim * bytes / 32);
+    int tph = 1;
+    while (tph < nvec) tph *= 2;
+    const QkEntry* e = nullptr;
+    int n = 0;
+    const QkEntry* table = qk_kernels(&n);
+    for (int i = 0; i < n; ++i)
+        if (table[i].dt == dt && table[i].tph == tph) e = &table[i];
+    if (!e) return RMSN_EUNSUPPORTED;
+    const int threads = 256;
+    const int64_t heads = (n_q_heads + n_k_heads) * n_tokens;
+    const int64_t need = (heads * tph + threads - 1) / threads;
+    const int bps = blocks_per_sm(d, e->fn, threads, 0);
+    const int64_t resident = (int64_t)d->num_sms * (bps > 0 ? bps : 1);
+    const int64_t grid = need < resident ? need : resident;
+
+    QkArgs a;
+    a.q = q;
+    a.k = k;
+    a.qw = q_weight;
+    a.kw = k_weight;
+    a.T = n_tokens;
+    a.qs = q_token_stride;
+    a.ks = k_token_stride;
+    a.Hq = (int32_t)n_q_heads;
+    a.Hk = (int32_t)n_k_heads;
+    a.D = (int32_t)head_dim;
+    a.nvec = nvec;
+    a.eps = eps;
+    a.woff = weight_offset;
+    a.pdl = (flags & RMSN_PDL) ? 1 : 0;
+    void* args[] = {&a};
+    cudaError_t err;
+    if (flags & RMSN_PDL) {
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3((unsigned)grid);
+        lc.blockDim = dim3(threads);
+        lc.stream = stream;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        err = cudaLaunchKernelExC(&lc, e->fn, args);
+    } else {
+        err = cudaLaunchKernel(e->fn, dim3((unsigned)grid), dim3(threads), args, 0, stream);
+    }
+    return err == cudaSuccess ? RMSN_OK : RMSN_ECUDA;
 }

@@ -127,18 +127,20 @@ __device__ __forceinline__ uint32_t ones_word() {
 }
 
 // ---------------------------------------------------------------- programmatic dependent launch
-// A kernel launched with programmatic stream serialization may start before
-// the preceding kernel in its stream has finished.  Every kernel here lets
+// A kernel launched with programmatic stream serialization (a.pdl) may start
+// before the preceding kernel in its stream has finished.  Such a kernel lets
 // its own dependents start at once, and waits for its prerequisite grid (and
 // that grid's memory) before its first global read of anything the caller
 // did not declare constant (a.early_params: weight and bias may be read
-// first).  Without the launch attribute the wait returns immediately.
+// first).  Kernels launched the ordinary way skip both instructions.
 
-__device__ __forceinline__ void pdl_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+__device__ __forceinline__ void pdl_launch_dependents(int pdl) {
+    if (pdl) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait(int pdl) {
+    if (pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 // ---------------------------------------------------------------- reductions
 
@@ -351,12 +353,12 @@ __global__ void __launch_bounds__(Bounds<WMAX, CH>::kThreads, Bounds<WMAX, CH>::
     int64_t row = WARP_ROWS ? (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)
                             : (int64_t)blockIdx.x;
 
-    pdl_launch_dependents();
-    if (!a.early_params) pdl_wait();
+    pdl_launch_dependents(a.pdl);
+    if (!a.early_params) pdl_wait(a.pdl);
     V8 wv[CH];
     V8 bv[BIAS ? CH : 1];
     load_params<TI, CH>(a, G, t, wv, bv, BIAS);
-    if (a.early_params) pdl_wait();
+    if (a.early_params) pdl_wait(a.pdl);
 
     int parity = 0;
     for (; row < a.T; row += rows_per_step) {
@@ -482,11 +484,11 @@ __global__ void __launch_bounds__(WMAX * 32, 1) rmsn_bulk_kernel(const RmsnArgs 
     // rows of this block: blockIdx.x + k * gridDim.x
     const int64_t n_my = a.T > blockIdx.x ? (a.T - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
-    pdl_launch_dependents();
+    pdl_launch_dependents(a.pdl);
     V8 wv[CH];
     V8 bv[BIAS ? CH : 1];
     if (a.early_params) load_params<TI, CH>(a, G, t, wv, bv, BIAS);
-    pdl_wait();
+    pdl_wait(a.pdl);
     if (t == 0) {
         abort_flag = 0;
         for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
@@ -592,8 +594,8 @@ template <class TI, class TO, bool RES>
 __global__ void __launch_bounds__(256) rmsn_generic_kernel(const RmsnArgs a) {
     __shared__ float red[4][32];
     const int H = a.H;
-    pdl_launch_dependents();
-    pdl_wait();
+    pdl_launch_dependents(a.pdl);
+    pdl_wait(a.pdl);
     int parity = 0;
     for (int64_t row = blockIdx.x; row < a.T; row += gridDim.x) {
         const int64_t base = row * (int64_t)H;

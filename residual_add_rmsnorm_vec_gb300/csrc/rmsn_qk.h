@@ -1,0 +1,32 @@
+// QK-norm kernel table shared by its instantiation unit and the C-ABI layer.
+#pragma once
+
+#include <stdint.h>
+
+namespace rmsn {
+
+// Kernel arguments (by value).  q / k: first element of token 0's first head;
+// qs / ks: token strides in elements; weights [D] or NULL (1).
+struct QkArgs {
+    void* q;
+    void* k;
+    const void* qw;
+    const void* kw;
+    int64_t T;
+    int64_t qs, ks;
+    int32_t Hq, Hk, D;
+    int32_t nvec;  // 32-byte vectors per head
+    float eps;
+    float woff;
+    int32_t pdl;   // launched as a programmatic dependent
+};
+
+struct QkEntry {
+    int32_t dt;   // DType of q, k and the weights
+    int32_t tph;  // lanes per head
+    const void* fn;
+};
+
+const QkEntry* qk_kernels(int* n);
+
+}  // namespace rmsn

@@ -22,6 +22,7 @@ struct RmsnArgs {
     float woff;
     int32_t has_w;
     int32_t stages;      // shared-memory row buffers (bulk kernel)
+    int32_t pdl;           // launched as a programmatic dependent
     int32_t early_params;  // weight / bias may be read before the prerequisite grid ends
     uint32_t* status;    // device status word: bit 0 = a bounded wait ran out
 };

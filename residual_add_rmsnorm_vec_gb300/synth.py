@@ -244,3 +244,17 @@ def sample_rows(n_tokens: int, n: int, seed: int = 12345) -> np.ndarray:
     g = np.random.default_rng(seed)
     mid = g.choice(np.arange(1, n_tokens - 1), size=max(0, n - 2), replace=False)
     return np.unique(np.concatenate([[0, n_tokens - 1], mid]).astype(np.int64))
+
+
+def qk_inputs(n_tokens: int, n_q_heads: int, n_k_heads: int, head_dim: int, dtype: str = "bf16",
+              seed: int = 60, pad: int = 0) -> dict:
+    """Seeded QK-norm inputs: a fused qkv matrix [T, (Hq + 2 Hk) * D + pad]
+    ~ N(0,1) (query heads first, then key, then value heads), and query / key
+    weights 1 + 0.1 N(0,1) of length D.  Returned as torch CPU tensors."""
+    width = (n_q_heads + 2 * n_k_heads) * head_dim + pad
+    qkv = _draw_range("normal", seed, TAG_X, 0, n_tokens, width)
+    g = _rng(seed, TAG_W, 0)
+    wq = (1.0 + 0.1 * g.standard_normal(head_dim, dtype=np.float32)).astype(np.float32)
+    wk = (1.0 + 0.1 * g.standard_normal(head_dim, dtype=np.float32)).astype(np.float32)
+    return {"qkv": to_storage(qkv, dtype), "q_weight": to_storage(wq, dtype),
+            "k_weight": to_storage(wk, dtype)}
