@@ -27,6 +27,8 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD_DIR, "liboracle_rmsnorm.so")
 
 F32, BF16, FP8E4M3, F64 = 0, 1, 2, 3
+MXFP8, MXFP4, NVFP4 = 10, 11, 12
+_BLOCK = {"mxfp8": (MXFP8, 32, 1), "mxfp4": (MXFP4, 32, 2), "nvfp4": (NVFP4, 16, 2)}
 _DTYPES = {"f32": F32, "bf16": BF16, "fp8": FP8E4M3, "f64": F64}
 
 _lock = threading.Lock()
@@ -66,6 +68,14 @@ class Oracle:
         lib.oracle_e4m3_to_f64.restype = ctypes.c_double
         lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
         lib.oracle_num_cpus.restype = ctypes.c_int
+        lib.oracle_e2m1_to_f64.restype = ctypes.c_double
+        lib.oracle_e2m1_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_e2m1_from_f64.restype = ctypes.c_uint8
+        lib.oracle_e2m1_from_f64.argtypes = [ctypes.c_double]
+        lib.oracle_e8m0_to_f64.restype = ctypes.c_double
+        lib.oracle_e8m0_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_block_quantize.restype = ctypes.c_int
+        lib.oracle_block_quantize.argtypes = [vp, i64, i64, ctypes.c_int, vp, vp, vp]
         lib.oracle_qk_norm.restype = ctypes.c_int
         lib.oracle_qk_norm.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
                                        ctypes.c_double, ctypes.c_double, ctypes.c_int]
@@ -86,6 +96,41 @@ class Oracle:
 
     def e4m3_to_f64(self, c: int) -> float:
         return float(self.lib.oracle_e4m3_to_f64(int(c)))
+
+    def e2m1_from_f64(self, v: float) -> int:
+        return int(self.lib.oracle_e2m1_from_f64(float(v)))
+
+    def e2m1_to_f64(self, c: int) -> float:
+        return float(self.lib.oracle_e2m1_to_f64(int(c)))
+
+    def e8m0_to_f64(self, c: int) -> float:
+        return float(self.lib.oracle_e8m0_to_f64(int(c)))
+
+    def block_quantize(self, y64: np.ndarray, fmt: str) -> dict:
+        """Block-scaled quantisation of fp64 rows [T, H] (see the C file):
+        returns ``q`` (bytes; FP4 packed two per byte), ``block_scale`` and,
+        for NVFP4, ``token_scale``."""
+        code, blk, per_byte = _BLOCK[fmt]
+        y = np.ascontiguousarray(y64, dtype=np.float64)
+        T, H = y.shape
+        q = np.zeros((T, H // per_byte), dtype=np.uint8)
+        bs = np.zeros((T, H // blk), dtype=np.uint8)
+        ts = np.zeros(T, dtype=np.float32) if fmt == "nvfp4" else None
+        st = self.lib.oracle_block_quantize(y.ctypes.data, T, H, code, q.ctypes.data,
+                                            bs.ctypes.data, None if ts is None else ts.ctypes.data)
+        if st != 0:
+            raise RuntimeError(f"oracle_block_quantize failed with status {st}")
+        return {"q": q, "block_scale": bs, "token_scale": ts}
+
+    def rmsnorm_block(self, x, residual=None, weight=None, bias=None, *, eps: float,
+                      in_dtype: str, fmt: str, weight_offset: float = 0.0) -> dict:
+        """The norm (fp64 output) followed by the block-scaled quantisation."""
+        o = self.rmsnorm(x, residual, weight, bias, eps=eps, in_dtype=in_dtype, out_dtype="f64",
+                         weight_offset=weight_offset)
+        b = self.block_quantize(o["out"], fmt)
+        b["residual_out"] = o["residual_out"]
+        b["y64"] = o["out"]
+        return b
 
     def qk_norm(self, q, k, q_weight=None, k_weight=None, *, n_q_heads: int, n_k_heads: int,
                 head_dim: int, eps: float, dtype: str, weight_offset: float = 0.0):
@@ -207,3 +252,8 @@ def _rmsnorm(lib, x, residual=None, weight=None, bias=None, *, eps: float, in_dt
 def qk_norm(q, k, q_weight=None, k_weight=None, **kw):
     """Per-head QK norm on CPU copies; see ``Oracle.qk_norm``."""
     return default().qk_norm(q, k, q_weight, k_weight, **kw)
+
+
+def rmsnorm_block(x, residual=None, weight=None, bias=None, **kw):
+    """Norm + block-scaled quantisation on CPU; see ``Oracle.rmsnorm_block``."""
+    return default().rmsnorm_block(x, residual, weight, bias, **kw)

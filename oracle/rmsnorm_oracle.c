@@ -348,3 +348,141 @@ int oracle_qk_norm(void *q, void *k, const void *q_weight, const void *k_weight,
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* block-scaled quantisation of the normalised rows                    */
+/*
+ * Section "Blackwell support" of the blog: MXFP8, MXFP4 and NVFP4 outputs,
+ * with the absolute maximum taken over 32 (MX) or 16 (NVFP4) elements.
+ * Applied to the fp64 output yhat of the norm, row by row:
+ *
+ *  MXFP8 / MXFP4 (OCP Microscaling formats): blocks of 32 elements share a
+ *   power-of-two scale X = 2^s, s = floor(log2(max|y|)) - emax, where emax is
+ *   the exponent of the element format's largest normal (8 for E4M3, 2 for
+ *   E2M1), clamped to [-127, 127] and stored as E8M0 (code s + 127); each
+ *   element is y / X rounded to the element format (RNE, saturating).  An
+ *   all-zero block stores scale code 0 and zero elements.
+ *  NVFP4: a per-token fp32 scale g = max|row| / (448 * 6) (stored), blocks of
+ *   16 elements with an E4M3 scale s_b = E4M3(max|block| / (6 g)) (RNE,
+ *   saturating) and E2M1 elements RN_sat(y / (s_b g)); zero scales give zero
+ *   elements.
+ *
+ * FP4 codes are packed two per byte, element 2j in the low nibble.  The
+ * E2M1 format (OCP): sign, 2 exponent bits with bias 1, 1 mantissa bit;
+ * magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.  E8M0: 2^(code - 127), 255 = NaN.
+ */
+enum { ORC_MXFP8 = 10, ORC_MXFP4 = 11, ORC_NVFP4 = 12 };
+
+double oracle_e2m1_to_f64(uint8_t c) {
+    int s = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -v : v;
+}
+
+uint8_t oracle_e2m1_from_f64(double v) {
+    if (isnan(v)) return 0;
+    int neg = signbit(v) ? 1 : 0;
+    double a = fabs(v), r;
+    if (a == 0.0) {
+        r = 0.0;
+    } else if (isinf(a)) {
+        r = 6.0;
+    } else {
+        int e;
+        frexp(a, &e);              /* a in [2^(e-1), 2^e) */
+        int q = e - 2;             /* 2 significant bits */
+        if (q < -1) q = -1;        /* subnormal quantum 0.5 */
+        r = round_to_quantum(a, q);
+        if (r > 6.0) r = 6.0;
+    }
+    uint8_t code;
+    if (r < 1.0) {
+        code = (uint8_t)(r * 2.0); /* 0 or 0.5 */
+    } else {
+        int e;
+        double f = frexp(r, &e);   /* r = f * 2^e, exponent field e - 1 + 1 */
+        code = (uint8_t)((e << 1) | ((int)ldexp(f, 2) - 2));
+    }
+    return (uint8_t)(code | (neg ? 0x8 : 0));
+}
+
+double oracle_e8m0_to_f64(uint8_t c) { return c == 255 ? NAN : ldexp(1.0, (int)c - 127); }
+
+static void quantize_mx_row(const double *y, int64_t H, int elem_fp4, uint8_t *q, uint8_t *sc) {
+    const int emax = elem_fp4 ? 2 : 8;
+    for (int64_t b = 0; b < H / 32; ++b) {
+        const double *yb = y + 32 * b;
+        double amax = 0.0;
+        for (int j = 0; j < 32; ++j)
+            if (fabs(yb[j]) > amax) amax = fabs(yb[j]);
+        int s = -127;
+        if (amax > 0.0) {
+            int e;
+            frexp(amax, &e);       /* floor(log2(amax)) = e - 1 */
+            s = e - 1 - emax;
+            if (s < -127) s = -127;
+            if (s > 127) s = 127;
+        }
+        sc[b] = (uint8_t)(s + 127);
+        for (int j = 0; j < 32; ++j) {
+            const double v = amax > 0.0 ? ldexp(yb[j], -s) : 0.0;
+            const int64_t i = 32 * b + j;
+            if (elem_fp4) {
+                const uint8_t c = oracle_e2m1_from_f64(v);
+                if (i & 1) q[i / 2] = (uint8_t)((q[i / 2] & 0x0F) | (c << 4));
+                else q[i / 2] = c;
+            } else {
+                q[i] = oracle_e4m3_from_f64(v);
+            }
+        }
+    }
+}
+
+static void quantize_nvfp4_row(const double *y, int64_t H, uint8_t *q, uint8_t *sc, float *g_out) {
+    double a = 0.0;
+    for (int64_t j = 0; j < H; ++j)
+        if (fabs(y[j]) > a) a = fabs(y[j]);
+    const float g = oracle_f32_from_f64(a / (448.0 * 6.0));
+    *g_out = g;
+    for (int64_t b = 0; b < H / 16; ++b) {
+        const double *yb = y + 16 * b;
+        double amax = 0.0;
+        for (int j = 0; j < 16; ++j)
+            if (fabs(yb[j]) > amax) amax = fabs(yb[j]);
+        uint8_t sb = 0;
+        if (g > 0.0f) sb = oracle_e4m3_from_f64(amax / (6.0 * (double)g));
+        sc[b] = sb;
+        const double s = oracle_e4m3_to_f64(sb) * (double)g;
+        for (int j = 0; j < 16; ++j) {
+            const int64_t i = 16 * b + j;
+            const uint8_t c = s > 0.0 ? oracle_e2m1_from_f64(yb[j] / s) : 0;
+            if (i & 1) q[i / 2] = (uint8_t)((q[i / 2] & 0x0F) | (c << 4));
+            else q[i / 2] = c;
+        }
+    }
+}
+
+/*
+ * y: [n_tokens, hidden] fp64 rows (the norm's output).  q: [n_tokens,
+ * hidden] bytes (MXFP8) or [n_tokens, hidden / 2] (FP4 packed); block_scale:
+ * [n_tokens, hidden / 32] (MX) or [n_tokens, hidden / 16] (NVFP4);
+ * token_scale: [n_tokens] fp32 (NVFP4 only).  Returns 0, or -1 on a bad
+ * argument (hidden must be a multiple of the block size).
+ */
+int oracle_block_quantize(const double *y, int64_t n_tokens, int64_t hidden, int fmt, uint8_t *q,
+                          uint8_t *block_scale, float *token_scale) {
+    if (n_tokens < 0 || hidden <= 0 || !y || !q || !block_scale) return -1;
+    if (fmt == ORC_NVFP4) {
+        if (hidden % 16 || !token_scale) return -1;
+        for (int64_t t = 0; t < n_tokens; ++t)
+            quantize_nvfp4_row(y + t * hidden, hidden, q + t * (hidden / 2),
+                               block_scale + t * (hidden / 16), token_scale + t);
+        return 0;
+    }
+    if ((fmt != ORC_MXFP8 && fmt != ORC_MXFP4) || hidden % 32) return -1;
+    const int fp4 = fmt == ORC_MXFP4;
+    for (int64_t t = 0; t < n_tokens; ++t)
+        quantize_mx_row(y + t * hidden, hidden, fp4, q + t * (fp4 ? hidden / 2 : hidden),
+                        block_scale + t * (hidden / 32));
+    return 0;
+}

@@ -467,6 +467,159 @@ def test_qk_norm_strided_fused_qkv(oracle_mod):
     _check_qk_strided_fused_qkv(oracle_mod.default())
 
 
+# ---------------------------------------------------------------- block-scaled outputs
+
+
+def test_e2m1_decoder_matches_spec_table(oracle_mod):
+    orc = oracle_mod.default()
+    with open(os.path.join(GOLDEN, "e2m1_spec_values.txt")) as f:
+        rows = [l.split("#")[0].split() for l in f if l.split("#")[0].strip()]
+    assert len(rows) == 16
+    for c, v in rows:
+        got = orc.e2m1_to_f64(int(c, 16))
+        assert got == float(v) and math.copysign(1, got) == math.copysign(1, float(v))
+
+
+def _check_e2m1_encoder(orc):
+    for c in range(16):
+        assert orc.e2m1_from_f64(orc.e2m1_to_f64(c)) == c
+    for c in range(7):
+        lo, hi = orc.e2m1_to_f64(c), orc.e2m1_to_f64(c + 1)
+        want = c if c % 2 == 0 else c + 1
+        assert orc.e2m1_from_f64((lo + hi) / 2) == want, c
+        assert orc.e2m1_from_f64(-(lo + hi) / 2) == want | 8
+        assert orc.e2m1_from_f64(lo + (hi - lo) * 0.49) == c
+        assert orc.e2m1_from_f64(lo + (hi - lo) * 0.51) == c + 1
+    for v in (6.0, 6.5, 7.0, 100.0, float("inf")):
+        assert orc.e2m1_from_f64(v) == 7 and orc.e2m1_from_f64(-v) == 15
+
+
+def test_e2m1_encoder_round_trip_ties_saturation(oracle_mod):
+    _check_e2m1_encoder(oracle_mod.default())
+
+
+def test_e8m0_decoder(oracle_mod):
+    orc = oracle_mod.default()
+    assert orc.e8m0_to_f64(127) == 1.0 and orc.e8m0_to_f64(128) == 2.0
+    assert orc.e8m0_to_f64(0) == 2.0 ** -127 and orc.e8m0_to_f64(254) == 2.0 ** 127
+    assert math.isnan(orc.e8m0_to_f64(255))
+
+
+def _unpack_fp4(q):
+    out = np.empty(q.shape[:-1] + (q.shape[-1] * 2,), dtype=np.uint8)
+    out[..., 0::2] = q & 0xF
+    out[..., 1::2] = q >> 4
+    return out
+
+
+def _dequant(orc, fmt, b, H):
+    T = b["q"].shape[0]
+    if fmt == "mxfp8":
+        el = np.array([orc.e4m3_to_f64(c) for c in range(256)])[b["q"]]
+    else:
+        el = np.array([orc.e2m1_to_f64(c) for c in range(16)])[_unpack_fp4(b["q"])]
+    if fmt == "nvfp4":
+        sb = np.array([orc.e4m3_to_f64(c) for c in range(256)])[b["block_scale"]]
+        scale = np.repeat(sb, 16, axis=1) * b["token_scale"].astype(np.float64)[:, None]
+    else:
+        scale = np.repeat(np.array([orc.e8m0_to_f64(c) for c in range(256)])[b["block_scale"]],
+                          32, axis=1)
+    return el * scale
+
+
+def _check_mx_exact_blocks(orc):
+    # rows whose blocks hold exactly representable values: every block of 32
+    # has max |y| = 2^k, so the scale is 2^(k - emax) and y / X is a value of
+    # the element format -> dequantisation is exact
+    rng = np.random.default_rng(50)
+    T, H = 3, 128
+    for fmt, vals in (("mxfp8", [1.0, 0.5, -0.75, 0.125, 1.5 / 4, -1.0]),
+                      ("mxfp4", [1.0, 0.5, -0.75, 0.25, -1.0, 0.375])):
+        kb = rng.integers(-20, 20, size=(T, H // 32)).astype(float)
+        v = rng.choice(vals, size=(T, H))
+        v[:, ::32] = 1.0                       # the block maximum, |v| <= 1 elsewhere
+        y = v * 2.0 ** np.repeat(kb, 32, axis=1)
+        b = orc.block_quantize(y, fmt)
+        k = np.log2(np.abs(y[:, ::32]))
+        emax = 8 if fmt == "mxfp8" else 2
+        assert np.array_equal(b["block_scale"].astype(int), (k - emax + 127).astype(int))
+        assert np.array_equal(_dequant(orc, fmt, b, H), y)
+
+
+def _check_block_error_bounds(orc):
+    rng = np.random.default_rng(51)
+    T, H = 4, 256
+    y = rng.standard_normal((T, H)) * np.exp(rng.uniform(-6, 6, (T, 1)))
+    y[2] = 0.0
+    for fmt, mant, top in (("mxfp8", 3, 448.0), ("mxfp4", 1, 6.0), ("nvfp4", 1, 6.0)):
+        b = orc.block_quantize(y, fmt)
+        d = _dequant(orc, fmt, b, H)
+        blk = 16 if fmt == "nvfp4" else 32
+        for t in range(T):
+            for j0 in range(0, H, blk):
+                yb, db = y[t, j0:j0 + blk], d[t, j0:j0 + blk]
+                if not np.any(yb):
+                    assert not np.any(db)
+                    continue
+                if fmt == "nvfp4":
+                    s = orc.e4m3_to_f64(b["block_scale"][t, j0 // 16]) * float(b["token_scale"][t])
+                else:
+                    s = orc.e8m0_to_f64(b["block_scale"][t, j0 // 32])
+                v = np.abs(yb) / s
+                # half the spacing of the element format at v (normals), or the
+                # subnormal spacing, plus the saturation above the largest value
+                e = np.floor(np.log2(np.maximum(v, 1e-300)))
+                e = np.maximum(e, 0 if fmt != "mxfp8" else -6)
+                half = 2.0 ** (e - mant - 1)
+                bound = (half + np.maximum(v - top, 0)) * s * (1 + 1e-12)
+                assert np.all(np.abs(db - yb) <= bound), (fmt, t, j0)
+        # each non-zero block's largest element lands at the top of the element
+        # range: NVFP4 +-6 (the block scale is max / 6 up to its E4M3
+        # rounding), MX in [2^emax, 2^(emax+1)) after the power-of-two scale
+        codes = b["q"] if fmt == "mxfp8" else _unpack_fp4(b["q"])
+        for t in range(T):
+            for j0 in range(0, H, blk):
+                yb = y[t, j0:j0 + blk]
+                if not np.any(yb):
+                    continue
+                c = int(codes[t, j0 + int(np.argmax(np.abs(yb)))])
+                if fmt == "nvfp4":
+                    assert c & 7 == 7, (t, j0, c)
+                elif fmt == "mxfp4":
+                    assert c & 7 in (6, 7), (t, j0, c)
+                else:
+                    assert c & 0x7F >= 0x78, (t, j0, c)
+        if fmt == "nvfp4":
+            for t in (0, 1, 3):
+                a = np.abs(y[t]).max()
+                assert b["token_scale"][t] == np.float32(a / 2688.0)
+                jb = int(np.argmax(np.abs(y[t]))) // 16
+                assert b["block_scale"][t, jb] == 0x7E       # 448
+                assert _unpack_fp4(b["q"])[t, int(np.argmax(np.abs(y[t])))] in (7, 15)
+            assert b["token_scale"][2] == 0 and not b["block_scale"][2].any()
+        else:
+            assert not b["block_scale"][2].any() and not b["q"][2].any()
+
+
+def test_mx_exact_blocks(oracle_mod):
+    _check_mx_exact_blocks(oracle_mod.default())
+
+
+def test_block_formats_error_bounds_and_scales(oracle_mod):
+    _check_block_error_bounds(oracle_mod.default())
+
+
+def test_rmsnorm_block_is_norm_then_quantize(oracle_mod):
+    orc = oracle_mod.default()
+    rng = np.random.default_rng(52)
+    x = bf16_tensor(rng.standard_normal((3, 64)))
+    r = bf16_tensor(rng.standard_normal((3, 64)))
+    o = orc.rmsnorm_block(x, r, None, None, eps=1e-6, in_dtype="bf16", fmt="mxfp8")
+    y = orc.rmsnorm(x, r, None, None, eps=1e-6, in_dtype="bf16", out_dtype="f64")
+    assert np.array_equal(o["y64"], y["out"]) and np.array_equal(o["residual_out"], y["residual_out"])
+    assert np.array_equal(o["q"], orc.block_quantize(y["out"], "mxfp8")["q"])
+
+
 # ---------------------------------------------------------------- mutants
 
 # Each mutant plants one plausible mistake in the oracle's C source: a dropped
@@ -490,6 +643,10 @@ MUTANTS = {
     "qk_weights_swapped": ("k_weight, eps,\n                    weight_offset);",
                            "q_weight, eps,\n                    weight_offset);"),
     "qk_divisor_off_by_one": ("ss / (double)head_dim + eps", "ss / (double)(head_dim - 1) + eps"),
+    "mx_emax_off_by_one": ("const int emax = elem_fp4 ? 2 : 8;", "const int emax = elem_fp4 ? 2 : 7;"),
+    "nvfp4_scale_uses_4": ("amax / (6.0 * (double)g)", "amax / (4.0 * (double)g)"),
+    "e2m1_ties_up": ("r = round_to_quantum(a, q);\n        if (r > 6.0)",
+                     "r = ldexp(floor(ldexp(a, -q) + 0.5), q);\n        if (r > 6.0)"),
     "e4m3_ties_up": ("r = round_to_quantum(a, q);\n        if (r > 448.0)",
                      "r = ldexp(floor(ldexp(a, -q) + 0.5), q);\n        if (r > 448.0)"),
 }
@@ -513,6 +670,9 @@ def all_pin_checks(orc):
     checks.append(lambda: _check_qk_equals_rows(orc))
     checks.append(lambda: _check_qk_constant_heads(orc))
     checks.append(lambda: _check_qk_strided_fused_qkv(orc))
+    checks.append(lambda: _check_e2m1_encoder(orc))
+    checks.append(lambda: _check_mx_exact_blocks(orc))
+    checks.append(lambda: _check_block_error_bounds(orc))
     failed = 0
     for chk in checks:
         try:
