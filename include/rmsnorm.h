@@ -128,6 +128,37 @@ int rmsnorm_fwd_ex(const void* x, const void* residual, const void* weight, cons
                    int64_t hidden, float eps, uint32_t flags, float weight_offset,
                    const rmsn_config* cfg, cudaStream_t stream);
 
+/* block-scaled output formats of rmsnorm_fwd_blockscaled */
+#define RMSN_FMT_MXFP8 1 /* E4M3 codes, one E8M0 scale per 32 elements */
+#define RMSN_FMT_MXFP4 2 /* E2M1 codes (two per byte, low nibble first), E8M0 per 32 */
+#define RMSN_FMT_NVFP4 3 /* E2M1 codes (packed), E4M3 scale per 16, fp32 scale per token */
+
+/*
+ * Fused residual-add + RMSNorm with a block-scaled quantised output (blog
+ * section "Blackwell support": MXFP8 / MXFP4 / NVFP4, absolute maximum over
+ * 32 or 16 elements).  The norm is that of rmsnorm_fwd; y is then encoded:
+ *
+ *   MXFP8 / MXFP4: per block of 32 elements, s = floor(log2(max|y|)) - emax
+ *     (emax 8 for E4M3, 2 for E2M1) clamped to [-127, 127], stored as E8M0
+ *     code s + 127 in block_scale[T, hidden/32]; codes RN_sat(y * 2^-s).
+ *     An all-zero block stores code 0 and zero codes.
+ *   NVFP4: token_scale[t] = g = max|row| / (448 * 6) (fp32); per block of 16
+ *     elements E4M3 scale c_b = RN_sat(max|block| / (6 g)) in
+ *     block_scale[T, hidden/16]; codes E2M1 RN_sat(y / (c_b g)).
+ *
+ * out is [T, hidden] bytes (MXFP8) or [T, hidden/2] bytes (FP4, element 2j
+ * in the low nibble).  Rounding is to nearest even with saturation.  flags
+ * as for rmsnorm_fwd with the output-dtype bits 0; the input must be bf16,
+ * hidden a multiple of 32 (MX) or 16 (NVFP4), and the vector-path
+ * alignment of rmsnorm_fwd must hold (else RMSN_EUNSUPPORTED).  token_scale
+ * is required iff NVFP4.  `cfg` as in rmsnorm_fwd_ex (NULL = selector).
+ */
+int rmsnorm_fwd_blockscaled(const void* x, const void* residual, const void* weight,
+                            const void* bias, void* out, void* block_scale, float* token_scale,
+                            void* residual_out, int64_t n_tokens, int64_t hidden, float eps,
+                            uint32_t flags, int format, float weight_offset,
+                            const rmsn_config* cfg, cudaStream_t stream);
+
 /*
  * rmsnorm_fwd_ex on rows that live in HOST memory: the kernel itself reads x,
  * residual (and weight, bias) across the CPU-GPU link and writes out,

@@ -35,7 +35,14 @@ VARIANT_BULK_ROW = 2
 VARIANT_GENERIC = 3
 VARIANT_NAMES = {0: "warp_rows", 1: "block_row", 2: "bulk_row", 3: "generic"}
 
-EXPORTED = ("rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_fwd_host", "rmsnorm_qk_fwd",
+RMSN_FMT_MXFP8 = 1
+RMSN_FMT_MXFP4 = 2
+RMSN_FMT_NVFP4 = 3
+BLOCK_FORMATS = {"mxfp8": (RMSN_FMT_MXFP8, 32, 1), "mxfp4": (RMSN_FMT_MXFP4, 32, 2),
+                 "nvfp4": (RMSN_FMT_NVFP4, 16, 2)}
+
+EXPORTED = ("rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_fwd_blockscaled", "rmsnorm_fwd_host",
+            "rmsnorm_qk_fwd",
             "rmsnorm_query_config", "rmsnorm_list_configs", "rmsnorm_read_status",
             "rmsnorm_status_string")
 
@@ -90,6 +97,10 @@ def load() -> ctypes.CDLL:
             lib.rmsnorm_fwd_ex.restype = ctypes.c_int
             lib.rmsnorm_fwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, f32, u32, f32,
                                            ctypes.POINTER(RmsnConfig), vp]
+            lib.rmsnorm_fwd_blockscaled.restype = ctypes.c_int
+            lib.rmsnorm_fwd_blockscaled.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, f32,
+                                                    u32, ctypes.c_int, f32,
+                                                    ctypes.POINTER(RmsnConfig), vp]
             lib.rmsnorm_fwd_host.restype = ctypes.c_int
             lib.rmsnorm_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, f32, u32, f32,
                                              vp]
@@ -128,6 +139,18 @@ def rmsnorm_fwd_ex(x, residual, weight, bias, out, residual_out, out_scale, n_to
                                      int(n_tokens), int(hidden), float(eps), int(flags),
                                      float(weight_offset),
                                      None if cfg is None else ctypes.byref(cfg), stream))
+
+
+def rmsnorm_fwd_blockscaled(x, residual, weight, bias, out, block_scale, token_scale,
+                            residual_out, n_tokens: int, hidden: int, eps: float, flags: int,
+                            fmt: int, weight_offset: float, cfg: RmsnConfig | None, stream) -> int:
+    """Direct call of ``rmsnorm_fwd_blockscaled`` with raw pointers."""
+    return int(load().rmsnorm_fwd_blockscaled(x, residual, weight, bias, out, block_scale,
+                                              token_scale, residual_out, int(n_tokens),
+                                              int(hidden), float(eps), int(flags), int(fmt),
+                                              float(weight_offset),
+                                              None if cfg is None else ctypes.byref(cfg),
+                                              stream))
 
 
 def rmsnorm_fwd_host(x, residual, weight, bias, out, residual_out, out_scale, n_tokens: int,

@@ -166,3 +166,34 @@ def qk_norm_(q: torch.Tensor | None, k: torch.Tensor | None, q_weight: torch.Ten
     if st != _lib.RMSN_OK:
         raise _lib.RmsnError(st, "rmsnorm_qk_fwd")
     return q, k
+
+
+def fused_add_rmsnorm_blockscaled(x: torch.Tensor, residual: torch.Tensor | None = None,
+                                  weight: torch.Tensor | None = None,
+                                  bias: torch.Tensor | None = None, *, eps: float, fmt: str,
+                                  weight_offset: float = 0.0,
+                                  residual_out: torch.Tensor | None = None,
+                                  config: _lib.RmsnConfig | None = None,
+                                  stream: torch.cuda.Stream | None = None):
+    """Fused residual-add + RMSNorm with an MXFP8 / MXFP4 / NVFP4 output
+    (``rmsnorm_fwd_blockscaled``).  Returns ``(q, block_scale, token_scale,
+    residual_out)``: q uint8 [T, H] (MXFP8) or [T, H / 2] (FP4, two codes per
+    byte, low nibble first), block_scale uint8 [T, H / block], token_scale
+    float32 [T] for NVFP4 (else None)."""
+    if x.dim() != 2 or x.dtype != torch.bfloat16:
+        raise TypeError("x must be a 2-D bfloat16 tensor")
+    T, H = x.shape
+    code, block, per_byte = _lib.BLOCK_FORMATS[fmt]
+    q = torch.empty((T, H // per_byte), dtype=torch.uint8, device=x.device)
+    bs = torch.empty((T, H // block), dtype=torch.uint8, device=x.device)
+    ts = torch.empty((T,), dtype=torch.float32, device=x.device) if fmt == "nvfp4" else None
+    if residual is not None and residual_out is None:
+        residual_out = torch.empty_like(x)
+    flags = make_flags("bf16", "f32", residual is not None, weight is not None, bias is not None)
+    s = stream if stream is not None else torch.cuda.current_stream(x.device)
+    st = _lib.rmsnorm_fwd_blockscaled(_ptr(x), _ptr(residual), _ptr(weight), _ptr(bias), _ptr(q),
+                                      _ptr(bs), _ptr(ts), _ptr(residual_out), T, H, eps, flags,
+                                      code, weight_offset, config, s.cuda_stream)
+    if st != _lib.RMSN_OK:
+        raise _lib.RmsnError(st, "rmsnorm_fwd_blockscaled")
+    return q, bs, ts, residual_out

@@ -104,8 +104,11 @@ int enable_smem(DeviceInfo* d, const void* fn) {
 const std::vector<KernelEntry>& registry() {
     static const std::vector<KernelEntry> all = [] {
         std::vector<KernelEntry> v;
-        const KernelEntry* (*fns[])(int*) = {kernels_f32_f32,  kernels_f32_bf16,  kernels_f32_fp8,
-                                             kernels_bf16_f32, kernels_bf16_bf16, kernels_bf16_fp8};
+        const KernelEntry* (*fns[])(int*) = {kernels_f32_f32,    kernels_f32_bf16,
+                                             kernels_f32_fp8,    kernels_bf16_f32,
+                                             kernels_bf16_bf16,  kernels_bf16_fp8,
+                                             kernels_bf16_mxfp8, kernels_bf16_mxfp4,
+                                             kernels_bf16_nvfp4};
         for (auto fn : fns) {
             int n = 0;
             const KernelEntry* t = fn(&n);
@@ -322,9 +325,14 @@ namespace {
 int validate(const void* x, const void* residual, const void* weight, const void* bias,
              const void* out, const void* residual_out, const float* out_scale,
              int64_t n_tokens, int64_t hidden, float eps, uint32_t flags, float weight_offset,
-             Problem* p) {
+             Problem* p, int block_fmt = -1) {
     int st = decode_flags(flags, p);
     if (st != RMSN_OK) return st;
+    if (block_fmt >= 0) {  // block-scaled output: byte codes, FP4 packed two per byte
+        if (flags & RMSN_OUT_MASK) return RMSN_EINVAL;
+        p->out_dt = block_fmt;
+        p->out_bytes = 1;
+    }
     if ((st = check_shape(n_tokens, hidden, p)) != RMSN_OK) return st;
     if (!(eps >= 0.f) || !isfinite(eps) || !isfinite(weight_offset)) return RMSN_EINVAL;
     // an empty batch touches nothing (its buffers may be NULL)
@@ -333,7 +341,7 @@ int validate(const void* x, const void* residual, const void* weight, const void
     if (p->res != (residual != nullptr) || p->res != (residual_out != nullptr)) return RMSN_EINVAL;
     if (((flags & RMSN_HAS_WEIGHT) != 0) != (weight != nullptr)) return RMSN_EINVAL;
     if (p->bias != (bias != nullptr)) return RMSN_EINVAL;
-    if ((p->out_dt == kFP8) != (out_scale != nullptr)) return RMSN_EINVAL;
+    if ((p->out_dt == kFP8 || p->out_dt == kNVFP4) != (out_scale != nullptr)) return RMSN_EINVAL;
     if (!x || !out) return RMSN_EINVAL;
     const void* ins[] = {x, residual, weight, bias, residual_out};
     for (const void* q : ins)
@@ -347,8 +355,9 @@ int validate(const void* x, const void* residual, const void* weight, const void
 int launch(const KernelEntry* e, const rmsn_config& c, DeviceInfo* d, const Problem& p,
            const void* x, const void* residual, const void* weight, const void* bias, void* out,
            void* residual_out, float* out_scale, float eps, float weight_offset,
-           cudaStream_t stream) {
+           cudaStream_t stream, void* block_scale = nullptr) {
     RmsnArgs a;
+    a.bscale = block_scale;
     a.x = x;
     a.r = residual;
     a.w = weight;
@@ -476,6 +485,42 @@ RMSN_API int rmsnorm_fwd_ex(const void* x, const void* residual, const void* wei
     }
     return launch(e, c, d, p, x, residual, weight, bias, out, residual_out, out_scale, eps,
                   weight_offset, stream);
+}
+
+RMSN_API int rmsnorm_fwd_blockscaled(const void* x, const void* residual, const void* weight,
+                                     const void* bias, void* out, void* block_scale,
+                                     float* token_scale, void* residual_out, int64_t n_tokens,
+                                     int64_t hidden, float eps, uint32_t flags, int format,
+                                     float weight_offset, const rmsn_config* cfg,
+                                     cudaStream_t stream) {
+    int fmt, block;
+    switch (format) {
+        case RMSN_FMT_MXFP8: fmt = kMXFP8; block = 32; break;
+        case RMSN_FMT_MXFP4: fmt = kMXFP4; block = 32; break;
+        case RMSN_FMT_NVFP4: fmt = kNVFP4; block = 16; break;
+        default: return RMSN_EINVAL;
+    }
+    Problem p{};
+    int st = validate(x, residual, weight, bias, out, residual_out, token_scale, n_tokens, hidden,
+                      eps, flags, weight_offset, &p, fmt);
+    if (st != RMSN_OK || n_tokens == 0) return st;
+    if (p.H % block != 0 || !block_scale) return RMSN_EINVAL;
+    if (p.in_dt != kBF16 || !p.vec_ok) return RMSN_EUNSUPPORTED;
+    DeviceInfo* d = device_info();
+    if (!d) return RMSN_ECUDA;
+    rmsn_config c;
+    const KernelEntry* e = nullptr;
+    if (cfg) {
+        if (cfg->variant == kGeneric) return RMSN_EUNSUPPORTED;
+        e = find_kernel(p, cfg->variant, cfg->chunks, cfg->max_warps);
+        if (!e || !shape_config(p, *e, d, cfg->grid, cfg->stages, &c)) return RMSN_EUNSUPPORTED;
+    } else {
+        if (!select(p, d, &c)) return RMSN_EUNSUPPORTED;
+        e = find_kernel(p, c.variant, c.chunks, c.max_warps);
+        if (!e) return RMSN_EUNSUPPORTED;
+    }
+    return launch(e, c, d, p, x, residual, weight, bias, out, residual_out, token_scale, eps,
+                  weight_offset, stream, block_scale);
 }
 
 RMSN_API int rmsnorm_fwd_host(const void* x, const void* residual, const void* weight,

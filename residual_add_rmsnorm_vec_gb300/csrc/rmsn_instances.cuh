@@ -34,8 +34,10 @@ static const KernelEntry kTable[] = {
     // prefill: rows streamed through shared memory by bulk async copies
     RMSN_BULK4(1, 8), RMSN_BULK4(2, 8), RMSN_BULK4(1, 16), RMSN_BULK4(2, 16),
     RMSN_BULK4(1, 32), RMSN_BULK4(2, 32),
+#ifndef RMSN_NO_GENERIC
     // any shape
     RMSN_GEN(false), RMSN_GEN(true),
+#endif
 };
 
 const KernelEntry* RMSN_TABLE_FN(int* n) {

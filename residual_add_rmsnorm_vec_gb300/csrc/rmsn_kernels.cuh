@@ -24,6 +24,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "rmsn_registry.h"
 
 namespace rmsn {
@@ -36,6 +38,35 @@ struct BF16 {
 };
 struct FP8 {
     static constexpr int kBytes = 1;
+};
+// Block-scaled outputs (codes plus one scale per kBlock elements).
+struct MXFP8 {
+    static constexpr int kBytes = 1;
+    static constexpr int kBlock = 32;
+};
+struct MXFP4 {
+    static constexpr int kBytes = 1;
+    static constexpr int kBlock = 32;
+};
+struct NVFP4 {
+    static constexpr int kBytes = 1;
+    static constexpr int kBlock = 16;
+};
+template <class T>
+struct IsBlockFmt {
+    static constexpr bool value = false;
+};
+template <>
+struct IsBlockFmt<MXFP8> {
+    static constexpr bool value = true;
+};
+template <>
+struct IsBlockFmt<MXFP4> {
+    static constexpr bool value = true;
+};
+template <>
+struct IsBlockFmt<NVFP4> {
+    static constexpr bool value = true;
 };
 
 // 32-byte register vector.
@@ -102,6 +133,33 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a0, float a1, float a2, fl
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(a1), "f"(a0));
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(a3), "f"(a2));
     return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+// Round two floats to FP4 E2M1 (nearest-even, saturating to +-6): element lo
+// in bits 0-3, hi in bits 4-7 of the result.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+    uint16_t d;
+    asm("{\n\t.reg .b8 q;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q, %1, %2;\n\t"
+        "cvt.u16.u8 %0, q;\n\t}"
+        : "=h"(d)
+        : "f"(hi), "f"(lo));
+    return (uint32_t)d & 0xFFu;
+}
+
+// Eight floats to E2M1, packed two per byte, element 0 in the lowest nibble.
+__device__ __forceinline__ uint32_t pack_e2m1x8(float v0, float v1, float v2, float v3, float v4,
+                                                float v5, float v6, float v7) {
+    return cvt_e2m1x2(v0, v1) | (cvt_e2m1x2(v2, v3) << 8) | (cvt_e2m1x2(v4, v5) << 16) |
+           (cvt_e2m1x2(v6, v7) << 24);
+}
+
+// Value of an E4M3 code (OCP FP8: bias 7, 3 mantissa bits), exact in fp32.
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+    const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+    const float mag = e == 0 ? (float)m * 0.001953125f  // m * 2^-9
+                             : (float)(8u + m) * __uint_as_float((e + 117u) << 23);  // 2^(e-10)
+    return (c & 0x80u) ? -mag : mag;
 }
 
 // Element k of a 32-byte vector of TI as float.
@@ -290,12 +348,123 @@ __device__ __forceinline__ float residual_sumsq(const RmsnArgs& a, int64_t rbase
     return acc;
 }
 
+// Block-scaled outputs (blog section "Blackwell support": MXFP8 / MXFP4 /
+// NVFP4 with the absolute maximum over 32 or 16 elements).  A block spans
+// LPB = kBlock / VE neighbouring lanes (their vectors are adjacent), so the
+// block maximum is a butterfly over LPB lanes.
+//   MX:    scale 2^s, s = floor(log2 max|y|) - emax (8 for E4M3, 2 for E2M1),
+//          clamped to [-127, 127], stored as E8M0 (s + 127); codes y * 2^-s.
+//   NVFP4: per-token fp32 g = max|row| / (448 * 6) (the row max all-reduce),
+//          block scale E4M3(max|block| / (6 g)), codes E2M1(y / (scale * g)).
+// All conversions round to nearest even and saturate.
+template <class TI, class TO, int CH, bool BIAS, class ReduceMax>
+__device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row, int64_t rbase,
+                                                  int G, int t, float inv, const V8 (&hv)[CH],
+                                                  V8 (&wv)[CH], V8* bv, ReduceMax reduce_max) {
+    constexpr int VE = 32 / TI::kBytes;
+    constexpr int LPB = TO::kBlock / VE;
+    constexpr bool NV = TO::kBlock == 16;
+    constexpr bool FP4 = !std::is_same<TO, MXFP8>::value;
+    static_assert(LPB >= 1 && LPB <= 4, "block spans 1..4 lanes");
+    float g = 0.f;
+    if constexpr (NV) {
+        float amax = 0.f;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int v = c * G + t;
+            if (v < a.nvec) {
+                opaque(wv[c]);
+                if constexpr (BIAS) opaque(bv[c]);
+#pragma unroll
+                for (int k = 0; k < VE; ++k)
+                    amax = fmaxf(amax, fabsf(scale_elem<BIAS>(elem<TI>(hv[c], k), inv,
+                                                              elem<TI>(wv[c], k), a.woff,
+                                                              BIAS ? elem<TI>(bv[c], k) : 0.f)));
+            }
+        }
+        amax = reduce_max(amax);
+        g = __fdiv_rn(amax, 2688.f);
+        if (t == 0) a.scale[row] = g;
+    }
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        const int v = c * G + t;
+        const bool valid = v < a.nvec;
+        float y[VE];
+        float bmax = 0.f;
+        if (valid) {
+            opaque(wv[c]);
+            if constexpr (BIAS) opaque(bv[c]);
+#pragma unroll
+            for (int k = 0; k < VE; ++k) {
+                y[k] = scale_elem<BIAS>(elem<TI>(hv[c], k), inv, elem<TI>(wv[c], k), a.woff,
+                                        BIAS ? elem<TI>(bv[c], k) : 0.f);
+                bmax = fmaxf(bmax, fabsf(y[k]));
+            }
+        }
+        // every lane takes part; a block's lanes are all valid or all invalid
+#pragma unroll
+        for (int o = LPB / 2; o > 0; o >>= 1)
+            bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, o));
+        if (!valid) continue;
+        float mul;     // code = convert(y * mul)
+        uint8_t sbyte;  // block scale code
+        if constexpr (NV) {
+            uint32_t sc = 0;
+            if (g > 0.f) {
+                uint16_t two;
+                asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+                    : "=h"(two)
+                    : "f"(0.f), "f"(__fdiv_rn(bmax, __fmul_rn(6.f, g))));
+                sc = two & 0xFFu;
+            }
+            const float s = __fmul_rn(e4m3_value(sc), g);
+            mul = s > 0.f ? __fdiv_rn(1.f, s) : 0.f;
+            sbyte = (uint8_t)sc;
+        } else {
+            constexpr int emax = FP4 ? 2 : 8;
+            const int ef = (int)((__float_as_uint(bmax) >> 23) & 0xFFu);
+            int sx = ef == 0 ? -127 : ef - 127 - emax;  // zero / subnormal maxima clamp
+            sx = sx < -127 ? -127 : (sx > 126 ? 126 : sx);
+            mul = __uint_as_float((uint32_t)(127 - sx) << 23);  // 2^-s, exact
+            sbyte = (uint8_t)(sx + 127);
+        }
+#pragma unroll
+        for (int k = 0; k < VE; ++k) y[k] = __fmul_rn(y[k], mul);
+        const int64_t e = rbase + (int64_t)v * VE;  // element index of this vector
+        if constexpr (FP4) {
+            uint32_t u[VE / 8];
+#pragma unroll
+            for (int k = 0; k < VE / 8; ++k)
+                u[k] = pack_e2m1x8(y[8 * k], y[8 * k + 1], y[8 * k + 2], y[8 * k + 3],
+                                   y[8 * k + 4], y[8 * k + 5], y[8 * k + 6], y[8 * k + 7]);
+            uint8_t* o = reinterpret_cast<uint8_t*>(a.out) + e / 2;
+            if constexpr (VE == 16) st_stream8(o, u);
+            else asm volatile("st.global.b32 [%0], %1;" ::"l"(o), "r"(u[0]) : "memory");
+        } else {
+            uint32_t u[VE / 4];
+#pragma unroll
+            for (int k = 0; k < VE / 4; ++k)
+                u[k] = pack_e4m3x4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
+            uint8_t* o = reinterpret_cast<uint8_t*>(a.out) + e;
+            if constexpr (VE == 16) st_stream16(o, u);
+            else st_stream8(o, u);
+        }
+        if (v % LPB == 0)
+            static_cast<uint8_t*>(a.bscale)[e / TO::kBlock] = sbyte;
+    }
+}
+
 // Scale, (FP8: absmax reduction and per-token scale) and store the row.
 // `reduce_max` is the row-wide max all-reduce (only used for FP8 output).
 template <class TI, class TO, int CH, bool BIAS, class ReduceMax>
 __device__ __forceinline__ void scale_store(const RmsnArgs& a, int64_t row, int64_t rbase, int G,
                                             int t, float inv, const V8 (&hv)[CH], V8 (&wv)[CH],
                                             V8* bv, ReduceMax reduce_max) {
+    if constexpr (IsBlockFmt<TO>::value) {
+        scale_store_block<TI, TO, CH, BIAS>(a, row, rbase, G, t, inv, hv, wv, bv, reduce_max);
+        return;
+    }
     constexpr int VE = 32 / TI::kBytes;
     float qmul = 0.f;
     if constexpr (TO::kBytes == 1) {

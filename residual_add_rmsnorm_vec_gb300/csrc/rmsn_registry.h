@@ -14,7 +14,8 @@ struct RmsnArgs {
     const void* b;
     void* out;
     void* res_out;
-    float* scale;
+    float* scale;   // per-token fp32 scale (FP8, NVFP4)
+    void* bscale;   // block scales (MXFP8 / MXFP4: E8M0 per 32; NVFP4: E4M3 per 16)
     int64_t T;
     int32_t H;
     int32_t nvec;
@@ -27,7 +28,7 @@ struct RmsnArgs {
     uint32_t* status;    // device status word: bit 0 = a bounded wait ran out
 };
 
-enum DType : int32_t { kF32 = 0, kBF16 = 1, kFP8 = 2 };
+enum DType : int32_t { kF32 = 0, kBF16 = 1, kFP8 = 2, kMXFP8 = 3, kMXFP4 = 4, kNVFP4 = 5 };
 
 enum Variant : int32_t { kWarpRows = 0, kBlockRow = 1, kBulkRow = 2, kGeneric = 3 };
 
@@ -44,5 +45,8 @@ const KernelEntry* kernels_f32_fp8(int* n);
 const KernelEntry* kernels_bf16_f32(int* n);
 const KernelEntry* kernels_bf16_bf16(int* n);
 const KernelEntry* kernels_bf16_fp8(int* n);
+const KernelEntry* kernels_bf16_mxfp8(int* n);
+const KernelEntry* kernels_bf16_mxfp4(int* n);
+const KernelEntry* kernels_bf16_nvfp4(int* n);
 
 }  // namespace rmsn

@@ -27,7 +27,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    assert names == sorted(["rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_fwd_host",
+    assert names == sorted(["rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_fwd_blockscaled",
+                            "rmsnorm_fwd_host",
                             "rmsnorm_qk_fwd", "rmsnorm_query_config", "rmsnorm_list_configs",
                             "rmsnorm_read_status", "rmsnorm_status_string"]), names
 

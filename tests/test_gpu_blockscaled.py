@@ -1,0 +1,176 @@
+"""GPU parity of the block-scaled outputs (rmsnorm_fwd_blockscaled: MXFP8,
+MXFP4, NVFP4) against the CPU oracle's norm + block quantisation.
+
+Tolerances, as for the per-token FP8 output: residual_out bit-exact, every
+code equal to the oracle's or one step away.  A block scale is an integer
+decided from floating point: the GPU decides it from its fp32 row, the
+oracle from fp64.  Where the two scale codes differ (by one step), the
+block's maximum must sit within fp32 rounding of the decision boundary, and
+the GPU's codes are then checked against the oracle's quantisation of the
+fp64 values under the GPU's scale.  NVFP4's per-token scale has relative
+error <= 1e-6.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+from residual_add_rmsnorm_vec_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+FORMATS = ("mxfp8", "mxfp4", "nvfp4")
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from residual_add_rmsnorm_vec_gb300 import build
+
+    build.build()
+    import residual_add_rmsnorm_vec_gb300 as p
+
+    torch.cuda.set_device(0)
+    return p
+
+
+def unpack4(q):
+    out = np.empty(q.shape[:-1] + (q.shape[-1] * 2,), dtype=np.uint8)
+    out[..., 0::2] = q & 0xF
+    out[..., 1::2] = q >> 4
+    return out
+
+
+def ordered4(c):
+    c = c.astype(np.int32)
+    return np.where(c & 8, -(c & 7), c & 7)
+
+
+def check_block(fmt, got_q, got_bs, got_ts, ref, where):
+    orc = oracle.default()
+    y = ref["y64"]
+    T, H = y.shape
+    blk = 16 if fmt == "nvfp4" else 32
+    if fmt == "mxfp8":
+        gq, rq, order = got_q, ref["q"], parity.ordered8
+    else:
+        gq, rq, order = unpack4(got_q), unpack4(ref["q"]), ordered4
+    enc = orc.e4m3_from_f64 if fmt == "mxfp8" else orc.e2m1_from_f64
+    if fmt == "nvfp4":
+        rs = ref["token_scale"].astype(np.float64)
+        rel = np.where(rs == 0, np.abs(got_ts), np.abs(got_ts - rs) / np.where(rs == 0, 1, rs))
+        assert rel.max() <= parity.SCALE_RTOL, f"{where}: token scale rel {rel.max()}"
+    if fmt == "nvfp4":
+        scale_diff = np.abs(parity.ordered8(got_bs) - parity.ordered8(ref["block_scale"]))
+    else:
+        scale_diff = np.abs(got_bs.astype(np.int32) - ref["block_scale"].astype(np.int32))
+    assert scale_diff.max() <= 1, f"{where}: block scale codes {scale_diff.max()} apart"
+    mism = 0
+    for t, b in zip(*np.nonzero(scale_diff)):
+        mism += 1
+        yb = y[t, b * blk:(b + 1) * blk]
+        amax = np.abs(yb).max()
+        if fmt == "nvfp4":
+            g = float(got_ts[t])
+            # the decision max/(6 g) sits within fp32 error of an E4M3 rounding boundary
+            v = amax / (6 * g)
+            lo = orc.e4m3_to_f64(min(got_bs[t, b], ref["block_scale"][t, b]))
+            hi = orc.e4m3_to_f64(max(got_bs[t, b], ref["block_scale"][t, b]))
+            assert abs(v - (lo + hi) / 2) <= 1e-5 * v, f"{where}: scale split away from a tie"
+            s = orc.e4m3_to_f64(int(got_bs[t, b])) * g
+            want = [enc(yy / s) if s > 0 else 0 for yy in yb]
+        else:
+            # floor(log2(max)) decided in fp32: max within fp32 error of a power of two
+            assert abs(math.log2(amax) - round(math.log2(amax))) <= 1e-6, \
+                f"{where}: E8M0 split away from a power of two"
+            s = int(got_bs[t, b]) - 127
+            want = [enc(math.ldexp(yy, -s)) for yy in yb]
+        d = np.abs(order(gq[t, b * blk:(b + 1) * blk]) - order(np.array(want, dtype=np.uint8)))
+        assert d.max() <= 1, f"{where}: codes under the GPU's scale {d.max()} steps apart"
+    same = np.repeat(scale_diff == 0, blk, axis=1)
+    d = np.abs(order(gq) - order(rq))[same]
+    assert (d.max() if d.size else 0) <= 1, f"{where}: codes {d.max()} steps apart"
+    return {"scale_mismatch_blocks": mism, "exact_frac": float((d == 0).mean()) if d.size else 1.0}
+
+
+def run(pkg, fmt, wl, config=None):
+    inp = synth.make_inputs(wl)
+    g = parity.to_device(inp, "cuda")
+    q, bs, ts, res = pkg.fused_add_rmsnorm_blockscaled(g["x"], g["residual"], g["weight"],
+                                                       g["bias"], eps=wl.eps, fmt=fmt,
+                                                       config=config)
+    torch.cuda.synchronize()
+    ref = oracle.rmsnorm_block(inp["x"], inp["residual"], inp["weight"], inp["bias"],
+                               eps=float(np.float32(wl.eps)), in_dtype="bf16", fmt=fmt)
+    if wl.has_residual:
+        assert np.array_equal(parity.bits16(res), ref["residual_out"]), "residual_out"
+    else:
+        assert res is None and ref["residual_out"] is None
+    return check_block(fmt, q.cpu().numpy(), bs.cpu().numpy(),
+                       None if ts is None else ts.cpu().numpy(), ref, f"{fmt} {wl.name}")
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("wl", [
+    synth.Workload("bs_T1", 1, 4096, 71, "bf16", "bf16", 1e-6),
+    synth.Workload("bs_T37_H5120_bias", 37, 5120, 72, "bf16", "bf16", 1e-6, has_bias=True),
+    synth.Workload("bs_T4096_H7168_bias", 4096, 7168, 40, "bf16", "bf16", 1e-6, has_bias=True),
+    synth.Workload("bs_T2048_H8192", 2048, 8192, 73, "bf16", "bf16", 1e-5, r_std=2.0,
+                   outlier_frac=0.01),
+    synth.Workload("bs_noresidual", 64, 2048, 74, "bf16", "bf16", 1e-6, has_residual=False),
+], ids=lambda w: w.name)
+def test_block_formats_parity(pkg, fmt, wl):
+    st = run(pkg, fmt, wl)
+    assert st["exact_frac"] > 0.98
+    assert pkg.rmsnorm_read_status() == 0
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_block_formats_every_config(pkg, fmt):
+    wl = synth.Workload("bs_cfg", 37, 2048, 75, "bf16", "bf16", 1e-6, has_bias=True)
+    flags = pkg.make_flags("bf16", "fp8", True, True, True)
+    cfgs = [c for c in pkg.rmsnorm_list_configs(37, 2048, flags)
+            if c.variant != pkg.VARIANT_GENERIC]
+    assert cfgs
+    for c in cfgs:
+        run(pkg, fmt, wl, config=c)
+
+
+def test_block_formats_zero_rows_and_rejections(pkg):
+    x = torch.zeros((3, 64), dtype=torch.bfloat16, device="cuda")
+    x[1] = 2.0
+    for fmt in FORMATS:
+        q, bs, ts, _ = pkg.fused_add_rmsnorm_blockscaled(x, None, None, None, eps=1e-6, fmt=fmt)
+        torch.cuda.synchronize()
+        q, bs = q.cpu().numpy(), bs.cpu().numpy()
+        assert not q[0].any() and not q[2].any()
+        if fmt == "nvfp4":
+            assert ts[0].item() == 0 and not bs[0].any()
+            assert np.all(unpack4(q[1:2]) == 7) and np.all(bs[1] == 0x7E)
+        else:
+            assert not bs[0].any()
+            # constant row 2.0 -> y = 2 / sqrt(4 + eps) ~ 1: scale 2^(-1 - emax)
+            emax = 8 if fmt == "mxfp8" else 2
+            assert np.all(bs[1] == 127 - 1 - emax)
+    s = torch.cuda.current_stream().cuda_stream
+    flags = pkg.make_flags("bf16", "f32", False, False, False)
+    buf = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    p = buf.data_ptr()
+    # hidden not a multiple of the block; unknown format; output-dtype bits set; f32 input
+    assert pkg.rmsnorm_fwd_blockscaled(p, None, None, None, p, p, None, None, 2, 48, 1e-6, flags,
+                                       pkg.RMSN_FMT_MXFP8, 0.0, None, s) == pkg.RMSN_EINVAL
+    assert pkg.rmsnorm_fwd_blockscaled(p, None, None, None, p, p, None, None, 2, 64, 1e-6, flags,
+                                       9, 0.0, None, s) == pkg.RMSN_EINVAL
+    assert pkg.rmsnorm_fwd_blockscaled(p, None, None, None, p, p, None, None, 2, 64, 1e-6,
+                                       flags | pkg.RMSN_OUT_BF16, pkg.RMSN_FMT_MXFP8, 0.0, None,
+                                       s) == pkg.RMSN_EINVAL
+    assert pkg.rmsnorm_fwd_blockscaled(p, None, None, None, p, p, None, None, 2, 64, 1e-6,
+                                       pkg.make_flags("f32", "f32", False, False, False),
+                                       pkg.RMSN_FMT_MXFP8, 0.0, None, s) == pkg.RMSN_EUNSUPPORTED
+    # NVFP4 needs the per-token scale
+    assert pkg.rmsnorm_fwd_blockscaled(p, None, None, None, p, p, None, None, 2, 64, 1e-6, flags,
+                                       pkg.RMSN_FMT_NVFP4, 0.0, None, s) == pkg.RMSN_EINVAL
