@@ -14,6 +14,8 @@ residual_out and y.  Prints ONE JSON line on rank 0:
              L2-hot back-to-back, CUDA-graph replay, and graph replay of
              programmatic-dependent launches, next to the measured empty-kernel
              launch time
+  quantized  per-token FP8 and block-scaled MXFP8 / MXFP4 / NVFP4 outputs on
+             4096 x {5120, 7168} with bias, algorithmic GB/s
   qk_norm    per-head QK norm (one launch, fused qkv, in place) against the
              row norm on the head views (two launches), us per call
   cpu_baseline  the CPU oracle on the host cores (rank 0, N = 1)
@@ -264,6 +266,7 @@ def run_ours(args):
 
     decode = None if args.skip_decode else run_decode(pkg, synth, dev, stream)
     qk = None if args.skip_decode else run_qk(pkg, synth, dev, stream)
+    quant = None if args.skip_decode else run_quantized(pkg, synth, dev, stream)
 
     peak, peak_src = load_peaks()
     achieved = bytes_step / (kernel_ms / 1e3) / 1e9
@@ -303,6 +306,8 @@ def run_ours(args):
         line["decode"] = decode
     if qk is not None:
         line["qk_norm"] = qk
+    if quant is not None:
+        line["quantized"] = quant
     if rank == 0 and world == 1 and not args.skip_cpu:
         line["cpu_baseline"] = run_cpu_baseline(wl, host, args.cpu_seconds)
     if rank == 0:
@@ -529,6 +534,83 @@ def run_qk(pkg, synth, dev, stream):
                         "row_norm_us": round(us_rows, 3),
                         "row_norm_gbs": round(nbytes / us_rows / 1e3, 1),
                         "speedup": round(us_rows / us_qk, 2)}
+    return out
+
+
+def run_quantized(pkg, synth, dev, stream):
+    """Quantised outputs on the FP8 configuration's shapes (4096 tokens x
+    hidden 5120 / 7168, bf16 x and residual, weight and bias): per-token FP8
+    and the block-scaled MXFP8 / MXFP4 / NVFP4.  CUDA-graph replay of
+    launches alternating over two input sets (above the L2 size),
+    algorithmic GB/s."""
+    import torch
+
+    T = 4096
+    out = {"unit": "GB/s", "timing": "cuda graph, 2 rotating input sets"}
+    for H in synth.FP8_HIDDEN:
+        wl = synth.fp8_workload(H)
+        inp = synth.make_inputs(wl)
+        sets = []
+        for k in range(2):
+            x = inp["x"].to(dev) if k == 0 else inp["x"].to(dev).flip(0).contiguous()
+            r = inp["residual"].to(dev) if k == 0 else inp["residual"].to(dev).flip(0).contiguous()
+            sets.append((x, r, torch.empty_like(x)))
+        w, b = inp["weight"].to(dev), inp["bias"].to(dev)
+        res = {}
+        for fmt in ("fp8", "mxfp8", "mxfp4", "nvfp4"):
+            if fmt == "fp8":
+                bufs = [(torch.empty((T, H), dtype=torch.uint8, device=dev),
+                         torch.empty((T,), dtype=torch.float32, device=dev)) for _ in sets]
+                nbytes = wl.algorithmic_bytes()
+
+                def call(i, bufs=bufs):
+                    x, r, ro = sets[i % 2]
+                    q, sc = bufs[i % 2]
+                    pkg.fused_add_rmsnorm(x, r, w, b, eps=wl.eps, out_dtype="fp8", out=q,
+                                          residual_out=ro, out_scale=sc)
+            else:
+                code, blk, per_byte = pkg.BLOCK_FORMATS[fmt]
+                nbytes = (T * H * 2 * 3 + T * H // per_byte + T * H // blk + 4 * H
+                          + (4 * T if fmt == "nvfp4" else 0))
+                flags = pkg.make_flags("bf16", "f32", True, True, True)
+                bufs = [(torch.empty((T, H // per_byte), dtype=torch.uint8, device=dev),
+                         torch.empty((T, H // blk), dtype=torch.uint8, device=dev),
+                         torch.empty((T,), dtype=torch.float32, device=dev)) for _ in sets]
+
+                def call(i, bufs=bufs, code=code, fmt=fmt, flags=flags):
+                    x, r, ro = sets[i % 2]
+                    q, bs, ts = bufs[i % 2]
+                    st = pkg.rmsnorm_fwd_blockscaled(
+                        x.data_ptr(), r.data_ptr(), w.data_ptr(), b.data_ptr(), q.data_ptr(),
+                        bs.data_ptr(), ts.data_ptr() if fmt == "nvfp4" else None, ro.data_ptr(),
+                        T, H, wl.eps, flags, code, 0.0, None,
+                        torch.cuda.current_stream().cuda_stream)
+                    if st != pkg.RMSN_OK:
+                        raise pkg.RmsnError(st, "rmsnorm_fwd_blockscaled")
+            for i in range(2):
+                call(i)
+            torch.cuda.synchronize(dev)
+            g = torch.cuda.CUDAGraph()
+            s = torch.cuda.Stream(dev)
+            s.wait_stream(stream)
+            n = 20
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s):
+                    for i in range(n):
+                        call(i)
+            stream.wait_stream(s)
+            g.replay()
+            torch.cuda.synchronize(dev)
+            a = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(5):
+                g.replay()
+            e.record(stream)
+            torch.cuda.synchronize(dev)
+            us = a.elapsed_time(e) * 1e3 / (5 * n)
+            res[fmt] = {"us": round(us, 2), "gbs": round(nbytes / us / 1e3, 1)}
+        out[f"T{T}_H{H}"] = res
     return out
 
 

@@ -26,10 +26,10 @@ SRC = os.path.join(HERE, "rmsnorm_oracle.c")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD_DIR, "liboracle_rmsnorm.so")
 
-F32, BF16, FP8E4M3, F64 = 0, 1, 2, 3
+F32, BF16, FP8E4M3, F64, F16 = 0, 1, 2, 3, 4
 MXFP8, MXFP4, NVFP4 = 10, 11, 12
 _BLOCK = {"mxfp8": (MXFP8, 32, 1), "mxfp4": (MXFP4, 32, 2), "nvfp4": (NVFP4, 16, 2)}
-_DTYPES = {"f32": F32, "bf16": BF16, "fp8": FP8E4M3, "f64": F64}
+_DTYPES = {"f32": F32, "bf16": BF16, "fp8": FP8E4M3, "f64": F64, "f16": F16}
 
 _lock = threading.Lock()
 _default = None
@@ -68,6 +68,10 @@ class Oracle:
         lib.oracle_e4m3_to_f64.restype = ctypes.c_double
         lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
         lib.oracle_num_cpus.restype = ctypes.c_int
+        lib.oracle_f16_from_f64.restype = ctypes.c_uint16
+        lib.oracle_f16_from_f64.argtypes = [ctypes.c_double]
+        lib.oracle_f16_to_f64.restype = ctypes.c_double
+        lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
         lib.oracle_e2m1_to_f64.restype = ctypes.c_double
         lib.oracle_e2m1_to_f64.argtypes = [ctypes.c_uint8]
         lib.oracle_e2m1_from_f64.restype = ctypes.c_uint8
@@ -96,6 +100,12 @@ class Oracle:
 
     def e4m3_to_f64(self, c: int) -> float:
         return float(self.lib.oracle_e4m3_to_f64(int(c)))
+
+    def f16_from_f64(self, v: float) -> int:
+        return int(self.lib.oracle_f16_from_f64(float(v)))
+
+    def f16_to_f64(self, h: int) -> float:
+        return float(self.lib.oracle_f16_to_f64(int(h)))
 
     def e2m1_from_f64(self, v: float) -> int:
         return int(self.lib.oracle_e2m1_from_f64(float(v)))
@@ -197,13 +207,13 @@ def _host_bits(a, dtype: str) -> np.ndarray:
         import torch
         if isinstance(a, torch.Tensor):
             a = a.detach().cpu().contiguous()
-            if dtype == "bf16":
+            if dtype in ("bf16", "f16"):
                 return a.view(torch.int16).numpy().view(np.uint16)
             return a.numpy()
     except ImportError:  # pragma: no cover
         pass
     a = np.ascontiguousarray(a)
-    if dtype == "bf16":
+    if dtype in ("bf16", "f16"):
         return a.view(np.uint16)
     return a.astype(np.float32, copy=False)
 
@@ -233,7 +243,8 @@ def _rmsnorm(lib, x, residual=None, weight=None, bias=None, *, eps: float, in_dt
     rb = None if residual is None else _host_bits(residual, in_dtype)
     wb = None if weight is None else _host_bits(weight, in_dtype)
     bb = None if bias is None else _host_bits(bias, in_dtype)
-    out_np = {"f32": np.float32, "bf16": np.uint16, "fp8": np.uint8, "f64": np.float64}[out_dtype]
+    out_np = {"f32": np.float32, "bf16": np.uint16, "fp8": np.uint8, "f64": np.float64,
+              "f16": np.uint16}[out_dtype]
     out = np.empty((T, H), dtype=out_np)
     res_out = None if rb is None else np.empty_like(xb)
     scale = np.empty(T, dtype=np.float32) if out_dtype == "fp8" else None

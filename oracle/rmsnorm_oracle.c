@@ -42,7 +42,7 @@
 #include <string.h>
 #include <unistd.h>
 
-enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_FP8E4M3 = 2, ORC_F64 = 3 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_FP8E4M3 = 2, ORC_F64 = 3, ORC_F16 = 4 };
 
 /* ------------------------------------------------------------------ */
 /* number formats                                                      */
@@ -95,6 +95,47 @@ uint16_t oracle_bf16_from_f64(double v) {
 }
 
 float oracle_f32_from_f64(double v) { return (float)v; /* IEEE cast: RNE */ }
+
+/* IEEE-754 binary16: 11 significant bits, normal >= 2^-14, subnormal quantum
+ * 2^-24, largest finite 65504 = (2 - 2^-10) * 2^15; rounding past it gives
+ * infinity. */
+double oracle_f16_to_f64(uint16_t h) {
+    int s = h >> 15, e = (h >> 10) & 31, m = h & 1023;
+    double v;
+    if (e == 31) v = m ? NAN : INFINITY;
+    else if (e == 0) v = ldexp((double)m, -24);
+    else v = ldexp((double)(1024 + m), e - 25);
+    return s ? -v : v;
+}
+
+uint16_t oracle_f16_from_f64(double v) {
+    if (isnan(v)) return 0x7E00;
+    int neg = signbit(v) ? 1 : 0;
+    double a = fabs(v), r;
+    if (isinf(a)) {
+        r = INFINITY;
+    } else if (a == 0.0) {
+        r = 0.0;
+    } else {
+        int e;
+        frexp(a, &e);              /* a in [2^(e-1), 2^e) */
+        int q = e - 11;            /* 11 significant bits */
+        if (q < -24) q = -24;      /* subnormal quantum */
+        r = round_to_quantum(a, q);
+        if (r > 65504.0) r = INFINITY;
+    }
+    uint16_t h;
+    if (isinf(r)) {
+        h = 0x7C00;
+    } else if (r < ldexp(1.0, -14)) {
+        h = (uint16_t)ldexp(r, 24);          /* subnormal: m * 2^-24 */
+    } else {
+        int e;
+        double f = frexp(r, &e);             /* r = f * 2^e, f in [0.5, 1) */
+        h = (uint16_t)(((e - 1 + 15) << 10) | ((int)ldexp(f, 11) - 1024));
+    }
+    return (uint16_t)(h | (neg ? 0x8000 : 0));
+}
 
 double oracle_e4m3_to_f64(uint8_t c) {
     int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
@@ -155,7 +196,7 @@ static double load_in(const void *p, int dtype, int64_t i) {
     if (dtype == ORC_F32) return f32_bits_to_f64(p, i);
     uint16_t b;
     memcpy(&b, (const char *)p + 2 * i, 2);
-    return oracle_bf16_to_f64(b);
+    return dtype == ORC_F16 ? oracle_f16_to_f64(b) : oracle_bf16_to_f64(b);
 }
 
 /* RN to the input type; returns the rounded value and stores its bits. */
@@ -164,6 +205,11 @@ static double round_store_in(void *p, int dtype, int64_t i, double v) {
         float f = oracle_f32_from_f64(v);
         if (p) memcpy((char *)p + 4 * i, &f, 4);
         return (double)f;
+    }
+    if (dtype == ORC_F16) {
+        uint16_t h = oracle_f16_from_f64(v);
+        if (p) memcpy((char *)p + 2 * i, &h, 2);
+        return oracle_f16_to_f64(h);
     }
     uint16_t b = oracle_bf16_from_f64(v);
     if (p) memcpy((char *)p + 2 * i, &b, 2);
@@ -209,6 +255,12 @@ static void norm_row(const job_t *J, int64_t t, double *h, double *yhat) {
         for (int64_t j = 0; j < H; ++j) {
             uint16_t b = oracle_bf16_from_f64(yhat[j]);
             memcpy((char *)J->out + 2 * (base + j), &b, 2);
+        }
+        break;
+    case ORC_F16:
+        for (int64_t j = 0; j < H; ++j) {
+            uint16_t h = oracle_f16_from_f64(yhat[j]);
+            memcpy((char *)J->out + 2 * (base + j), &h, 2);
         }
         break;
     case ORC_FP8E4M3: {
@@ -258,8 +310,8 @@ int oracle_rmsnorm(const void *x, const void *residual, const void *weight, cons
                    int64_t hidden, double eps, double weight_offset, int in_dtype,
                    int out_dtype, int n_threads) {
     if (n_tokens < 0 || hidden <= 0) return -1;
-    if (in_dtype != ORC_F32 && in_dtype != ORC_BF16) return -1;
-    if (out_dtype < ORC_F32 || out_dtype > ORC_F64) return -1;
+    if (in_dtype != ORC_F32 && in_dtype != ORC_BF16 && in_dtype != ORC_F16) return -1;
+    if (out_dtype < ORC_F32 || out_dtype > ORC_F16) return -1;
     if (!x || !out || (residual && !residual_out)) return -1;
     if (out_dtype == ORC_FP8E4M3 && !out_scale) return -1;
     if (n_tokens == 0) return 0;
@@ -335,7 +387,7 @@ int oracle_qk_norm(void *q, void *k, const void *q_weight, const void *k_weight,
                    int64_t q_token_stride, int64_t k_token_stride, double eps,
                    double weight_offset, int dtype) {
     if (n_tokens < 0 || n_q_heads < 0 || n_k_heads < 0 || head_dim <= 0) return -1;
-    if (dtype != ORC_F32 && dtype != ORC_BF16) return -1;
+    if (dtype != ORC_F32 && dtype != ORC_BF16 && dtype != ORC_F16) return -1;
     if (q_token_stride < n_q_heads * head_dim || k_token_stride < n_k_heads * head_dim) return -1;
     if ((n_q_heads && !q) || (n_k_heads && !k)) return -1;
     for (int64_t t = 0; t < n_tokens; ++t) {

@@ -103,6 +103,88 @@ def test_bf16_encoder_rounds_f64_once(oracle_mod):
             assert oracle_mod.bf16_from_f64(v) == exact_round_bf16(Fraction(v))
 
 
+# ---------------------------------------------------------------- f16 encoder
+
+
+def _f16_value(h: int) -> Fraction:
+    return Fraction(float(np.array([h], dtype=np.uint16).view(np.float16)[0]))
+
+
+def exact_round_f16(v: Fraction) -> int:
+    """binary16 bits of finite v rounded to nearest, ties to the even code."""
+    neg = v < 0
+    a = -v if neg else v
+    if a == 0:
+        return 0x8000 if neg else 0
+    lo, hi = 0x0000, 0x7C00
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if _f16_value(mid) <= a:
+            lo = mid
+        else:
+            hi = mid
+    d0, d1 = a - _f16_value(lo), (_f16_value(hi) - a) if hi < 0x7C00 else None
+    if hi == 0x7C00:  # beyond the largest finite: overflow threshold max + half ulp
+        c = lo if a - _f16_value(0x7BFF) < Fraction(16) else 0x7C00
+    elif d0 < d1 or (d0 == d1 and lo % 2 == 0):
+        c = lo
+    else:
+        c = hi
+    return c | (0x8000 if neg else 0)
+
+
+def _check_f16_encoder(orc):
+    rng = np.random.default_rng(60)
+    bits = rng.integers(0, 2**32, size=20000, dtype=np.uint64).astype(np.uint32)
+    vals = bits.view(np.float32)
+    vals = vals[np.isfinite(vals)]
+    ref = torch.from_numpy(vals.copy()).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([orc.f16_from_f64(float(v)) for v in vals], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+    # every tie and its f32 neighbours in a normal and the subnormal binade, overflow edge
+    codes = np.concatenate([np.arange(0x3800, 0x3C00), np.arange(0x0000, 0x0400)]).astype(np.uint16)
+    f = codes.view(np.float16).astype(np.float32)
+    nxt = (codes + 1).astype(np.uint16).view(np.float16).astype(np.float32)
+    mids = ((f.astype(np.float64) + nxt) / 2).astype(np.float32)
+    cand = np.concatenate([mids, np.nextafter(mids, 0), np.nextafter(mids, 1)])
+    ref = torch.from_numpy(cand).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([orc.f16_from_f64(float(v)) for v in cand], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+    assert orc.f16_from_f64(65504.0) == 0x7BFF and orc.f16_from_f64(65519.99) == 0x7BFF
+    assert orc.f16_from_f64(65520.0) == 0x7C00 and orc.f16_from_f64(-1e9) == 0xFC00
+    for c in rng.integers(0x0400, 0x7B00, size=200):
+        mid = float(_f16_value(int(c)) + _f16_value(int(c) + 1)) / 2
+        for v in (mid * (1 + 2.0**-40), mid * (1 - 2.0**-40)):
+            assert orc.f16_from_f64(v) == exact_round_f16(Fraction(v))
+
+
+def test_f16_encoder(oracle_mod):
+    _check_f16_encoder(oracle_mod.default())
+
+
+def _check_f16_norm(orc):
+    # residual: the f32 sum of two fp16 values rounded to fp16 (torch) equals
+    # the exact sum rounded once; the fp16 output is the f64 output rounded
+    rng = np.random.default_rng(61)
+    x = torch.from_numpy(rng.standard_normal((8, 256)).astype(np.float32) * 30).to(torch.float16)
+    r = torch.from_numpy(rng.standard_normal((8, 256)).astype(np.float32)).to(torch.float16)
+    w = torch.from_numpy((1 + 0.1 * rng.standard_normal(256)).astype(np.float32)).to(torch.float16)
+    o = orc.rmsnorm(x, r, w, None, eps=1e-6, in_dtype="f16", out_dtype="f16")
+    ref_res = (x.float() + r.float()).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(o["residual_out"], ref_res)
+    y = orc.rmsnorm(x, r, w, None, eps=1e-6, in_dtype="f16", out_dtype="f64")["out"]
+    for i in range(0, 8 * 256, 29):
+        assert o["out"].flat[i] == exact_round_f16(Fraction(float(y.flat[i])))
+    # the fp16 norm equals the fp32-input norm of the widened rounded residual
+    h = torch.from_numpy(o["residual_out"].view(np.int16)).view(torch.float16).float()
+    o_h = orc.rmsnorm(h, None, w.float(), None, eps=1e-6, in_dtype="f32", out_dtype="f64")["out"]
+    assert np.array_equal(y, o_h)
+
+
+def test_f16_norm_paths(oracle_mod):
+    _check_f16_norm(oracle_mod.default())
+
+
 # ---------------------------------------------------------------- e4m3 encoder
 
 
@@ -647,6 +729,9 @@ MUTANTS = {
     "nvfp4_scale_uses_4": ("amax / (6.0 * (double)g)", "amax / (4.0 * (double)g)"),
     "e2m1_ties_up": ("r = round_to_quantum(a, q);\n        if (r > 6.0)",
                      "r = ldexp(floor(ldexp(a, -q) + 0.5), q);\n        if (r > 6.0)"),
+    "f16_max_wrong": ("if (r > 65504.0) r = INFINITY;", "if (r > 65472.0) r = INFINITY;"),
+    "f16_loads_as_bf16": ("return dtype == ORC_F16 ? oracle_f16_to_f64(b) : oracle_bf16_to_f64(b);",
+                          "return oracle_bf16_to_f64(b);"),
     "e4m3_ties_up": ("r = round_to_quantum(a, q);\n        if (r > 448.0)",
                      "r = ldexp(floor(ldexp(a, -q) + 0.5), q);\n        if (r > 448.0)"),
 }
@@ -671,6 +756,8 @@ def all_pin_checks(orc):
     checks.append(lambda: _check_qk_constant_heads(orc))
     checks.append(lambda: _check_qk_strided_fused_qkv(orc))
     checks.append(lambda: _check_e2m1_encoder(orc))
+    checks.append(lambda: _check_f16_encoder(orc))
+    checks.append(lambda: _check_f16_norm(orc))
     checks.append(lambda: _check_mx_exact_blocks(orc))
     checks.append(lambda: _check_block_error_bounds(orc))
     failed = 0
