@@ -50,11 +50,13 @@ typedef enum {
 /* flags: input dtype (x, residual, weight, bias, residual_out share it) */
 #define RMSN_IN_F32 0x0u
 #define RMSN_IN_BF16 0x1u
+#define RMSN_IN_F16 0x2u
 #define RMSN_IN_MASK 0x3u
 /* output dtype of `out` */
 #define RMSN_OUT_F32 0x0u
 #define RMSN_OUT_BF16 0x4u
 #define RMSN_OUT_FP8E4M3 0x8u
+#define RMSN_OUT_F16 0xCu
 #define RMSN_OUT_MASK 0xCu
 /* optional operands; each must match a non-NULL pointer */
 #define RMSN_HAS_RESIDUAL 0x10u /* residual and residual_out */
@@ -193,8 +195,9 @@ int rmsnorm_fwd_host(const void* x, const void* residual, const void* weight, co
  * of q (n_q_heads heads of head_dim elements, back to back); likewise k.  The
  * strides let q and k sit inside a fused qkv row; elements outside the heads
  * are not touched.  The q buffer must span (n_tokens - 1) * q_token_stride +
- * n_q_heads * head_dim elements (likewise k).  flags: RMSN_IN_F32 or
- * RMSN_IN_BF16 (q, k and weights share it), optionally RMSN_PDL.  One launch
+ * n_q_heads * head_dim elements (likewise k).  flags: RMSN_IN_F32,
+ * RMSN_IN_BF16 or RMSN_IN_F16 (q, k and weights share it), optionally
+ * RMSN_PDL.  One launch
  * covers both q and k.  The fast path needs head_dim * element size to be a
  * multiple of 32 bytes and at most 1024 bytes (head_dim 64, 128, 256 in bf16
  * and fp32, 512 in bf16), 32-byte aligned pointers and token strides;

@@ -20,9 +20,11 @@ RMSN_ECUDA = -4
 
 RMSN_IN_F32 = 0x0
 RMSN_IN_BF16 = 0x1
+RMSN_IN_F16 = 0x2
 RMSN_OUT_F32 = 0x0
 RMSN_OUT_BF16 = 0x4
 RMSN_OUT_FP8E4M3 = 0x8
+RMSN_OUT_F16 = 0xC
 RMSN_HAS_RESIDUAL = 0x10
 RMSN_HAS_WEIGHT = 0x20
 RMSN_HAS_BIAS = 0x40

@@ -10,15 +10,16 @@ import torch
 
 from . import _lib
 
-_IN = {torch.float32: _lib.RMSN_IN_F32, torch.bfloat16: _lib.RMSN_IN_BF16}
+_IN = {torch.float32: _lib.RMSN_IN_F32, torch.bfloat16: _lib.RMSN_IN_BF16,
+       torch.float16: _lib.RMSN_IN_F16}
 _OUT = {"f32": (_lib.RMSN_OUT_F32, torch.float32), "bf16": (_lib.RMSN_OUT_BF16, torch.bfloat16),
-        "fp8": (_lib.RMSN_OUT_FP8E4M3, torch.uint8)}
-_DT_NAME = {torch.float32: "f32", torch.bfloat16: "bf16"}
+        "fp8": (_lib.RMSN_OUT_FP8E4M3, torch.uint8), "f16": (_lib.RMSN_OUT_F16, torch.float16)}
+_DT_NAME = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}
 
 
 def make_flags(in_dtype: str, out_dtype: str, residual: bool, weight: bool, bias: bool,
                pdl: bool = False, early_params: bool = False) -> int:
-    f = {"f32": _lib.RMSN_IN_F32, "bf16": _lib.RMSN_IN_BF16}[in_dtype]
+    f = {"f32": _lib.RMSN_IN_F32, "bf16": _lib.RMSN_IN_BF16, "f16": _lib.RMSN_IN_F16}[in_dtype]
     if pdl:
         f |= _lib.RMSN_PDL
     if early_params:

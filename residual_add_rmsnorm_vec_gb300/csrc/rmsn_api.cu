@@ -104,11 +104,11 @@ int enable_smem(DeviceInfo* d, const void* fn) {
 const std::vector<KernelEntry>& registry() {
     static const std::vector<KernelEntry> all = [] {
         std::vector<KernelEntry> v;
-        const KernelEntry* (*fns[])(int*) = {kernels_f32_f32,    kernels_f32_bf16,
-                                             kernels_f32_fp8,    kernels_bf16_f32,
-                                             kernels_bf16_bf16,  kernels_bf16_fp8,
-                                             kernels_bf16_mxfp8, kernels_bf16_mxfp4,
-                                             kernels_bf16_nvfp4};
+        const KernelEntry* (*fns[])(int*) = {
+            kernels_f32_f32,  kernels_f32_bf16,  kernels_f32_fp8,    kernels_f32_f16,
+            kernels_bf16_f32, kernels_bf16_bf16, kernels_bf16_fp8,   kernels_f16_f16,
+            kernels_f16_f32,  kernels_f16_fp8,   kernels_bf16_mxfp8, kernels_bf16_mxfp4,
+            kernels_bf16_nvfp4};
         for (auto fn : fns) {
             int n = 0;
             const KernelEntry* t = fn(&n);
@@ -130,7 +130,7 @@ struct Problem {
     bool vec_ok;
 };
 
-int dtype_bytes(int dt) { return dt == kF32 ? 4 : (dt == kBF16 ? 2 : 1); }
+int dtype_bytes(int dt) { return dt == kF32 ? 4 : ((dt == kBF16 || dt == kF16) ? 2 : 1); }
 
 bool aligned(const void* p, uintptr_t a) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -141,11 +141,12 @@ int decode_flags(uint32_t flags, Problem* p) {
     const uint32_t in = flags & RMSN_IN_MASK, out = flags & RMSN_OUT_MASK;
     if (in == RMSN_IN_F32) p->in_dt = kF32;
     else if (in == RMSN_IN_BF16) p->in_dt = kBF16;
+    else if (in == RMSN_IN_F16) p->in_dt = kF16;
     else return RMSN_EINVAL;
     if (out == RMSN_OUT_F32) p->out_dt = kF32;
     else if (out == RMSN_OUT_BF16) p->out_dt = kBF16;
     else if (out == RMSN_OUT_FP8E4M3) p->out_dt = kFP8;
-    else return RMSN_EINVAL;
+    else p->out_dt = kF16;  // RMSN_OUT_F16
     if ((flags & RMSN_PDL_EARLY_PARAMS) && !(flags & RMSN_PDL)) return RMSN_EINVAL;
     p->pdl = (flags & RMSN_PDL) != 0;
     p->early_params = (flags & RMSN_PDL_EARLY_PARAMS) != 0;
@@ -630,8 +631,8 @@ RMSN_API int rmsnorm_qk_fwd(void* q, void* k, const void* q_weight, const void* 
                             float eps, float weight_offset, uint32_t flags, cudaStream_t stream) {
     if (flags & ~(RMSN_IN_MASK | RMSN_PDL)) return RMSN_EINVAL;
     const uint32_t in = flags & RMSN_IN_MASK;
-    if (in != RMSN_IN_F32 && in != RMSN_IN_BF16) return RMSN_EINVAL;
-    const int dt = in == RMSN_IN_F32 ? kF32 : kBF16;
+    if (in != RMSN_IN_F32 && in != RMSN_IN_BF16 && in != RMSN_IN_F16) return RMSN_EINVAL;
+    const int dt = in == RMSN_IN_F32 ? kF32 : (in == RMSN_IN_BF16 ? kBF16 : kF16);
     const int64_t bytes = dt == kF32 ? 4 : 2;
     if (n_tokens < 0 || n_q_heads < 0 || n_k_heads < 0 || head_dim < 1 || head_dim > 4096)
         return RMSN_EINVAL;

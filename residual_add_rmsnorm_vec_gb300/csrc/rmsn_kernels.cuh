@@ -36,6 +36,17 @@ struct F32 {
 struct BF16 {
     static constexpr int kBytes = 2;
 };
+struct F16 {
+    static constexpr int kBytes = 2;
+};
+template <class T>
+struct IsF16 {
+    static constexpr bool value = false;
+};
+template <>
+struct IsF16<F16> {
+    static constexpr bool value = true;
+};
 struct FP8 {
     static constexpr int kBytes = 1;
 };
@@ -126,6 +137,37 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return d;
 }
 
+__device__ __forceinline__ float f16_to_f32(uint32_t bits) {
+    float f;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"((uint16_t)(bits & 0xFFFFu)));
+    return f;
+}
+
+// Round two floats to IEEE binary16 (nearest-even) and pack them, `lo` in the
+// low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// The two 16-bit elements of a word of a 2-byte type T, and the reverse.
+template <class T>
+__device__ __forceinline__ float lo2(uint32_t u) {
+    if constexpr (IsF16<T>::value) return f16_to_f32(u);
+    else return bf16_lo(u);
+}
+template <class T>
+__device__ __forceinline__ float hi2(uint32_t u) {
+    if constexpr (IsF16<T>::value) return f16_to_f32(u >> 16);
+    else return bf16_hi(u);
+}
+template <class T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (IsF16<T>::value) return pack_f16x2(lo, hi);
+    else return pack_bf16x2(lo, hi);
+}
+
 // Round four floats to E4M3 (nearest-even, saturating to +-448), element 0
 // in the lowest byte.
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a0, float a1, float a2, float a3) {
@@ -166,7 +208,7 @@ __device__ __forceinline__ float e4m3_value(uint32_t c) {
 template <class TI>
 __device__ __forceinline__ float elem(const V8& v, int k) {
     if constexpr (TI::kBytes == 2) {
-        return (k & 1) ? bf16_hi(v.u[k >> 1]) : bf16_lo(v.u[k >> 1]);
+        return (k & 1) ? hi2<TI>(v.u[k >> 1]) : lo2<TI>(v.u[k >> 1]);
     } else {
         return __uint_as_float(v.u[k]);
     }
@@ -181,6 +223,7 @@ __device__ __forceinline__ void opaque(V8& v) {
 
 template <class TI>
 __device__ __forceinline__ uint32_t ones_word() {
+    if constexpr (IsF16<TI>::value) return 0x3C003C00u;
     return TI::kBytes == 2 ? 0x3F803F80u : 0x3F800000u;
 }
 
@@ -258,7 +301,7 @@ __device__ __forceinline__ void store_out(void* out, int64_t e, const float (&y)
     } else if constexpr (TO::kBytes == 2) {
         uint32_t u[VE / 2];
 #pragma unroll
-        for (int k = 0; k < VE / 2; ++k) u[k] = pack_bf16x2(y[2 * k], y[2 * k + 1]);
+        for (int k = 0; k < VE / 2; ++k) u[k] = pack2<TO>(y[2 * k], y[2 * k + 1]);
         uint16_t* o = reinterpret_cast<uint16_t*>(out) + e;
         if constexpr (VE == 16) st_stream32(o, u);
         else st_stream16(o, u);
@@ -325,9 +368,9 @@ __device__ __forceinline__ float residual_sumsq(const RmsnArgs& a, int64_t rbase
                 if constexpr (TI::kBytes == 2) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const float lo = __fadd_rn(bf16_lo(hv[c].u[k]), bf16_lo(rv[c].u[k]));
-                        const float hi = __fadd_rn(bf16_hi(hv[c].u[k]), bf16_hi(rv[c].u[k]));
-                        hv[c].u[k] = pack_bf16x2(lo, hi);
+                        const float lo = __fadd_rn(lo2<TI>(hv[c].u[k]), lo2<TI>(rv[c].u[k]));
+                        const float hi = __fadd_rn(hi2<TI>(hv[c].u[k]), hi2<TI>(rv[c].u[k]));
+                        hv[c].u[k] = pack2<TI>(lo, hi);
                     }
                 } else {
 #pragma unroll
@@ -726,7 +769,7 @@ __global__ void __launch_bounds__(WMAX * 32, 1) rmsn_bulk_kernel(const RmsnArgs 
 template <class T>
 __device__ __forceinline__ float ld_elem(const void* p, int64_t i) {
     if constexpr (T::kBytes == 2) {
-        return __uint_as_float((uint32_t)(static_cast<const uint16_t*>(p)[i]) << 16);
+        return lo2<T>((uint32_t)(static_cast<const uint16_t*>(p)[i]));
     } else {
         return static_cast<const float*>(p)[i];
     }
@@ -735,7 +778,7 @@ __device__ __forceinline__ float ld_elem(const void* p, int64_t i) {
 template <class T>
 __device__ __forceinline__ float round_to(float v) {
     if constexpr (T::kBytes == 2) {
-        return bf16_lo(pack_bf16x2(v, 0.f));
+        return lo2<T>(pack2<T>(v, 0.f));
     } else {
         return v;
     }
@@ -744,7 +787,7 @@ __device__ __forceinline__ float round_to(float v) {
 template <class T>
 __device__ __forceinline__ void st_elem(void* p, int64_t i, float v) {
     if constexpr (T::kBytes == 2) {
-        static_cast<uint16_t*>(p)[i] = (uint16_t)(pack_bf16x2(v, 0.f) & 0xFFFFu);
+        static_cast<uint16_t*>(p)[i] = (uint16_t)(pack2<T>(v, 0.f) & 0xFFFFu);
     } else {
         static_cast<float*>(p)[i] = v;
     }

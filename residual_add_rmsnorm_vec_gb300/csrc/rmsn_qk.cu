@@ -77,6 +77,8 @@ static const QkEntry kQkTable[] = {
     RMSN_QK(BF16, kBF16, 8), RMSN_QK(BF16, kBF16, 16), RMSN_QK(BF16, kBF16, 32),
     RMSN_QK(F32, kF32, 1),   RMSN_QK(F32, kF32, 2),    RMSN_QK(F32, kF32, 4),
     RMSN_QK(F32, kF32, 8),   RMSN_QK(F32, kF32, 16),   RMSN_QK(F32, kF32, 32),
+    RMSN_QK(F16, kF16, 1),   RMSN_QK(F16, kF16, 2),    RMSN_QK(F16, kF16, 4),
+    RMSN_QK(F16, kF16, 8),   RMSN_QK(F16, kF16, 16),   RMSN_QK(F16, kF16, 32),
 };
 
 const QkEntry* qk_kernels(int* n) {

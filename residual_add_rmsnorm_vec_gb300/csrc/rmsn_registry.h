@@ -28,7 +28,9 @@ struct RmsnArgs {
     uint32_t* status;    // device status word: bit 0 = a bounded wait ran out
 };
 
-enum DType : int32_t { kF32 = 0, kBF16 = 1, kFP8 = 2, kMXFP8 = 3, kMXFP4 = 4, kNVFP4 = 5 };
+enum DType : int32_t {
+    kF32 = 0, kBF16 = 1, kFP8 = 2, kMXFP8 = 3, kMXFP4 = 4, kNVFP4 = 5, kF16 = 6
+};
 
 enum Variant : int32_t { kWarpRows = 0, kBlockRow = 1, kBulkRow = 2, kGeneric = 3 };
 
@@ -45,6 +47,10 @@ const KernelEntry* kernels_f32_fp8(int* n);
 const KernelEntry* kernels_bf16_f32(int* n);
 const KernelEntry* kernels_bf16_bf16(int* n);
 const KernelEntry* kernels_bf16_fp8(int* n);
+const KernelEntry* kernels_f16_f16(int* n);
+const KernelEntry* kernels_f16_f32(int* n);
+const KernelEntry* kernels_f16_fp8(int* n);
+const KernelEntry* kernels_f32_f16(int* n);
 const KernelEntry* kernels_bf16_mxfp8(int* n);
 const KernelEntry* kernels_bf16_mxfp4(int* n);
 const KernelEntry* kernels_bf16_nvfp4(int* n);

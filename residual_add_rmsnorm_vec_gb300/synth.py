@@ -58,8 +58,8 @@ class Workload:
     n_tokens: int
     hidden: int
     seed: int
-    in_dtype: str              # "f32" | "bf16"
-    out_dtype: str             # "f32" | "bf16" | "fp8"
+    in_dtype: str              # "f32" | "bf16" | "f16"
+    out_dtype: str             # "f32" | "bf16" | "f16" | "fp8"
     eps: float
     has_residual: bool = True
     has_weight: bool = True
@@ -72,11 +72,11 @@ class Workload:
 
     @property
     def in_bytes(self) -> int:
-        return 4 if self.in_dtype == "f32" else 2
+        return 4 if self.in_dtype == "f32" else 2  # bf16 / f16
 
     @property
     def out_bytes(self) -> int:
-        return {"f32": 4, "bf16": 2, "fp8": 1}[self.out_dtype]
+        return {"f32": 4, "bf16": 2, "f16": 2, "fp8": 1}[self.out_dtype]
 
     def algorithmic_bytes(self) -> int:
         """Minimum HBM bytes one call must move (each tensor touched once)."""
@@ -201,6 +201,8 @@ def to_storage(a: np.ndarray, dtype: str):
         return t
     if dtype == "bf16":
         return t.to(torch.bfloat16)
+    if dtype == "f16":
+        return t.to(torch.float16)
     raise ValueError(dtype)
 
 

@@ -2,7 +2,8 @@
 and compare with the tolerances of the fused residual-add + RMSNorm:
 
 * residual_out: bit-exact;
-* bf16 output: at most 1 bf16 ulp (signed-magnitude ordering, +0 == -0);
+* bf16 / fp16 output: at most 1 ulp of the output type (signed-magnitude
+  ordering, +0 == -0);
 * fp32 output: relative error <= 1e-5, measured against |y| + |b_j| when a
   bias is present (the fp32 rounding of w*h*inv is carried into y even where
   the bias cancels it; without a bias this is the plain relative error);
@@ -49,7 +50,7 @@ def oracle_run(wl, inp: dict, weight_offset: float = 0.0) -> dict:
 
 
 def gpu_outputs_to_host(wl, out, res, scale) -> dict:
-    if wl.out_dtype == "bf16":
+    if wl.out_dtype in ("bf16", "f16"):
         o = bits16(out)
     elif wl.out_dtype == "fp8":
         o = out.detach().cpu().numpy()
@@ -57,7 +58,7 @@ def gpu_outputs_to_host(wl, out, res, scale) -> dict:
         o = out.detach().cpu().numpy()
     r = None
     if res is not None:
-        r = bits16(res) if wl.in_dtype == "bf16" else res.detach().cpu().numpy()
+        r = bits16(res) if wl.in_dtype in ("bf16", "f16") else res.detach().cpu().numpy()
     s = None if scale is None else scale.detach().cpu().numpy()
     return {"out": o, "residual_out": r, "out_scale": s}
 
@@ -68,12 +69,13 @@ def compare(wl, got: dict, ref: dict, where: str = "", bias=None) -> dict:
     stats = {}
     if ref["residual_out"] is not None:
         g, r = got["residual_out"], ref["residual_out"]
-        if wl.in_dtype == "bf16":
+        if wl.in_dtype in ("bf16", "f16"):
             bad = np.count_nonzero(g != r)
         else:
             bad = np.count_nonzero(g.view(np.uint32) != r.view(np.uint32))
         assert bad == 0, f"{where}: residual_out differs in {bad} elements"
-    if wl.out_dtype == "bf16":
+    if wl.out_dtype in ("bf16", "f16"):
+        # 1 ulp of the output type (signed-magnitude order works for both)
         d = np.abs(ordered16(got["out"]) - ordered16(ref["out"]))
         stats["max_ulp"] = int(d.max()) if d.size else 0
         stats["exact_frac"] = float((d == 0).mean()) if d.size else 1.0

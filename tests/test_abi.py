@@ -67,7 +67,6 @@ BF16_RES = 0x1 | 0x4 | 0x10 | 0x20  # bf16 in/out, residual, weight
     ("unknown flag bit", (16, 16, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES | 0x200)),
     ("early params without pdl", (16, 16, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES | 0x100)),
     ("bad input dtype", (16, 16, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES | 0x2)),
-    ("bad output dtype", (16, 16, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES | 0xC)),
     ("residual flag without pointer", (16, None, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES)),
     ("residual_out missing", (16, 16, 16, None, 16, None, None, 4, 64, 1e-6, BF16_RES)),
     ("pointer without flag", (16, 16, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES & ~0x20 | 0)),

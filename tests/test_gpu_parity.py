@@ -117,6 +117,11 @@ FLAG_SETS = [
     ("f32", "f32", True, True, True),
     ("f32", "bf16", True, True, False),
     ("f32", "fp8", True, True, True),
+    ("f16", "f16", True, True, False),
+    ("f16", "f16", True, True, True),
+    ("f16", "fp8", True, True, True),
+    ("f16", "f32", False, True, False),
+    ("f32", "f16", True, True, False),
 ]
 
 
@@ -144,6 +149,19 @@ def test_every_config(pkg, fs, H):
     assert pkg.VARIANT_GENERIC in variants and pkg.VARIANT_BLOCK_ROW in variants
     assert pkg.VARIANT_BULK_ROW in variants
     assert pkg.rmsnorm_read_status() == 0
+
+
+@pytest.mark.parametrize("T,H", [(1, 4096), (256, 4096), (2048, 8192), (4096, 5120)])
+def test_fp16_io(pkg, T, H):
+    wl = synth.Workload(f"f16_T{T}_H{H}", T, H, 80, "f16", "f16", 1e-6, has_bias=H == 5120,
+                        r_std=2.0)
+    st = check(pkg, wl)
+    assert st["exact_frac"] > 0.99
+
+
+@pytest.mark.parametrize("H", [1, 7, 1000, 4097])
+def test_fp16_ragged_generic(pkg, H):
+    check(pkg, synth.Workload(f"f16_ragged_H{H}", 21, H, 81, "f16", "f16", 1e-6, has_bias=True))
 
 
 def test_weight_offset(pkg):

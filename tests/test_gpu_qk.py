@@ -28,11 +28,11 @@ def pkg():
 
 def bits(t, dtype):
     t = t.detach().cpu().contiguous()
-    return t.view(torch.int16).numpy().view(np.uint16) if dtype == "bf16" else t.numpy()
+    return t.view(torch.int16).numpy().view(np.uint16) if dtype in ("bf16", "f16") else t.numpy()
 
 
 def compare(dtype, got, ref, where):
-    if dtype == "bf16":
+    if dtype in ("bf16", "f16"):
         d = np.abs(parity.ordered16(got) - parity.ordered16(ref))
         assert d.max() <= parity.BF16_ULP, f"{where}: {d.max()} ulp"
         return float((d == 0).mean())
@@ -45,6 +45,7 @@ def compare(dtype, got, ref, where):
     (1, 32, 8, 128, "bf16"), (7, 16, 4, 64, "bf16"), (512, 32, 8, 128, "bf16"),
     (4096, 32, 8, 128, "bf16"), (33, 8, 2, 256, "bf16"), (3, 2, 1, 512, "bf16"),
     (5, 4, 4, 128, "f32"), (65, 6, 2, 64, "f32"), (9, 3, 1, 256, "f32"), (2, 1, 1, 16, "bf16"),
+    (17, 32, 8, 128, "f16"), (3, 4, 2, 64, "f16"), (5, 2, 2, 256, "f16"),
 ])
 @pytest.mark.parametrize("pad", [0, 16])
 def test_qk_norm_fused_qkv(pkg, T, Hq, Hk, D, dtype, pad):
