@@ -59,6 +59,10 @@ class Oracle:
         lib.oracle_rmsnorm.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64,
                                        ctypes.c_double, ctypes.c_double,
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        lib.oracle_rmsnorm_res.restype = ctypes.c_int
+        lib.oracle_rmsnorm_res.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64,
+                                           ctypes.c_double, ctypes.c_double,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
         lib.oracle_bf16_from_f64.restype = ctypes.c_uint16
         lib.oracle_bf16_from_f64.argtypes = [ctypes.c_double]
         lib.oracle_bf16_to_f64.restype = ctypes.c_double
@@ -167,10 +171,10 @@ class Oracle:
 
     def rmsnorm(self, x, residual=None, weight=None, bias=None, *, eps: float,
                 in_dtype: str, out_dtype: str, weight_offset: float = 0.0,
-                n_threads: int = 0) -> dict:
+                n_threads: int = 0, residual_dtype: str | None = None) -> dict:
         return _rmsnorm(self.lib, x, residual, weight, bias, eps=eps, in_dtype=in_dtype,
                         out_dtype=out_dtype, weight_offset=weight_offset,
-                        n_threads=n_threads)
+                        n_threads=n_threads, residual_dtype=residual_dtype)
 
 
 def default() -> Oracle:
@@ -219,42 +223,47 @@ def _host_bits(a, dtype: str) -> np.ndarray:
 
 
 def rmsnorm(x, residual=None, weight=None, bias=None, *, eps: float, in_dtype: str,
-            out_dtype: str, weight_offset: float = 0.0, n_threads: int = 0) -> dict:
+            out_dtype: str, weight_offset: float = 0.0, n_threads: int = 0,
+            residual_dtype: str | None = None) -> dict:
     """Run the oracle on CPU inputs; see ``_rmsnorm``."""
     return default().rmsnorm(x, residual, weight, bias, eps=eps, in_dtype=in_dtype,
                              out_dtype=out_dtype, weight_offset=weight_offset,
-                             n_threads=n_threads)
+                             n_threads=n_threads, residual_dtype=residual_dtype)
 
 
 def _rmsnorm(lib, x, residual=None, weight=None, bias=None, *, eps: float, in_dtype: str,
-             out_dtype: str, weight_offset: float = 0.0, n_threads: int = 0) -> dict:
+             out_dtype: str, weight_offset: float = 0.0, n_threads: int = 0,
+             residual_dtype: str | None = None) -> dict:
     """Run the oracle on CPU inputs ([T, H] x / residual, [H] weight / bias).
 
     Inputs are torch CPU tensors or numpy arrays of the storage dtype
     (bf16 given as uint16 bits when numpy).  Returns numpy arrays:
-    ``out`` (float32 for f32, uint16 bits for bf16, uint8 codes for fp8,
-    float64 for f64), ``residual_out`` (same storage as the inputs, or None)
+    ``out`` (float32 for f32, uint16 bits for bf16 / f16, uint8 codes for fp8,
+    float64 for f64), ``residual_out`` (storage of the residual, which is the
+    input dtype unless ``residual_dtype`` says otherwise; or None)
     and ``out_scale`` (float32 [T], fp8 only).
     """
     xb = _host_bits(x, in_dtype)
     if xb.ndim != 2:
         raise ValueError("x must be [T, H]")
     T, H = xb.shape
-    rb = None if residual is None else _host_bits(residual, in_dtype)
+    res_dt = residual_dtype or in_dtype
+    rb = None if residual is None else _host_bits(residual, res_dt)
     wb = None if weight is None else _host_bits(weight, in_dtype)
     bb = None if bias is None else _host_bits(bias, in_dtype)
     out_np = {"f32": np.float32, "bf16": np.uint16, "fp8": np.uint8, "f64": np.float64,
               "f16": np.uint16}[out_dtype]
     out = np.empty((T, H), dtype=out_np)
-    res_out = None if rb is None else np.empty_like(xb)
+    res_out = None if rb is None else np.empty_like(rb)
     scale = np.empty(T, dtype=np.float32) if out_dtype == "fp8" else None
 
     def ptr(a):
         return None if a is None else a.ctypes.data
 
-    st = lib.oracle_rmsnorm(ptr(xb), ptr(rb), ptr(wb), ptr(bb), ptr(out), ptr(res_out),
-                            ptr(scale), T, H, float(eps), float(weight_offset),
-                            _DTYPES[in_dtype], _DTYPES[out_dtype], int(n_threads))
+    st = lib.oracle_rmsnorm_res(ptr(xb), ptr(rb), ptr(wb), ptr(bb), ptr(out), ptr(res_out),
+                                ptr(scale), T, H, float(eps), float(weight_offset),
+                                _DTYPES[in_dtype], _DTYPES[res_dt], _DTYPES[out_dtype],
+                                int(n_threads))
     if st != 0:
         raise RuntimeError(f"oracle_rmsnorm failed with status {st}")
     return {"out": out, "residual_out": res_out, "out_scale": scale}

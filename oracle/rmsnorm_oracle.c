@@ -188,6 +188,7 @@ typedef struct {
     int64_t n_tokens, hidden;
     double eps, weight_offset;
     int in_dtype, out_dtype;
+    int res_dtype; /* storage of residual and residual_out */
     int64_t row_begin, row_end;
     int status;
 } job_t;
@@ -223,8 +224,8 @@ static void norm_row(const job_t *J, int64_t t, double *h, double *yhat) {
     for (int64_t j = 0; j < H; ++j) {
         double xv = load_in(J->x, J->in_dtype, base + j);
         if (J->residual) {
-            double rv = load_in(J->residual, J->in_dtype, base + j);
-            h[j] = round_store_in(J->residual_out, J->in_dtype, base + j, xv + rv);
+            double rv = load_in(J->residual, J->res_dtype, base + j);
+            h[j] = round_store_in(J->residual_out, J->res_dtype, base + j, xv + rv);
         } else {
             h[j] = xv;
         }
@@ -305,12 +306,33 @@ int oracle_num_cpus(void) {
  * n_threads <= 0 uses every online CPU.  Returns 0, or -1 on a bad
  * argument, -2 when a buffer could not be allocated.
  */
+int oracle_rmsnorm_res(const void *x, const void *residual, const void *weight, const void *bias,
+                       void *out, void *residual_out, float *out_scale, int64_t n_tokens,
+                       int64_t hidden, double eps, double weight_offset, int in_dtype,
+                       int res_dtype, int out_dtype, int n_threads);
+
 int oracle_rmsnorm(const void *x, const void *residual, const void *weight, const void *bias,
                    void *out, void *residual_out, float *out_scale, int64_t n_tokens,
                    int64_t hidden, double eps, double weight_offset, int in_dtype,
                    int out_dtype, int n_threads) {
+    return oracle_rmsnorm_res(x, residual, weight, bias, out, residual_out, out_scale, n_tokens,
+                              hidden, eps, weight_offset, in_dtype, in_dtype, out_dtype,
+                              n_threads);
+}
+
+/*
+ * As oracle_rmsnorm, with the residual stream in its own storage type
+ * res_dtype (residual and residual_out): h = RN_res(x + r), the norm taken
+ * on that h.  An fp32 residual stream with bf16 / fp16 activations keeps h
+ * in fp32 (the exact sum rounded once to fp32).
+ */
+int oracle_rmsnorm_res(const void *x, const void *residual, const void *weight, const void *bias,
+                       void *out, void *residual_out, float *out_scale, int64_t n_tokens,
+                       int64_t hidden, double eps, double weight_offset, int in_dtype,
+                       int res_dtype, int out_dtype, int n_threads) {
     if (n_tokens < 0 || hidden <= 0) return -1;
     if (in_dtype != ORC_F32 && in_dtype != ORC_BF16 && in_dtype != ORC_F16) return -1;
+    if (res_dtype != ORC_F32 && res_dtype != ORC_BF16 && res_dtype != ORC_F16) return -1;
     if (out_dtype < ORC_F32 || out_dtype > ORC_F16) return -1;
     if (!x || !out || (residual && !residual_out)) return -1;
     if (out_dtype == ORC_FP8E4M3 && !out_scale) return -1;
@@ -330,7 +352,7 @@ int oracle_rmsnorm(const void *x, const void *residual, const void *weight, cons
         J->out = out; J->residual_out = residual_out; J->out_scale = out_scale;
         J->n_tokens = n_tokens; J->hidden = hidden;
         J->eps = eps; J->weight_offset = weight_offset;
-        J->in_dtype = in_dtype; J->out_dtype = out_dtype;
+        J->in_dtype = in_dtype; J->out_dtype = out_dtype; J->res_dtype = res_dtype;
         J->row_begin = n_tokens * i / n_threads;
         J->row_end = n_tokens * (i + 1) / n_threads;
         J->status = -3;

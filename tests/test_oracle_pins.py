@@ -181,6 +181,27 @@ def _check_f16_norm(orc):
     assert np.array_equal(y, o_h)
 
 
+def _check_f32_residual_stream(orc):
+    # bf16 / fp16 activations with an fp32 residual stream: h is the fp32 sum
+    # (torch's f32 add of the widened values, correctly rounded), not rounded
+    # to the activation type, and the norm is taken on that h
+    rng = np.random.default_rng(62)
+    for dt, tdt in (("bf16", torch.bfloat16), ("f16", torch.float16)):
+        x = torch.from_numpy(rng.standard_normal((6, 320)).astype(np.float32)).to(tdt)
+        r = torch.from_numpy(rng.standard_normal((6, 320)).astype(np.float32) * 7)
+        w = torch.from_numpy((1 + 0.1 * rng.standard_normal(320)).astype(np.float32)).to(tdt)
+        o = orc.rmsnorm(x, r, w, None, eps=1e-6, in_dtype=dt, out_dtype="f64",
+                        residual_dtype="f32")
+        assert np.array_equal(o["residual_out"], (x.float() + r).numpy())
+        h = torch.from_numpy(o["residual_out"])
+        ref = orc.rmsnorm(h, None, w.float(), None, eps=1e-6, in_dtype="f32", out_dtype="f64")
+        assert np.array_equal(o["out"], ref["out"])
+
+
+def test_f32_residual_stream(oracle_mod):
+    _check_f32_residual_stream(oracle_mod.default())
+
+
 def test_f16_norm_paths(oracle_mod):
     _check_f16_norm(oracle_mod.default())
 
@@ -716,9 +737,13 @@ MUTANTS = {
     "residual_sign": ("xv + rv)", "xv - rv)"),
     "weight_reversed": ("load_in(J->weight, J->in_dtype, j)",
                         "load_in(J->weight, J->in_dtype, H - 1 - j)"),
-    "unrounded_norm": ("h[j] = round_store_in(J->residual_out, J->in_dtype, base + j, xv + rv);",
-                       "round_store_in(J->residual_out, J->in_dtype, base + j, xv + rv); "
+    "unrounded_norm": ("h[j] = round_store_in(J->residual_out, J->res_dtype, base + j, xv + rv);",
+                       "round_store_in(J->residual_out, J->res_dtype, base + j, xv + rv); "
                        "h[j] = xv + rv;"),
+    "residual_stream_rounded_to_input": (
+        "h[j] = round_store_in(J->residual_out, J->res_dtype, base + j, xv + rv);",
+        "h[j] = round_store_in(J->residual_out, J->res_dtype, base + j, "
+        "oracle_bf16_to_f64(oracle_bf16_from_f64(xv + rv)));"),
     "fp8_max_240": ("a / 448.0", "a / 240.0"),
     "bf16_truncates": ("r = round_to_quantum(a, q);\n        const double maxf",
                        "r = ldexp(floor(ldexp(a, -q)), q);\n        const double maxf"),
@@ -758,6 +783,7 @@ def all_pin_checks(orc):
     checks.append(lambda: _check_e2m1_encoder(orc))
     checks.append(lambda: _check_f16_encoder(orc))
     checks.append(lambda: _check_f16_norm(orc))
+    checks.append(lambda: _check_f32_residual_stream(orc))
     checks.append(lambda: _check_mx_exact_blocks(orc))
     checks.append(lambda: _check_block_error_bounds(orc))
     failed = 0
