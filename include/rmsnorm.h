@@ -62,6 +62,12 @@ typedef enum {
 #define RMSN_HAS_RESIDUAL 0x10u /* residual and residual_out */
 #define RMSN_HAS_WEIGHT 0x20u   /* weight (else 1) */
 #define RMSN_HAS_BIAS 0x40u     /* bias (else 0) */
+#define RMSN_RESIDUAL_F32 0x200u /* with RMSN_HAS_RESIDUAL and bf16 / fp16 input: residual
+                                   and residual_out are fp32 (an fp32 residual stream);
+                                   h = x + residual is kept in fp32, not rounded to the
+                                   input type, and the norm is taken on it.  Vector
+                                   kernels need hidden % 8 == 0, 16-byte aligned
+                                   x / weight / bias and 32-byte aligned residuals. */
 /* launch options (blog section "Grid synchronisation": programmatic dependent
  * launch cuts the launch overhead of chained kernels) */
 #define RMSN_PDL 0x80u /* launch with programmatic stream serialization: the kernel

@@ -29,6 +29,7 @@ RMSN_HAS_RESIDUAL = 0x10
 RMSN_HAS_WEIGHT = 0x20
 RMSN_HAS_BIAS = 0x40
 RMSN_PDL = 0x80
+RMSN_RESIDUAL_F32 = 0x200
 RMSN_PDL_EARLY_PARAMS = 0x100
 
 VARIANT_WARP_ROWS = 0

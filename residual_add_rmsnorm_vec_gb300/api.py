@@ -68,12 +68,16 @@ def fused_add_rmsnorm(x: torch.Tensor, residual: torch.Tensor | None = None,
             raise ValueError(f"{name} must be contiguous")
     if out is None:
         out = torch.empty((T, H), dtype=out_torch, device=x.device)
+    # an fp32 residual under bf16 / fp16 activations is an fp32 residual stream
+    res_f32 = residual is not None and residual.dtype == torch.float32 and x.dtype != torch.float32
     if residual is not None and residual_out is None:
-        residual_out = torch.empty_like(x)
+        residual_out = torch.empty_like(residual)
     if out_dtype == "fp8" and out_scale is None:
         out_scale = torch.empty((T,), dtype=torch.float32, device=x.device)
     flags = make_flags(in_name, out_dtype, residual is not None, weight is not None,
                        bias is not None, pdl, early_params)
+    if res_f32:
+        flags |= _lib.RMSN_RESIDUAL_F32
     s = stream if stream is not None else torch.cuda.current_stream(x.device)
     st = _lib.rmsnorm_fwd_ex(_ptr(x.contiguous()), _ptr(residual), _ptr(weight), _ptr(bias),
                              _ptr(out), _ptr(residual_out), _ptr(out_scale), T, H, eps, flags,

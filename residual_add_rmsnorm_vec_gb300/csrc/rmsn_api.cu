@@ -108,7 +108,8 @@ const std::vector<KernelEntry>& registry() {
             kernels_f32_f32,  kernels_f32_bf16,  kernels_f32_fp8,    kernels_f32_f16,
             kernels_bf16_f32, kernels_bf16_bf16, kernels_bf16_fp8,   kernels_f16_f16,
             kernels_f16_f32,  kernels_f16_fp8,   kernels_bf16_mxfp8, kernels_bf16_mxfp4,
-            kernels_bf16_nvfp4};
+            kernels_bf16_nvfp4, kernels_bf16r32_bf16, kernels_bf16r32_fp8, kernels_f16r32_f16,
+            kernels_f16r32_fp8};
         for (auto fn : fns) {
             int n = 0;
             const KernelEntry* t = fn(&n);
@@ -125,6 +126,8 @@ struct Problem {
     bool res, bias;
     bool pdl, early_params;  // launch options
     int in_bytes, out_bytes;
+    bool res_f32;   // fp32 residual stream (residual, residual_out, h) under bf16 / fp16 x
+    int res_bytes;  // element size of the residual stream
     int ve;     // elements per 32-byte vector
     int nvec;   // vectors per row (valid when vec_ok)
     bool vec_ok;
@@ -136,7 +139,7 @@ bool aligned(const void* p, uintptr_t a) { return p == nullptr || (reinterpret_c
 
 int decode_flags(uint32_t flags, Problem* p) {
     const uint32_t known = RMSN_IN_MASK | RMSN_OUT_MASK | RMSN_HAS_RESIDUAL | RMSN_HAS_WEIGHT |
-                           RMSN_HAS_BIAS | RMSN_PDL | RMSN_PDL_EARLY_PARAMS;
+                           RMSN_HAS_BIAS | RMSN_PDL | RMSN_PDL_EARLY_PARAMS | RMSN_RESIDUAL_F32;
     if (flags & ~known) return RMSN_EINVAL;
     const uint32_t in = flags & RMSN_IN_MASK, out = flags & RMSN_OUT_MASK;
     if (in == RMSN_IN_F32) p->in_dt = kF32;
@@ -152,9 +155,12 @@ int decode_flags(uint32_t flags, Problem* p) {
     p->early_params = (flags & RMSN_PDL_EARLY_PARAMS) != 0;
     p->res = (flags & RMSN_HAS_RESIDUAL) != 0;
     p->bias = (flags & RMSN_HAS_BIAS) != 0;
+    p->res_f32 = (flags & RMSN_RESIDUAL_F32) != 0;
+    if (p->res_f32 && (!p->res || p->in_dt == kF32)) return RMSN_EINVAL;
     p->in_bytes = dtype_bytes(p->in_dt);
+    p->res_bytes = p->res_f32 ? 4 : p->in_bytes;
     p->out_bytes = dtype_bytes(p->out_dt);
-    p->ve = 32 / p->in_bytes;
+    p->ve = 32 / p->res_bytes;  // elements per 32-byte vector of the residual stream
     return RMSN_OK;
 }
 
@@ -166,19 +172,23 @@ int check_shape(int64_t T, int64_t H, Problem* p) {
     return RMSN_OK;
 }
 
-// Can the 32-byte vector kernels run with these pointers?
-bool vector_path_ok(const Problem& p, const void* const* ptrs, int n, const void* out) {
-    if ((p.H * p.in_bytes) % 32 != 0) return false;
-    for (int i = 0; i < n; ++i)
-        if (!aligned(ptrs[i], 32)) return false;
-    const int out_vec = p.ve * p.out_bytes;  // bytes stored per input vector
+// Can the 32-byte vector kernels run with these pointers?  Each thread moves
+// one 32-byte vector of the residual stream per chunk: ve elements, so
+// ve * in_bytes bytes of x / weight / bias (32, or 16 under an fp32 stream).
+bool vector_path_ok(const Problem& p, const void* x, const void* r, const void* w,
+                    const void* b, const void* ro, const void* out) {
+    const int xv = p.ve * p.in_bytes;
+    if ((p.H * p.res_bytes) % 32 != 0 || (p.H * p.in_bytes) % xv != 0) return false;
+    if (!aligned(x, xv) || !aligned(w, xv) || !aligned(b, xv)) return false;
+    if (!aligned(r, 32) || !aligned(ro, 32)) return false;
+    const int out_vec = p.ve * p.out_bytes;  // bytes stored per vector
     return aligned(out, out_vec < 32 ? out_vec : 32);
 }
 
 const KernelEntry* find_kernel(const Problem& p, int variant, int ch, int wmax) {
     for (const KernelEntry& e : registry()) {
         if (e.in_dt != p.in_dt || e.out_dt != p.out_dt || e.variant != variant) continue;
-        if (e.res != (p.res ? 1 : 0)) continue;
+        if (e.res != (p.res ? 1 : 0) || e.res_f32 != (p.res_f32 ? 1 : 0)) continue;
         if (variant == kGeneric) return &e;
         if (e.bias != (p.bias ? 1 : 0)) continue;
         if (e.chunks == ch && e.max_warps == wmax) return &e;
@@ -344,11 +354,13 @@ int validate(const void* x, const void* residual, const void* weight, const void
     if (p->bias != (bias != nullptr)) return RMSN_EINVAL;
     if ((p->out_dt == kFP8 || p->out_dt == kNVFP4) != (out_scale != nullptr)) return RMSN_EINVAL;
     if (!x || !out) return RMSN_EINVAL;
-    const void* ins[] = {x, residual, weight, bias, residual_out};
+    const void* ins[] = {x, weight, bias};
     for (const void* q : ins)
         if (!aligned(q, (uintptr_t)p->in_bytes)) return RMSN_EALIGN;
+    if (!aligned(residual, (uintptr_t)p->res_bytes) || !aligned(residual_out, (uintptr_t)p->res_bytes))
+        return RMSN_EALIGN;
     if (!aligned(out, (uintptr_t)p->out_bytes) || !aligned(out_scale, 4)) return RMSN_EALIGN;
-    p->vec_ok = vector_path_ok(*p, ins, 5, out);
+    p->vec_ok = vector_path_ok(*p, x, residual, weight, bias, residual_out, out);
     p->nvec = p->vec_ok ? (int)(p->H / p->ve) : 0;
     return RMSN_OK;
 }
@@ -547,8 +559,7 @@ RMSN_API int rmsnorm_fwd_host(const void* x, const void* residual, const void* w
         !device_view(d, out_scale, &dscale))
         return RMSN_EINVAL;
     // the mapped addresses decide the vector path
-    const void* ins[] = {dx, dr, dw, db, dres};
-    p.vec_ok = vector_path_ok(p, ins, 5, dout);
+    p.vec_ok = vector_path_ok(p, dx, dr, dw, db, dres, dout);
     p.nvec = p.vec_ok ? (int)(p.H / p.ve) : 0;
     rmsn_config c;
     if (!select_host(p, d, &c)) return RMSN_EUNSUPPORTED;
@@ -571,7 +582,7 @@ static int query_problem(int64_t n_tokens, int64_t hidden, uint32_t flags, Probl
     int st = decode_flags(flags, p);
     if (st != RMSN_OK) return st;
     if ((st = check_shape(n_tokens, hidden, p)) != RMSN_OK) return st;
-    p->vec_ok = (p->H * p->in_bytes) % 32 == 0;
+    p->vec_ok = (p->H * p->res_bytes) % 32 == 0;
     p->nvec = p->vec_ok ? (int)(p->H / p->ve) : 0;
     return RMSN_OK;
 }
@@ -598,6 +609,7 @@ RMSN_API int rmsnorm_list_configs(int64_t n_tokens, int64_t hidden, uint32_t fla
     int count = 0;
     for (const KernelEntry& e : registry()) {
         if (e.in_dt != p.in_dt || e.out_dt != p.out_dt || e.res != (p.res ? 1 : 0)) continue;
+        if (e.res_f32 != (p.res_f32 ? 1 : 0)) continue;
         if (e.variant != kGeneric && (e.bias != (p.bias ? 1 : 0) || !p.vec_ok)) continue;
         // the bulk kernel is listed once per ring depth
         const int stage_opts[] = {0, 2, 3, 4, 6, 8};

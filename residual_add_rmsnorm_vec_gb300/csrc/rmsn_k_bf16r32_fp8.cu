@@ -1,0 +1,12 @@
+// Kernel instantiations: bf16 activations with an fp32 residual stream,
+// fp8 output (register kernels, residual variants only).
+#define RMSN_TI ::rmsn::F32
+#define RMSN_TX ::rmsn::BF16
+#define RMSN_TO ::rmsn::FP8
+#define RMSN_DTI kBF16
+#define RMSN_DTO kFP8
+#define RMSN_RF32 1
+#define RMSN_RES_ONLY
+#define RMSN_NO_BULK
+#define RMSN_TABLE_FN kernels_bf16r32_fp8
+#include "rmsn_instances.cuh"

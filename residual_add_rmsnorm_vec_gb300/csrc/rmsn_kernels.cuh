@@ -98,6 +98,22 @@ __device__ __forceinline__ V8 ld_stream32(const void* p) {
     return v;
 }
 
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_keep16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ V8 ld_keep32(const void* p) {
     V8 v;
     asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
@@ -221,6 +237,30 @@ __device__ __forceinline__ void opaque(V8& v) {
     for (int k = 0; k < 8; ++k) asm volatile("" : "+r"(v.u[k]));
 }
 
+// One vector of VE = 32 / TI::kBytes elements of a TX array starting at
+// element `e`, as a TI vector.  TX == TI: one 32-byte access.  A 2-byte TX
+// under an fp32 TI (bf16 / fp16 activations with an fp32 residual stream):
+// one 16-byte access, widened exactly.
+template <class TX, class TI, bool STREAM>
+__device__ __forceinline__ V8 ld_vec(const void* base, int64_t e) {
+    if constexpr (TX::kBytes == TI::kBytes) {
+        const void* p = static_cast<const char*>(base) + e * TI::kBytes;
+        return STREAM ? ld_stream32(p) : ld_keep32(p);
+    } else {
+        static_assert(TX::kBytes == 2 && TI::kBytes == 4, "2-byte values under fp32 only");
+        const void* p = static_cast<const char*>(base) + e * 2;
+        const uint4 w = STREAM ? ld_stream16(p) : ld_keep16(p);
+        const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+        V8 v;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            v.u[2 * k] = __float_as_uint(lo2<TX>(in[k]));
+            v.u[2 * k + 1] = __float_as_uint(hi2<TX>(in[k]));
+        }
+        return v;
+    }
+}
+
 template <class TI>
 __device__ __forceinline__ uint32_t ones_word() {
     if constexpr (IsF16<TI>::value) return 0x3C003C00u;
@@ -335,20 +375,21 @@ struct Bounds {
 // memory per chunk.  hv holds x on entry (and rv the residual); on exit hv
 // holds h = RN_in(x + r), which was also stored to residual_out.
 
-template <class TI, int CH>
+template <class TX, class TI, int CH>
 __device__ __forceinline__ void load_params(const RmsnArgs& a, int G, int t, V8 (&wv)[CH],
                                             V8* bv, bool bias) {
+    constexpr int VE = 32 / TI::kBytes;
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
         const int v = c * G + t;
         if (v < a.nvec) {
             if (a.has_w) {
-                wv[c] = ld_keep32(static_cast<const char*>(a.w) + (int64_t)v * 32);
+                wv[c] = ld_vec<TX, TI, false>(a.w, (int64_t)v * VE);
             } else {
 #pragma unroll
                 for (int k = 0; k < 8; ++k) wv[c].u[k] = ones_word<TI>();
             }
-            if (bias) bv[c] = ld_keep32(static_cast<const char*>(a.b) + (int64_t)v * 32);
+            if (bias) bv[c] = ld_vec<TX, TI, false>(a.b, (int64_t)v * VE);
         }
     }
 }
@@ -552,7 +593,10 @@ __device__ __forceinline__ void scale_store(const RmsnArgs& a, int64_t row, int6
 // one row and has up to WMAX warps.  Each thread loads its CH vectors of x
 // (and the residual) straight into registers; rows are visited grid-stride;
 // weight and bias stay in registers across rows.
-template <class TI, class TO, int CH, int WMAX, bool WARP_ROWS, bool RES, bool BIAS>
+// TX: storage of x, weight and bias; TI: of the residual stream and h (TX
+// unless an fp32 residual stream carries bf16 / fp16 activations).
+template <class TI, class TO, int CH, int WMAX, bool WARP_ROWS, bool RES, bool BIAS,
+          class TX = TI>
 __global__ void __launch_bounds__(Bounds<WMAX, CH>::kThreads, Bounds<WMAX, CH>::kMinBlocks)
     rmsn_vec_kernel(const RmsnArgs a) {
     constexpr int VE = 32 / TI::kBytes;  // elements per 32-byte vector
@@ -569,7 +613,7 @@ __global__ void __launch_bounds__(Bounds<WMAX, CH>::kThreads, Bounds<WMAX, CH>::
     if (!a.early_params) pdl_wait(a.pdl);
     V8 wv[CH];
     V8 bv[BIAS ? CH : 1];
-    load_params<TI, CH>(a, G, t, wv, bv, BIAS);
+    load_params<TX, TI, CH>(a, G, t, wv, bv, BIAS);
     if (a.early_params) pdl_wait(a.pdl);
 
     int parity = 0;
@@ -581,9 +625,9 @@ __global__ void __launch_bounds__(Bounds<WMAX, CH>::kThreads, Bounds<WMAX, CH>::
         for (int c = 0; c < CH; ++c) {
             const int v = c * G + t;
             if (v < a.nvec) {
-                const int64_t off = (rbase + (int64_t)v * VE) * TI::kBytes;
-                hv[c] = ld_stream32(static_cast<const char*>(a.x) + off);
-                if constexpr (RES) rv[c] = ld_stream32(static_cast<const char*>(a.r) + off);
+                const int64_t e = rbase + (int64_t)v * VE;
+                hv[c] = ld_vec<TX, TI, true>(a.x, e);
+                if constexpr (RES) rv[c] = ld_stream32(static_cast<const char*>(a.r) + e * TI::kBytes);
             }
         }
         const float acc = residual_sumsq<TI, CH, RES>(a, rbase, G, t, hv, rv);
@@ -699,7 +743,7 @@ __global__ void __launch_bounds__(WMAX * 32, 1) rmsn_bulk_kernel(const RmsnArgs 
     pdl_launch_dependents(a.pdl);
     V8 wv[CH];
     V8 bv[BIAS ? CH : 1];
-    if (a.early_params) load_params<TI, CH>(a, G, t, wv, bv, BIAS);
+    if (a.early_params) load_params<TI, TI, CH>(a, G, t, wv, bv, BIAS);
     pdl_wait(a.pdl);
     if (t == 0) {
         abort_flag = 0;
@@ -710,7 +754,7 @@ __global__ void __launch_bounds__(WMAX * 32, 1) rmsn_bulk_kernel(const RmsnArgs 
                            smem_u32(&full[k]), row_bytes);
     }
     __syncthreads();
-    if (!a.early_params) load_params<TI, CH>(a, G, t, wv, bv, BIAS);
+    if (!a.early_params) load_params<TI, TI, CH>(a, G, t, wv, bv, BIAS);
 
     int parity = 0;
     int64_t k_abort = 0;
@@ -793,16 +837,17 @@ __device__ __forceinline__ void st_elem(void* p, int64_t i, float v) {
     }
 }
 
-template <class TI>
+template <class TH, class TX>
 __device__ __forceinline__ float generic_y(const RmsnArgs& a, const void* hsrc, int64_t base,
                                            int j, float inv) {
-    const float h = ld_elem<TI>(hsrc, base + j);
-    const float w = a.has_w ? ld_elem<TI>(a.w, j) : 1.f;
-    if (a.b) return scale_elem<true>(h, inv, w, a.woff, ld_elem<TI>(a.b, j));
+    const float h = ld_elem<TH>(hsrc, base + j);
+    const float w = a.has_w ? ld_elem<TX>(a.w, j) : 1.f;
+    if (a.b) return scale_elem<true>(h, inv, w, a.woff, ld_elem<TX>(a.b, j));
     return scale_elem<false>(h, inv, w, a.woff, 0.f);
 }
 
-template <class TI, class TO, bool RES>
+// TX / TI as in rmsn_vec_kernel.
+template <class TI, class TO, bool RES, class TX = TI>
 __global__ void __launch_bounds__(256) rmsn_generic_kernel(const RmsnArgs a) {
     __shared__ float red[4][32];
     const int H = a.H;
@@ -813,7 +858,7 @@ __global__ void __launch_bounds__(256) rmsn_generic_kernel(const RmsnArgs a) {
         const int64_t base = row * (int64_t)H;
         float acc = 0.f;
         for (int j = threadIdx.x; j < H; j += blockDim.x) {
-            float h = ld_elem<TI>(a.x, base + j);
+            float h = ld_elem<TX>(a.x, base + j);
             if constexpr (RES) {
                 h = round_to<TI>(__fadd_rn(h, ld_elem<TI>(a.r, base + j)));
                 st_elem<TI>(a.res_out, base + j, h);
@@ -821,19 +866,21 @@ __global__ void __launch_bounds__(256) rmsn_generic_kernel(const RmsnArgs a) {
             acc = __fmaf_rn(h, h, acc);
         }
         const float inv = inv_rms(block_allreduce<false>(acc, red[parity]), H, a.eps);
+        // h is re-read from residual_out (TI) or, without a residual, from x (TX == TI)
+        using HSrc = TI;
         const void* hsrc = RES ? static_cast<const void*>(a.res_out) : a.x;
         float qmul = 0.f;
         if constexpr (TO::kBytes == 1) {
             float amax = 0.f;
             for (int j = threadIdx.x; j < H; j += blockDim.x) {
-                amax = fmaxf(amax, fabsf(generic_y<TI>(a, hsrc, base, j, inv)));
+                amax = fmaxf(amax, fabsf(generic_y<HSrc, TX>(a, hsrc, base, j, inv)));
             }
             amax = block_allreduce<true>(amax, red[2 + parity]);
             qmul = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
             if (threadIdx.x == 0) a.scale[row] = __fdiv_rn(amax, 448.f);
         }
         for (int j = threadIdx.x; j < H; j += blockDim.x) {
-            const float y = generic_y<TI>(a, hsrc, base, j, inv);
+            const float y = generic_y<HSrc, TX>(a, hsrc, base, j, inv);
             if constexpr (TO::kBytes == 1) {
                 uint16_t q;
                 asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"

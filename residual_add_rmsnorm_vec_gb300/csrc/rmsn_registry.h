@@ -37,6 +37,7 @@ enum Variant : int32_t { kWarpRows = 0, kBlockRow = 1, kBulkRow = 2, kGeneric = 
 // One compiled kernel.
 struct KernelEntry {
     int32_t in_dt, out_dt, variant, chunks, max_warps, stages, res, bias;
+    int32_t res_f32;  // fp32 residual stream under a bf16 / fp16 in_dt
     const void* fn;
 };
 
@@ -51,6 +52,10 @@ const KernelEntry* kernels_f16_f16(int* n);
 const KernelEntry* kernels_f16_f32(int* n);
 const KernelEntry* kernels_f16_fp8(int* n);
 const KernelEntry* kernels_f32_f16(int* n);
+const KernelEntry* kernels_bf16r32_bf16(int* n);
+const KernelEntry* kernels_bf16r32_fp8(int* n);
+const KernelEntry* kernels_f16r32_f16(int* n);
+const KernelEntry* kernels_f16r32_fp8(int* n);
 const KernelEntry* kernels_bf16_mxfp8(int* n);
 const KernelEntry* kernels_bf16_mxfp4(int* n);
 const KernelEntry* kernels_bf16_nvfp4(int* n);

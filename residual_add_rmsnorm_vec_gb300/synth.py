@@ -68,7 +68,12 @@ class Workload:
     r_std: float = 1.0
     outlier_frac: float = 0.0  # fraction of channels of x scaled by outlier_scale
     outlier_scale: float = 50.0
+    res_dtype: str | None = None  # residual stream storage; None = in_dtype ("f32" under bf16 / f16)
     extra: dict = field(default_factory=dict, compare=False, hash=False)
+
+    @property
+    def res_storage(self) -> str:
+        return self.res_dtype or self.in_dtype
 
     @property
     def in_bytes(self) -> int:
@@ -83,7 +88,8 @@ class Workload:
         T, H = self.n_tokens, self.hidden
         b = T * H * self.in_bytes                      # read x
         if self.has_residual:
-            b += 2 * T * H * self.in_bytes             # read r, write residual_out
+            rb = 4 if self.res_storage == "f32" else 2
+            b += 2 * T * H * rb                        # read r, write residual_out
         b += T * H * self.out_bytes                    # write y (or q)
         if self.out_dtype == "fp8":
             b += 4 * T                                 # per-token scales
@@ -233,7 +239,7 @@ def make_inputs(wl: Workload, rows=None) -> dict:
         b = 0.01 * _rng(wl.seed, TAG_B, 0).standard_normal(H, dtype=np.float32)
     return {
         "x": to_storage(x, wl.in_dtype),
-        "residual": None if r is None else to_storage(r, wl.in_dtype),
+        "residual": None if r is None else to_storage(r, wl.res_storage),
         "weight": None if w is None else to_storage(w.astype(np.float32), wl.in_dtype),
         "bias": None if b is None else to_storage(b.astype(np.float32), wl.in_dtype),
     }

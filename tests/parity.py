@@ -46,7 +46,8 @@ def to_device(inp: dict, dev) -> dict:
 def oracle_run(wl, inp: dict, weight_offset: float = 0.0) -> dict:
     return oracle.rmsnorm(inp["x"], inp["residual"], inp["weight"], inp["bias"],
                           eps=float(np.float32(wl.eps)), in_dtype=wl.in_dtype,
-                          out_dtype=wl.out_dtype, weight_offset=weight_offset)
+                          out_dtype=wl.out_dtype, weight_offset=weight_offset,
+                          residual_dtype=wl.res_storage)
 
 
 def gpu_outputs_to_host(wl, out, res, scale) -> dict:
@@ -58,7 +59,7 @@ def gpu_outputs_to_host(wl, out, res, scale) -> dict:
         o = out.detach().cpu().numpy()
     r = None
     if res is not None:
-        r = bits16(res) if wl.in_dtype in ("bf16", "f16") else res.detach().cpu().numpy()
+        r = bits16(res) if wl.res_storage in ("bf16", "f16") else res.detach().cpu().numpy()
     s = None if scale is None else scale.detach().cpu().numpy()
     return {"out": o, "residual_out": r, "out_scale": s}
 
@@ -69,7 +70,7 @@ def compare(wl, got: dict, ref: dict, where: str = "", bias=None) -> dict:
     stats = {}
     if ref["residual_out"] is not None:
         g, r = got["residual_out"], ref["residual_out"]
-        if wl.in_dtype in ("bf16", "f16"):
+        if wl.res_storage in ("bf16", "f16"):
             bad = np.count_nonzero(g != r)
         else:
             bad = np.count_nonzero(g.view(np.uint32) != r.view(np.uint32))

@@ -64,7 +64,11 @@ BF16_RES = 0x1 | 0x4 | 0x10 | 0x20  # bf16 in/out, residual, weight
 
 @pytest.mark.parametrize("case", [
     # (x, r, w, b, out, res_out, scale, T, H, eps, flags)
-    ("unknown flag bit", (16, 16, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES | 0x200)),
+    ("unknown flag bit", (16, 16, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES | 0x400)),
+    ("f32 stream without residual", (16, None, 16, None, 16, None, None, 4, 64, 1e-6,
+                                     0x1 | 0x4 | 0x20 | 0x200)),
+    ("f32 stream under f32 input", (16, 16, 16, None, 16, 16, None, 4, 64, 1e-6,
+                                    0x0 | 0x10 | 0x20 | 0x200)),
     ("early params without pdl", (16, 16, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES | 0x100)),
     ("bad input dtype", (16, 16, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES | 0x2)),
     ("residual flag without pointer", (16, None, 16, None, 16, 16, None, 4, 64, 1e-6, BF16_RES)),

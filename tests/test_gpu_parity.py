@@ -159,6 +159,40 @@ def test_fp16_io(pkg, T, H):
     assert st["exact_frac"] > 0.99
 
 
+@pytest.mark.parametrize("T,H,in_dt,out_dt,bias", [
+    (1, 4096, "bf16", "bf16", False), (256, 4096, "bf16", "bf16", False),
+    (2048, 8192, "bf16", "bf16", False), (4096, 5120, "bf16", "fp8", True),
+    (64, 4096, "f16", "f16", True), (300, 2048, "f16", "fp8", False),
+    (33, 1000, "bf16", "bf16", True), (5, 12, "f16", "f16", False),
+])
+def test_f32_residual_stream(pkg, T, H, in_dt, out_dt, bias):
+    # bf16 / fp16 activations, fp32 residual stream: residual_out is the fp32
+    # sum (bit-exact), the norm is taken on it
+    wl = synth.Workload(f"r32_{in_dt}_{out_dt}_T{T}_H{H}", T, H, 90, in_dt, out_dt, 1e-6,
+                        has_bias=bias, r_std=4.0, res_dtype="f32")
+    check(pkg, wl)
+
+
+def test_f32_residual_stream_every_config_and_in_place(pkg):
+    wl = synth.Workload("r32_cfg", 37, 2048, 91, "bf16", "bf16", 1e-6, has_bias=True,
+                        res_dtype="f32")
+    flags = pkg.make_flags("bf16", "bf16", True, True, True) | pkg.RMSN_RESIDUAL_F32
+    cfgs = pkg.rmsnorm_list_configs(37, 2048, flags)
+    assert cfgs and all(c.variant != pkg.VARIANT_BULK_ROW for c in cfgs)
+    inp = synth.make_inputs(wl)
+    ref = parity.oracle_run(wl, inp)
+    for c in cfgs:
+        parity.compare(wl, run_gpu(pkg, wl, inp, config=c), ref, f"r32 {c.as_dict()}",
+                       bias=inp["bias"])
+    # residual_out written over the residual itself (the usual in-place update)
+    g = parity.to_device(inp, DEV)
+    out, res, _ = pkg.fused_add_rmsnorm(g["x"], g["residual"], g["weight"], g["bias"],
+                                        eps=wl.eps, residual_out=g["residual"])
+    torch.cuda.synchronize()
+    parity.compare(wl, parity.gpu_outputs_to_host(wl, out, res, None), ref, "r32 in place",
+                   bias=inp["bias"])
+
+
 @pytest.mark.parametrize("H", [1, 7, 1000, 4097])
 def test_fp16_ragged_generic(pkg, H):
     check(pkg, synth.Workload(f"f16_ragged_H{H}", 21, H, 81, "f16", "f16", 1e-6, has_bias=True))
