@@ -439,7 +439,8 @@ __device__ __forceinline__ float residual_sumsq(const RmsnArgs& a, int64_t rbase
 //   MX:    scale 2^s, s = floor(log2 max|y|) - emax (8 for E4M3, 2 for E2M1),
 //          clamped to [-127, 127], stored as E8M0 (s + 127); codes y * 2^-s.
 //   NVFP4: per-token fp32 g = max|row| / (448 * 6) (the row max all-reduce),
-//          block scale E4M3(max|block| / (6 g)), codes E2M1(y / (scale * g)).
+//          block scale E4M3(max|block| * (1 / (6 g))), codes
+//          E2M1(y * (1 / (scale * g))), with correctly rounded reciprocals.
 // All conversions round to nearest even and saturate.
 template <class TI, class TO, int CH, bool BIAS, class ReduceMax>
 __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row, int64_t rbase,
@@ -450,7 +451,7 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
     constexpr bool NV = TO::kBlock == 16;
     constexpr bool FP4 = !std::is_same<TO, MXFP8>::value;
     static_assert(LPB >= 1 && LPB <= 4, "block spans 1..4 lanes");
-    float g = 0.f;
+    float g = 0.f, rcp6g = 0.f;
     if constexpr (NV) {
         float amax = 0.f;
 #pragma unroll
@@ -469,6 +470,7 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
         amax = reduce_max(amax);
         g = __fdiv_rn(amax, 2688.f);
         if (t == 0) a.scale[row] = g;
+        rcp6g = g > 0.f ? __frcp_rn(__fmul_rn(6.f, g)) : 0.f;  // one reciprocal per row
     }
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
@@ -499,11 +501,11 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
                 uint16_t two;
                 asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
                     : "=h"(two)
-                    : "f"(0.f), "f"(__fdiv_rn(bmax, __fmul_rn(6.f, g))));
+                    : "f"(0.f), "f"(__fmul_rn(bmax, rcp6g)));
                 sc = two & 0xFFu;
             }
             const float s = __fmul_rn(e4m3_value(sc), g);
-            mul = s > 0.f ? __fdiv_rn(1.f, s) : 0.f;
+            mul = s > 0.f ? __frcp_rn(s) : 0.f;
             sbyte = (uint8_t)sc;
         } else {
             constexpr int emax = FP4 ? 2 : 8;

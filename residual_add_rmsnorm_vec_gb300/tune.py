@@ -28,17 +28,23 @@ import time
 L2_BYTES = 129 * 10**6
 TOKENS = (1, 4, 16, 64, 256, 1024, 4096, 16384, 65536)
 HIDDEN = (2048, 4096, 8192, 16384)
-DTYPE_CODES = {"f32": 0, "bf16": 1, "fp8": 2}
+DTYPE_CODES = {"f32": 0, "bf16": 1, "fp8": 2, "mxfp8": 3, "mxfp4": 4, "nvfp4": 5, "f16": 6}
+BLOCK_FMTS = ("mxfp8", "mxfp4", "nvfp4")
 
 
-def _algorithmic_bytes(T, H, in_b, out_b, res, bias, fp8):
-    b = T * H * in_b + T * H * out_b + H * in_b
+def _algorithmic_bytes(T, H, in_b, out_b, res, bias, fp8, fmt=None):
+    if fmt in BLOCK_FMTS:
+        blk, per_byte = (16, 2) if fmt == "nvfp4" else (32, 1 if fmt == "mxfp8" else 2)
+        b = T * H * in_b + T * H // per_byte + T * H // blk + H * in_b
+        b += 4 * T if fmt == "nvfp4" else 0
+    else:
+        b = T * H * in_b + T * H * out_b + H * in_b
+        if fp8:
+            b += 4 * T
     if res:
         b += 2 * T * H * in_b
     if bias:
         b += H * in_b
-    if fp8:
-        b += 4 * T
     return b
 
 
@@ -47,37 +53,54 @@ def measure(pkg, T, H, in_dt="bf16", out_dt="bf16", res=True, bias=False, reps=3
     import torch
 
     dev = torch.device("cuda")
-    tin = torch.bfloat16 if in_dt == "bf16" else torch.float32
-    in_b = 2 if in_dt == "bf16" else 4
-    out_b = {"bf16": 2, "f32": 4, "fp8": 1}[out_dt]
-    tout = {"bf16": torch.bfloat16, "f32": torch.float32, "fp8": torch.uint8}[out_dt]
-    flags = pkg.make_flags(in_dt, out_dt, res, True, bias)
+    tin = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[in_dt]
+    in_b = 4 if in_dt == "f32" else 2
+    block = out_dt in BLOCK_FMTS
+    out_b = {"bf16": 2, "f16": 2, "f32": 4, "fp8": 1}.get(out_dt, 1)
+    tout = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}.get(
+        out_dt, torch.uint8)
+    # block formats share the launch shapes of the per-token FP8 output
+    flags = pkg.make_flags(in_dt, "fp8" if block else out_dt, res, True, bias)
+    call_flags = pkg.make_flags(in_dt, "f32", res, True, bias) if block else flags
     set_bytes = T * H * (in_b * (3 if res else 1) + out_b)
     n_sets = 1 if l2_hot else max(1, min(64, -(-3 * L2_BYTES // max(1, set_bytes))))
     sets = []
     for _ in range(n_sets):
         x = torch.randn(T, H, device=dev).to(tin)
         r = torch.randn(T, H, device=dev).to(tin) if res else None
-        sets.append((x, r, torch.empty(T, H, device=dev, dtype=tout),
-                     torch.empty_like(x) if res else None,
-                     torch.empty(T, device=dev, dtype=torch.float32) if out_dt == "fp8" else None))
+        if block:
+            code, blk, per_byte = pkg.BLOCK_FORMATS[out_dt]
+            q = torch.empty(T, H // per_byte, device=dev, dtype=torch.uint8)
+            bsc = torch.empty(T, H // blk, device=dev, dtype=torch.uint8)
+        else:
+            q, bsc = torch.empty(T, H, device=dev, dtype=tout), None
+        sets.append((x, r, q, torch.empty_like(x) if res else None,
+                     torch.empty(T, device=dev, dtype=torch.float32)
+                     if out_dt in ("fp8", "nvfp4") else None, bsc))
     w = (1 + 0.1 * torch.randn(H, device=dev)).to(tin)
     b = (0.01 * torch.randn(H, device=dev)).to(tin) if bias else None
     stream = torch.cuda.current_stream()
     if configs is None:
         configs = pkg.rmsnorm_list_configs(T, H, flags)
-    algo = _algorithmic_bytes(T, H, in_b, out_b, res, bias, out_dt == "fp8")
+        if block:
+            configs = [c for c in configs if c.variant != pkg.VARIANT_GENERIC]
+    algo = _algorithmic_bytes(T, H, in_b, out_b, res, bias, out_dt == "fp8", out_dt)
     results = []
     for cfg in configs:
         def launch_on(i, s):
-            x, r, o, ro, sc = sets[i % n_sets]
-            st = pkg.rmsnorm_fwd_ex(x.data_ptr(), None if r is None else r.data_ptr(),
-                                    w.data_ptr(), None if b is None else b.data_ptr(),
-                                    o.data_ptr(), None if ro is None else ro.data_ptr(),
-                                    None if sc is None else sc.data_ptr(), T, H, 1e-6, flags,
-                                    0.0, cfg, s.cuda_stream)
+            x, r, o, ro, sc, bsc = sets[i % n_sets]
+            ptr = (lambda t: None if t is None else t.data_ptr())
+            if block:
+                st = pkg.rmsnorm_fwd_blockscaled(
+                    x.data_ptr(), ptr(r), w.data_ptr(), ptr(b), o.data_ptr(), bsc.data_ptr(),
+                    ptr(sc), ptr(ro), T, H, 1e-6, call_flags, pkg.BLOCK_FORMATS[out_dt][0], 0.0,
+                    cfg, s.cuda_stream)
+            else:
+                st = pkg.rmsnorm_fwd_ex(x.data_ptr(), ptr(r), w.data_ptr(), ptr(b), o.data_ptr(),
+                                        ptr(ro), ptr(sc), T, H, 1e-6, flags, 0.0, cfg,
+                                        s.cuda_stream)
             if st != pkg.RMSN_OK:
-                raise pkg.RmsnError(st, "rmsnorm_fwd_ex")
+                raise pkg.RmsnError(st, "launch")
 
         def launch(i):
             launch_on(i, stream)
@@ -130,7 +153,24 @@ def sweep(pkg, shapes, in_dt, out_dt, res, bias, reps, l2_hot_below=0):
     return out
 
 
-def write_table(entries, path):
+def merge_table(entries, path):
+    """Replace, in the table at `path`, the rows of the (input, output) dtype
+    pairs measured in `entries` and keep every other row."""
+    import re
+
+    measured = {(DTYPE_CODES[e["in"]], DTYPE_CODES[e["out"]]) for e in entries}
+    kept = []
+    for line in open(path):
+        m = re.match(r"\s*\{(-?\d+), (-?\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)\},"
+                     r"(?:\s*// ([\d.]+) us, ([\d.]+) GB/s)?", line)
+        if m and (int(m.group(1)), int(m.group(2))) not in measured and int(m.group(1)) >= 0:
+            v = [int(m.group(i)) for i in range(1, 9)]
+            kept.append(tuple(v[:4]) + tuple(v[4:8]) + (None, None,
+                        float(m.group(9) or 0), float(m.group(10) or 0)))
+    write_table(entries, path, extra_rows=kept)
+
+
+def write_table(entries, path, extra_rows=()):
     """Selector rows from the sweep: per (dtypes, hidden), the best shape from
     each measured token count upward.  Ties within 1 % prefer fewer warps,
     then the register kernel, then fewer ring stages."""
@@ -145,7 +185,8 @@ def write_table(entries, path):
         rows.append((DTYPE_CODES[e["in"]], DTYPE_CODES[e["out"]], e["H"], e["T"], pick["variant"],
                      pick["chunks"], pick["max_warps"], pick["stages"], e["res"], e["bias"],
                      pick["us"], pick["gbs"]))
-    rows.sort()
+    rows.extend(extra_rows)
+    rows.sort(key=lambda r: r[:4])
     lines = [
         "// Launch shapes chosen from measured bandwidth on a GB300 by",
         "// residual_add_rmsnorm_vec_gb300/tune.py (CUDA-graph replay of back-to-back",
@@ -208,6 +249,8 @@ def main():
     ap.add_argument("--quick", action="store_true", help="a few shapes only")
     ap.add_argument("--l2-hot-below", type=int, default=512,
                     help="time shapes with fewer tokens L2-hot (decode sizes)")
+    ap.add_argument("--block-formats", action="store_true",
+                    help="sweep only the block-scaled outputs and merge their rows into the table")
     args = ap.parse_args()
     build.build()
     torch.cuda.set_device(0)
@@ -215,6 +258,19 @@ def main():
     if args.quick:
         grid = [(1, 4096), (256, 4096), (16384, 8192)]
     hot = args.l2_hot_below
+    if args.block_formats:
+        entries = []
+        for fmt in BLOCK_FMTS:
+            entries += sweep(pkg, [(T, H) for H in (4096, 5120, 7168, 8192)
+                                   for T in (1, 64, 1024, 4096, 16384)],
+                             "bf16", fmt, True, True, args.reps, hot)
+        with open(args.out, "w") as f:
+            json.dump({"meta": {"gpu": torch.cuda.get_device_name(0), "reps": args.reps,
+                                "l2_hot_below": hot, "timing": "cuda graph replay"},
+                       "entries": entries}, f)
+        if args.write_table:
+            merge_table(entries, args.table_out)
+        return
     entries = sweep(pkg, grid, "bf16", "bf16", True, False, args.reps, hot)
     # the other dtype paths of the hot-path workloads
     entries += sweep(pkg, [(T, H) for H in (5120, 7168) for T in (1, 64, 1024, 4096)],
