@@ -543,7 +543,10 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
 
 // Scale, (FP8: absmax reduction and per-token scale) and store the row.
 // `reduce_max` is the row-wide max all-reduce (only used for FP8 output).
-template <class TI, class TO, int CH, bool BIAS, class ReduceMax>
+// KEEP: hold the row's y in registers between the FP8 max pass and the
+// quantising pass instead of recomputing it (for kernels with a large
+// register budget).
+template <class TI, class TO, int CH, bool BIAS, bool KEEP = false, class ReduceMax>
 __device__ __forceinline__ void scale_store(const RmsnArgs& a, int64_t row, int64_t rbase, int G,
                                             int t, float inv, const V8 (&hv)[CH], V8 (&wv)[CH],
                                             V8* bv, ReduceMax reduce_max) {
@@ -552,6 +555,8 @@ __device__ __forceinline__ void scale_store(const RmsnArgs& a, int64_t row, int6
         return;
     }
     constexpr int VE = 32 / TI::kBytes;
+    constexpr bool HOLD = KEEP && TO::kBytes == 1;
+    float ys[HOLD ? CH : 1][HOLD ? VE : 1];
     float qmul = 0.f;
     if constexpr (TO::kBytes == 1) {
         float amax = 0.f;
@@ -565,6 +570,7 @@ __device__ __forceinline__ void scale_store(const RmsnArgs& a, int64_t row, int6
                 for (int k = 0; k < VE; ++k) {
                     const float y = scale_elem<BIAS>(elem<TI>(hv[c], k), inv, elem<TI>(wv[c], k),
                                                      a.woff, BIAS ? elem<TI>(bv[c], k) : 0.f);
+                    if constexpr (HOLD) ys[c][k] = y;
                     amax = fmaxf(amax, fabsf(y));
                 }
             }
@@ -577,14 +583,18 @@ __device__ __forceinline__ void scale_store(const RmsnArgs& a, int64_t row, int6
     for (int c = 0; c < CH; ++c) {
         const int v = c * G + t;
         if (v < a.nvec) {
-            opaque(wv[c]);
-            if constexpr (BIAS) opaque(bv[c]);
-            float y[VE];
+            if constexpr (HOLD) {
+                store_out<TI, TO>(a.out, rbase + (int64_t)v * VE, ys[c], qmul);
+            } else {
+                opaque(wv[c]);
+                if constexpr (BIAS) opaque(bv[c]);
+                float y[VE];
 #pragma unroll
-            for (int k = 0; k < VE; ++k)
-                y[k] = scale_elem<BIAS>(elem<TI>(hv[c], k), inv, elem<TI>(wv[c], k), a.woff,
-                                        BIAS ? elem<TI>(bv[c], k) : 0.f);
-            store_out<TI, TO>(a.out, rbase + (int64_t)v * VE, y, qmul);
+                for (int k = 0; k < VE; ++k)
+                    y[k] = scale_elem<BIAS>(elem<TI>(hv[c], k), inv, elem<TI>(wv[c], k), a.woff,
+                                            BIAS ? elem<TI>(bv[c], k) : 0.f);
+                store_out<TI, TO>(a.out, rbase + (int64_t)v * VE, y, qmul);
+            }
         }
     }
 }
@@ -792,7 +802,8 @@ __global__ void __launch_bounds__(WMAX * 32, 1) rmsn_bulk_kernel(const RmsnArgs 
         }
         const float inv = inv_rms(sumsq, a.H, a.eps);
         float* slot = red[2 + parity];
-        scale_store<TI, TO, CH, BIAS>(a, row, rbase, G, t, inv, hv, wv, bv,
+        scale_store<TI, TO, CH, BIAS, (WMAX <= 16 && CH * VE <= 32)>(a, row, rbase, G, t, inv, hv,
+                                                                    wv, bv,
                                       [&](float m) { return block_allreduce<true>(m, slot); });
         parity ^= 1;
     }

@@ -251,6 +251,9 @@ def main():
                     help="time shapes with fewer tokens L2-hot (decode sizes)")
     ap.add_argument("--block-formats", action="store_true",
                     help="sweep only the block-scaled outputs and merge their rows into the table")
+    ap.add_argument("--outs", default="",
+                    help="comma list of quantised outputs (fp8, mxfp8, mxfp4, nvfp4) to sweep on "
+                         "the quantised shapes; rows merged into the table")
     args = ap.parse_args()
     build.build()
     torch.cuda.set_device(0)
@@ -258,9 +261,9 @@ def main():
     if args.quick:
         grid = [(1, 4096), (256, 4096), (16384, 8192)]
     hot = args.l2_hot_below
-    if args.block_formats:
+    if args.block_formats or args.outs:
         entries = []
-        for fmt in BLOCK_FMTS:
+        for fmt in (args.outs.split(",") if args.outs else BLOCK_FMTS):
             entries += sweep(pkg, [(T, H) for H in (4096, 5120, 7168, 8192)
                                    for T in (1, 64, 1024, 4096, 16384)],
                              "bf16", fmt, True, True, args.reps, hot)
