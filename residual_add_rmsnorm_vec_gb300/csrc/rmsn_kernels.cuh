@@ -442,7 +442,7 @@ __device__ __forceinline__ float residual_sumsq(const RmsnArgs& a, int64_t rbase
 //          block scale E4M3(max|block| * (1 / (6 g))), codes
 //          E2M1(y * (1 / (scale * g))), with correctly rounded reciprocals.
 // All conversions round to nearest even and saturate.
-template <class TI, class TO, int CH, bool BIAS, class ReduceMax>
+template <class TI, class TO, int CH, bool BIAS, bool KEEP, class ReduceMax>
 __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row, int64_t rbase,
                                                   int G, int t, float inv, const V8 (&hv)[CH],
                                                   V8 (&wv)[CH], V8* bv, ReduceMax reduce_max) {
@@ -450,7 +450,9 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
     constexpr int LPB = TO::kBlock / VE;
     constexpr bool NV = TO::kBlock == 16;
     constexpr bool FP4 = !std::is_same<TO, MXFP8>::value;
+    constexpr bool HOLD = KEEP && NV;  // keep y between NVFP4's row-max and block passes
     static_assert(LPB >= 1 && LPB <= 4, "block spans 1..4 lanes");
+    float ys[HOLD ? CH : 1][HOLD ? VE : 1];
     float g = 0.f, rcp6g = 0.f;
     if constexpr (NV) {
         float amax = 0.f;
@@ -461,10 +463,12 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
                 opaque(wv[c]);
                 if constexpr (BIAS) opaque(bv[c]);
 #pragma unroll
-                for (int k = 0; k < VE; ++k)
-                    amax = fmaxf(amax, fabsf(scale_elem<BIAS>(elem<TI>(hv[c], k), inv,
-                                                              elem<TI>(wv[c], k), a.woff,
-                                                              BIAS ? elem<TI>(bv[c], k) : 0.f)));
+                for (int k = 0; k < VE; ++k) {
+                    const float y = scale_elem<BIAS>(elem<TI>(hv[c], k), inv, elem<TI>(wv[c], k),
+                                                     a.woff, BIAS ? elem<TI>(bv[c], k) : 0.f);
+                    if constexpr (HOLD) ys[c][k] = y;
+                    amax = fmaxf(amax, fabsf(y));
+                }
             }
         }
         amax = reduce_max(amax);
@@ -479,13 +483,21 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
         float y[VE];
         float bmax = 0.f;
         if (valid) {
-            opaque(wv[c]);
-            if constexpr (BIAS) opaque(bv[c]);
+            if constexpr (HOLD) {
 #pragma unroll
-            for (int k = 0; k < VE; ++k) {
-                y[k] = scale_elem<BIAS>(elem<TI>(hv[c], k), inv, elem<TI>(wv[c], k), a.woff,
-                                        BIAS ? elem<TI>(bv[c], k) : 0.f);
-                bmax = fmaxf(bmax, fabsf(y[k]));
+                for (int k = 0; k < VE; ++k) {
+                    y[k] = ys[c][k];
+                    bmax = fmaxf(bmax, fabsf(y[k]));
+                }
+            } else {
+                opaque(wv[c]);
+                if constexpr (BIAS) opaque(bv[c]);
+#pragma unroll
+                for (int k = 0; k < VE; ++k) {
+                    y[k] = scale_elem<BIAS>(elem<TI>(hv[c], k), inv, elem<TI>(wv[c], k), a.woff,
+                                            BIAS ? elem<TI>(bv[c], k) : 0.f);
+                    bmax = fmaxf(bmax, fabsf(y[k]));
+                }
             }
         }
         // every lane takes part; a block's lanes are all valid or all invalid
@@ -551,7 +563,8 @@ __device__ __forceinline__ void scale_store(const RmsnArgs& a, int64_t row, int6
                                             int t, float inv, const V8 (&hv)[CH], V8 (&wv)[CH],
                                             V8* bv, ReduceMax reduce_max) {
     if constexpr (IsBlockFmt<TO>::value) {
-        scale_store_block<TI, TO, CH, BIAS>(a, row, rbase, G, t, inv, hv, wv, bv, reduce_max);
+        scale_store_block<TI, TO, CH, BIAS, KEEP>(a, row, rbase, G, t, inv, hv, wv, bv,
+                                                  reduce_max);
         return;
     }
     constexpr int VE = 32 / TI::kBytes;
