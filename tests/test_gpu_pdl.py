@@ -4,7 +4,8 @@ x and residual, as consecutive norms of a layer stack do).  With PDL the next
 kernel may start before the previous one ends, so a missing wait would read
 stale rows; the chain must be bit-identical to the chain launched without
 PDL (same launch shapes), eagerly and in a CUDA graph, and its first call
-must match the oracle."""
+must match the oracle.  The 16384 x 8192 case is the prefill step that
+bench.py times, in its launch configuration (selector's choice + RMSN_PDL)."""
 import numpy as np
 import pytest
 import torch
@@ -60,7 +61,8 @@ def chain(pkg, inp, eps, n, pdl, early, graph=False):
     return [parity.bits16(t) for t in xs[1:] + rs[1:]]
 
 
-@pytest.mark.parametrize("T,H", [(1, 4096), (8, 4096), (256, 4096), (2048, 8192), (37, 1000)])
+@pytest.mark.parametrize("T,H", [(1, 4096), (8, 4096), (256, 4096), (2048, 8192), (37, 1000),
+                                 (16384, 8192)])
 @pytest.mark.parametrize("early", [False, True])
 def test_pdl_chain_matches_plain_chain(pkg, T, H, early):
     wl = synth.Workload(f"pdl_T{T}_H{H}", T, H, 21, "bf16", "bf16", 1e-6)
