@@ -269,6 +269,7 @@ def run_ours(args):
     decode = None if args.skip_decode else run_decode(pkg, synth, dev, stream)
     qk = None if args.skip_decode else run_qk(pkg, synth, dev, stream)
     quant = None if args.skip_decode else run_quantized(pkg, synth, dev, stream)
+    dtypes = None if args.skip_decode else run_dtype_paths(pkg, dev, stream, T, H)
 
     peak, peak_src = load_peaks()
     achieved = bytes_step / (kernel_ms / 1e3) / 1e9
@@ -310,6 +311,8 @@ def run_ours(args):
         line["qk_norm"] = qk
     if quant is not None:
         line["quantized"] = quant
+    if dtypes is not None:
+        line["dtype_paths"] = dtypes
     if rank == 0 and world == 1 and not args.skip_cpu:
         line["cpu_baseline"] = run_cpu_baseline(wl, host, args.cpu_seconds)
     if rank == 0:
@@ -616,25 +619,83 @@ def run_quantized(pkg, synth, dev, stream):
     return out
 
 
+def run_dtype_paths(pkg, dev, stream, T=16384, H=8192, n=200):
+    """The other storage types of the prefill step at the bench shape: fp16
+    in and out, and bf16 / fp16 activations over an fp32 residual stream.
+    Seeded device inputs above the L2 size, the selector's launch, n eager
+    launches back to back between two CUDA events; algorithmic GB/s."""
+    import torch
+
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(60)
+    out = {"unit": "GB/s", "tokens": T, "hidden": H,
+           "timing": f"{n} launches back to back, selector's launch, no PDL"}
+    for name, act, res_dt in (("f16", torch.float16, torch.float16),
+                              ("bf16_act_f32_stream", torch.bfloat16, torch.float32),
+                              ("f16_act_f32_stream", torch.float16, torch.float32)):
+        x = torch.randn((T, H), device=dev, generator=gen).to(act)
+        r = (2 * torch.randn((T, H), device=dev, generator=gen)).to(res_dt)
+        w = (1 + 0.1 * torch.randn((H,), device=dev, generator=gen)).to(act)
+        y, ro = torch.empty_like(x), torch.empty_like(r)
+
+        def call():
+            pkg.fused_add_rmsnorm(x, r, w, None, eps=1e-5, out=y, residual_out=ro)
+
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            call()
+        e.record(stream)
+        torch.cuda.synchronize(dev)
+        us = a.elapsed_time(e) * 1e3 / n
+        nbytes = T * H * (2 * x.element_size() + 2 * r.element_size()) + H * w.element_size()
+        flags = pkg.make_flags("f16" if act == torch.float16 else "bf16",
+                               "f16" if act == torch.float16 else "bf16", True, True, False)
+        if res_dt == torch.float32:
+            flags |= pkg.RMSN_RESIDUAL_F32
+        cfg = pkg.rmsnorm_query_config(T, H, flags)
+        out[name] = {"us": round(us, 2), "gbs": round(nbytes / us / 1e3, 1),
+                     "algorithmic_bytes": nbytes,
+                     "launch": f"{pkg.VARIANT_NAMES[cfg.variant]} ch{cfg.chunks} "
+                               f"w{cfg.warps_per_block} st{cfg.stages} grid{cfg.grid}"}
+        del x, r, w, y, ro
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_cpu_baseline(wl, host, seconds: float) -> dict:
     """The oracle as it stands, on every host core, over the whole workload
-    (repeated until `seconds` have passed)."""
+    (repeated until `seconds` have passed); and on one thread over the first
+    1024 rows (repeated for a quarter of that time)."""
     import oracle
 
     cores = oracle.num_cpus()
     eps = float(np.float32(wl.eps))
-    reps, t0 = 0, time.time()
-    while True:
-        oracle.rmsnorm(host["x"], host["residual"], host["weight"], None, eps=eps,
-                       in_dtype="bf16", out_dtype="bf16", n_threads=cores)
-        reps += 1
-        if time.time() - t0 >= seconds or reps >= 50:
-            break
-    dt = time.time() - t0
+
+    def timed(x, r, threads, budget):
+        reps, t0 = 0, time.time()
+        while True:
+            oracle.rmsnorm(x, r, host["weight"], None, eps=eps, in_dtype="bf16",
+                           out_dtype="bf16", n_threads=threads)
+            reps += 1
+            if time.time() - t0 >= budget or reps >= 50:
+                return reps, time.time() - t0
+
+    reps, dt = timed(host["x"], host["residual"], cores, seconds)
+    rows = min(1024, wl.n_tokens)
+    reps1, dt1 = timed(host["x"][:rows], host["residual"][:rows], 1, seconds / 4)
+    row_bytes = wl.algorithmic_bytes() / wl.n_tokens
     return {"value": round(wl.algorithmic_bytes() * reps / dt / 1e9, 3), "unit": UNIT,
             "cores": cores, "kind": "oracle",
             "sample": f"full {wl.n_tokens}x{wl.hidden} workload x {reps} passes ({dt:.1f} s), "
-                      f"fp64 C oracle, {cores} threads"}
+                      f"fp64 C oracle, {cores} threads",
+            "single_thread": {"value": round(row_bytes * rows * reps1 / dt1 / 1e9, 3),
+                              "unit": UNIT, "cores": 1,
+                              "sample": f"first {rows} rows x {reps1} passes ({dt1:.1f} s)"}}
 
 
 # ---------------------------------------------------------------------------- reference arm

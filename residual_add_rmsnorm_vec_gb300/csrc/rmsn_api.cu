@@ -218,7 +218,10 @@ int blocks_per_sm(DeviceInfo* d, const void* fn, int threads, int smem) {
 constexpr int kMaxStages = 8;
 constexpr int kBulkSmemTarget = 220 * 1024;
 
-int bulk_stage_bytes(const Problem& p) { return (int)((p.res ? 2 : 1) * p.H * p.in_bytes); }
+// One ring stage: the row of x, then (with a residual) the residual's row.
+int bulk_stage_bytes(const Problem& p) {
+    return (int)(p.H * p.in_bytes + (p.res ? p.H * p.res_bytes : 0));
+}
 
 // Fill block shape, grid (persistent: at most one resident wave) for an entry.
 bool shape_config(const Problem& p, const KernelEntry& e, DeviceInfo* d, int grid_req,
@@ -277,6 +280,11 @@ bool shape_config(const Problem& p, const KernelEntry& e, DeviceInfo* d, int gri
     return true;
 }
 
+// Table keys of the input side: the DType of x, or one of these two for
+// bf16 / fp16 activations over an fp32 residual stream.
+constexpr int kTableBF16R32 = 7;
+constexpr int kTableF16R32 = 8;
+
 #include "rmsn_selector_table.inc"
 
 // The selector (see the file comment): the measured table first, then the
@@ -288,7 +296,17 @@ bool select(const Problem& p, DeviceInfo* d, rmsn_config* c) {
         return e && shape_config(p, *e, d, 0, 0, c);
     }
     int variant = 0, ch = 0, wmax = 0, stages = 0;
-    if (table_lookup(p.in_dt, p.out_dt, p.H, p.T, &variant, &ch, &wmax, &stages)) {
+    int tin = p.res_f32 ? (p.in_dt == kF16 ? kTableF16R32 : kTableBF16R32) : p.in_dt;
+    int tout = p.out_dt;
+    bool found = table_lookup(tin, tout, p.H, p.T, &variant, &ch, &wmax, &stages);
+    if (!found && (tin == kF16 || tin == kTableF16R32)) {
+        // fp16 moves the same bytes through the same kernels as bf16: without
+        // rows of its own it takes the bf16 rows
+        tin = tin == kF16 ? kBF16 : kTableBF16R32;
+        if (tout == kF16) tout = kBF16;
+        found = table_lookup(tin, tout, p.H, p.T, &variant, &ch, &wmax, &stages);
+    }
+    if (found) {
         const KernelEntry* e = find_kernel(p, variant, ch, wmax);
         if (e && shape_config(p, *e, d, 0, stages, c)) return true;
     }

@@ -3,8 +3,8 @@
 // RMSN_TI / RMSN_TO (types), RMSN_DTI / RMSN_DTO (DType codes) and
 // RMSN_TABLE_FN (the table accessor declared in rmsn_registry.h).  For an
 // fp32 residual stream under bf16 / fp16 activations they also define
-// RMSN_TX (the activation type; RMSN_TI is then F32), RMSN_RF32 1,
-// RMSN_RES_ONLY and RMSN_NO_BULK.
+// RMSN_TX (the activation type; RMSN_TI is then F32), RMSN_RF32 1 and
+// RMSN_RES_ONLY.
 #include "rmsn_kernels.cuh"
 
 namespace rmsn {
@@ -27,11 +27,15 @@ namespace rmsn {
         RMSN_VEC(CH, WMAX, WR, false, true), RMSN_VEC(CH, WMAX, WR, true, true)
 #endif
 #define RMSN_BULK(CH, WMAX, RES, BIAS)                                                       \
-    {RMSN_DTI, RMSN_DTO, kBulkRow, CH, WMAX, 0, RES, BIAS, 0,                                \
-     (const void*)&rmsn_bulk_kernel<RMSN_TI, RMSN_TO, CH, WMAX, RES, BIAS>}
+    {RMSN_DTI, RMSN_DTO, kBulkRow, CH, WMAX, 0, RES, BIAS, RMSN_RF32,                        \
+     (const void*)&rmsn_bulk_kernel<RMSN_TI, RMSN_TO, CH, WMAX, RES, BIAS, RMSN_TX>}
+#ifdef RMSN_RES_ONLY
+#define RMSN_BULK4(CH, WMAX) RMSN_BULK(CH, WMAX, true, false), RMSN_BULK(CH, WMAX, true, true)
+#else
 #define RMSN_BULK4(CH, WMAX)                                                                 \
     RMSN_BULK(CH, WMAX, false, false), RMSN_BULK(CH, WMAX, true, false),                     \
         RMSN_BULK(CH, WMAX, false, true), RMSN_BULK(CH, WMAX, true, true)
+#endif
 #define RMSN_GEN(RES)                                                                        \
     {RMSN_DTI, RMSN_DTO, kGeneric, 0, 8, 0, RES, -1, RMSN_RF32,                              \
      (const void*)&rmsn_generic_kernel<RMSN_TI, RMSN_TO, RES, RMSN_TX>}

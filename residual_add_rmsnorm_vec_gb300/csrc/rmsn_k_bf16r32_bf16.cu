@@ -7,6 +7,5 @@
 #define RMSN_DTO kBF16
 #define RMSN_RF32 1
 #define RMSN_RES_ONLY
-#define RMSN_NO_BULK
 #define RMSN_TABLE_FN kernels_bf16r32_bf16
 #include "rmsn_instances.cuh"

@@ -715,24 +715,25 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     return true;
 }
 
-// Thread 0: expect `bytes` on `bar`, then copy x (and r) of `row` into `dst`.
+// Thread 0: expect the row's bytes on `bar`, then copy x (x_bytes) of `row`
+// into `dst` and, with a residual, its residual row (r_bytes) right after it.
 template <bool RES>
 __device__ __forceinline__ void issue_row(const RmsnArgs& a, int64_t row, uint32_t dst,
-                                          uint32_t bar, uint32_t row_bytes) {
-    const uint32_t bytes = RES ? 2 * row_bytes : row_bytes;
+                                          uint32_t bar, uint32_t x_bytes, uint32_t r_bytes) {
+    const uint32_t bytes = RES ? x_bytes + r_bytes : x_bytes;
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
-    const char* src = static_cast<const char*>(a.x) + row * (int64_t)row_bytes;
+    const char* src = static_cast<const char*>(a.x) + row * (int64_t)x_bytes;
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(src), "r"(row_bytes), "r"(bar)
+        ::"r"(dst), "l"(src), "r"(x_bytes), "r"(bar)
         : "memory");
     if constexpr (RES) {
-        const char* rsrc = static_cast<const char*>(a.r) + row * (int64_t)row_bytes;
+        const char* rsrc = static_cast<const char*>(a.r) + row * (int64_t)r_bytes;
         asm volatile(
             "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-            "[%3];" ::"r"(dst + row_bytes),
-            "l"(rsrc), "r"(row_bytes), "r"(bar)
+            "[%3];" ::"r"(dst + x_bytes),
+            "l"(rsrc), "r"(r_bytes), "r"(bar)
             : "memory");
     }
 }
@@ -748,9 +749,34 @@ __device__ __forceinline__ V8 ld_shared32(uint32_t addr) {
     return v;
 }
 
-template <class TI, class TO, int CH, int WMAX, bool RES, bool BIAS>
+// One vector of VE = 32 / TI::kBytes elements from shared memory: 32 bytes,
+// or 16 bytes of 2-byte values widened exactly to fp32 under an fp32 stream.
+template <class TX, class TI>
+__device__ __forceinline__ V8 ld_shared_vec(uint32_t addr) {
+    if constexpr (TX::kBytes == TI::kBytes) {
+        return ld_shared32(addr);
+    } else {
+        static_assert(TX::kBytes == 2 && TI::kBytes == 4, "2-byte values under fp32 only");
+        uint32_t in[4];
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(in[0]), "=r"(in[1]), "=r"(in[2]), "=r"(in[3])
+                     : "r"(addr));
+        V8 v;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            v.u[2 * k] = __float_as_uint(lo2<TX>(in[k]));
+            v.u[2 * k + 1] = __float_as_uint(hi2<TX>(in[k]));
+        }
+        return v;
+    }
+}
+
+// TX: storage of x, weight and bias, as in rmsn_vec_kernel; a stage holds
+// the row of x followed by the row of the residual (TI).
+template <class TI, class TO, int CH, int WMAX, bool RES, bool BIAS, class TX = TI>
 __global__ void __launch_bounds__(WMAX * 32, 1) rmsn_bulk_kernel(const RmsnArgs a) {
     constexpr int VE = 32 / TI::kBytes;
+    constexpr int XVB = VE * TX::kBytes;  // bytes of one x vector
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full[kMaxStages];
     __shared__ float red[4][32];
@@ -759,8 +785,9 @@ __global__ void __launch_bounds__(WMAX * 32, 1) rmsn_bulk_kernel(const RmsnArgs 
     const int G = blockDim.x;
     const int t = threadIdx.x;
     const int S = a.stages;
-    const uint32_t row_bytes = (uint32_t)a.H * TI::kBytes;
-    const uint32_t stage_bytes = RES ? 2 * row_bytes : row_bytes;
+    const uint32_t x_bytes = (uint32_t)a.H * TX::kBytes;
+    const uint32_t r_bytes = (uint32_t)a.H * TI::kBytes;
+    const uint32_t stage_bytes = RES ? x_bytes + r_bytes : x_bytes;
     const uint32_t ring0 = smem_u32(ring);
     // rows of this block: blockIdx.x + k * gridDim.x
     const int64_t n_my = a.T > blockIdx.x ? (a.T - 1 - blockIdx.x) / gridDim.x + 1 : 0;
@@ -768,7 +795,7 @@ __global__ void __launch_bounds__(WMAX * 32, 1) rmsn_bulk_kernel(const RmsnArgs 
     pdl_launch_dependents(a.pdl);
     V8 wv[CH];
     V8 bv[BIAS ? CH : 1];
-    if (a.early_params) load_params<TI, TI, CH>(a, G, t, wv, bv, BIAS);
+    if (a.early_params) load_params<TX, TI, CH>(a, G, t, wv, bv, BIAS);
     pdl_wait(a.pdl);
     if (t == 0) {
         abort_flag = 0;
@@ -776,10 +803,10 @@ __global__ void __launch_bounds__(WMAX * 32, 1) rmsn_bulk_kernel(const RmsnArgs 
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         for (int64_t k = 0; k < S && k < n_my; ++k)
             issue_row<RES>(a, blockIdx.x + k * gridDim.x, ring0 + (uint32_t)k * stage_bytes,
-                           smem_u32(&full[k]), row_bytes);
+                           smem_u32(&full[k]), x_bytes, r_bytes);
     }
     __syncthreads();
-    if (!a.early_params) load_params<TI, TI, CH>(a, G, t, wv, bv, BIAS);
+    if (!a.early_params) load_params<TX, TI, CH>(a, G, t, wv, bv, BIAS);
 
     int parity = 0;
     int64_t k_abort = 0;
@@ -800,8 +827,8 @@ __global__ void __launch_bounds__(WMAX * 32, 1) rmsn_bulk_kernel(const RmsnArgs 
         for (int c = 0; c < CH; ++c) {
             const int v = c * G + t;
             if (v < a.nvec) {
-                hv[c] = ld_shared32(base + (uint32_t)v * 32);
-                if constexpr (RES) rv[c] = ld_shared32(base + row_bytes + (uint32_t)v * 32);
+                hv[c] = ld_shared_vec<TX, TI>(base + (uint32_t)v * XVB);
+                if constexpr (RES) rv[c] = ld_shared32(base + x_bytes + (uint32_t)v * 32);
             }
         }
         const float acc = residual_sumsq<TI, CH, RES>(a, rbase, G, t, hv, rv);
@@ -811,7 +838,7 @@ __global__ void __launch_bounds__(WMAX * 32, 1) rmsn_bulk_kernel(const RmsnArgs 
         if (t == 0 && k + S < n_my) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             issue_row<RES>(a, blockIdx.x + (k + S) * gridDim.x, base, smem_u32(&full[s]),
-                           row_bytes);
+                           x_bytes, r_bytes);
         }
         const float inv = inv_rms(sumsq, a.H, a.eps);
         float* slot = red[2 + parity];

@@ -28,11 +28,13 @@ import time
 L2_BYTES = 129 * 10**6
 TOKENS = (1, 4, 16, 64, 256, 1024, 4096, 16384, 65536)
 HIDDEN = (2048, 4096, 8192, 16384)
-DTYPE_CODES = {"f32": 0, "bf16": 1, "fp8": 2, "mxfp8": 3, "mxfp4": 4, "nvfp4": 5, "f16": 6}
+# table keys; "+r32": bf16 / fp16 activations over an fp32 residual stream
+DTYPE_CODES = {"f32": 0, "bf16": 1, "fp8": 2, "mxfp8": 3, "mxfp4": 4, "nvfp4": 5, "f16": 6,
+               "bf16+r32": 7, "f16+r32": 8}
 BLOCK_FMTS = ("mxfp8", "mxfp4", "nvfp4")
 
 
-def _algorithmic_bytes(T, H, in_b, out_b, res, bias, fp8, fmt=None):
+def _algorithmic_bytes(T, H, in_b, out_b, res, bias, fp8, fmt=None, res_b=None):
     if fmt in BLOCK_FMTS:
         blk, per_byte = (16, 2) if fmt == "nvfp4" else (32, 1 if fmt == "mxfp8" else 2)
         b = T * H * in_b + T * H // per_byte + T * H // blk + H * in_b
@@ -42,7 +44,7 @@ def _algorithmic_bytes(T, H, in_b, out_b, res, bias, fp8, fmt=None):
         if fp8:
             b += 4 * T
     if res:
-        b += 2 * T * H * in_b
+        b += 2 * T * H * (in_b if res_b is None else res_b)
     if bias:
         b += H * in_b
     return b
@@ -53,28 +55,33 @@ def measure(pkg, T, H, in_dt="bf16", out_dt="bf16", res=True, bias=False, reps=3
     import torch
 
     dev = torch.device("cuda")
+    r32 = in_dt.endswith("+r32")
+    in_dt = in_dt.split("+")[0]
     tin = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[in_dt]
+    tres = torch.float32 if r32 else tin
     in_b = 4 if in_dt == "f32" else 2
+    res_b = 4 if r32 else in_b
     block = out_dt in BLOCK_FMTS
     out_b = {"bf16": 2, "f16": 2, "f32": 4, "fp8": 1}.get(out_dt, 1)
     tout = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}.get(
         out_dt, torch.uint8)
     # block formats share the launch shapes of the per-token FP8 output
-    flags = pkg.make_flags(in_dt, "fp8" if block else out_dt, res, True, bias)
-    call_flags = pkg.make_flags(in_dt, "f32", res, True, bias) if block else flags
-    set_bytes = T * H * (in_b * (3 if res else 1) + out_b)
+    rflag = pkg.RMSN_RESIDUAL_F32 if r32 else 0
+    flags = pkg.make_flags(in_dt, "fp8" if block else out_dt, res, True, bias) | rflag
+    call_flags = pkg.make_flags(in_dt, "f32", res, True, bias) | rflag if block else flags
+    set_bytes = T * H * (in_b + (2 * res_b if res else 0) + out_b)
     n_sets = 1 if l2_hot else max(1, min(64, -(-3 * L2_BYTES // max(1, set_bytes))))
     sets = []
     for _ in range(n_sets):
         x = torch.randn(T, H, device=dev).to(tin)
-        r = torch.randn(T, H, device=dev).to(tin) if res else None
+        r = torch.randn(T, H, device=dev).to(tres) if res else None
         if block:
             code, blk, per_byte = pkg.BLOCK_FORMATS[out_dt]
             q = torch.empty(T, H // per_byte, device=dev, dtype=torch.uint8)
             bsc = torch.empty(T, H // blk, device=dev, dtype=torch.uint8)
         else:
             q, bsc = torch.empty(T, H, device=dev, dtype=tout), None
-        sets.append((x, r, q, torch.empty_like(x) if res else None,
+        sets.append((x, r, q, torch.empty_like(r) if res else None,
                      torch.empty(T, device=dev, dtype=torch.float32)
                      if out_dt in ("fp8", "nvfp4") else None, bsc))
     w = (1 + 0.1 * torch.randn(H, device=dev)).to(tin)
@@ -84,7 +91,7 @@ def measure(pkg, T, H, in_dt="bf16", out_dt="bf16", res=True, bias=False, reps=3
         configs = pkg.rmsnorm_list_configs(T, H, flags)
         if block:
             configs = [c for c in configs if c.variant != pkg.VARIANT_GENERIC]
-    algo = _algorithmic_bytes(T, H, in_b, out_b, res, bias, out_dt == "fp8", out_dt)
+    algo = _algorithmic_bytes(T, H, in_b, out_b, res, bias, out_dt == "fp8", out_dt, res_b)
     results = []
     for cfg in configs:
         def launch_on(i, s):
@@ -193,7 +200,8 @@ def write_table(entries, path, extra_rows=()):
         "// launches; inputs rotated past the L2 size from 512 tokens up, L2-hot below).",
         "// For one (input dtype, output dtype, hidden) the row with the largest",
         "// t_min <= n_tokens applies; other shapes fall back to the fixed rule in the",
-        "// selector.",
+        "// selector.  Input keys are DType codes, or 7 / 8 for bf16 / fp16",
+        "// activations over an fp32 residual stream.",
         "struct TableRow {",
         "    int in_dt, out_dt;",
         "    int64_t hidden, t_min;",
@@ -251,6 +259,9 @@ def main():
                     help="time shapes with fewer tokens L2-hot (decode sizes)")
     ap.add_argument("--block-formats", action="store_true",
                     help="sweep only the block-scaled outputs and merge their rows into the table")
+    ap.add_argument("--pairs", default="",
+                    help="comma list of input:output pairs (e.g. f16:f16,bf16+r32:bf16) to sweep "
+                         "on the hidden sizes 2048..16384; rows merged into the table")
     ap.add_argument("--outs", default="",
                     help="comma list of quantised outputs (fp8, mxfp8, mxfp4, nvfp4) to sweep on "
                          "the quantised shapes; rows merged into the table")
@@ -261,6 +272,19 @@ def main():
     if args.quick:
         grid = [(1, 4096), (256, 4096), (16384, 8192)]
     hot = args.l2_hot_below
+    if args.pairs:
+        entries = []
+        for pair in args.pairs.split(","):
+            i, o = pair.split(":")
+            entries += sweep(pkg, [(T, H) for H in HIDDEN for T in (1, 16, 256, 1024, 4096, 16384)],
+                             i, o, True, False, args.reps, hot)
+        with open(args.out, "w") as f:
+            json.dump({"meta": {"gpu": torch.cuda.get_device_name(0), "reps": args.reps,
+                                "l2_hot_below": hot, "timing": "cuda graph replay"},
+                       "entries": entries}, f)
+        if args.write_table:
+            merge_table(entries, args.table_out)
+        return
     if args.block_formats or args.outs:
         entries = []
         for fmt in (args.outs.split(",") if args.outs else BLOCK_FMTS):

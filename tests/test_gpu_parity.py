@@ -164,6 +164,7 @@ def test_fp16_io(pkg, T, H):
     (2048, 8192, "bf16", "bf16", False), (4096, 5120, "bf16", "fp8", True),
     (64, 4096, "f16", "f16", True), (300, 2048, "f16", "fp8", False),
     (33, 1000, "bf16", "bf16", True), (5, 12, "f16", "f16", False),
+    (16384, 8192, "bf16", "bf16", False), (4096, 8192, "f16", "f16", True),
 ])
 def test_f32_residual_stream(pkg, T, H, in_dt, out_dt, bias):
     # bf16 / fp16 activations, fp32 residual stream: residual_out is the fp32
@@ -173,24 +174,28 @@ def test_f32_residual_stream(pkg, T, H, in_dt, out_dt, bias):
     check(pkg, wl)
 
 
-def test_f32_residual_stream_every_config_and_in_place(pkg):
-    wl = synth.Workload("r32_cfg", 37, 2048, 91, "bf16", "bf16", 1e-6, has_bias=True,
-                        res_dtype="f32")
-    flags = pkg.make_flags("bf16", "bf16", True, True, True) | pkg.RMSN_RESIDUAL_F32
+@pytest.mark.parametrize("in_dt,out_dt", [("bf16", "bf16"), ("f16", "f16"), ("bf16", "fp8")])
+def test_f32_residual_stream_every_config_and_in_place(pkg, in_dt, out_dt):
+    wl = synth.Workload(f"r32_cfg_{in_dt}_{out_dt}", 37, 2048, 91, in_dt, out_dt, 1e-6,
+                        has_bias=True, res_dtype="f32")
+    flags = pkg.make_flags(in_dt, out_dt, True, True, True) | pkg.RMSN_RESIDUAL_F32
     cfgs = pkg.rmsnorm_list_configs(37, 2048, flags)
-    assert cfgs and all(c.variant != pkg.VARIANT_BULK_ROW for c in cfgs)
+    assert cfgs and any(c.variant == pkg.VARIANT_BULK_ROW for c in cfgs)
     inp = synth.make_inputs(wl)
     ref = parity.oracle_run(wl, inp)
     for c in cfgs:
         parity.compare(wl, run_gpu(pkg, wl, inp, config=c), ref, f"r32 {c.as_dict()}",
                        bias=inp["bias"])
-    # residual_out written over the residual itself (the usual in-place update)
-    g = parity.to_device(inp, DEV)
-    out, res, _ = pkg.fused_add_rmsnorm(g["x"], g["residual"], g["weight"], g["bias"],
-                                        eps=wl.eps, residual_out=g["residual"])
-    torch.cuda.synchronize()
-    parity.compare(wl, parity.gpu_outputs_to_host(wl, out, res, None), ref, "r32 in place",
-                   bias=inp["bias"])
+    # residual_out written over the residual itself (the usual in-place
+    # update), with the selector's launch and with every ring shape
+    for c in [None] + [c for c in cfgs if c.variant == pkg.VARIANT_BULK_ROW]:
+        g = parity.to_device(inp, DEV)
+        out, res, scale = pkg.fused_add_rmsnorm(g["x"], g["residual"], g["weight"], g["bias"],
+                                                eps=wl.eps, out_dtype=out_dt,
+                                                residual_out=g["residual"], config=c)
+        torch.cuda.synchronize()
+        parity.compare(wl, parity.gpu_outputs_to_host(wl, out, res, scale), ref,
+                       f"r32 in place {c}", bias=inp["bias"])
 
 
 @pytest.mark.parametrize("H", [1, 7, 1000, 4097])
