@@ -393,7 +393,8 @@ def run_e2e(pkg, wl, host, dev, stream, flags, steps, pg):
 
 def run_decode(pkg, synth, dev, stream):
     """us per call at decode sizes (inputs L2-resident), back-to-back and in a
-    CUDA graph, and the same for an empty kernel (torch.cuda._sleep(0))."""
+    CUDA graph, and the same for an empty kernel (torch.cuda._sleep(0)) and,
+    in a graph, for torch's add of the same two inputs."""
     import torch
 
     res = {"hidden": 4096, "unit": "us/call"}
@@ -464,9 +465,13 @@ def run_decode(pkg, synth, dev, stream):
         us = timeit(call, n)
         gus = graph_time(call)
         gus_pdl = graph_time(call_pdl)
+        # floor for comparison: torch's elementwise add of the same x and r
+        # (reads both, writes one tensor; no reduction), in a graph likewise
+        gus_add = graph_time(lambda: torch.add(x, r, out=out))
         cfg = pkg.rmsnorm_query_config(T, 4096, flags)
         per_t[str(T)] = {"us": round(us, 3), "graph_us": round(gus, 3),
                          "graph_pdl_us": round(gus_pdl, 3),
+                         "torch_add_graph_us": round(gus_add, 3),
                          "gbs_l2_hot": round(wl.algorithmic_bytes() / (us * 1e-6) / 1e9, 1),
                          "launch": f"{pkg.VARIANT_NAMES[cfg.variant]} ch{cfg.chunks} "
                                    f"w{cfg.warps_per_block} grid{cfg.grid}"}

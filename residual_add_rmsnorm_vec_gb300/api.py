@@ -38,6 +38,50 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+def _check(name, t, shape, dtypes, device=None):
+    """A tensor the kernels will index as `shape`: anything else is refused
+    here, before a launch could read or write past it."""
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} must be one of {[str(d) for d in dtypes]}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def check_row_args(x, residual, weight, bias, out, residual_out, out_scale, out_dtype,
+                   device=None):
+    """Shapes, dtypes, devices and layout of the row norm's tensors.
+
+    x is [T, H] bf16 / fp16 / fp32; the residual and residual_out are [T, H]
+    of x's dtype, or both fp32 over bf16 / fp16 x (an fp32 residual stream);
+    weight and bias are [H] of x's dtype; out is [T, H] of the output dtype
+    (uint8 codes for FP8); out_scale is [T] fp32.  ``device``: where every
+    tensor must live (None: anywhere, as for the host-memory entry)."""
+    if x.dim() != 2:
+        raise ValueError("x must be [n_tokens, hidden]")
+    if x.dtype not in _IN:
+        raise TypeError(f"unsupported input dtype {x.dtype}")
+    T, H = x.shape
+    _check("x", x, (T, H), (x.dtype,), device)
+    res_dtypes = (x.dtype,) if x.dtype == torch.float32 else (x.dtype, torch.float32)
+    _check("residual", residual, (T, H), res_dtypes, device)
+    if residual_out is not None and residual is None:
+        raise ValueError("residual_out needs a residual")
+    if residual is not None:
+        _check("residual_out", residual_out, (T, H), (residual.dtype,), device)
+    _check("weight", weight, (H,), (x.dtype,), device)
+    _check("bias", bias, (H,), (x.dtype,), device)
+    _check("out", out, (T, H), (_OUT[out_dtype][1],), device)
+    if out_scale is not None and out_dtype != "fp8":
+        raise ValueError("out_scale is only written for the fp8 output")
+    _check("out_scale", out_scale, (T,), (torch.float32,), device)
+
+
 def fused_add_rmsnorm(x: torch.Tensor, residual: torch.Tensor | None = None,
                       weight: torch.Tensor | None = None, bias: torch.Tensor | None = None, *,
                       eps: float, out_dtype: str | None = None, weight_offset: float = 0.0,
@@ -54,18 +98,15 @@ def fused_add_rmsnorm(x: torch.Tensor, residual: torch.Tensor | None = None,
     launches with programmatic dependent launch (``early_params``: weight and
     bias are not written by the preceding kernel).
     """
-    if x.dim() != 2:
-        raise ValueError("x must be [n_tokens, hidden]")
-    if x.dtype not in _IN:
-        raise TypeError(f"unsupported input dtype {x.dtype}")
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor (host rows: fused_add_rmsnorm_host)")
+    out_dtype = out_dtype or _DT_NAME.get(x.dtype, "")
+    if out_dtype not in _OUT:
+        raise ValueError(f"unsupported output dtype {out_dtype!r}")
+    check_row_args(x, residual, weight, bias, out, residual_out, out_scale, out_dtype, x.device)
     T, H = x.shape
     in_name = _DT_NAME[x.dtype]
-    out_dtype = out_dtype or in_name
     out_flag, out_torch = _OUT[out_dtype]
-    for name, t in (("residual", residual), ("weight", weight), ("bias", bias),
-                    ("out", out), ("residual_out", residual_out), ("out_scale", out_scale)):
-        if t is not None and not t.is_contiguous():
-            raise ValueError(f"{name} must be contiguous")
     if out is None:
         out = torch.empty((T, H), dtype=out_torch, device=x.device)
     # an fp32 residual under bf16 / fp16 activations is an fp32 residual stream
@@ -79,7 +120,7 @@ def fused_add_rmsnorm(x: torch.Tensor, residual: torch.Tensor | None = None,
     if res_f32:
         flags |= _lib.RMSN_RESIDUAL_F32
     s = stream if stream is not None else torch.cuda.current_stream(x.device)
-    st = _lib.rmsnorm_fwd_ex(_ptr(x.contiguous()), _ptr(residual), _ptr(weight), _ptr(bias),
+    st = _lib.rmsnorm_fwd_ex(_ptr(x), _ptr(residual), _ptr(weight), _ptr(bias),
                              _ptr(out), _ptr(residual_out), _ptr(out_scale), T, H, eps, flags,
                              weight_offset, config, s.cuda_stream)
     if st != _lib.RMSN_OK:
@@ -102,26 +143,23 @@ def fused_add_rmsnorm_host(x: torch.Tensor, residual: torch.Tensor | None = None
     ``(out, residual_out, out_scale)`` like ``fused_add_rmsnorm``; the call is
     asynchronous, so synchronise ``stream`` before reading them.
     """
-    if x.dim() != 2:
-        raise ValueError("x must be [n_tokens, hidden]")
-    if x.dtype not in _IN:
-        raise TypeError(f"unsupported input dtype {x.dtype}")
+    out_dtype = out_dtype or _DT_NAME.get(x.dtype, "")
+    if out_dtype not in _OUT:
+        raise ValueError(f"unsupported output dtype {out_dtype!r}")
+    check_row_args(x, residual, weight, bias, out, residual_out, out_scale, out_dtype)
     T, H = x.shape
     in_name = _DT_NAME[x.dtype]
-    out_dtype = out_dtype or in_name
     _, out_torch = _OUT[out_dtype]
-    for name, t in (("x", x), ("residual", residual), ("weight", weight), ("bias", bias),
-                    ("out", out), ("residual_out", residual_out), ("out_scale", out_scale)):
-        if t is not None and not t.is_contiguous():
-            raise ValueError(f"{name} must be contiguous")
     if out is None:
         out = torch.empty((T, H), dtype=out_torch, pin_memory=True)
     if residual is not None and residual_out is None:
-        residual_out = torch.empty((T, H), dtype=x.dtype, pin_memory=True)
+        residual_out = torch.empty((T, H), dtype=residual.dtype, pin_memory=True)
     if out_dtype == "fp8" and out_scale is None:
         out_scale = torch.empty((T,), dtype=torch.float32, pin_memory=True)
     flags = make_flags(in_name, out_dtype, residual is not None, weight is not None,
                        bias is not None)
+    if residual is not None and residual.dtype == torch.float32 and x.dtype != torch.float32:
+        flags |= _lib.RMSN_RESIDUAL_F32
     dev = torch.cuda.current_device() if device is None else device
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     with torch.cuda.device(dev):
@@ -155,15 +193,29 @@ def qk_norm_(q: torch.Tensor | None, k: torch.Tensor | None, q_weight: torch.Ten
             raise ValueError("q/k must be [T, heads*head_dim] with unit column stride")
         return t, t.shape[1] // head_dim, t.stride(0)
 
+    if head_dim < 1:
+        raise ValueError("head_dim must be positive")
+    for name, t in (("q", q), ("k", k)):
+        if t is None:
+            continue
+        if (t.shape[-1] != head_dim) if t.dim() == 3 else (t.shape[-1] % head_dim != 0):
+            raise ValueError(f"{name}: rows must hold whole heads of head_dim elements")
     q2, hq, qs = view2d(q)
     k2, hk, ks = view2d(k)
     ref = q2 if q2 is not None else k2
     if ref is None:
         return q, k
-    if q2 is not None and k2 is not None and q2.shape[0] != k2.shape[0]:
-        raise ValueError("q and k need the same number of tokens")
+    if q2 is not None and k2 is not None:
+        if q2.shape[0] != k2.shape[0]:
+            raise ValueError("q and k need the same number of tokens")
+        if q2.dtype != k2.dtype or q2.device != k2.device:
+            raise TypeError("q and k need the same dtype and device")
     if ref.dtype not in _IN:
         raise TypeError(f"unsupported dtype {ref.dtype}")
+    if not ref.is_cuda:
+        raise ValueError("q / k must be CUDA tensors")
+    _check("q_weight", q_weight, (head_dim,), (ref.dtype,), ref.device)
+    _check("k_weight", k_weight, (head_dim,), (ref.dtype,), ref.device)
     flags = _IN[ref.dtype] | (_lib.RMSN_PDL if pdl else 0)
     s = stream if stream is not None else torch.cuda.current_stream(ref.device)
     st = _lib.rmsnorm_qk_fwd(_ptr(q2), _ptr(k2), _ptr(q_weight), _ptr(k_weight), ref.shape[0],
@@ -187,7 +239,19 @@ def fused_add_rmsnorm_blockscaled(x: torch.Tensor, residual: torch.Tensor | None
     float32 [T] for NVFP4 (else None)."""
     if x.dim() != 2 or x.dtype != torch.bfloat16:
         raise TypeError("x must be a 2-D bfloat16 tensor")
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    if fmt not in _lib.BLOCK_FORMATS:
+        raise ValueError(f"unknown block format {fmt!r}")
     T, H = x.shape
+    bf16 = (torch.bfloat16,)
+    _check("x", x, (T, H), bf16, x.device)
+    _check("residual", residual, (T, H), bf16, x.device)
+    if residual_out is not None and residual is None:
+        raise ValueError("residual_out needs a residual")
+    _check("residual_out", residual_out, (T, H), bf16, x.device)
+    _check("weight", weight, (H,), bf16, x.device)
+    _check("bias", bias, (H,), bf16, x.device)
     code, block, per_byte = _lib.BLOCK_FORMATS[fmt]
     q = torch.empty((T, H // per_byte), dtype=torch.uint8, device=x.device)
     bs = torch.empty((T, H // block), dtype=torch.uint8, device=x.device)
