@@ -795,12 +795,15 @@ __global__ void __launch_bounds__(WMAX * 32, 1) rmsn_bulk_kernel(const RmsnArgs 
     pdl_launch_dependents(a.pdl);
     V8 wv[CH];
     V8 bv[BIAS ? CH : 1];
-    if (a.early_params) load_params<TX, TI, CH>(a, G, t, wv, bv, BIAS);
-    pdl_wait(a.pdl);
     if (t == 0) {
+        // shared memory only: done before waiting for the prerequisite grid
         abort_flag = 0;
         for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (a.early_params) load_params<TX, TI, CH>(a, G, t, wv, bv, BIAS);
+    pdl_wait(a.pdl);
+    if (t == 0) {
         for (int64_t k = 0; k < S && k < n_my; ++k)
             issue_row<RES>(a, blockIdx.x + k * gridDim.x, ring0 + (uint32_t)k * stage_bytes,
                            smem_u32(&full[k]), x_bytes, r_bytes);

@@ -87,6 +87,18 @@ def test_prefill_full_size_bulk_ring(pkg, stages, ch, wmax):
     assert pkg.rmsnorm_read_status() == 0
 
 
+@pytest.mark.parametrize("stages", [2, 5, 8])
+@pytest.mark.parametrize("grid", [0, 7])
+def test_deep_ring_wraps(pkg, stages, grid):
+    # short rows through a deep ring: every stage is refilled many times
+    # (3000 rows over 7 blocks: ~430 rows per block)
+    wl = synth.Workload(f"ring_st{stages}", 3000, 2048, 78, "bf16", "bf16", 1e-6, has_bias=True)
+    cfg = pkg.RmsnConfig.from_dict({"variant": pkg.VARIANT_BULK_ROW, "chunks": 1,
+                                    "max_warps": 8, "stages": stages, "grid": grid})
+    check(pkg, wl, config=cfg)
+    assert pkg.rmsnorm_read_status() == 0
+
+
 @pytest.mark.parametrize("H", synth.FP8_HIDDEN)
 def test_fp8_bias(pkg, H):
     st = check(pkg, synth.fp8_workload(H))
