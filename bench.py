@@ -20,6 +20,10 @@ residual_out and y.  Prints ONE JSON line on rank 0:
              row norm on the head views (two launches), us per call
   cpu_baseline  the CPU oracle on the host cores (rank 0, N = 1)
 
+--out fp8 makes the timed step the quantised-output workload instead
+(per-token FP8 E4M3 with bias; use --tokens 4096 --hidden 5120 or 7168).
+A step whose bytes fit in L2 rotates over enough buffer sets to exceed it.
+
 --impl reference times the CPU oracle instead (the only reference of this
 method), on a bounded row sample per step.
 
@@ -195,6 +199,21 @@ def rank_rows(rank: int, world: int, tokens_per_rank: int) -> range:
 # ---------------------------------------------------------------------------- our arm
 
 
+def step_workload(synth, args, n_tokens):
+    """The timed step's workload: the bf16 prefill (default) or, with
+    --out fp8, the per-token FP8 output with bias (4096 x 5120 / 7168)."""
+    if args.out == "fp8":
+        return synth.fp8_workload(args.hidden, n_tokens=n_tokens)
+    return synth.prefill_workload(n_tokens, args.hidden)
+
+
+def workload_name(wl) -> str:
+    if wl.out_dtype == "fp8":
+        return (f"fused residual-add + RMSNorm bf16 -> per-token FP8 E4M3 with bias "
+                f"T={wl.n_tokens} H={wl.hidden} eps=1e-6")
+    return f"prefill fused residual-add + RMSNorm bf16 T={wl.n_tokens} H={wl.hidden} eps=1e-5"
+
+
 def run_ours(args):
     import torch
 
@@ -207,29 +226,40 @@ def run_ours(args):
     build.build()
 
     # each rank owns a contiguous slice of one seeded global batch (weak scaling)
-    wl = synth.prefill_workload(args.tokens, args.hidden)
-    wl_global = synth.prefill_workload(args.tokens * world, args.hidden)
+    wl = step_workload(synth, args, args.tokens)
+    wl_global = step_workload(synth, args, args.tokens * world)
     T, H = wl.n_tokens, wl.hidden
-    flags = pkg.make_flags("bf16", "bf16", True, True, False)
+    fp8 = wl.out_dtype == "fp8"
+    flags = pkg.make_flags("bf16", wl.out_dtype, True, True, wl.has_bias)
     # consecutive steps are chained by programmatic dependent launch: a step's
     # grid is scheduled while the previous one drains and waits for it to
     # complete before its first read
     step_flags = flags if args.no_pdl else flags | pkg.RMSN_PDL
     host = synth.make_inputs(wl_global, rows=rank_rows(rank, world, T))
-    x = host["x"].to(dev)
-    r = host["residual"].to(dev)
     w = host["weight"].to(dev)
-    out = torch.empty_like(x)
-    res = torch.empty_like(x)
+    b = host["bias"].to(dev) if wl.has_bias else None
+    # a step whose bytes fit in L2 rotates over enough copies of its buffers
+    # that consecutive steps never find their inputs in L2
+    bytes_step = wl.algorithmic_bytes()
+    n_sets = max(1, -(-3 * L2_BYTES // bytes_step)) if bytes_step < 3 * L2_BYTES else 1
+    sets = []
+    for k in range(n_sets):
+        x = host["x"].to(dev)
+        r = host["residual"].to(dev)
+        out = torch.empty((T, H), dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
+        res = torch.empty_like(x)
+        scale = torch.empty((T,), dtype=torch.float32, device=dev) if fp8 else None
+        sets.append((x.data_ptr(), r.data_ptr(), w.data_ptr(), None if b is None else b.data_ptr(),
+                     out.data_ptr(), res.data_ptr(), None if scale is None else scale.data_ptr(),
+                     (x, r, out, res, scale)))
     forced = None
     if args.config:
         forced = pkg.RmsnConfig.from_dict(json.loads(args.config))
     cfg = forced if forced is not None else pkg.rmsnorm_query_config(T, H, flags)
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
-    ptrs = (x.data_ptr(), r.data_ptr(), w.data_ptr(), None, out.data_ptr(), res.data_ptr(), None)
-
-    def step():
+    def step(i):
+        ptrs = sets[i % n_sets][:7]
         if forced is None:
             st = pkg.rmsnorm_fwd(*ptrs, T, H, wl.eps, step_flags, sptr)
         else:
@@ -237,8 +267,8 @@ def run_ours(args):
         if st != pkg.RMSN_OK:
             raise pkg.RmsnError(st, "rmsnorm_fwd")
 
-    for _ in range(args.warmup):
-        step()
+    for i in range(args.warmup):
+        step(i)
     torch.cuda.synchronize(dev)
     K = args.steps
     t_start = torch.cuda.Event(enable_timing=True)
@@ -249,8 +279,8 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     wall0 = time.time()
     t_start.record(stream)
-    for _ in range(K):
-        step()
+    for i in range(K):
+        step(i)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     wall1 = time.time()
@@ -259,7 +289,6 @@ def run_ours(args):
     # the timed region holds only the K launches: its length / K is the
     # kernel's average launch duration, gaps between launches included
     kernel_ms = t_start.elapsed_time(t_end) / K
-    bytes_step = wl.algorithmic_bytes()
     elapsed_ms, total_bytes, value = aggregate(pg, t_start.elapsed_time(t_end),
                                                float(bytes_step * K), dev)
 
@@ -274,6 +303,8 @@ def run_ours(args):
     peak, peak_src = load_peaks()
     achieved = bytes_step / (kernel_ms / 1e3) / 1e9
     vkey = f"{pkg.VARIANT_NAMES[cfg.variant]}_ch{cfg.chunks}_w{cfg.warps_per_block}_T{T}_H{H}"
+    if fp8:
+        vkey += "_fp8"
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -286,13 +317,18 @@ def run_ours(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
-        "data": "synthetic, seeded: x ~ N(0,1) with 1% outlier channels x50, residual ~ N(0,4), "
-                "weight = 1 + 0.1 N(0,1)",
-        "config": {"workload": f"prefill fused residual-add + RMSNorm bf16 T={T} H={H} eps=1e-5",
+        "data": ("synthetic, seeded: x, residual ~ N(0,1), weight = 1 + 0.1 N(0,1), "
+                 "bias = 0.01 N(0,1)") if fp8 else
+                ("synthetic, seeded: x ~ N(0,1) with 1% outlier channels x50, residual ~ N(0,4), "
+                 "weight = 1 + 0.1 N(0,1)"),
+        "config": {"workload": workload_name(wl),
                    "n_tokens": T, "hidden": H, "global_batch_tokens": T * world,
                    "parallelism": f"rows sharded, {world} independent replica(s)",
-                   "l2": f"inputs larger than L2 ({2 * T * H * 2 / 2**20:.0f} MiB read per step "
-                         f"vs {L2_BYTES / 1e6:.0f} MB L2), no flush",
+                   "l2": (f"inputs larger than L2 ({2 * T * H * 2 / 2**20:.0f} MiB read per step "
+                          f"vs {L2_BYTES / 1e6:.0f} MB L2), no flush") if n_sets == 1 else
+                         (f"{n_sets} rotating buffer sets of {bytes_step / 2**20:.0f} MiB per step "
+                          f"({n_sets * bytes_step / 2**20:.0f} MiB vs {L2_BYTES / 1e6:.0f} MB "
+                          f"L2), no flush"),
                    "launch": dict(cfg.as_dict(), pdl=not args.no_pdl)},
         "clocks": clocks,
         "e2e": e2e,
@@ -334,14 +370,21 @@ def run_e2e(pkg, wl, host, dev, stream, flags, steps, pg):
     import torch
 
     T, H = wl.n_tokens, wl.hidden
+    fp8 = wl.out_dtype == "fp8"
     hx = host["x"].pin_memory()
     hr = host["residual"].pin_memory()
     hw = host["weight"].pin_memory()
-    hy = torch.empty_like(hx).pin_memory()
+    hb = host["bias"].pin_memory() if wl.has_bias else None
+    hy = torch.empty((T, H), dtype=torch.uint8 if fp8 else torch.bfloat16).pin_memory()
     hres = torch.empty_like(hx).pin_memory()
+    hsc = torch.empty((T,), dtype=torch.float32).pin_memory() if fp8 else None
     sptr = stream.cuda_stream
-    hptrs = (hx.data_ptr(), hr.data_ptr(), hw.data_ptr(), None, hy.data_ptr(), hres.data_ptr(),
-             None)
+
+    def p(t):
+        return None if t is None else t.data_ptr()
+
+    hptrs = (hx.data_ptr(), hr.data_ptr(), hw.data_ptr(), p(hb), hy.data_ptr(), hres.data_ptr(),
+             p(hsc))
 
     def step_host():
         st = pkg.rmsnorm_fwd_host(*hptrs, T, H, wl.eps, flags, 0.0, sptr)
@@ -351,16 +394,23 @@ def run_e2e(pkg, wl, host, dev, stream, flags, steps, pg):
     dx = torch.empty_like(hx, device=dev)
     dr = torch.empty_like(hx, device=dev)
     dw = torch.empty_like(hw, device=dev)
-    dy = torch.empty_like(dx)
+    db = None if hb is None else torch.empty_like(hb, device=dev)
+    dy = torch.empty_like(hy, device=dev)
     dres = torch.empty_like(dx)
+    dsc = None if hsc is None else torch.empty_like(hsc, device=dev)
 
     def step_copies():
         dx.copy_(hx, non_blocking=True)
         dr.copy_(hr, non_blocking=True)
         dw.copy_(hw, non_blocking=True)
-        pkg.fused_add_rmsnorm(dx, dr, dw, None, eps=wl.eps, out=dy, residual_out=dres)
+        if db is not None:
+            db.copy_(hb, non_blocking=True)
+        pkg.fused_add_rmsnorm(dx, dr, dw, db, eps=wl.eps, out_dtype=wl.out_dtype, out=dy,
+                              residual_out=dres, out_scale=dsc)
         hy.copy_(dy, non_blocking=True)
         hres.copy_(dres, non_blocking=True)
+        if dsc is not None:
+            hsc.copy_(dsc, non_blocking=True)
 
     def timed(step):
         for _ in range(2):
@@ -377,8 +427,8 @@ def run_e2e(pkg, wl, host, dev, stream, flags, steps, pg):
         return max_over_ranks(pg, a.elapsed_time(b), dev)
 
     world = 1 if pg is None else pg.get_world_size()
-    h2d = (hx.numel() + hr.numel() + hw.numel()) * 2
-    d2h = (hy.numel() + hres.numel()) * 2
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hr, hw, hb) if t is not None)
+    d2h = sum(t.numel() * t.element_size() for t in (hy, hres, hsc) if t is not None)
     ms = timed(step_host)
     ms_copies = timed(step_copies)
     gbs = wl.algorithmic_bytes() * steps * world / (ms / 1e3) / 1e9
@@ -551,12 +601,37 @@ def run_quantized(pkg, synth, dev, stream):
     """Quantised outputs on the FP8 configuration's shapes (4096 tokens x
     hidden 5120 / 7168, bf16 x and residual, weight and bias): per-token FP8
     and the block-scaled MXFP8 / MXFP4 / NVFP4.  CUDA-graph replay of
-    launches alternating over two input sets (above the L2 size),
-    algorithmic GB/s."""
+    launches alternating over two input sets (above the L2 size), plain and
+    chained by programmatic dependent launch; algorithmic GB/s."""
     import torch
 
     T = 4096
-    out = {"unit": "GB/s", "timing": "cuda graph, 2 rotating input sets"}
+    out = {"unit": "GB/s", "timing": "cuda graph, 2 rotating input sets; *_pdl: launches "
+                                      "chained by programmatic dependent launch"}
+
+    def graph_us(call, n=20, replays=5):
+        for i in range(2):
+            call(i)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(stream)
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for i in range(n):
+                    call(i)
+        stream.wait_stream(s)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(replays):
+            g.replay()
+        e.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(e) * 1e3 / (replays * n)
+
     for H in synth.FP8_HIDDEN:
         wl = synth.fp8_workload(H)
         inp = synth.make_inputs(wl)
@@ -573,11 +648,11 @@ def run_quantized(pkg, synth, dev, stream):
                          torch.empty((T,), dtype=torch.float32, device=dev)) for _ in sets]
                 nbytes = wl.algorithmic_bytes()
 
-                def call(i, bufs=bufs):
+                def call(i, pdl=False, bufs=bufs):
                     x, r, ro = sets[i % 2]
                     q, sc = bufs[i % 2]
                     pkg.fused_add_rmsnorm(x, r, w, b, eps=wl.eps, out_dtype="fp8", out=q,
-                                          residual_out=ro, out_scale=sc)
+                                          residual_out=ro, out_scale=sc, pdl=pdl)
             else:
                 code, blk, per_byte = pkg.BLOCK_FORMATS[fmt]
                 nbytes = (T * H * 2 * 3 + T * H // per_byte + T * H // blk + 4 * H
@@ -587,39 +662,20 @@ def run_quantized(pkg, synth, dev, stream):
                          torch.empty((T, H // blk), dtype=torch.uint8, device=dev),
                          torch.empty((T,), dtype=torch.float32, device=dev)) for _ in sets]
 
-                def call(i, bufs=bufs, code=code, fmt=fmt, flags=flags):
+                def call(i, pdl=False, bufs=bufs, code=code, fmt=fmt, flags=flags):
                     x, r, ro = sets[i % 2]
                     q, bs, ts = bufs[i % 2]
                     st = pkg.rmsnorm_fwd_blockscaled(
                         x.data_ptr(), r.data_ptr(), w.data_ptr(), b.data_ptr(), q.data_ptr(),
                         bs.data_ptr(), ts.data_ptr() if fmt == "nvfp4" else None, ro.data_ptr(),
-                        T, H, wl.eps, flags, code, 0.0, None,
+                        T, H, wl.eps, flags | (pkg.RMSN_PDL if pdl else 0), code, 0.0, None,
                         torch.cuda.current_stream().cuda_stream)
                     if st != pkg.RMSN_OK:
                         raise pkg.RmsnError(st, "rmsnorm_fwd_blockscaled")
-            for i in range(2):
-                call(i)
-            torch.cuda.synchronize(dev)
-            g = torch.cuda.CUDAGraph()
-            s = torch.cuda.Stream(dev)
-            s.wait_stream(stream)
-            n = 20
-            with torch.cuda.stream(s):
-                with torch.cuda.graph(g, stream=s):
-                    for i in range(n):
-                        call(i)
-            stream.wait_stream(s)
-            g.replay()
-            torch.cuda.synchronize(dev)
-            a = torch.cuda.Event(enable_timing=True)
-            e = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for _ in range(5):
-                g.replay()
-            e.record(stream)
-            torch.cuda.synchronize(dev)
-            us = a.elapsed_time(e) * 1e3 / (5 * n)
-            res[fmt] = {"us": round(us, 2), "gbs": round(nbytes / us / 1e3, 1)}
+            us = graph_us(call)
+            us_pdl = graph_us(lambda i, call=call: call(i, pdl=True))
+            res[fmt] = {"us": round(us, 2), "gbs": round(nbytes / us / 1e3, 1),
+                        "us_pdl": round(us_pdl, 2), "gbs_pdl": round(nbytes / us_pdl / 1e3, 1)}
         out[f"T{T}_H{H}"] = res
     return out
 
@@ -684,8 +740,8 @@ def run_cpu_baseline(wl, host, seconds: float) -> dict:
     def timed(x, r, threads, budget):
         reps, t0 = 0, time.time()
         while True:
-            oracle.rmsnorm(x, r, host["weight"], None, eps=eps, in_dtype="bf16",
-                           out_dtype="bf16", n_threads=threads)
+            oracle.rmsnorm(x, r, host["weight"], host["bias"], eps=eps, in_dtype="bf16",
+                           out_dtype=wl.out_dtype, n_threads=threads)
             reps += 1
             if time.time() - t0 >= budget or reps >= 50:
                 return reps, time.time() - t0
@@ -713,7 +769,7 @@ def run_reference(args):
     import oracle
     from residual_add_rmsnorm_vec_gb300 import synth
 
-    wl = synth.prefill_workload(args.tokens, args.hidden)
+    wl = step_workload(synth, args, args.tokens)
     T, H = wl.n_tokens, wl.hidden
     cores = oracle.num_cpus()
     eps = float(np.float32(wl.eps))
@@ -721,22 +777,22 @@ def run_reference(args):
     probe_rows = synth.sample_rows(T, 64)
     probe = synth.make_inputs(wl, rows=probe_rows)
     t0 = time.time()
-    oracle.rmsnorm(probe["x"], probe["residual"], probe["weight"], None, eps=eps,
-                   in_dtype="bf16", out_dtype="bf16", n_threads=cores)
+    oracle.rmsnorm(probe["x"], probe["residual"], probe["weight"], probe["bias"], eps=eps,
+                   in_dtype="bf16", out_dtype=wl.out_dtype, n_threads=cores)
     per_row = max((time.time() - t0) / len(probe_rows), 1e-7)
     n_steps = args.steps + args.warmup
     rows = int(max(1, min(T, args.ref_seconds / n_steps / per_row)))
     sample = synth.sample_rows(T, rows)
     inp = synth.make_inputs(wl, rows=sample)
     for _ in range(args.warmup):
-        oracle.rmsnorm(inp["x"], inp["residual"], inp["weight"], None, eps=eps, in_dtype="bf16",
-                       out_dtype="bf16", n_threads=cores)
+        oracle.rmsnorm(inp["x"], inp["residual"], inp["weight"], inp["bias"], eps=eps,
+                       in_dtype="bf16", out_dtype=wl.out_dtype, n_threads=cores)
     t0 = time.time()
     for _ in range(args.steps):
-        oracle.rmsnorm(inp["x"], inp["residual"], inp["weight"], None, eps=eps, in_dtype="bf16",
-                       out_dtype="bf16", n_threads=cores)
+        oracle.rmsnorm(inp["x"], inp["residual"], inp["weight"], inp["bias"], eps=eps,
+                       in_dtype="bf16", out_dtype=wl.out_dtype, n_threads=cores)
     dt = time.time() - t0
-    bytes_step = len(sample) * H * 8 + 2 * H
+    bytes_step = wl.algorithmic_bytes() * len(sample) // T
     value = bytes_step * args.steps / dt / 1e9
     sample_txt = (f"{len(sample)} seeded rows of the {T}x{H} workload per step, fp64 C oracle, "
                   f"{cores} threads")
@@ -745,8 +801,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic, seeded",
-        "config": {"workload": f"prefill fused residual-add + RMSNorm bf16 T={T} H={H} eps=1e-5",
-                   "n_tokens": T, "hidden": H},
+        "config": {"workload": workload_name(wl), "n_tokens": T, "hidden": H},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores,
                          "kind": "oracle", "sample": sample_txt},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -767,6 +822,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
+    ap.add_argument("--out", choices=["bf16", "fp8"], default="bf16",
+                    help="output of the timed step: bf16 (the prefill workload) or per-token "
+                         "FP8 with bias (use --tokens 4096 --hidden 5120 or 7168)")
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--no-pdl", action="store_true",
                     help="launch the timed prefill steps without programmatic dependent launch")

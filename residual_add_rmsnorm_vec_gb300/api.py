@@ -231,12 +231,13 @@ def fused_add_rmsnorm_blockscaled(x: torch.Tensor, residual: torch.Tensor | None
                                   weight_offset: float = 0.0,
                                   residual_out: torch.Tensor | None = None,
                                   config: _lib.RmsnConfig | None = None,
-                                  stream: torch.cuda.Stream | None = None):
+                                  stream: torch.cuda.Stream | None = None, pdl: bool = False):
     """Fused residual-add + RMSNorm with an MXFP8 / MXFP4 / NVFP4 output
     (``rmsnorm_fwd_blockscaled``).  Returns ``(q, block_scale, token_scale,
     residual_out)``: q uint8 [T, H] (MXFP8) or [T, H / 2] (FP4, two codes per
     byte, low nibble first), block_scale uint8 [T, H / block], token_scale
-    float32 [T] for NVFP4 (else None)."""
+    float32 [T] for NVFP4 (else None).  ``pdl``: launch with programmatic
+    dependent launch."""
     if x.dim() != 2 or x.dtype != torch.bfloat16:
         raise TypeError("x must be a 2-D bfloat16 tensor")
     if not x.is_cuda:
@@ -258,7 +259,8 @@ def fused_add_rmsnorm_blockscaled(x: torch.Tensor, residual: torch.Tensor | None
     ts = torch.empty((T,), dtype=torch.float32, device=x.device) if fmt == "nvfp4" else None
     if residual is not None and residual_out is None:
         residual_out = torch.empty_like(x)
-    flags = make_flags("bf16", "f32", residual is not None, weight is not None, bias is not None)
+    flags = make_flags("bf16", "f32", residual is not None, weight is not None, bias is not None,
+                       pdl)
     s = stream if stream is not None else torch.cuda.current_stream(x.device)
     st = _lib.rmsnorm_fwd_blockscaled(_ptr(x), _ptr(residual), _ptr(weight), _ptr(bias), _ptr(q),
                                       _ptr(bs), _ptr(ts), _ptr(residual_out), T, H, eps, flags,

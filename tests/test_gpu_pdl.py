@@ -86,3 +86,38 @@ def test_early_params_needs_pdl(pkg):
     st = pkg.rmsnorm_fwd(x.data_ptr(), None, None, None, x.data_ptr(), None, None, 4, 64, 1e-6,
                          flags, torch.cuda.current_stream().cuda_stream)
     assert st == pkg.RMSN_EINVAL
+
+
+def quant_chain(pkg, inp, eps, n, fmt, pdl):
+    """n calls where call k takes the residual_out of call k - 1 as its
+    residual (x, weight and bias fixed); returns every call's outputs."""
+    x = inp["x"].cuda()
+    w, b = inp["weight"].cuda(), inp["bias"].cuda()
+    rs = [inp["residual"].cuda()] + [torch.empty_like(x) for _ in range(n)]
+    outs = []
+    for k in range(n):
+        if fmt == "fp8":
+            q, ro, sc = pkg.fused_add_rmsnorm(x, rs[k], w, b, eps=eps, out_dtype="fp8",
+                                              residual_out=rs[k + 1], pdl=pdl)
+            outs.append((q, sc))
+        else:
+            q, bs, ts, ro = pkg.fused_add_rmsnorm_blockscaled(x, rs[k], w, b, eps=eps, fmt=fmt,
+                                                              residual_out=rs[k + 1], pdl=pdl)
+            outs.append((q, bs) if ts is None else (q, bs, ts))
+    torch.cuda.synchronize()
+    return [[t.cpu() for t in o] for o in outs] + [[r.cpu()] for r in rs[1:]]
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "mxfp8", "mxfp4", "nvfp4"])
+@pytest.mark.parametrize("T,H", [(4096, 5120), (33, 2048)])
+def test_pdl_chain_quantised_outputs(pkg, fmt, T, H):
+    # the quantised launches that bench.py times with RMSN_PDL: a chain over
+    # the residual stream is bit-identical with and without PDL
+    wl = synth.Workload(f"pdlq_{fmt}_T{T}_H{H}", T, H, 22, "bf16", "bf16", 1e-6, has_bias=True)
+    inp = synth.make_inputs(wl)
+    ref = quant_chain(pkg, inp, wl.eps, 4, fmt, pdl=False)
+    got = quant_chain(pkg, inp, wl.eps, 4, fmt, pdl=True)
+    for k, (a, b) in enumerate(zip(got, ref)):
+        for ta, tb in zip(a, b):
+            assert torch.equal(ta, tb), (fmt, k)
+    assert pkg.rmsnorm_read_status() == 0
