@@ -539,25 +539,33 @@ def run_qk(pkg, synth, dev, stream):
     """QK norm (per-head, in place) on Qwen3-8B-like heads (32 query, 8 key,
     head_dim 128, bf16): one rmsnorm_qk_fwd launch on a fused qkv buffer
     against the regular row norm applied to the query and key head views
-    (two rmsnorm_fwd launches).  CUDA-graph replay, us per call."""
+    (two rmsnorm_fwd launches).  CUDA-graph replay, us per call.  From 16384
+    tokens the launches alternate over two buffer sets (the q and k heads of
+    one set alone exceed L2), so those figures are HBM-bound and are also
+    given as a fraction of the measured copy peak."""
     import torch
 
     Hq, Hk, D = 32, 8, 128
+    peak, _ = load_peaks()
     out = {"heads": f"{Hq} q + {Hk} k heads x {D}, bf16", "unit": "us/call"}
-    for T in (1, 64, 4096):
+    for T in (1, 64, 4096, 16384):
         inp = synth.qk_inputs(T, Hq, Hk, D, "bf16")
-        qkv = inp["qkv"].to(dev)
+        n_sets = 2 if T >= 16384 else 1
         wq, wk = inp["q_weight"].to(dev), inp["k_weight"].to(dev)
-        q = qkv[:, :Hq * D]
-        k = qkv[:, Hq * D:(Hq + Hk) * D]
-        qc = q.contiguous()
-        kc = k.contiguous()
+        sets = []
+        for _ in range(n_sets):
+            qkv = inp["qkv"].to(dev)
+            q = qkv[:, :Hq * D]
+            k = qkv[:, Hq * D:(Hq + Hk) * D]
+            sets.append((qkv, q, k, q.contiguous(), k.contiguous()))
         fl = pkg.make_flags("bf16", "bf16", False, True, False)
 
-        def qk_call():
+        def qk_call(i):
+            _, q, k, _, _ = sets[i % n_sets]
             pkg.qk_norm_(q, k, wq, wk, head_dim=D, eps=1e-6)
 
-        def rows_call():
+        def rows_call(i):
+            _, _, _, qc, kc = sets[i % n_sets]
             s = torch.cuda.current_stream().cuda_stream
             for t, w, h in ((qc, wq, Hq), (kc, wk, Hk)):
                 st = pkg.rmsnorm_fwd(t.data_ptr(), None, w.data_ptr(), None, t.data_ptr(), None,
@@ -566,15 +574,15 @@ def run_qk(pkg, synth, dev, stream):
                     raise pkg.RmsnError(st, "rmsnorm_fwd")
 
         def graph_us(fn, per_graph=50, replays=10):
-            fn()
+            fn(0)
             torch.cuda.synchronize(dev)
             g = torch.cuda.CUDAGraph()
             s = torch.cuda.Stream(dev)
             s.wait_stream(stream)
             with torch.cuda.stream(s):
                 with torch.cuda.graph(g, stream=s):
-                    for _ in range(per_graph):
-                        fn()
+                    for i in range(per_graph):
+                        fn(i)
             stream.wait_stream(s)
             g.replay()
             torch.cuda.synchronize(dev)
@@ -590,10 +598,16 @@ def run_qk(pkg, synth, dev, stream):
         nbytes = 2 * T * (Hq + Hk) * D * 2 + 2 * D * 2
         us_qk = graph_us(qk_call)
         us_rows = graph_us(rows_call)
-        out[f"T{T}"] = {"qk_us": round(us_qk, 3), "qk_gbs": round(nbytes / us_qk / 1e3, 1),
-                        "row_norm_us": round(us_rows, 3),
-                        "row_norm_gbs": round(nbytes / us_rows / 1e3, 1),
-                        "speedup": round(us_rows / us_qk, 2)}
+        res = {"qk_us": round(us_qk, 3), "qk_gbs": round(nbytes / us_qk / 1e3, 1),
+               "row_norm_us": round(us_rows, 3),
+               "row_norm_gbs": round(nbytes / us_rows / 1e3, 1),
+               "speedup": round(us_rows / us_qk, 2)}
+        if n_sets > 1:
+            res["qk_frac_of_peak"] = round(nbytes / us_qk / 1e3 / peak, 4)
+            res["buffer_sets"] = n_sets
+        out[f"T{T}"] = res
+        del sets
+    torch.cuda.empty_cache()
     return out
 
 

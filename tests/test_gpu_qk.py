@@ -43,7 +43,8 @@ def compare(dtype, got, ref, where):
 
 @pytest.mark.parametrize("T,Hq,Hk,D,dtype", [
     (1, 32, 8, 128, "bf16"), (7, 16, 4, 64, "bf16"), (512, 32, 8, 128, "bf16"),
-    (4096, 32, 8, 128, "bf16"), (33, 8, 2, 256, "bf16"), (3, 2, 1, 512, "bf16"),
+    (4096, 32, 8, 128, "bf16"), (16384, 32, 8, 128, "bf16"), (33, 8, 2, 256, "bf16"),
+    (3, 2, 1, 512, "bf16"),
     (5, 4, 4, 128, "f32"), (65, 6, 2, 64, "f32"), (9, 3, 1, 256, "f32"), (2, 1, 1, 16, "bf16"),
     (17, 32, 8, 128, "f16"), (3, 4, 2, 64, "f16"), (5, 2, 2, 256, "f16"),
 ])
