@@ -212,12 +212,14 @@ __device__ __forceinline__ uint32_t pack_e2m1x8(float v0, float v1, float v2, fl
            (cvt_e2m1x2(v6, v7) << 24);
 }
 
-// Value of an E4M3 code (OCP FP8: bias 7, 3 mantissa bits), exact in fp32.
+// Value of an E4M3 code (OCP FP8: bias 7, 3 mantissa bits), exact: every
+// E4M3 value is a binary16 value, so the hardware widening is exact.  The
+// code sits in the low byte, as cvt.rn.satfinite.e4m3x2.f32 writes its
+// second operand.
 __device__ __forceinline__ float e4m3_value(uint32_t c) {
-    const uint32_t e = (c >> 3) & 15u, m = c & 7u;
-    const float mag = e == 0 ? (float)m * 0.001953125f  // m * 2^-9
-                             : (float)(8u + m) * __uint_as_float((e + 117u) << 23);  // 2^(e-10)
-    return (c & 0x80u) ? -mag : mag;
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)(c & 0xFFu)));
+    return f16_to_f32(h2);
 }
 
 // Element k of a 32-byte vector of TI as float.
@@ -453,6 +455,7 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
     constexpr bool HOLD = KEEP && NV;  // keep y between NVFP4's row-max and block passes
     static_assert(LPB >= 1 && LPB <= 4, "block spans 1..4 lanes");
     float ys[HOLD ? CH : 1][HOLD ? VE : 1];
+    float bms[HOLD ? CH : 1];  // with HOLD: the lane's maximum of each vector
     float g = 0.f, rcp6g = 0.f;
     if constexpr (NV) {
         float amax = 0.f;
@@ -462,13 +465,16 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
             if (v < a.nvec) {
                 opaque(wv[c]);
                 if constexpr (BIAS) opaque(bv[c]);
+                float m = 0.f;
 #pragma unroll
                 for (int k = 0; k < VE; ++k) {
                     const float y = scale_elem<BIAS>(elem<TI>(hv[c], k), inv, elem<TI>(wv[c], k),
                                                      a.woff, BIAS ? elem<TI>(bv[c], k) : 0.f);
                     if constexpr (HOLD) ys[c][k] = y;
-                    amax = fmaxf(amax, fabsf(y));
+                    m = fmaxf(m, fabsf(y));
                 }
+                if constexpr (HOLD) bms[c] = m;
+                amax = fmaxf(amax, m);
             }
         }
         amax = reduce_max(amax);
@@ -485,10 +491,8 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
         if (valid) {
             if constexpr (HOLD) {
 #pragma unroll
-                for (int k = 0; k < VE; ++k) {
-                    y[k] = ys[c][k];
-                    bmax = fmaxf(bmax, fabsf(y[k]));
-                }
+                for (int k = 0; k < VE; ++k) y[k] = ys[c][k];
+                bmax = bms[c];
             } else {
                 opaque(wv[c]);
                 if constexpr (BIAS) opaque(bv[c]);
