@@ -361,11 +361,14 @@ __device__ __forceinline__ void store_out(void* out, int64_t e, const float (&y)
 
 // Register budget: blocks of up to WMAX warps; at least 1024 resident threads
 // per SM for CH <= 2 (64 registers / thread), 512 for CH = 4 (128) and 256
-// for CH = 8 (255, one-warp decode rows).
-template <int WMAX, int CH>
+// for CH = 8 (255, one-warp decode rows).  With both a residual and a bias a
+// thread holds four vectors per chunk (x, residual, weight, bias: 32
+// registers), so from CH = 2 on the budget is doubled rather than spilled.
+template <int WMAX, int CH, bool HEAVY = false>
 struct Bounds {
     static constexpr int kThreads = WMAX * 32;
-    static constexpr int kTarget = CH <= 2 ? 1024 : (CH <= 4 ? 512 : 256);
+    static constexpr int kTarget = (CH <= 2 ? 1024 : (CH <= 4 ? 512 : 256)) /
+                                   (HEAVY && CH >= 2 ? 2 : 1);
     static constexpr int kMinBlocks = kTarget / kThreads > 0 ? kTarget / kThreads : 1;
 };
 
@@ -626,7 +629,8 @@ __device__ __forceinline__ void scale_store(const RmsnArgs& a, int64_t row, int6
 // unless an fp32 residual stream carries bf16 / fp16 activations).
 template <class TI, class TO, int CH, int WMAX, bool WARP_ROWS, bool RES, bool BIAS,
           class TX = TI>
-__global__ void __launch_bounds__(Bounds<WMAX, CH>::kThreads, Bounds<WMAX, CH>::kMinBlocks)
+__global__ void __launch_bounds__(Bounds<WMAX, CH, RES && BIAS>::kThreads,
+                                  Bounds<WMAX, CH, RES && BIAS>::kMinBlocks)
     rmsn_vec_kernel(const RmsnArgs a) {
     constexpr int VE = 32 / TI::kBytes;  // elements per 32-byte vector
     __shared__ float red[4][32];
@@ -638,27 +642,36 @@ __global__ void __launch_bounds__(Bounds<WMAX, CH>::kThreads, Bounds<WMAX, CH>::
     int64_t row = WARP_ROWS ? (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)
                             : (int64_t)blockIdx.x;
 
-    pdl_launch_dependents(a.pdl);
-    if (!a.early_params) pdl_wait(a.pdl);
-    V8 wv[CH];
-    V8 bv[BIAS ? CH : 1];
-    load_params<TX, TI, CH>(a, G, t, wv, bv, BIAS);
-    if (a.early_params) pdl_wait(a.pdl);
-
-    int parity = 0;
-    for (; row < a.T; row += rows_per_step) {
-        const int64_t rbase = row * (int64_t)a.H;  // element offset of the row
-        V8 hv[CH];
-        V8 rv[RES ? CH : 1];
+    V8 hv[CH];
+    V8 rv[RES ? CH : 1];
+    auto load_row = [&](int64_t rw) {
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
             const int v = c * G + t;
             if (v < a.nvec) {
-                const int64_t e = rbase + (int64_t)v * VE;
+                const int64_t e = rw * (int64_t)a.H + (int64_t)v * VE;
                 hv[c] = ld_vec<TX, TI, true>(a.x, e);
                 if constexpr (RES) rv[c] = ld_stream32(static_cast<const char*>(a.r) + e * TI::kBytes);
             }
         }
+    };
+    pdl_launch_dependents(a.pdl);
+    V8 wv[CH];
+    V8 bv[BIAS ? CH : 1];
+    if (a.early_params) load_params<TX, TI, CH>(a, G, t, wv, bv, BIAS);
+    pdl_wait(a.pdl);
+    // without a bias the first row's loads go out before the weight's (a
+    // single-row call then waits on the row, not on the weight behind it);
+    // with one, the four vectors per chunk would all be live at once
+    constexpr bool EARLY_ROW = !BIAS;
+    const int64_t first = row;
+    if (EARLY_ROW && row < a.T) load_row(row);
+    if (!a.early_params) load_params<TX, TI, CH>(a, G, t, wv, bv, BIAS);
+
+    int parity = 0;
+    for (; row < a.T; row += rows_per_step) {
+        const int64_t rbase = row * (int64_t)a.H;  // element offset of the row
+        if (!EARLY_ROW || row != first) load_row(row);
         const float acc = residual_sumsq<TI, CH, RES>(a, rbase, G, t, hv, rv);
         const float sumsq = WARP_ROWS ? warp_sum(acc) : block_allreduce<false>(acc, red[parity]);
         const float inv = inv_rms(sumsq, a.H, a.eps);
