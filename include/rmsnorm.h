@@ -116,8 +116,9 @@ typedef struct {
  * element size; the 256-bit vector kernels are used when hidden * element
  * size is a multiple of 32 bytes and every pointer is 32-byte aligned,
  * otherwise the generic kernel runs.  residual_out may be the same buffer as
- * residual or x; out may be the same buffer as x or residual when the output
- * and input dtypes are equal; any other overlap is undefined.  n_tokens == 0
+ * residual, or as x when both have the same dtype; out may be the same
+ * buffer as x or residual when their dtypes are equal; any other overlap is
+ * undefined.  n_tokens == 0
  * is a no-op once the flags, hidden and eps have been checked (its pointers
  * may then be NULL).  Returns an rmsn_status.
  */
