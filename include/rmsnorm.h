@@ -84,7 +84,10 @@ typedef enum {
     RMSN_VARIANT_BLOCK_ROW = 1, /* prefill: one block (W warps) per row, register-resident */
     RMSN_VARIANT_BULK_ROW = 2,  /* prefill: persistent blocks; rows streamed into a ring of
                                    shared-memory buffers by bulk async copies (cp.async.bulk) */
-    RMSN_VARIANT_GENERIC = 3    /* any hidden size / alignment (element-wise, three passes) */
+    RMSN_VARIANT_GENERIC = 3,   /* any hidden size / alignment (element-wise, three passes) */
+    RMSN_VARIANT_RAGGED = 4     /* rows off the 32-byte grid, same dtype in and out, all row
+                                   pointers equally aligned mod 16 bytes: 16-byte vectors for
+                                   the row's interior, single elements for head and tail */
 } rmsn_variant;
 
 /* One launch configuration. */

@@ -36,7 +36,8 @@ VARIANT_WARP_ROWS = 0
 VARIANT_BLOCK_ROW = 1
 VARIANT_BULK_ROW = 2
 VARIANT_GENERIC = 3
-VARIANT_NAMES = {0: "warp_rows", 1: "block_row", 2: "bulk_row", 3: "generic"}
+VARIANT_RAGGED = 4
+VARIANT_NAMES = {0: "warp_rows", 1: "block_row", 2: "bulk_row", 3: "generic", 4: "ragged"}
 
 RMSN_FMT_MXFP8 = 1
 RMSN_FMT_MXFP4 = 2

@@ -109,7 +109,7 @@ const std::vector<KernelEntry>& registry() {
             kernels_bf16_f32, kernels_bf16_bf16, kernels_bf16_fp8,   kernels_f16_f16,
             kernels_f16_f32,  kernels_f16_fp8,   kernels_bf16_mxfp8, kernels_bf16_mxfp4,
             kernels_bf16_nvfp4, kernels_bf16r32_bf16, kernels_bf16r32_fp8, kernels_f16r32_f16,
-            kernels_f16r32_fp8};
+            kernels_f16r32_fp8, kernels_ragged};
         for (auto fn : fns) {
             int n = 0;
             const KernelEntry* t = fn(&n);
@@ -131,6 +131,7 @@ struct Problem {
     int ve;     // elements per 32-byte vector
     int nvec;   // vectors per row (valid when vec_ok)
     bool vec_ok;
+    bool ragged_ok;  // off the 32-byte grid, but the ragged-row kernel applies
 };
 
 int dtype_bytes(int dt) { return dt == kF32 ? 4 : ((dt == kBF16 || dt == kF16) ? 2 : 1); }
@@ -185,6 +186,24 @@ bool vector_path_ok(const Problem& p, const void* x, const void* r, const void* 
     return aligned(out, out_vec < 32 ? out_vec : 32);
 }
 
+// The ragged-row kernel: the same 2- or 4-byte dtype in and out, no fp32
+// stream, and every row pointer equally aligned modulo 16 bytes (so a row's
+// 16-byte vectors sit at the same columns in all of them).
+bool ragged_dtypes_ok(const Problem& p) {
+    return p.in_dt == p.out_dt && (p.in_dt == kBF16 || p.in_dt == kF16 || p.in_dt == kF32) &&
+           !p.res_f32;
+}
+
+bool ragged_path_ok(const Problem& p, const void* x, const void* r, const void* ro,
+                    const void* out) {
+    if (!ragged_dtypes_ok(p)) return false;
+    const uintptr_t m = reinterpret_cast<uintptr_t>(x) & 15u;
+    const void* others[] = {r, ro, out};
+    for (const void* q : others)
+        if (q && (reinterpret_cast<uintptr_t>(q) & 15u) != m) return false;
+    return true;
+}
+
 const KernelEntry* find_kernel(const Problem& p, int variant, int ch, int wmax) {
     for (const KernelEntry& e : registry()) {
         if (e.in_dt != p.in_dt || e.out_dt != p.out_dt || e.variant != variant) continue;
@@ -234,7 +253,19 @@ bool shape_config(const Problem& p, const KernelEntry& e, DeviceInfo* d, int gri
     c->num_sms = sms;
     int threads;
     int64_t units;  // rows handled per block-step
-    if (e.variant == kGeneric) {
+    if (e.variant == kRagged) {
+        // at most ceil(H / (16 / size)) interior vectors: CH per thread x 256
+        const int64_t vecs = (p.H * p.in_bytes + 15) / 16;
+        if (vecs > (int64_t)e.chunks * 256) return false;
+        const int64_t smem = p.H * 4 * (p.bias ? 2 : 1);
+        if (smem > 48 * 1024 && smem > enable_smem(d, e.fn)) return false;
+        c->vec_bytes = 16;
+        c->warps_per_block = 8;
+        c->warps_per_row = 8;
+        c->smem_bytes = (int32_t)smem;
+        threads = 256;
+        units = p.T;
+    } else if (e.variant == kGeneric) {
         c->vec_bytes = p.in_bytes;
         int w = (int)((p.H + 31) / 32);
         if (w > 8) w = 8;
@@ -292,6 +323,12 @@ constexpr int kTableF16R32 = 8;
 // than there are SMs), then the fixed prefill rule (fewest warps with CH <= 2).
 bool select(const Problem& p, DeviceInfo* d, rmsn_config* c) {
     if (!p.vec_ok) {
+        if (p.ragged_ok) {
+            for (int ch = 1; ch <= 8; ch *= 2) {
+                const KernelEntry* e = find_kernel(p, kRagged, ch, 8);
+                if (e && shape_config(p, *e, d, 0, 0, c)) return true;
+            }
+        }
         const KernelEntry* e = find_kernel(p, kGeneric, 0, 0);
         return e && shape_config(p, *e, d, 0, 0, c);
     }
@@ -380,6 +417,7 @@ int validate(const void* x, const void* residual, const void* weight, const void
     if (!aligned(out, (uintptr_t)p->out_bytes) || !aligned(out_scale, 4)) return RMSN_EALIGN;
     p->vec_ok = vector_path_ok(*p, x, residual, weight, bias, residual_out, out);
     p->nvec = p->vec_ok ? (int)(p->H / p->ve) : 0;
+    p->ragged_ok = !p->vec_ok && ragged_path_ok(*p, x, residual, residual_out, out);
     return RMSN_OK;
 }
 
@@ -468,6 +506,11 @@ bool select_host(const Problem& p, DeviceInfo* d, rmsn_config* c) {
             const KernelEntry* e = find_kernel(p, kBlockRow, s[0], s[1]);
             if (e && shape_config(p, *e, d, 0, 0, c)) return true;
         }
+    } else if (p.ragged_ok) {
+        for (int ch = 1; ch <= 8; ch *= 2) {
+            const KernelEntry* e = find_kernel(p, kRagged, ch, 8);
+            if (e && shape_config(p, *e, d, 0, 0, c)) return true;
+        }
     }
     const KernelEntry* e = find_kernel(p, kGeneric, 0, 0);
     return e && shape_config(p, *e, d, 0, 0, c);
@@ -490,11 +533,13 @@ RMSN_API int rmsnorm_fwd_ex(const void* x, const void* residual, const void* wei
     rmsn_config c;
     const KernelEntry* e = nullptr;
     if (cfg) {
-        if (cfg->variant != kGeneric && !p.vec_ok) return RMSN_EUNSUPPORTED;
+        if (cfg->variant == kRagged ? !p.ragged_ok : (cfg->variant != kGeneric && !p.vec_ok))
+            return RMSN_EUNSUPPORTED;
         e = find_kernel(p, cfg->variant, cfg->chunks, cfg->max_warps);
         if (!e || !shape_config(p, *e, d, cfg->grid, cfg->stages, &c)) return RMSN_EUNSUPPORTED;
     } else {
-        const uint64_t key = mix(mix(mix((uint64_t)p.T, (uint64_t)p.H), flags), p.vec_ok ? 1 : 0);
+        const uint64_t key = mix(mix(mix((uint64_t)p.T, (uint64_t)p.H), flags),
+                                 (p.vec_ok ? 1 : 0) | (p.ragged_ok ? 2 : 0));
         bool hit = false;
         {
             std::lock_guard<std::mutex> lock(d->mu);
@@ -542,7 +587,7 @@ RMSN_API int rmsnorm_fwd_blockscaled(const void* x, const void* residual, const 
     rmsn_config c;
     const KernelEntry* e = nullptr;
     if (cfg) {
-        if (cfg->variant == kGeneric) return RMSN_EUNSUPPORTED;
+        if (cfg->variant == kGeneric || cfg->variant == kRagged) return RMSN_EUNSUPPORTED;
         e = find_kernel(p, cfg->variant, cfg->chunks, cfg->max_warps);
         if (!e || !shape_config(p, *e, d, cfg->grid, cfg->stages, &c)) return RMSN_EUNSUPPORTED;
     } else {
@@ -579,6 +624,7 @@ RMSN_API int rmsnorm_fwd_host(const void* x, const void* residual, const void* w
     // the mapped addresses decide the vector path
     p.vec_ok = vector_path_ok(p, dx, dr, dw, db, dres, dout);
     p.nvec = p.vec_ok ? (int)(p.H / p.ve) : 0;
+    p.ragged_ok = !p.vec_ok && ragged_path_ok(p, dx, dr, dres, dout);
     rmsn_config c;
     if (!select_host(p, d, &c)) return RMSN_EUNSUPPORTED;
     const KernelEntry* e = find_kernel(p, c.variant, c.chunks, c.max_warps);
@@ -602,6 +648,7 @@ static int query_problem(int64_t n_tokens, int64_t hidden, uint32_t flags, Probl
     if ((st = check_shape(n_tokens, hidden, p)) != RMSN_OK) return st;
     p->vec_ok = (p->H * p->res_bytes) % 32 == 0;
     p->nvec = p->vec_ok ? (int)(p->H / p->ve) : 0;
+    p->ragged_ok = !p->vec_ok && ragged_dtypes_ok(*p);  // equally aligned buffers assumed
     return RMSN_OK;
 }
 
@@ -628,7 +675,11 @@ RMSN_API int rmsnorm_list_configs(int64_t n_tokens, int64_t hidden, uint32_t fla
     for (const KernelEntry& e : registry()) {
         if (e.in_dt != p.in_dt || e.out_dt != p.out_dt || e.res != (p.res ? 1 : 0)) continue;
         if (e.res_f32 != (p.res_f32 ? 1 : 0)) continue;
-        if (e.variant != kGeneric && (e.bias != (p.bias ? 1 : 0) || !p.vec_ok)) continue;
+        if (e.variant == kRagged) {
+            if (e.bias != (p.bias ? 1 : 0) || !p.ragged_ok) continue;
+        } else if (e.variant != kGeneric && (e.bias != (p.bias ? 1 : 0) || !p.vec_ok)) {
+            continue;
+        }
         // the bulk kernel is listed once per ring depth
         const int stage_opts[] = {0, 2, 3, 4, 6, 8};
         const int n_opts = e.variant == kBulkRow ? 6 : 1;

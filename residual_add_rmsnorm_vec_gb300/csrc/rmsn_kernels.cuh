@@ -968,4 +968,134 @@ __global__ void __launch_bounds__(256) rmsn_generic_kernel(const RmsnArgs a) {
     }
 }
 
+// ---------------------------------------------------------------- ragged kernel
+//
+// Rows whose 32-byte vectors do not line up with the row (hidden not a
+// multiple of the vector, or every pointer offset from a 32-byte boundary by
+// the same amount) in the same dtype in and out.  x, residual, residual_out
+// and out share one alignment modulo 16 bytes, so each row splits the same
+// way in all four: a head (the elements before the row's first 16-byte
+// boundary), an interior of 16-byte vectors, CH per thread, held in
+// registers between the load and the store, and a tail.  Head and tail
+// together hold at most 2 (16 / size - 1) elements, one per thread.  Weight
+// (plus the scalar offset) and bias are staged once per block in shared
+// memory as fp32: their alignment relative to a row's vectors changes from
+// row to row.  One block of 256 threads per row, rows grid-stride; the
+// arithmetic (fp32 add rounded to the stream type, fp32 sum of squares,
+// correctly rounded mean, reciprocal square root, scale) is that of the
+// vector kernels.
+
+template <class TI>
+__device__ __forceinline__ float elem4(const uint32_t (&u)[4], int k) {
+    if constexpr (TI::kBytes == 2) {
+        return (k & 1) ? hi2<TI>(u[k >> 1]) : lo2<TI>(u[k >> 1]);
+    } else {
+        return __uint_as_float(u[k]);
+    }
+}
+
+template <class TI, int CH, bool RES, bool BIAS>
+__global__ void __launch_bounds__(256, CH <= 2 ? 4 : (CH <= 4 ? 2 : 1))
+    rmsn_ragged_kernel(const RmsnArgs a) {
+    constexpr int S = TI::kBytes;
+    constexpr int VE = 16 / S;  // elements per 16-byte vector
+    extern __shared__ __align__(16) float wsm[];  // [H] weight + offset, then [H] bias
+    __shared__ float red[2][32];
+    const int H = a.H;
+    const int t = threadIdx.x;
+    const int G = blockDim.x;
+    float* bsm = wsm + H;
+    pdl_launch_dependents(a.pdl);
+    pdl_wait(a.pdl);
+    for (int j = t; j < H; j += G) {
+        wsm[j] = __fadd_rn(a.has_w ? ld_elem<TI>(a.w, j) : 1.f, a.woff);
+        if constexpr (BIAS) bsm[j] = ld_elem<TI>(a.b, j);
+    }
+    __syncthreads();
+    const char* xb = static_cast<const char*>(a.x);
+    int parity = 0;
+    for (int64_t row = blockIdx.x; row < a.T; row += gridDim.x) {
+        const int64_t e0 = row * (int64_t)H;
+        const int mis = (int)(((reinterpret_cast<uintptr_t>(xb) + (uintptr_t)e0 * S) & 15u) / S);
+        const int head = mis ? min(H, VE - mis) : 0;
+        const int nv = (H - head) / VE;
+        const int ne = H - nv * VE;  // head + tail elements
+        // this thread's edge element (if any), as a column of the row
+        const int je = t < head ? t : head + nv * VE + (t - head);
+        uint32_t hu[CH][4];
+        float he = 0.f;
+        float acc = 0.f;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int v = c * G + t;
+            if (v < nv) {
+                const int64_t off = e0 + head + (int64_t)v * VE;
+                const uint4 xw = ld_stream16(xb + off * S);
+                hu[c][0] = xw.x;
+                hu[c][1] = xw.y;
+                hu[c][2] = xw.z;
+                hu[c][3] = xw.w;
+                if constexpr (RES) {
+                    const uint4 rw = ld_stream16(static_cast<const char*>(a.r) + off * S);
+                    const uint32_t ru[4] = {rw.x, rw.y, rw.z, rw.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        if constexpr (S == 2) {
+                            hu[c][k] = pack2<TI>(__fadd_rn(lo2<TI>(hu[c][k]), lo2<TI>(ru[k])),
+                                                 __fadd_rn(hi2<TI>(hu[c][k]), hi2<TI>(ru[k])));
+                        } else {
+                            hu[c][k] = __float_as_uint(
+                                __fadd_rn(__uint_as_float(hu[c][k]), __uint_as_float(ru[k])));
+                        }
+                    }
+                    st_stream16(static_cast<char*>(a.res_out) + off * S, hu[c]);
+                }
+#pragma unroll
+                for (int k = 0; k < VE; ++k) {
+                    const float h = elem4<TI>(hu[c], k);
+                    acc = __fmaf_rn(h, h, acc);
+                }
+            }
+        }
+        if (t < ne) {
+            he = ld_elem<TI>(a.x, e0 + je);
+            if constexpr (RES) {
+                he = round_to<TI>(__fadd_rn(he, ld_elem<TI>(a.r, e0 + je)));
+                st_elem<TI>(a.res_out, e0 + je, he);
+            }
+            acc = __fmaf_rn(he, he, acc);
+        }
+        const float inv = inv_rms(block_allreduce<false>(acc, red[parity]), H, a.eps);
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int v = c * G + t;
+            if (v < nv) {
+                const int col = head + v * VE;
+                float y[VE];
+#pragma unroll
+                for (int k = 0; k < VE; ++k) {
+                    const float tk = __fmul_rn(elem4<TI>(hu[c], k), inv);
+                    y[k] = BIAS ? __fmaf_rn(wsm[col + k], tk, bsm[col + k])
+                                : __fmul_rn(wsm[col + k], tk);
+                }
+                uint32_t u[4];
+                if constexpr (S == 2) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) u[k] = pack2<TI>(y[2 * k], y[2 * k + 1]);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) u[k] = __float_as_uint(y[k]);
+                }
+                st_stream16(static_cast<char*>(a.out) + (e0 + col) * S, u);
+            }
+        }
+        if (t < ne) {
+            const float tk = __fmul_rn(he, inv);
+            st_elem<TI>(a.out, e0 + je,
+                        BIAS ? __fmaf_rn(wsm[je], tk, bsm[je]) : __fmul_rn(wsm[je], tk));
+        }
+        parity ^= 1;
+    }
+}
+
 }  // namespace rmsn

@@ -32,7 +32,7 @@ enum DType : int32_t {
     kF32 = 0, kBF16 = 1, kFP8 = 2, kMXFP8 = 3, kMXFP4 = 4, kNVFP4 = 5, kF16 = 6
 };
 
-enum Variant : int32_t { kWarpRows = 0, kBlockRow = 1, kBulkRow = 2, kGeneric = 3 };
+enum Variant : int32_t { kWarpRows = 0, kBlockRow = 1, kBulkRow = 2, kGeneric = 3, kRagged = 4 };
 
 // One compiled kernel.
 struct KernelEntry {
@@ -59,5 +59,6 @@ const KernelEntry* kernels_f16r32_fp8(int* n);
 const KernelEntry* kernels_bf16_mxfp8(int* n);
 const KernelEntry* kernels_bf16_mxfp4(int* n);
 const KernelEntry* kernels_bf16_nvfp4(int* n);
+const KernelEntry* kernels_ragged(int* n);
 
 }  // namespace rmsn

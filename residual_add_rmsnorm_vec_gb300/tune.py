@@ -259,6 +259,10 @@ def main():
                     help="time shapes with fewer tokens L2-hot (decode sizes)")
     ap.add_argument("--block-formats", action="store_true",
                     help="sweep only the block-scaled outputs and merge their rows into the table")
+    ap.add_argument("--shapes", default="",
+                    help="comma list of TxH shapes (e.g. 16384x8190) to measure for --pairs (or "
+                         "bf16:bf16) instead of the default grid; the table is left alone unless "
+                         "--write-table")
     ap.add_argument("--pairs", default="",
                     help="comma list of input:output pairs (e.g. f16:f16,bf16+r32:bf16) to sweep "
                          "on the hidden sizes 2048..16384; rows merged into the table")
@@ -272,12 +276,14 @@ def main():
     if args.quick:
         grid = [(1, 4096), (256, 4096), (16384, 8192)]
     hot = args.l2_hot_below
-    if args.pairs:
+    if args.pairs or args.shapes:
+        shapes = [(T, H) for H in HIDDEN for T in (1, 16, 256, 1024, 4096, 16384)]
+        if args.shapes:
+            shapes = [tuple(int(v) for v in sh.split("x")) for sh in args.shapes.split(",")]
         entries = []
-        for pair in args.pairs.split(","):
+        for pair in (args.pairs or "bf16:bf16").split(","):
             i, o = pair.split(":")
-            entries += sweep(pkg, [(T, H) for H in HIDDEN for T in (1, 16, 256, 1024, 4096, 16384)],
-                             i, o, True, False, args.reps, hot)
+            entries += sweep(pkg, shapes, i, o, True, False, args.reps, hot)
         with open(args.out, "w") as f:
             json.dump({"meta": {"gpu": torch.cuda.get_device_name(0), "reps": args.reps,
                                 "l2_hot_below": hot, "timing": "cuda graph replay"},

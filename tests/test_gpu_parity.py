@@ -266,6 +266,76 @@ def test_misaligned_pointers_take_generic_path(pkg):
     parity.compare(wl, got, ref, "misaligned")
 
 
+def test_unequally_misaligned_pointers_take_generic_path(pkg):
+    # x one element off a 16-byte boundary, the residual two: the ragged-row
+    # kernel needs every row pointer equally aligned, so the generic one runs
+    wl = synth.Workload("misaligned2", 24, 2048, 12, "bf16", "bf16", 1e-6)
+    inp = synth.make_inputs(wl)
+    ref = parity.oracle_run(wl, inp)
+    T, H = wl.n_tokens, wl.hidden
+    xb = torch.zeros(T * H + 8, dtype=torch.bfloat16, device=DEV)
+    rb = torch.zeros(T * H + 8, dtype=torch.bfloat16, device=DEV)
+    x, r = xb[1:1 + T * H].view(T, H), rb[2:2 + T * H].view(T, H)
+    x.copy_(inp["x"])
+    r.copy_(inp["residual"])
+    out, res, _ = pkg.fused_add_rmsnorm(x, r, inp["weight"].to(DEV), None, eps=wl.eps)
+    torch.cuda.synchronize()
+    parity.compare(wl, parity.gpu_outputs_to_host(wl, out, res, None), ref, "unequal offsets")
+
+
+RAGGED_H = [1, 7, 9, 100, 1000, 4097, 8190]
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("res,bias", [(True, True), (True, False), (False, True), (False, False)])
+@pytest.mark.parametrize("H", RAGGED_H)
+def test_ragged_kernel_every_config(pkg, dt, res, bias, H):
+    # rows off the 32-byte grid: the selector takes the ragged-row kernel, and
+    # every listed shape of it (and a 3-block grid looping over rows) matches
+    # the oracle
+    T = 37
+    if H * (4 if dt == "f32" else 2) % 32 == 0:
+        pytest.skip("rows on the 32-byte grid take the vector kernels")
+    wl = synth.Workload(f"rag_{dt}_H{H}", T, H, 79, dt, dt, 1e-6, has_residual=res,
+                        has_bias=bias)
+    flags = pkg.make_flags(dt, dt, res, True, bias)
+    assert pkg.rmsnorm_query_config(T, H, flags).variant == pkg.VARIANT_RAGGED
+    cfgs = [c for c in pkg.rmsnorm_list_configs(T, H, flags) if c.variant == pkg.VARIANT_RAGGED]
+    assert cfgs
+    inp = synth.make_inputs(wl)
+    ref = parity.oracle_run(wl, inp)
+    for c in cfgs:
+        for grid in (0, 3):
+            c2 = pkg.RmsnConfig.from_dict({**c.as_dict(), "grid": grid})
+            parity.compare(wl, run_gpu(pkg, wl, inp, config=c2), ref,
+                           f"{wl.name} {c2.as_dict()}", bias=inp["bias"])
+    assert pkg.rmsnorm_read_status() == 0
+
+
+@pytest.mark.parametrize("T,H,dt", [(3000, 4097, "bf16"), (2048, 8190, "bf16"),
+                                    (16384, 8190, "bf16"), (1000, 6001, "f32")])
+def test_ragged_kernel_large(pkg, T, H, dt):
+    rows = synth.sample_rows(T, 1024) if T > 4096 else None
+    check(pkg, synth.Workload(f"rag_large_T{T}_H{H}", T, H, 80, dt, dt, 1e-5, has_bias=True,
+                              r_std=2.0), rows=rows)
+
+
+@pytest.mark.parametrize("alias", ["residual_out=residual", "out=x", "out=residual"])
+def test_ragged_kernel_in_place(pkg, alias):
+    wl = synth.Workload("rag_inplace", 29, 1000, 81, "bf16", "bf16", 1e-6, has_bias=True)
+    inp = synth.make_inputs(wl)
+    ref = parity.oracle_run(wl, inp)
+    g = parity.to_device(inp, DEV)
+    kw = {"residual_out=residual": dict(residual_out=g["residual"]),
+          "out=x": dict(out=g["x"]),
+          "out=residual": dict(out=g["residual"], residual_out=torch.empty_like(g["residual"]))}[alias]
+    out, res, _ = pkg.fused_add_rmsnorm(g["x"], g["residual"], g["weight"], g["bias"],
+                                        eps=wl.eps, **kw)
+    torch.cuda.synchronize()
+    parity.compare(wl, parity.gpu_outputs_to_host(wl, out, res, None), ref, alias,
+                   bias=inp["bias"])
+
+
 def test_odd_byte_pointer_rejected(pkg):
     buf = torch.zeros(2 * 64 * 64 + 2, dtype=torch.uint8, device=DEV)
     base = buf.data_ptr()
@@ -363,7 +433,11 @@ def test_selector_decode_vs_prefill(pkg):
         c = pkg.rmsnorm_query_config(T, H, flags)
         assert any(_same_shape(c, o) for o in pkg.rmsnorm_list_configs(T, H, flags)), (T, H)
         assert 1 <= c.grid <= max(T, 1)
+    # rows off the 32-byte grid: the ragged-row kernel for the same dtype in
+    # and out, the generic one otherwise (here: an FP8 output)
     c = pkg.rmsnorm_query_config(16, 1000, flags)
+    assert c.variant == pkg.VARIANT_RAGGED
+    c = pkg.rmsnorm_query_config(16, 1000, pkg.make_flags("bf16", "fp8", True, True, False))
     assert c.variant == pkg.VARIANT_GENERIC
 
 
