@@ -117,8 +117,10 @@ typedef struct {
  * contiguous (row stride = hidden); for rows in host memory use
  * rmsnorm_fwd_host.  Each pointer must be aligned to its
  * element size; the 256-bit vector kernels are used when hidden * element
- * size is a multiple of 32 bytes and every pointer is 32-byte aligned,
- * otherwise the generic kernel runs.  residual_out may be the same buffer as
+ * size is a multiple of 32 bytes and every pointer is 32-byte aligned;
+ * otherwise rows with the same dtype in and out whose row pointers are all
+ * equally aligned modulo 16 bytes take the ragged-row kernel (16-byte
+ * vectors plus single-element row ends), and the rest the generic kernel.  residual_out may be the same buffer as
  * residual, or as x when both have the same dtype; out may be the same
  * buffer as x or residual when their dtypes are equal; any other overlap is
  * undefined.  n_tokens == 0
