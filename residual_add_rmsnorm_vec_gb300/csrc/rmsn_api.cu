@@ -257,7 +257,8 @@ bool shape_config(const Problem& p, const KernelEntry& e, DeviceInfo* d, int gri
         // at most ceil(H / (16 / size)) interior vectors: CH per thread x 256
         const int64_t vecs = (p.H * p.in_bytes + 15) / 16;
         if (vecs > (int64_t)e.chunks * 256) return false;
-        const int64_t smem = p.H * 4 * (p.bias ? 2 : 1);
+        // fp32 weight (and bias) rows with one pad word per 32 columns
+        const int64_t smem = (p.H + p.H / 32) * 4 * (p.bias ? 2 : 1);
         if (smem > 48 * 1024 && smem > enable_smem(d, e.fn)) return false;
         c->vec_bytes = 16;
         c->warps_per_block = 8;

@@ -994,22 +994,28 @@ __device__ __forceinline__ float elem4(const uint32_t (&u)[4], int k) {
     }
 }
 
+// Shared-memory slot of column j in the staged weight / bias rows: one pad
+// word per 32 columns, so that the threads of a warp, whose vectors start
+// 16 bytes of the row apart, read from 32 different banks.
+__device__ __forceinline__ int ragged_slot(int j) { return j + (j >> 5); }
+
 template <class TI, int CH, bool RES, bool BIAS>
 __global__ void __launch_bounds__(256, CH <= 2 ? 4 : (CH <= 4 ? 2 : 1))
     rmsn_ragged_kernel(const RmsnArgs a) {
     constexpr int S = TI::kBytes;
     constexpr int VE = 16 / S;  // elements per 16-byte vector
-    extern __shared__ __align__(16) float wsm[];  // [H] weight + offset, then [H] bias
+    // weight + offset, then bias, as fp32 in padded slots (ragged_slot)
+    extern __shared__ __align__(16) float wsm[];
     __shared__ float red[2][32];
     const int H = a.H;
     const int t = threadIdx.x;
     const int G = blockDim.x;
-    float* bsm = wsm + H;
+    float* bsm = wsm + ragged_slot(H);
     pdl_launch_dependents(a.pdl);
     pdl_wait(a.pdl);
     for (int j = t; j < H; j += G) {
-        wsm[j] = __fadd_rn(a.has_w ? ld_elem<TI>(a.w, j) : 1.f, a.woff);
-        if constexpr (BIAS) bsm[j] = ld_elem<TI>(a.b, j);
+        wsm[ragged_slot(j)] = __fadd_rn(a.has_w ? ld_elem<TI>(a.w, j) : 1.f, a.woff);
+        if constexpr (BIAS) bsm[ragged_slot(j)] = ld_elem<TI>(a.b, j);
     }
     __syncthreads();
     const char* xb = static_cast<const char*>(a.x);
@@ -1075,8 +1081,8 @@ __global__ void __launch_bounds__(256, CH <= 2 ? 4 : (CH <= 4 ? 2 : 1))
 #pragma unroll
                 for (int k = 0; k < VE; ++k) {
                     const float tk = __fmul_rn(elem4<TI>(hu[c], k), inv);
-                    y[k] = BIAS ? __fmaf_rn(wsm[col + k], tk, bsm[col + k])
-                                : __fmul_rn(wsm[col + k], tk);
+                    const int sl = ragged_slot(col + k);
+                    y[k] = BIAS ? __fmaf_rn(wsm[sl], tk, bsm[sl]) : __fmul_rn(wsm[sl], tk);
                 }
                 uint32_t u[4];
                 if constexpr (S == 2) {
@@ -1091,8 +1097,8 @@ __global__ void __launch_bounds__(256, CH <= 2 ? 4 : (CH <= 4 ? 2 : 1))
         }
         if (t < ne) {
             const float tk = __fmul_rn(he, inv);
-            st_elem<TI>(a.out, e0 + je,
-                        BIAS ? __fmaf_rn(wsm[je], tk, bsm[je]) : __fmul_rn(wsm[je], tk));
+            const int sl = ragged_slot(je);
+            st_elem<TI>(a.out, e0 + je, BIAS ? __fmaf_rn(wsm[sl], tk, bsm[sl]) : __fmul_rn(wsm[sl], tk));
         }
         parity ^= 1;
     }
