@@ -11,6 +11,7 @@
 // from a table of measured bandwidth (rmsn_selector_table.inc) and a fixed
 // rule where the table has no entry.  The SM count is queried from the
 // device once, not compiled in.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <math.h>
@@ -237,6 +238,19 @@ int blocks_per_sm(DeviceInfo* d, const void* fn, int threads, int smem) {
 constexpr int kMaxStages = 8;
 constexpr int kBulkSmemTarget = 220 * 1024;
 
+// Ring stages filled by 128-byte-swizzled 2-D tensor copies: each row (of x
+// and of the residual) must be whole 1024-byte units (the swizzle pattern
+// repeats every 1024 bytes and every stage starts on such a boundary), at
+// most 256 lines of 128 bytes (one tensor box), and the tensor's line index
+// must fit the copy's signed 32-bit coordinate.
+bool bulk_swizzle_ok(const Problem& p) {
+    const int64_t xb = p.H * p.in_bytes, rb = p.H * p.res_bytes;
+    if (xb % 1024 != 0 || xb > 256 * 128 || p.T * (xb / 128) >= (int64_t{1} << 31)) return false;
+    if (p.res && (rb % 1024 != 0 || rb > 256 * 128 || p.T * (rb / 128) >= (int64_t{1} << 31)))
+        return false;
+    return true;
+}
+
 // One ring stage: the row of x, then (with a residual) the residual's row.
 int bulk_stage_bytes(const Problem& p) {
     return (int)(p.H * p.in_bytes + (p.res ? p.H * p.res_bytes : 0));
@@ -295,11 +309,13 @@ bool shape_config(const Problem& p, const KernelEntry& e, DeviceInfo* d, int gri
             int st = stages_req > 0 ? stages_req : kBulkSmemTarget / sb;
             if (st > kMaxStages) st = kMaxStages;
             const int limit = enable_smem(d, e.fn);
+            const int pad = bulk_swizzle_ok(p) ? 1024 : 0;
             if (stages_req <= 0)
-                while (st > 2 && (int64_t)st * sb > limit) --st;
-            if (st < 2 || (int64_t)st * sb > limit) return false;
+                while (st > 2 && (int64_t)st * sb + pad > limit) --st;
+            if (st < 2 || (int64_t)st * sb + pad > limit) return false;
             c->stages = st;
-            c->smem_bytes = st * sb;
+            // room to round the ring up to a 1024-byte boundary for the swizzle
+            c->smem_bytes = st * sb + (bulk_swizzle_ok(p) ? 1024 : 0);
         }
     }
     const int bps = blocks_per_sm(d, e.fn, threads, c->smem_bytes);
@@ -422,6 +438,44 @@ int validate(const void* x, const void* residual, const void* weight, const void
     return RMSN_OK;
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once per process (no
+// link-time dependency on the driver library); null where unavailable.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            f = nullptr;
+        }
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// A [T, H] tensor of `bytes`-byte elements as 128-byte lines: a 2-D map of
+// (128 / bytes) x (T H bytes / 128) elements whose box is one row's lines,
+// copied with the 128-byte swizzle.
+bool encode_rows(CUtensorMap* m, const void* base, int64_t T, int64_t H, int bytes) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)(128 / bytes), (cuuint64_t)(T * H * bytes / 128)};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / bytes), (cuuint32_t)(H * bytes / 128)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32, 2,
+              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int launch(const KernelEntry* e, const rmsn_config& c, DeviceInfo* d, const Problem& p,
            const void* x, const void* residual, const void* weight, const void* bias, void* out,
            void* residual_out, float* out_scale, float eps, float weight_offset,
@@ -445,7 +499,20 @@ int launch(const KernelEntry* e, const rmsn_config& c, DeviceInfo* d, const Prob
     a.pdl = p.pdl ? 1 : 0;
     a.early_params = p.early_params ? 1 : 0;
     a.status = d->status;
-    void* args[] = {&a};
+    // the bulk kernel also takes the tensor-copy descriptors of x and the
+    // residual (zero and unused when its stages take 1-D copies)
+    alignas(64) CUtensorMap mx;
+    alignas(64) CUtensorMap mr;
+    memset(&mx, 0, sizeof(mx));
+    memset(&mr, 0, sizeof(mr));
+    a.swz = 0;
+    if (e->variant == kBulkRow && bulk_swizzle_ok(p) &&
+        encode_rows(&mx, x, p.T, p.H, p.in_bytes) &&
+        (!p.res || encode_rows(&mr, residual, p.T, p.H, p.res_bytes)))
+        a.swz = 1;
+    void* args_one[] = {&a};
+    void* args_bulk[] = {&a, &mx, &mr};
+    void** args = e->variant == kBulkRow ? args_bulk : args_one;
     cudaError_t err;
     if (p.pdl) {
         // programmatic dependent launch: the kernel may start while the

@@ -21,6 +21,7 @@
 //                       the row from the just-written residual_out.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (the bulk kernel's tensor-copy descriptors)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -766,6 +767,51 @@ __device__ __forceinline__ V8 ld_shared32(uint32_t addr) {
     return v;
 }
 
+// Stages filled by 2-D tensor copies with the 128-byte swizzle: the stage is
+// a run of 128-byte lines starting on a 1024-byte boundary, and 16-byte
+// chunk c of line l sits at chunk c ^ (l & 7).  A quarter warp reading 8
+// neighbouring 32-byte vectors then meets every bank once per load.
+__device__ __forceinline__ uint32_t swz128(uint32_t base, uint32_t off) {
+    return base + (off ^ (((off >> 7) & 7u) << 4));
+}
+
+__device__ __forceinline__ V8 ld_shared32_swz(uint32_t base, uint32_t v) {
+    V8 r;
+    const uint32_t off = v * 32u;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.u[0]), "=r"(r.u[1]), "=r"(r.u[2]), "=r"(r.u[3])
+                 : "r"(swz128(base, off)));
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.u[4]), "=r"(r.u[5]), "=r"(r.u[6]), "=r"(r.u[7])
+                 : "r"(swz128(base, off + 16u)));
+    return r;
+}
+
+// Thread 0: expect the row's bytes on `bar`, then copy x (and the residual
+// right after it) of `row` as 2-D tensor boxes of `xl` (`rl`) 128-byte lines.
+template <bool RES>
+__device__ __forceinline__ void issue_row_tensor(const CUtensorMap* mx, const CUtensorMap* mr,
+                                                 int64_t row, uint32_t dst, uint32_t bar,
+                                                 uint32_t x_bytes, uint32_t r_bytes) {
+    const uint32_t bytes = RES ? x_bytes + r_bytes : x_bytes;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(mx)), "r"(0), "r"((int)(row * (x_bytes / 128u))),
+        "r"(bar)
+        : "memory");
+    if constexpr (RES) {
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+            "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst + x_bytes),
+            "l"(reinterpret_cast<uint64_t>(mr)), "r"(0), "r"((int)(row * (r_bytes / 128u))),
+            "r"(bar)
+            : "memory");
+    }
+}
+
 // One vector of VE = 32 / TI::kBytes elements from shared memory: 32 bytes,
 // or 16 bytes of 2-byte values widened exactly to fp32 under an fp32 stream.
 template <class TX, class TI>
@@ -788,10 +834,33 @@ __device__ __forceinline__ V8 ld_shared_vec(uint32_t addr) {
     }
 }
 
+template <class TX, class TI>
+__device__ __forceinline__ V8 ld_shared_vec_swz(uint32_t base, uint32_t v) {
+    if constexpr (TX::kBytes == TI::kBytes) {
+        return ld_shared32_swz(base, v);
+    } else {
+        uint32_t in[4];
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(in[0]), "=r"(in[1]), "=r"(in[2]), "=r"(in[3])
+                     : "r"(swz128(base, v * 16u)));
+        V8 r;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            r.u[2 * k] = __float_as_uint(lo2<TX>(in[k]));
+            r.u[2 * k + 1] = __float_as_uint(hi2<TX>(in[k]));
+        }
+        return r;
+    }
+}
+
 // TX: storage of x, weight and bias, as in rmsn_vec_kernel; a stage holds
-// the row of x followed by the row of the residual (TI).
+// the row of x followed by the row of the residual (TI).  With a.swz the
+// stages are filled by swizzled 2-D tensor copies described by mx / mr (and
+// start on 1024-byte boundaries), else by 1-D bulk copies.
 template <class TI, class TO, int CH, int WMAX, bool RES, bool BIAS, class TX = TI>
-__global__ void __launch_bounds__(WMAX * 32, 1) rmsn_bulk_kernel(const RmsnArgs a) {
+__global__ void __launch_bounds__(WMAX * 32, 1)
+    rmsn_bulk_kernel(const RmsnArgs a, const __grid_constant__ CUtensorMap mx,
+                     const __grid_constant__ CUtensorMap mr) {
     constexpr int VE = 32 / TI::kBytes;
     constexpr int XVB = VE * TX::kBytes;  // bytes of one x vector
     extern __shared__ __align__(128) unsigned char ring[];
@@ -805,7 +874,7 @@ __global__ void __launch_bounds__(WMAX * 32, 1) rmsn_bulk_kernel(const RmsnArgs 
     const uint32_t x_bytes = (uint32_t)a.H * TX::kBytes;
     const uint32_t r_bytes = (uint32_t)a.H * TI::kBytes;
     const uint32_t stage_bytes = RES ? x_bytes + r_bytes : x_bytes;
-    const uint32_t ring0 = smem_u32(ring);
+    const uint32_t ring0 = a.swz ? (smem_u32(ring) + 1023u) & ~1023u : smem_u32(ring);
     // rows of this block: blockIdx.x + k * gridDim.x
     const int64_t n_my = a.T > blockIdx.x ? (a.T - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
@@ -821,9 +890,15 @@ __global__ void __launch_bounds__(WMAX * 32, 1) rmsn_bulk_kernel(const RmsnArgs 
     if (a.early_params) load_params<TX, TI, CH>(a, G, t, wv, bv, BIAS);
     pdl_wait(a.pdl);
     if (t == 0) {
-        for (int64_t k = 0; k < S && k < n_my; ++k)
-            issue_row<RES>(a, blockIdx.x + k * gridDim.x, ring0 + (uint32_t)k * stage_bytes,
-                           smem_u32(&full[k]), x_bytes, r_bytes);
+        for (int64_t k = 0; k < S && k < n_my; ++k) {
+            if (a.swz)
+                issue_row_tensor<RES>(&mx, &mr, blockIdx.x + k * gridDim.x,
+                                      ring0 + (uint32_t)k * stage_bytes, smem_u32(&full[k]),
+                                      x_bytes, r_bytes);
+            else
+                issue_row<RES>(a, blockIdx.x + k * gridDim.x, ring0 + (uint32_t)k * stage_bytes,
+                               smem_u32(&full[k]), x_bytes, r_bytes);
+        }
     }
     __syncthreads();
     if (!a.early_params) load_params<TX, TI, CH>(a, G, t, wv, bv, BIAS);
@@ -847,8 +922,13 @@ __global__ void __launch_bounds__(WMAX * 32, 1) rmsn_bulk_kernel(const RmsnArgs 
         for (int c = 0; c < CH; ++c) {
             const int v = c * G + t;
             if (v < a.nvec) {
-                hv[c] = ld_shared_vec<TX, TI>(base + (uint32_t)v * XVB);
-                if constexpr (RES) rv[c] = ld_shared32(base + x_bytes + (uint32_t)v * 32);
+                if (a.swz) {
+                    hv[c] = ld_shared_vec_swz<TX, TI>(base, (uint32_t)v);
+                    if constexpr (RES) rv[c] = ld_shared32_swz(base + x_bytes, (uint32_t)v);
+                } else {
+                    hv[c] = ld_shared_vec<TX, TI>(base + (uint32_t)v * XVB);
+                    if constexpr (RES) rv[c] = ld_shared32(base + x_bytes + (uint32_t)v * 32);
+                }
             }
         }
         const float acc = residual_sumsq<TI, CH, RES>(a, rbase, G, t, hv, rv);
@@ -857,8 +937,12 @@ __global__ void __launch_bounds__(WMAX * 32, 1) rmsn_bulk_kernel(const RmsnArgs 
         if (abort_flag) break;
         if (t == 0 && k + S < n_my) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue_row<RES>(a, blockIdx.x + (k + S) * gridDim.x, base, smem_u32(&full[s]),
-                           x_bytes, r_bytes);
+            if (a.swz)
+                issue_row_tensor<RES>(&mx, &mr, blockIdx.x + (k + S) * gridDim.x, base,
+                                      smem_u32(&full[s]), x_bytes, r_bytes);
+            else
+                issue_row<RES>(a, blockIdx.x + (k + S) * gridDim.x, base, smem_u32(&full[s]),
+                               x_bytes, r_bytes);
         }
         const float inv = inv_rms(sumsq, a.H, a.eps);
         float* slot = red[2 + parity];

@@ -25,6 +25,7 @@ struct RmsnArgs {
     int32_t stages;      // shared-memory row buffers (bulk kernel)
     int32_t pdl;           // launched as a programmatic dependent
     int32_t early_params;  // weight / bias may be read before the prerequisite grid ends
+    int32_t swz;           // bulk kernel: stages filled by 128-byte-swizzled tensor copies
     uint32_t* status;    // device status word: bit 0 = a bounded wait ran out
 };
 
