@@ -316,7 +316,8 @@ def main():
     with open(args.out, "w") as f:
         json.dump({"meta": meta, "entries": entries}, f)
     if args.write_table:
-        write_table(entries, args.table_out)
+        # the rows of the other dtype pairs (block formats, fp16, fp32 stream) stay
+        merge_table(entries, args.table_out)
 
 
 if __name__ == "__main__":
