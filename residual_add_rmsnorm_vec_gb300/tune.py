@@ -306,7 +306,8 @@ def main():
         return
     entries = sweep(pkg, grid, "bf16", "bf16", True, False, args.reps, hot)
     # the other dtype paths of the hot-path workloads
-    entries += sweep(pkg, [(T, H) for H in (5120, 7168) for T in (1, 64, 1024, 4096)],
+    entries += sweep(pkg, [(T, H) for H in (4096, 5120, 7168, 8192)
+                           for T in (1, 64, 1024, 4096, 16384)],
                      "bf16", "fp8", True, True, args.reps, hot)
     entries += sweep(pkg, [(T, 1024) for T in (1, 64, 4096)], "f32", "f32", False, False,
                      args.reps, hot)
