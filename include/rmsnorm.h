@@ -83,7 +83,9 @@ typedef enum {
     RMSN_VARIANT_WARP_ROWS = 0, /* decode: one warp per row, rows spread over SMs */
     RMSN_VARIANT_BLOCK_ROW = 1, /* prefill: one block (W warps) per row, register-resident */
     RMSN_VARIANT_BULK_ROW = 2,  /* prefill: persistent blocks; rows streamed into a ring of
-                                   shared-memory buffers by bulk async copies (cp.async.bulk) */
+                                   shared-memory buffers by TMA copies: 128-byte-swizzled 2-D
+                                   tensor copies where a row is whole 1 KiB units of at most
+                                   32 KiB, else 1-D bulk copies */
     RMSN_VARIANT_GENERIC = 3,   /* any hidden size / alignment (element-wise, three passes) */
     RMSN_VARIANT_RAGGED = 4     /* rows off the 32-byte grid, same dtype in and out, all row
                                    pointers equally aligned mod 16 bytes: 16-byte vectors for
