@@ -104,6 +104,8 @@ typedef struct {
     int32_t grid;            /* blocks launched */
     int32_t smem_bytes;      /* dynamic shared memory per block */
     int32_t num_sms;         /* SMs of the device the config was made for */
+    int32_t ring_copy;       /* bulk variant: 2 = swizzled 2-D tensor copies, 1 = 1-D bulk
+                                copies; 0 for the other variants (output only) */
 } rmsn_config;
 
 /*

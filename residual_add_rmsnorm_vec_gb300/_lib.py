@@ -55,7 +55,7 @@ class RmsnConfig(ctypes.Structure):
     """Mirror of ``rmsn_config``."""
     _fields_ = [(n, ctypes.c_int32) for n in (
         "variant", "vec_bytes", "warps_per_block", "warps_per_row", "chunks", "max_warps",
-        "stages", "grid", "smem_bytes", "num_sms")]
+        "stages", "grid", "smem_bytes", "num_sms", "ring_copy")]
 
     def as_dict(self) -> dict:
         d = {n: int(getattr(self, n)) for n, _ in self._fields_}

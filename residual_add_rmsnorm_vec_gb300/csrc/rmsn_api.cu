@@ -238,6 +238,12 @@ int blocks_per_sm(DeviceInfo* d, const void* fn, int threads, int smem) {
 constexpr int kMaxStages = 8;
 constexpr int kBulkSmemTarget = 220 * 1024;
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled();
+
 // Ring stages filled by 128-byte-swizzled 2-D tensor copies: each row (of x
 // and of the residual) must be whole 1024-byte units (the swizzle pattern
 // repeats every 1024 bytes and every stage starts on such a boundary), at
@@ -316,6 +322,7 @@ bool shape_config(const Problem& p, const KernelEntry& e, DeviceInfo* d, int gri
             c->stages = st;
             // room to round the ring up to a 1024-byte boundary for the swizzle
             c->smem_bytes = st * sb + (bulk_swizzle_ok(p) ? 1024 : 0);
+            c->ring_copy = bulk_swizzle_ok(p) && encode_tiled() ? 2 : 1;
         }
     }
     const int bps = blocks_per_sm(d, e.fn, threads, c->smem_bytes);
@@ -440,11 +447,6 @@ int validate(const void* x, const void* residual, const void* weight, const void
 
 // cuTensorMapEncodeTiled from the driver, looked up once per process (no
 // link-time dependency on the driver library); null where unavailable.
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
 EncodeTiledFn encode_tiled() {
     static EncodeTiledFn fn = [] {
         void* f = nullptr;
