@@ -16,7 +16,10 @@
 //                       holds CH 32-byte vectors of the row in registers
 //                       between the load and the store.
 //   rmsn_bulk_kernel    persistent blocks streaming whole rows into a ring of
-//                       shared-memory buffers with bulk async copies.
+//                       shared-memory buffers with TMA copies (swizzled 2-D
+//                       tensor copies, or 1-D bulk copies).
+//   rmsn_ragged_kernel  rows off the 32-byte grid: 16-byte vectors for the
+//                       row's interior, single elements at its ends.
 //   rmsn_generic_kernel any hidden size / alignment; element-wise, re-reads
 //                       the row from the just-written residual_out.
 #pragma once
@@ -688,8 +691,9 @@ __global__ void __launch_bounds__(Bounds<WMAX, CH, RES && BIAS>::kThreads,
 //
 // Persistent blocks (one row at a time, up to WMAX warps).  Whole rows of x
 // and the residual are moved into a ring of `a.stages` shared-memory buffers
-// by the bulk async-copy engine (cp.async.bulk, completion counted on an
-// mbarrier per buffer), issued by thread 0 up to `stages` rows ahead.  The
+// by the TMA engine (cp.async.bulk.tensor with the 128-byte swizzle, or
+// cp.async.bulk; completion counted on an mbarrier per buffer), issued by
+// thread 0 up to `stages` rows ahead.  The
 // threads copy their vectors from shared memory into registers, so a buffer
 // is free again after the row's sum-of-squares barrier, where thread 0
 // refills it with the row `stages` ahead.  Bytes in flight per SM are set by
