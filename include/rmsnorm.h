@@ -65,9 +65,11 @@ typedef enum {
 #define RMSN_RESIDUAL_F32 0x200u /* with RMSN_HAS_RESIDUAL and bf16 / fp16 input: residual
                                    and residual_out are fp32 (an fp32 residual stream);
                                    h = x + residual is kept in fp32, not rounded to the
-                                   input type, and the norm is taken on it.  Vector
-                                   kernels need hidden % 8 == 0, 16-byte aligned
-                                   x / weight / bias and 32-byte aligned residuals. */
+                                   input type, and the norm is taken on it.  Built for
+                                   outputs of the input dtype and FP8 (other outputs:
+                                   RMSN_EUNSUPPORTED).  Vector kernels need
+                                   hidden % 8 == 0, 16-byte aligned x / weight / bias
+                                   and 32-byte aligned residuals. */
 /* launch options (blog section "Grid synchronisation": programmatic dependent
  * launch cuts the launch overhead of chained kernels) */
 #define RMSN_PDL 0x80u /* launch with programmatic stream serialization: the kernel
