@@ -449,7 +449,8 @@ __device__ __forceinline__ float residual_sumsq(const RmsnArgs& a, int64_t rbase
 //          clamped to [-127, 127], stored as E8M0 (s + 127); codes y * 2^-s.
 //   NVFP4: per-token fp32 g = max|row| / (448 * 6) (the row max all-reduce),
 //          block scale E4M3(max|block| * (1 / (6 g))), codes
-//          E2M1(y * (1 / (scale * g))), with correctly rounded reciprocals.
+//          E2M1(y * (1 / (scale * g))); 1 / (6 g) is correctly rounded, the
+//          per-block reciprocal is the hardware approximation.
 // All conversions round to nearest even and saturate.
 template <class TI, class TO, int CH, bool BIAS, bool KEEP, class ReduceMax>
 __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row, int64_t rbase,
@@ -528,7 +529,10 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
                 sc = two & 0xFFu;
             }
             const float s = __fmul_rn(e4m3_value(sc), g);
-            mul = s > 0.f ? __frcp_rn(s) : 0.f;
+            // one reciprocal per block of 16: the hardware approximation
+            // (within 1 ulp) is far inside E2M1's half-step of 1/4 to 1/2
+            if (s > 0.f) asm("rcp.approx.f32 %0, %1;" : "=f"(mul) : "f"(s));
+            else mul = 0.f;
             sbyte = (uint8_t)sc;
         } else {
             constexpr int emax = FP4 ? 2 : 8;
