@@ -38,6 +38,39 @@ constexpr int64_t kMaxHidden = int64_t(1) << 24;
 // Status word of the kernels on each device (bit 0: a bounded wait ran out).
 __device__ uint32_t g_status;
 
+// Cache keys compared in full (a hash only picks the bucket): two problems
+// that hash alike must never share a launch.
+struct SelKey {
+    int64_t T, H;
+    uint32_t flags;
+    int paths;  // bit 0: vector path, bit 1: ragged-row path
+    bool operator==(const SelKey& o) const {
+        return T == o.T && H == o.H && flags == o.flags && paths == o.paths;
+    }
+};
+struct OccKey {
+    const void* fn;
+    int threads, smem;
+    bool operator==(const OccKey& o) const {
+        return fn == o.fn && threads == o.threads && smem == o.smem;
+    }
+};
+inline uint64_t mix(uint64_t h, uint64_t v) {
+    h ^= v + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+    return h;
+}
+struct SelKeyHash {
+    size_t operator()(const SelKey& k) const {
+        return (size_t)mix(mix(mix((uint64_t)k.T, (uint64_t)k.H), k.flags), (uint64_t)k.paths);
+    }
+};
+struct OccKeyHash {
+    size_t operator()(const OccKey& k) const {
+        return (size_t)mix(mix(reinterpret_cast<uintptr_t>(k.fn), (uint64_t)k.threads),
+                           (uint64_t)k.smem);
+    }
+};
+
 struct DeviceInfo {
     std::once_flag once;
     int num_sms = 0;
@@ -48,15 +81,10 @@ struct DeviceInfo {
     std::mutex mu;
     std::vector<std::pair<const void*, int>> smem_set;  // kernel -> raised dynamic smem limit
     // occupancy results: (kernel, threads, smem) -> resident blocks per SM
-    std::unordered_map<uint64_t, int> occ_cache;
+    std::unordered_map<OccKey, int, OccKeyHash> occ_cache;
     // selector results: (tokens, hidden, flags, vector path) -> configuration
-    std::unordered_map<uint64_t, std::pair<rmsn_config, const KernelEntry*>> sel_cache;
+    std::unordered_map<SelKey, std::pair<rmsn_config, const KernelEntry*>, SelKeyHash> sel_cache;
 };
-
-inline uint64_t mix(uint64_t h, uint64_t v) {
-    h ^= v + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
-    return h;
-}
 
 DeviceInfo g_dev[kMaxDevices];
 
@@ -217,7 +245,7 @@ const KernelEntry* find_kernel(const Problem& p, int variant, int ch, int wmax) 
 }
 
 int blocks_per_sm(DeviceInfo* d, const void* fn, int threads, int smem) {
-    const uint64_t key = mix(mix(reinterpret_cast<uintptr_t>(fn), (uint64_t)threads), (uint64_t)smem);
+    const OccKey key{fn, threads, smem};
     {
         std::lock_guard<std::mutex> lock(d->mu);
         auto it = d->occ_cache.find(key);
@@ -608,8 +636,7 @@ RMSN_API int rmsnorm_fwd_ex(const void* x, const void* residual, const void* wei
         e = find_kernel(p, cfg->variant, cfg->chunks, cfg->max_warps);
         if (!e || !shape_config(p, *e, d, cfg->grid, cfg->stages, &c)) return RMSN_EUNSUPPORTED;
     } else {
-        const uint64_t key = mix(mix(mix((uint64_t)p.T, (uint64_t)p.H), flags),
-                                 (p.vec_ok ? 1 : 0) | (p.ragged_ok ? 2 : 0));
+        const SelKey key{p.T, p.H, flags, (p.vec_ok ? 1 : 0) | (p.ragged_ok ? 2 : 0)};
         bool hit = false;
         {
             std::lock_guard<std::mutex> lock(d->mu);

@@ -454,6 +454,14 @@ def test_ring_copy_mode(pkg):
                if c.variant != pkg.VARIANT_BULK_ROW)
 
 
+def test_selection_cache_keeps_colliding_problems_apart(pkg):
+    # (8 x 8) and (2 x 384), fp32 with residual and weight, hash alike in the
+    # launch cache: the second call must get its own launch (the first one's
+    # single-warp shape would leave a third of its row unwritten)
+    for i, (T, H) in enumerate(((8, 8), (2, 384), (8, 8))):
+        check(pkg, synth.Workload(f"cache_{T}x{H}", T, H, 300 + i, "f32", "f32", 1e-6))
+
+
 def test_status_word_clear_after_all_runs(pkg):
     # no bounded wait in any kernel ran out during the suite
     assert pkg.rmsnorm_read_status(clear=False) == 0
