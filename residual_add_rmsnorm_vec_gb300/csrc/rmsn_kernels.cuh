@@ -188,6 +188,95 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     else return pack_bf16x2(lo, hi);
 }
 
+// ---------------------------------------------------------------- packed arithmetic
+//
+// sm_100 and later run two fp32 lanes per instruction (the .f32x2 forms of
+// add, mul and fma) and take 16-bit operands straight into fp32 adds and
+// FMAs.  Every lane is rounded once, as the scalar operation rounds it, so
+// these forms cut instructions without changing a single result.
+
+// Two fp32 lanes in one 64-bit register pair.
+struct F2 {
+    uint64_t v;
+};
+
+__device__ __forceinline__ F2 f2(float lo, float hi) {
+    F2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2split(F2 a, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+}
+
+__device__ __forceinline__ F2 add2(F2 a, F2 b) {
+    F2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+
+__device__ __forceinline__ F2 mul2(F2 a, F2 b) {
+    F2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+
+__device__ __forceinline__ F2 fma2(F2 a, F2 b, F2 c) {
+    F2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+    return r;
+}
+
+// The two 16-bit lanes of a word of T, widened to fp32 (exact).
+template <class T>
+__device__ __forceinline__ F2 widen2(uint32_t u) {
+    return f2(lo2<T>(u), hi2<T>(u));
+}
+
+// acc + lo^2, then + hi^2, for the two lanes of u (type T): each step one
+// fp32 rounding, as fmaf on the widened values (the square of a T value is
+// exact in fp32).
+template <class T>
+__device__ __forceinline__ float sumsq16x2(uint32_t u, float acc) {
+    float r;
+    if constexpr (IsF16<T>::value)
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\t"
+            "fma.rn.f32.f16 %0, l, l, %2;\n\tfma.rn.f32.f16 %0, h, h, %0;\n\t}"
+            : "=f"(r)
+            : "r"(u), "f"(acc));
+    else
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\t"
+            "fma.rn.f32.bf16 %0, l, l, %2;\n\tfma.rn.f32.bf16 %0, h, h, %0;\n\t}"
+            : "=f"(r)
+            : "r"(u), "f"(acc));
+    return r;
+}
+
+// Both 16-bit lanes of u (type T) plus the fp32 c, each rounded once to fp32.
+template <class T>
+__device__ __forceinline__ F2 add16x2_f32(uint32_t u, float c) {
+    float lo, hi;
+    if constexpr (IsF16<T>::value)
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+            "add.rn.f32.f16 %0, l, %3;\n\tadd.rn.f32.f16 %1, h, %3;\n\t}"
+            : "=f"(lo), "=f"(hi)
+            : "r"(u), "f"(c));
+    else
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+            "add.rn.f32.bf16 %0, l, %3;\n\tadd.rn.f32.bf16 %1, h, %3;\n\t}"
+            : "=f"(lo), "=f"(hi)
+            : "r"(u), "f"(c));
+    return f2(lo, hi);
+}
+
+// max(m, |a|, |b|) in one three-input maximum.
+__device__ __forceinline__ float absmax3(float m, float a, float b) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(m), "f"(fabsf(a)), "f"(fabsf(b)));
+    return r;
+}
+
 // Round four floats to E4M3 (nearest-even, saturating to +-448), element 0
 // in the lowest byte.
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a0, float a1, float a2, float a3) {
@@ -332,6 +421,43 @@ __device__ __forceinline__ float scale_elem(float h, float inv, float w, float w
     return BIAS ? __fmaf_rn(wo, t, b) : __fmul_rn(wo, t);
 }
 
+// scale_elem over the VE elements of one vector; `m` takes the maximum of
+// |y|.  PACK: two lanes per instruction (the same roundings, so the same
+// values); else one element at a time.
+template <class TI, bool BIAS, bool MAX = false, bool PACK = true>
+__device__ __forceinline__ void scale_vec(const V8& h, const V8& w, const V8& b, float inv,
+                                          float woff, float (&y)[32 / TI::kBytes], float& m) {
+    const F2 inv2 = f2(inv, inv);
+    if constexpr (!PACK) {
+#pragma unroll
+        for (int k = 0; k < 32 / TI::kBytes; ++k) {
+            y[k] = scale_elem<BIAS>(elem<TI>(h, k), inv, elem<TI>(w, k), woff,
+                                    BIAS ? elem<TI>(b, k) : 0.f);
+            if constexpr (MAX) m = fmaxf(m, fabsf(y[k]));
+        }
+    } else if constexpr (TI::kBytes == 2) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const F2 t = mul2(widen2<TI>(h.u[k]), inv2);
+            const F2 wo = add16x2_f32<TI>(w.u[k], woff);
+            const F2 r = BIAS ? fma2(wo, t, widen2<TI>(b.u[k])) : mul2(wo, t);
+            f2split(r, y[2 * k], y[2 * k + 1]);
+            if constexpr (MAX) m = absmax3(m, y[2 * k], y[2 * k + 1]);
+        }
+    } else {
+        const F2 woff2 = f2(woff, woff);
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+            const F2 t = mul2(f2(__uint_as_float(h.u[k]), __uint_as_float(h.u[k + 1])), inv2);
+            const F2 wo = add2(f2(__uint_as_float(w.u[k]), __uint_as_float(w.u[k + 1])), woff2);
+            const F2 r = BIAS ? fma2(wo, t, f2(__uint_as_float(b.u[k]), __uint_as_float(b.u[k + 1])))
+                              : mul2(wo, t);
+            f2split(r, y[k], y[k + 1]);
+            if constexpr (MAX) m = absmax3(m, y[k], y[k + 1]);
+        }
+    }
+}
+
 // Store the VE outputs of one input vector at element offset `e`.
 template <class TI, class TO>
 __device__ __forceinline__ void store_out(void* out, int64_t e, const float (&y)[32 / TI::kBytes],
@@ -404,8 +530,11 @@ __device__ __forceinline__ void load_params(const RmsnArgs& a, int G, int t, V8 
 }
 
 // h = RN_in(x + r) (the sum formed in fp32), stored to residual_out; returns
-// this thread's fp32 sum of h^2.
-template <class TI, int CH, bool RES>
+// this thread's fp32 sum of h^2.  A packed 16-bit add (add.rn.bf16x2) gives
+// the same h in fewer instructions, but measured on GB300 it made the
+// prefill ring ~15% slower, so the sum stays in fp32.  PACK: the squares take
+// the 16-bit lanes straight into the FMA.
+template <class TI, int CH, bool RES, bool PACK = true>
 __device__ __forceinline__ float residual_sumsq(const RmsnArgs& a, int64_t rbase, int G, int t,
                                                 V8 (&hv)[CH], const V8* rv) {
     constexpr int VE = 32 / TI::kBytes;
@@ -431,10 +560,15 @@ __device__ __forceinline__ float residual_sumsq(const RmsnArgs& a, int64_t rbase
                 const int64_t off = (rbase + (int64_t)v * VE) * TI::kBytes;
                 st_stream32(static_cast<char*>(a.res_out) + off, hv[c].u);
             }
+            if constexpr (TI::kBytes == 2 && PACK) {
 #pragma unroll
-            for (int k = 0; k < VE; ++k) {
-                const float h = elem<TI>(hv[c], k);
-                acc = __fmaf_rn(h, h, acc);
+                for (int k = 0; k < 8; ++k) acc = sumsq16x2<TI>(hv[c].u[k], acc);
+            } else {
+#pragma unroll
+                for (int k = 0; k < VE; ++k) {
+                    const float h = elem<TI>(hv[c], k);
+                    acc = __fmaf_rn(h, h, acc);
+                }
             }
         }
     }
@@ -473,15 +607,13 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
             if (v < a.nvec) {
                 opaque(wv[c]);
                 if constexpr (BIAS) opaque(bv[c]);
-                float m = 0.f;
+                float m = 0.f, y[VE];
+                scale_vec<TI, BIAS, true>(hv[c], wv[c], bv[BIAS ? c : 0], inv, a.woff, y, m);
+                if constexpr (HOLD) {
 #pragma unroll
-                for (int k = 0; k < VE; ++k) {
-                    const float y = scale_elem<BIAS>(elem<TI>(hv[c], k), inv, elem<TI>(wv[c], k),
-                                                     a.woff, BIAS ? elem<TI>(bv[c], k) : 0.f);
-                    if constexpr (HOLD) ys[c][k] = y;
-                    m = fmaxf(m, fabsf(y));
+                    for (int k = 0; k < VE; ++k) ys[c][k] = y[k];
+                    bms[c] = m;
                 }
-                if constexpr (HOLD) bms[c] = m;
                 amax = fmaxf(amax, m);
             }
         }
@@ -504,12 +636,7 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
             } else {
                 opaque(wv[c]);
                 if constexpr (BIAS) opaque(bv[c]);
-#pragma unroll
-                for (int k = 0; k < VE; ++k) {
-                    y[k] = scale_elem<BIAS>(elem<TI>(hv[c], k), inv, elem<TI>(wv[c], k), a.woff,
-                                            BIAS ? elem<TI>(bv[c], k) : 0.f);
-                    bmax = fmaxf(bmax, fabsf(y[k]));
-                }
+                scale_vec<TI, BIAS, true>(hv[c], wv[c], bv[BIAS ? c : 0], inv, a.woff, y, bmax);
             }
         }
         // every lane takes part; a block's lanes are all valid or all invalid
@@ -543,7 +670,8 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
             sbyte = (uint8_t)(sx + 127);
         }
 #pragma unroll
-        for (int k = 0; k < VE; ++k) y[k] = __fmul_rn(y[k], mul);
+        for (int k = 0; k < VE; k += 2)
+            f2split(mul2(f2(y[k], y[k + 1]), f2(mul, mul)), y[k], y[k + 1]);
         const int64_t e = rbase + (int64_t)v * VE;  // element index of this vector
         if constexpr (FP4) {
             uint32_t u[VE / 8];
@@ -572,8 +700,9 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
 // `reduce_max` is the row-wide max all-reduce (only used for FP8 output).
 // KEEP: hold the row's y in registers between the FP8 max pass and the
 // quantising pass instead of recomputing it (for kernels with a large
-// register budget).
-template <class TI, class TO, int CH, bool BIAS, bool KEEP = false, class ReduceMax>
+// register budget).  PACK: scale two lanes per instruction.
+template <class TI, class TO, int CH, bool BIAS, bool KEEP = false, bool PACK = true,
+          class ReduceMax>
 __device__ __forceinline__ void scale_store(const RmsnArgs& a, int64_t row, int64_t rbase, int G,
                                             int t, float inv, const V8 (&hv)[CH], V8 (&wv)[CH],
                                             V8* bv, ReduceMax reduce_max) {
@@ -594,12 +723,12 @@ __device__ __forceinline__ void scale_store(const RmsnArgs& a, int64_t row, int6
             if (v < a.nvec) {
                 opaque(wv[c]);
                 if constexpr (BIAS) opaque(bv[c]);
+                float y[VE];
+                scale_vec<TI, BIAS, true, PACK>(hv[c], wv[c], bv[BIAS ? c : 0], inv, a.woff, y,
+                                                amax);
+                if constexpr (HOLD) {
 #pragma unroll
-                for (int k = 0; k < VE; ++k) {
-                    const float y = scale_elem<BIAS>(elem<TI>(hv[c], k), inv, elem<TI>(wv[c], k),
-                                                     a.woff, BIAS ? elem<TI>(bv[c], k) : 0.f);
-                    if constexpr (HOLD) ys[c][k] = y;
-                    amax = fmaxf(amax, fabsf(y));
+                    for (int k = 0; k < VE; ++k) ys[c][k] = y[k];
                 }
             }
         }
@@ -616,11 +745,9 @@ __device__ __forceinline__ void scale_store(const RmsnArgs& a, int64_t row, int6
             } else {
                 opaque(wv[c]);
                 if constexpr (BIAS) opaque(bv[c]);
-                float y[VE];
-#pragma unroll
-                for (int k = 0; k < VE; ++k)
-                    y[k] = scale_elem<BIAS>(elem<TI>(hv[c], k), inv, elem<TI>(wv[c], k), a.woff,
-                                            BIAS ? elem<TI>(bv[c], k) : 0.f);
+                float y[VE], m = 0.f;
+                scale_vec<TI, BIAS, false, PACK>(hv[c], wv[c], bv[BIAS ? c : 0], inv, a.woff, y,
+                                                 m);
                 store_out<TI, TO>(a.out, rbase + (int64_t)v * VE, y, qmul);
             }
         }
@@ -871,6 +998,10 @@ __global__ void __launch_bounds__(WMAX * 32, 1)
                      const __grid_constant__ CUtensorMap mr) {
     constexpr int VE = 32 / TI::kBytes;
     constexpr int XVB = VE * TX::kBytes;  // bytes of one x vector
+    // per-token FP8 rows take one element per instruction here: measured on
+    // GB300, the paired fp32 forms made this kernel's long FP8 launches 1-5%
+    // slower (while they speed up every other output and the short rows)
+    constexpr bool PACK = !std::is_same<TO, FP8>::value;
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full[kMaxStages];
     __shared__ float red[4][32];
@@ -939,7 +1070,7 @@ __global__ void __launch_bounds__(WMAX * 32, 1)
                 }
             }
         }
-        const float acc = residual_sumsq<TI, CH, RES>(a, rbase, G, t, hv, rv);
+        const float acc = residual_sumsq<TI, CH, RES, PACK>(a, rbase, G, t, hv, rv);
         const float sumsq = block_allreduce<false>(acc, red[parity]);
         // every thread has read buffer s: refill it with the row S ahead
         if (abort_flag) break;
@@ -954,9 +1085,9 @@ __global__ void __launch_bounds__(WMAX * 32, 1)
         }
         const float inv = inv_rms(sumsq, a.H, a.eps);
         float* slot = red[2 + parity];
-        scale_store<TI, TO, CH, BIAS, (WMAX <= 16 && CH * VE <= 32)>(a, row, rbase, G, t, inv, hv,
-                                                                    wv, bv,
-                                      [&](float m) { return block_allreduce<true>(m, slot); });
+        scale_store<TI, TO, CH, BIAS, (WMAX <= 16 && CH * VE <= 32), PACK>(
+            a, row, rbase, G, t, inv, hv, wv, bv,
+            [&](float m) { return block_allreduce<true>(m, slot); });
         parity ^= 1;
     }
     if (abort_flag && t == 0) {
