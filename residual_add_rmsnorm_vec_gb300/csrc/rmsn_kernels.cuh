@@ -386,19 +386,30 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Maximum over the warp of absolute maxima.  REDUX: every v is +0 or above
+// and never NaN (they are maxima of |y| started from 0 with NaN-ignoring
+// max), and such floats order as their bit patterns do as unsigned integers,
+// so one redux.sync gives exactly the float maximum; else a butterfly.
+template <bool REDUX = true>
 __device__ __forceinline__ float warp_max(float v) {
+    if constexpr (REDUX) {
+        uint32_t r;
+        asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(__float_as_uint(v)));
+        return __uint_as_float(r);
+    } else {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    return v;
+        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+        return v;
+    }
 }
 
 // Sum (or max) over the warps of a block through shared memory.  `slot` is a
 // [32] float array that alternates between calls so one barrier per call
 // suffices; every thread adds the partials in the same order and so gets the
 // same total.
-template <bool MAX>
+template <bool MAX, bool REDUX = true>
 __device__ __forceinline__ float block_allreduce(float v, float* slot) {
-    v = MAX ? warp_max(v) : warp_sum(v);
+    v = MAX ? warp_max<REDUX>(v) : warp_sum(v);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane == 0) slot[warp] = v;
     __syncthreads();
@@ -998,9 +1009,10 @@ __global__ void __launch_bounds__(WMAX * 32, 1)
                      const __grid_constant__ CUtensorMap mr) {
     constexpr int VE = 32 / TI::kBytes;
     constexpr int XVB = VE * TX::kBytes;  // bytes of one x vector
-    // per-token FP8 rows take one element per instruction here: measured on
-    // GB300, the paired fp32 forms made this kernel's long FP8 launches 1-5%
-    // slower (while they speed up every other output and the short rows)
+    // per-token FP8 rows take one element per instruction and the butterfly
+    // row max here: measured on GB300, the paired fp32 forms and the redux
+    // max made this kernel's long FP8 launches 1-5% slower (while they speed
+    // up every other output and the short rows)
     constexpr bool PACK = !std::is_same<TO, FP8>::value;
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full[kMaxStages];
@@ -1087,7 +1099,7 @@ __global__ void __launch_bounds__(WMAX * 32, 1)
         float* slot = red[2 + parity];
         scale_store<TI, TO, CH, BIAS, (WMAX <= 16 && CH * VE <= 32), PACK>(
             a, row, rbase, G, t, inv, hv, wv, bv,
-            [&](float m) { return block_allreduce<true>(m, slot); });
+            [&](float m) { return block_allreduce<true, PACK>(m, slot); });
         parity ^= 1;
     }
     if (abort_flag && t == 0) {
