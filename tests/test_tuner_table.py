@@ -1,0 +1,106 @@
+"""The tuner's selector-table writer, on the CPU: among launches within 1% of
+the fastest it keeps the one with fewer warps, then the register kernel, then
+fewer ring stages, and never the generic kernel; merging replaces only the
+dtype pairs it measured; and the C++ lookup it writes, compiled with the host
+compiler, returns the row with the largest token threshold not above the
+token count, and nothing for a hidden size or dtype pair it has no rows for."""
+import re
+import shutil
+import subprocess
+
+import pytest
+
+from residual_add_rmsnorm_vec_gb300 import tune
+
+ROW = re.compile(r"\s*\{(-?\d+), (-?\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)\},")
+
+
+def cand(variant, warps, us, chunks=2, max_warps=16, stages=0):
+    return {"variant": variant, "chunks": chunks, "warps_per_block": warps,
+            "max_warps": max_warps, "stages": stages, "us": us, "gbs": 1e3 / us}
+
+
+def entry(T, H, cands, i="bf16", o="bf16"):
+    return {"T": T, "H": H, "in": i, "out": o, "res": True, "bias": False,
+            "best": min(cands, key=lambda d: d["us"]), "all": cands}
+
+
+def rows_of(path):
+    with open(path) as f:
+        return [tuple(int(v) for v in m.groups()) for m in map(ROW.match, f) if m]
+
+
+def test_tie_break_prefers_fewer_warps_then_register_kernel_then_fewer_stages(tmp_path):
+    bf = tune.DTYPE_CODES["bf16"]
+    entries = [
+        # the ring at 8 warps is fastest; the register kernel at 8 warps is
+        # within 1% and wins the tie; 4 warps is 1.2% slower and stays out;
+        # the generic kernel is never taken
+        entry(1, 4096, [cand(2, 8, 100.0, stages=4), cand(1, 8, 100.5), cand(1, 4, 101.2),
+                        cand(3, 2, 100.2)]),
+        # two rings within 1%: the one with fewer stages
+        entry(16, 4096, [cand(2, 4, 50.0, stages=6), cand(2, 4, 50.3, stages=2)]),
+        # fewer warps beat the fastest when within 1%
+        entry(256, 4096, [cand(1, 16, 10.0, max_warps=16), cand(1, 8, 10.09, max_warps=8)]),
+    ]
+    path = tmp_path / "t.inc"
+    tune.write_table(entries, str(path))
+    got = {r[3]: r[4:] for r in rows_of(path) if r[:3] == (bf, bf, 4096)}
+    assert got[1] == (1, 2, 16, 0)
+    assert got[16] == (2, 2, 16, 2)
+    assert got[256] == (1, 2, 8, 0)
+
+
+def test_merge_replaces_only_the_measured_pairs(tmp_path):
+    c = tune.DTYPE_CODES
+    path = tmp_path / "t.inc"
+    tune.write_table([entry(1, 4096, [cand(1, 8, 3.0)]),
+                      entry(1, 4096, [cand(1, 4, 4.0)], o="fp8"),
+                      entry(4096, 4096, [cand(2, 8, 30.0, stages=4)], o="fp8")], str(path))
+    before = rows_of(path)
+    tune.merge_table([entry(1, 4096, [cand(1, 16, 3.5)], o="fp8")], str(path))
+    after = rows_of(path)
+    assert [r for r in after if r[1] == c["bf16"]] == [r for r in before if r[1] == c["bf16"]]
+    fp8 = [r for r in after if r[1] == c["fp8"]]
+    assert fp8 == [(c["bf16"], c["fp8"], 4096, 1, 1, 2, 16, 0)]
+
+
+HARNESS = r"""
+#include <cstdint>
+#include <cstdio>
+#include "t.inc"
+int main() {
+    const long long q[][4] = {{1, 1, 4096, 1}, {1, 1, 4096, 15}, {1, 1, 4096, 16},
+                              {1, 1, 4096, 255}, {1, 1, 4096, 1000000}, {1, 1, 5120, 64},
+                              {1, 2, 4096, 64}};
+    for (auto& x : q) {
+        int v = -1, c = -1, w = -1, s = -1;
+        const bool f = table_lookup((int)x[0], (int)x[1], x[2], x[3], &v, &c, &w, &s);
+        std::printf("%d %d %d %d %d\n", f ? 1 : 0, v, c, w, s);
+    }
+    return 0;
+}
+"""
+
+
+@pytest.mark.skipif(shutil.which("g++") is None, reason="no host C++ compiler")
+def test_generated_lookup_takes_the_largest_threshold_not_above_the_tokens(tmp_path):
+    tune.write_table([entry(1, 4096, [cand(1, 8, 2.0, max_warps=8)]),
+                      entry(16, 4096, [cand(1, 16, 2.5, max_warps=16)]),
+                      entry(256, 4096, [cand(2, 8, 9.0, stages=4, max_warps=32)])],
+                     str(tmp_path / "t.inc"))
+    (tmp_path / "h.cpp").write_text(HARNESS)
+    subprocess.run(["g++", "-std=c++17", "-O1", "-o", str(tmp_path / "h"), str(tmp_path / "h.cpp")],
+                   check=True, cwd=tmp_path)
+    out = subprocess.run([str(tmp_path / "h")], check=True, capture_output=True,
+                         text=True).stdout.split("\n")
+    got = [tuple(int(v) for v in line.split()) for line in out if line.strip()]
+    assert got == [
+        (1, 1, 2, 8, 0),    # 1 token: the row from 1 up
+        (1, 1, 2, 8, 0),    # 15 tokens: still the row from 1
+        (1, 1, 2, 16, 0),   # 16 tokens: the row from 16
+        (1, 1, 2, 16, 0),   # 255 tokens
+        (1, 2, 2, 32, 4),   # far above the last threshold: its row
+        (0, -1, -1, -1, -1),  # a hidden size without rows
+        (0, -1, -1, -1, -1),  # a dtype pair without rows
+    ]
