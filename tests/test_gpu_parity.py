@@ -424,12 +424,13 @@ def test_selector_decode_vs_prefill(pkg):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     # a hidden size without measured rows: the decode rule (one warp per block
     # while the problem needs fewer warps than there are SMs), else multi-warp
-    c = pkg.rmsnorm_query_config(8, 3072, flags)
+    c = pkg.rmsnorm_query_config(8, 2560, flags)
     assert c.variant == pkg.VARIANT_WARP_ROWS and c.warps_per_block == 1 and c.num_sms == sms
-    c = pkg.rmsnorm_query_config(4096, 3072, flags)
+    c = pkg.rmsnorm_query_config(4096, 2560, flags)
     assert c.variant == pkg.VARIANT_BLOCK_ROW and c.warps_per_block > 1
     # measured shapes: whatever the table picked is a valid built configuration
-    for T, H in ((1, 4096), (8, 4096), (256, 4096), (16384, 8192), (4096, 16384)):
+    for T, H in ((1, 4096), (8, 4096), (256, 4096), (16384, 8192), (4096, 16384), (8, 3072),
+                 (4096, 6144), (16384, 7168)):
         c = pkg.rmsnorm_query_config(T, H, flags)
         assert any(_same_shape(c, o) for o in pkg.rmsnorm_list_configs(T, H, flags)), (T, H)
         assert 1 <= c.grid <= max(T, 1)
