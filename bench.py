@@ -70,10 +70,17 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# The measured selector table only picks launch shapes; a recorded capture is
+# keyed by the full launch shape instead, so the table is not part of the hash.
+SELECTION_DATA = ("rmsn_selector_table.inc",)
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "residual_add_rmsnorm_vec_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
+        if fn in SELECTION_DATA:
+            continue
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
@@ -302,7 +309,8 @@ def run_ours(args):
 
     peak, peak_src = load_peaks()
     achieved = bytes_step / (kernel_ms / 1e3) / 1e9
-    vkey = f"{pkg.VARIANT_NAMES[cfg.variant]}_ch{cfg.chunks}_w{cfg.warps_per_block}_T{T}_H{H}"
+    vkey = (f"{pkg.VARIANT_NAMES[cfg.variant]}_ch{cfg.chunks}_w{cfg.warps_per_block}"
+            f"_st{cfg.stages}_g{cfg.grid}_T{T}_H{H}")
     if fp8:
         vkey += "_fp8"
     line = {

@@ -5,6 +5,7 @@ reported while the kernel sources still match the capture; the workload of
 the timed step follows --out."""
 import json
 import os
+import shutil
 import subprocess
 import sys
 
@@ -63,6 +64,21 @@ def test_recorded_traffic_follows_the_sources(tmp_path, monkeypatch):
     assert bench.recorded_traffic("k_T1_H1") == 123
     assert bench.recorded_traffic("stale") is None
     assert bench.recorded_traffic("absent") is None
+
+
+def test_source_hash_leaves_out_only_the_selector_table(tmp_path, monkeypatch):
+    # a recorded capture stays valid when only the measured selector table
+    # changes (the record is keyed by the full launch shape), not when a
+    # kernel source does
+    csrc = tmp_path / "residual_add_rmsnorm_vec_gb300" / "csrc"
+    shutil.copytree(os.path.join(ROOT, "residual_add_rmsnorm_vec_gb300", "csrc"), csrc)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_source_hash()
+    (csrc / "rmsn_selector_table.inc").write_text("// other rows\n")
+    assert bench.kernel_source_hash() == h0
+    k = csrc / "rmsn_kernels.cuh"
+    k.write_text(k.read_text() + "\n// changed\n")
+    assert bench.kernel_source_hash() != h0
 
 
 def test_step_workload_follows_out():
