@@ -161,16 +161,18 @@ def sweep(pkg, shapes, in_dt, out_dt, res, bias, reps, l2_hot_below=0):
 
 
 def merge_table(entries, path):
-    """Replace, in the table at `path`, the rows of the (input, output) dtype
-    pairs measured in `entries` and keep every other row."""
+    """Replace, in the table at `path`, the rows of each (input dtype, output
+    dtype, hidden) measured in `entries` and keep every other row, so a sweep
+    of some hidden sizes leaves the rows of the others in place."""
     import re
 
-    measured = {(DTYPE_CODES[e["in"]], DTYPE_CODES[e["out"]]) for e in entries}
+    measured = {(DTYPE_CODES[e["in"]], DTYPE_CODES[e["out"]], e["H"]) for e in entries}
     kept = []
     for line in open(path):
         m = re.match(r"\s*\{(-?\d+), (-?\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)\},"
                      r"(?:\s*// ([\d.]+) us, ([\d.]+) GB/s)?", line)
-        if m and (int(m.group(1)), int(m.group(2))) not in measured and int(m.group(1)) >= 0:
+        key = m and (int(m.group(1)), int(m.group(2)), int(m.group(3)))
+        if m and key not in measured and int(m.group(1)) >= 0:
             v = [int(m.group(i)) for i in range(1, 9)]
             kept.append(tuple(v[:4]) + tuple(v[4:8]) + (None, None,
                         float(m.group(9) or 0), float(m.group(10) or 0)))

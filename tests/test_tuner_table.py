@@ -1,7 +1,7 @@
 """The tuner's selector-table writer, on the CPU: among launches within 1% of
 the fastest it keeps the one with fewer warps, then the register kernel, then
 fewer ring stages, and never the generic kernel; merging replaces only the
-dtype pairs it measured; and the C++ lookup it writes, compiled with the host
+(dtype pair, hidden) rows it measured; and the C++ lookup it writes, compiled with the host
 compiler, returns the row with the largest token threshold not above the
 token count, and nothing for a hidden size or dtype pair it has no rows for."""
 import re
@@ -51,17 +51,21 @@ def test_tie_break_prefers_fewer_warps_then_register_kernel_then_fewer_stages(tm
     assert got[256] == (1, 2, 8, 0)
 
 
-def test_merge_replaces_only_the_measured_pairs(tmp_path):
+def test_merge_replaces_only_the_measured_hidden_sizes(tmp_path):
     c = tune.DTYPE_CODES
     path = tmp_path / "t.inc"
     tune.write_table([entry(1, 4096, [cand(1, 8, 3.0)]),
                       entry(1, 4096, [cand(1, 4, 4.0)], o="fp8"),
-                      entry(4096, 4096, [cand(2, 8, 30.0, stages=4)], o="fp8")], str(path))
+                      entry(4096, 4096, [cand(2, 8, 30.0, stages=4)], o="fp8"),
+                      entry(1, 5120, [cand(1, 4, 4.5)], o="fp8")], str(path))
     before = rows_of(path)
     tune.merge_table([entry(1, 4096, [cand(1, 16, 3.5)], o="fp8")], str(path))
     after = rows_of(path)
+    # another dtype pair, and another hidden size of the measured pair, stay
     assert [r for r in after if r[1] == c["bf16"]] == [r for r in before if r[1] == c["bf16"]]
-    fp8 = [r for r in after if r[1] == c["fp8"]]
+    assert [r for r in after if r[2] == 5120] == [r for r in before if r[2] == 5120]
+    # the measured (pair, hidden) is replaced whole: its 4096-token row goes
+    fp8 = [r for r in after if r[1] == c["fp8"] and r[2] == 4096]
     assert fp8 == [(c["bf16"], c["fp8"], 4096, 1, 1, 2, 16, 0)]
 
 
