@@ -20,8 +20,9 @@
  * h, the value stored in residual_out.
  *
  * Ownership: every buffer belongs to the caller.  The library allocates no
- * device memory; it keeps a small per-device table of attributes (SM count)
- * that is filled on the first call on each device.  All calls are asynchronous
+ * device memory; it keeps per-device host-side caches (device attributes such
+ * as the SM count, occupancy, and the launch chosen for each problem shape),
+ * filled on first use and keyed exactly.  All calls are asynchronous
  * on `stream` (NULL = the legacy default stream) and thread-safe.
  *
  * Errors: argument errors are returned before anything is launched; a launch
