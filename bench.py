@@ -214,6 +214,18 @@ def step_workload(synth, args, n_tokens):
     return synth.prefill_workload(n_tokens, args.hidden)
 
 
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal (the ~8 TB/s the prefill gate is stated against)
+
+
+def step_config(wl, world: int) -> dict:
+    """The `config` object of the JSON line: the workload only, with the same
+    keys and values in both arms (timing details and the launch shape go in
+    their own keys)."""
+    return {"workload": workload_name(wl), "n_tokens": wl.n_tokens, "hidden": wl.hidden,
+            "global_batch_tokens": wl.n_tokens * world,
+            "parallelism": f"rows sharded, {world} independent replica(s)"}
+
+
 def workload_name(wl) -> str:
     if wl.out_dtype == "fp8":
         return (f"fused residual-add + RMSNorm bf16 -> per-token FP8 E4M3 with bias "
@@ -309,6 +321,7 @@ def run_ours(args):
 
     peak, peak_src = load_peaks()
     achieved = bytes_step / (kernel_ms / 1e3) / 1e9
+    box_peak = copy_peak_same_box(dev)
     vkey = (f"{pkg.VARIANT_NAMES[cfg.variant]}_ch{cfg.chunks}_w{cfg.warps_per_block}"
             f"_st{cfg.stages}_g{cfg.grid}_T{T}_H{H}")
     if fp8:
@@ -329,20 +342,22 @@ def run_ours(args):
                  "bias = 0.01 N(0,1)") if fp8 else
                 ("synthetic, seeded: x ~ N(0,1) with 1% outlier channels x50, residual ~ N(0,4), "
                  "weight = 1 + 0.1 N(0,1)"),
-        "config": {"workload": workload_name(wl),
-                   "n_tokens": T, "hidden": H, "global_batch_tokens": T * world,
-                   "parallelism": f"rows sharded, {world} independent replica(s)",
-                   "l2": (f"inputs larger than L2 ({2 * T * H * 2 / 2**20:.0f} MiB read per step "
-                          f"vs {L2_BYTES / 1e6:.0f} MB L2), no flush") if n_sets == 1 else
-                         (f"{n_sets} rotating buffer sets of {bytes_step / 2**20:.0f} MiB per step "
-                          f"({n_sets * bytes_step / 2**20:.0f} MiB vs {L2_BYTES / 1e6:.0f} MB "
-                          f"L2), no flush"),
-                   "launch": dict(cfg.as_dict(), pdl=not args.no_pdl)},
+        "config": step_config(wl, world),
+        "l2": (f"inputs larger than L2 ({2 * T * H * 2 / 2**20:.0f} MiB read per step "
+               f"vs {L2_BYTES / 1e6:.0f} MB L2), no flush") if n_sets == 1 else
+              (f"{n_sets} rotating buffer sets of {bytes_step / 2**20:.0f} MiB per step "
+               f"({n_sets * bytes_step / 2**20:.0f} MiB vs {L2_BYTES / 1e6:.0f} MB "
+               f"L2), no flush"),
+        "launch": dict(cfg.as_dict(), pdl=not args.no_pdl),
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": K,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "frac_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "peak_nominal": NOMINAL_HBM_GBS,
+                     "peak_same_box": round(box_peak, 1),
+                     "frac_same_box": round(achieved / box_peak, 4),
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                      else "fallback 6.8 TB/s",
                      "traffic": recorded_traffic(vkey),
@@ -363,6 +378,30 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
+
+
+def copy_peak_same_box(dev) -> float:
+    """HBM copy bandwidth on this GPU, now: torch copy_ of 1 Gi bf16 elements,
+    read + write bytes, best of 10 (the method of the measured-peaks record,
+    repeated here so the kernel can also be put against its own box)."""
+    import torch
+
+    n = 1 << 30
+    a = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    b = torch.empty_like(a)
+    a.fill_(1.0)
+    best = float("inf")
+    for _ in range(12):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        b.copy_(a)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        best = min(best, e0.elapsed_time(e1))
+    del a, b
+    torch.cuda.empty_cache()
+    return 2 * n * 2 / (best / 1e3) / 1e9
 
 
 def run_e2e(pkg, wl, host, dev, stream, flags, steps, pg):
@@ -449,6 +488,26 @@ def run_e2e(pkg, wl, host, dev, stream, flags, steps, pg):
                        "api": "cudaMemcpyAsync in, rmsnorm_fwd, cudaMemcpyAsync out"}}
 
 
+def host_cost_c(T: int, H: int, n: int = 3000, extra_flags: int = 0) -> dict:
+    """The library's host cost per rmsnorm_fwd call, and an empty kernel's,
+    both timed in a C loop (the bench's harness library; no Python in the
+    loop): host enqueue time and GPU time per call, back to back."""
+    import ctypes
+
+    from residual_add_rmsnorm_vec_gb300 import build
+
+    lib = ctypes.CDLL(build.HOSTCOST_PATH)
+    lib.rmsn_host_cost.restype = ctypes.c_int
+    lib.rmsn_host_cost.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32,
+                                   ctypes.POINTER(ctypes.c_double)]
+    out = (ctypes.c_double * 4)()
+    st = lib.rmsn_host_cost(T, H, n, extra_flags, out)
+    if st != 0:
+        raise RuntimeError(f"rmsn_host_cost failed with {st}")
+    return {"empty_host_us": round(out[0], 3), "empty_gpu_us": round(out[1], 3),
+            "lib_host_us": round(out[2], 3), "lib_gpu_us": round(out[3], 3)}
+
+
 def run_decode(pkg, synth, dev, stream):
     """us per call at decode sizes (inputs L2-resident), back-to-back and in a
     CUDA graph, and the same for an empty kernel (torch.cuda._sleep(0)) and,
@@ -523,6 +582,23 @@ def run_decode(pkg, synth, dev, stream):
         us = timeit(call, n)
         gus = graph_time(call)
         gus_pdl = graph_time(call_pdl)
+        # the split-row cluster variant, each built cluster size, in graphs
+        clusters = {}
+        for c in pkg.rmsnorm_list_configs(T, 4096, flags):
+            if c.variant != pkg.VARIANT_CLUSTER:
+                continue
+
+            def call_c(fl=flags, c=c):
+                st = pkg.rmsnorm_fwd_ex(*ptrs, T, 4096, wl.eps, fl, 0.0, c,
+                                        torch.cuda.current_stream().cuda_stream)
+                if st != pkg.RMSN_OK:
+                    raise pkg.RmsnError(st, "rmsnorm_fwd_ex")
+
+            clusters[f"k{c.cluster}_ch{c.chunks}"] = {
+                "graph_us": round(graph_time(call_c), 3),
+                "graph_pdl_us": round(graph_time(
+                    lambda c=c: call_c(flags | pkg.RMSN_PDL | pkg.RMSN_PDL_EARLY_PARAMS, c)), 3)}
+        hc = host_cost_c(T, 4096)
         # floor for comparison: torch's elementwise add of the same x and r
         # (reads both, writes one tensor; no reduction), in a graph likewise
         gus_add = graph_time(lambda: torch.add(x, r, out=out))
@@ -530,10 +606,16 @@ def run_decode(pkg, synth, dev, stream):
         per_t[str(T)] = {"us": round(us, 3), "graph_us": round(gus, 3),
                          "graph_pdl_us": round(gus_pdl, 3),
                          "torch_add_graph_us": round(gus_add, 3),
+                         "host_us_c": hc["lib_host_us"], "gpu_us_c": hc["lib_gpu_us"],
+                         "cluster": clusters,
                          "gbs_l2_hot": round(wl.algorithmic_bytes() / (us * 1e-6) / 1e9, 1),
                          "launch": f"{pkg.VARIANT_NAMES[cfg.variant]} ch{cfg.chunks} "
                                    f"w{cfg.warps_per_block} grid{cfg.grid}"}
     res["tokens"] = per_t
+    # an empty kernel launched from the same C loop (host cost, GPU time per launch)
+    hc = host_cost_c(1, 4096)
+    res["empty_kernel_host_us_c"] = hc["empty_host_us"]
+    res["empty_kernel_gpu_us_c"] = hc["empty_gpu_us"]
     res["gate"] = "us/call <= 2x empty-kernel launch"
     res["within_2x_launch"] = all(v["us"] <= 2 * res["empty_kernel_us"] for v in per_t.values())
     res["within_2x_launch_graph"] = all(v["graph_us"] <= 2 * res["empty_kernel_graph_us"]
@@ -823,7 +905,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic, seeded",
-        "config": {"workload": workload_name(wl), "n_tokens": T, "hidden": H},
+        "config": step_config(wl, args.gpus),
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores,
                          "kind": "oracle", "sample": sample_txt},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,

@@ -90,9 +90,13 @@ typedef enum {
                                    tensor copies where a row is whole 1 KiB units of at most
                                    32 KiB, else 1-D bulk copies */
     RMSN_VARIANT_GENERIC = 3,   /* any hidden size / alignment (element-wise, three passes) */
-    RMSN_VARIANT_RAGGED = 4     /* rows off the 32-byte grid, same dtype in and out, all row
+    RMSN_VARIANT_RAGGED = 4,    /* rows off the 32-byte grid, same dtype in and out, all row
                                    pointers equally aligned mod 16 bytes: 16-byte vectors for
                                    the row's interior, single elements for head and tail */
+    RMSN_VARIANT_CLUSTER = 5    /* decode: each row split over a thread-block cluster of
+                                   `cluster` one-warp blocks that exchange partial sums of
+                                   squares through distributed shared memory (bf16 / fp16 /
+                                   fp32 in with the same dtype out, not FP8) */
 } rmsn_variant;
 
 /* One launch configuration. */
@@ -109,6 +113,8 @@ typedef struct {
     int32_t num_sms;         /* SMs of the device the config was made for */
     int32_t ring_copy;       /* bulk variant: 2 = swizzled 2-D tensor copies, 1 = 1-D bulk
                                 copies; 0 for the other variants (output only) */
+    int32_t cluster;         /* cluster variant: blocks per row (its max_warps); else 0
+                                (output only) */
 } rmsn_config;
 
 /*
@@ -165,7 +171,10 @@ int rmsnorm_fwd_ex(const void* x, const void* residual, const void* weight, cons
  *     An all-zero block stores code 0 and zero codes.
  *   NVFP4: token_scale[t] = g = max|row| / (448 * 6) (fp32); per block of 16
  *     elements E4M3 scale c_b = RN_sat(max|block| / (6 g)) in
- *     block_scale[T, hidden/16]; codes E2M1 RN_sat(y / (c_b g)).
+ *     block_scale[T, hidden/16]; codes E2M1 RN_sat(y * r_b), where r_b is
+ *     1 / (c_b g) to within 1 fp32 ulp (a hardware reciprocal), so a code can
+ *     be one step from RN_sat(y / (c_b g)) when that quotient lies within a
+ *     few fp32 ulp of an E2M1 rounding midpoint.
  *
  * out is [T, hidden] bytes (MXFP8) or [T, hidden/2] bytes (FP4, element 2j
  * in the low nibble).  Rounding is to nearest even with saturation.  flags
@@ -186,11 +195,12 @@ int rmsnorm_fwd_blockscaled(const void* x, const void* residual, const void* wei
  * residual_out and out_scale back to host memory, with no staging buffer and
  * no allocation (on Grace-Blackwell the link is the coherent NVLink-C2C).
  *
- * Each pointer may be device or managed memory, page-locked host memory
- * (cudaHostAlloc, cudaMallocHost, cudaHostRegister, torch pin_memory), or
- * ordinary pageable host memory when the device reports pageable-memory
- * access (cudaDevAttrPageableMemoryAccess); any mix is allowed.  A pointer
- * the device cannot reach returns RMSN_EINVAL before any launch.  Only the
+ * Each pointer may be device memory of the current device, managed memory,
+ * page-locked host memory (cudaHostAlloc, cudaMallocHost, cudaHostRegister,
+ * torch pin_memory), or ordinary pageable host memory when the device
+ * reports pageable-memory access (cudaDevAttrPageableMemoryAccess); any mix
+ * is allowed.  A pointer the device cannot reach, including device memory of
+ * another GPU, returns RMSN_EINVAL before any launch.  Only the
  * register-streaming kernels run here (plain loads and stores), shaped for
  * the link's latency: one block per row, one 32-byte vector per thread where
  * the row allows it.  The call is asynchronous on `stream`: host outputs are
@@ -250,6 +260,20 @@ int rmsnorm_list_configs(int64_t n_tokens, int64_t hidden, uint32_t flags, rmsn_
  * the word.  Returns an rmsn_status.
  */
 int rmsnorm_read_status(uint32_t* status, int clear);
+
+/*
+ * Testing hook for the bounded waits of the bulk-copy variant (not needed in
+ * normal use).  Sets, for launches that follow on the current device, how
+ * many SM clock cycles a block waits for a row to arrive in shared memory
+ * before it gives up: it then sets bit 0 of the status word, leaves the
+ * remaining rows unwritten (the row it was waiting for may have a partly
+ * written residual_out and no output), waits with the default bound for the
+ * copies it has in flight, and returns.  0 restores the default (about one
+ * second); a negative value makes each wait test the row's barrier once and
+ * not wait at all, so that the give-up path runs on a healthy GPU.  Returns
+ * an rmsn_status.
+ */
+int rmsnorm_set_wait_limit(int64_t cycles);
 
 /* Human-readable name of an rmsn_status. */
 const char* rmsnorm_status_string(int status);

@@ -10,7 +10,11 @@ import ctypes
 import os
 import threading
 
-from .build import LIB_PATH
+from .build import LIB_PATH as _DEFAULT_LIB
+
+# RMSNORM_GB300_LIB names another build of the library to load instead (the
+# bounds-checked debug build, for instance); by default the in-tree one.
+LIB_PATH = os.environ.get("RMSNORM_GB300_LIB") or _DEFAULT_LIB
 
 RMSN_OK = 0
 RMSN_EINVAL = -1
@@ -37,7 +41,9 @@ VARIANT_BLOCK_ROW = 1
 VARIANT_BULK_ROW = 2
 VARIANT_GENERIC = 3
 VARIANT_RAGGED = 4
-VARIANT_NAMES = {0: "warp_rows", 1: "block_row", 2: "bulk_row", 3: "generic", 4: "ragged"}
+VARIANT_CLUSTER = 5
+VARIANT_NAMES = {0: "warp_rows", 1: "block_row", 2: "bulk_row", 3: "generic", 4: "ragged",
+                 5: "cluster"}
 
 RMSN_FMT_MXFP8 = 1
 RMSN_FMT_MXFP4 = 2
@@ -48,14 +54,14 @@ BLOCK_FORMATS = {"mxfp8": (RMSN_FMT_MXFP8, 32, 1), "mxfp4": (RMSN_FMT_MXFP4, 32,
 EXPORTED = ("rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_fwd_blockscaled", "rmsnorm_fwd_host",
             "rmsnorm_qk_fwd",
             "rmsnorm_query_config", "rmsnorm_list_configs", "rmsnorm_read_status",
-            "rmsnorm_status_string")
+            "rmsnorm_set_wait_limit", "rmsnorm_status_string")
 
 
 class RmsnConfig(ctypes.Structure):
     """Mirror of ``rmsn_config``."""
     _fields_ = [(n, ctypes.c_int32) for n in (
         "variant", "vec_bytes", "warps_per_block", "warps_per_row", "chunks", "max_warps",
-        "stages", "grid", "smem_bytes", "num_sms", "ring_copy")]
+        "stages", "grid", "smem_bytes", "num_sms", "ring_copy", "cluster")]
 
     def as_dict(self) -> dict:
         d = {n: int(getattr(self, n)) for n, _ in self._fields_}
@@ -118,6 +124,8 @@ def load() -> ctypes.CDLL:
                                                  ctypes.c_int]
             lib.rmsnorm_read_status.restype = ctypes.c_int
             lib.rmsnorm_read_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
+            lib.rmsnorm_set_wait_limit.restype = ctypes.c_int
+            lib.rmsnorm_set_wait_limit.argtypes = [i64]
             lib.rmsnorm_status_string.restype = ctypes.c_char_p
             lib.rmsnorm_status_string.argtypes = [ctypes.c_int]
             _lib = lib
@@ -202,3 +210,10 @@ def rmsnorm_read_status(clear: bool = False) -> int:
     if st != RMSN_OK:
         raise RmsnError(st, "rmsnorm_read_status")
     return int(v.value)
+
+
+def rmsnorm_set_wait_limit(cycles: int) -> int:
+    """Testing hook: the bound of the bulk-copy kernel's row waits on the
+    current device (0 = the default; negative = test each barrier once and
+    do not wait)."""
+    return int(load().rmsnorm_set_wait_limit(int(cycles)))

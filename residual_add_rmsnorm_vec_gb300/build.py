@@ -4,6 +4,13 @@ Each kernel translation unit is compiled by its own nvcc process in parallel,
 then linked with the C-ABI unit into one shared library that exports only
 the ``rmsnorm_*`` symbols of ``include/rmsnorm.h``.  The CUDA runtime is
 linked statically, so the library needs nothing but the driver at run time.
+
+``build(checked=True)`` makes the bounds-checked debug library
+(``_build/librmsnorm_gb300_checked.so``, compiled with -DRMSNORM_BOUNDS_CHECK):
+every global access and ring copy of its kernels is checked against its
+tensor's extent, and one out of range is skipped and reported in bit 1 of the
+status word.  Point the binding at it with the environment variable
+RMSNORM_GB300_LIB.
 """
 from __future__ import annotations
 
@@ -21,6 +28,10 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "librmsnorm_gb300.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
+CHECKED_PATH = os.path.join(BUILD_DIR, "librmsnorm_gb300_checked.so")
+# the bench's C timing harness (not part of the library)
+HOSTCOST_SRC = os.path.join(PKG, "bench_src", "host_cost.cu")
+HOSTCOST_PATH = os.path.join(BUILD_DIR, "librmsn_hostcost.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler",
@@ -44,25 +55,31 @@ def _inputs() -> list[str]:
             + [os.path.abspath(__file__)])
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(checked: bool = False) -> bool:
+    outs = [CHECKED_PATH] if checked else [LIB_PATH, HOSTCOST_PATH]
+    if not all(os.path.exists(o) for o in outs):
         return False
-    t = os.path.getmtime(LIB_PATH)
-    return all(os.path.getmtime(f) <= t for f in _inputs())
+    t = min(os.path.getmtime(o) for o in outs)
+    return all(os.path.getmtime(f) <= t for f in _inputs() + [HOSTCOST_SRC])
 
 
-def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -> str:
-    """Compile and link the library if a source is newer than it; return its path."""
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, jobs: int | None = None,
+          checked: bool = False) -> str:
+    """Compile and link the library (the bounds-checked one with ``checked``)
+    if a source is newer than it; return its path."""
+    out = CHECKED_PATH if checked else LIB_PATH
+    if not force and up_to_date(checked):
+        return out
+    obj_dir = os.path.join(BUILD_DIR, "checked") if checked else BUILD_DIR
+    os.makedirs(obj_dir, exist_ok=True)
     cc = nvcc()
     srcs = sources()
-    objs = [os.path.join(BUILD_DIR, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [os.path.join(obj_dir, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    extra = ["-DRMSNORM_BOUNDS_CHECK"] if checked else []
 
     def compile_one(pair):
         src, obj = pair
-        cmd = [cc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+        cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -76,14 +93,25 @@ def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -
     if verbose:
         for src, log in zip(srcs, logs):
             sys.stderr.write(f"== {os.path.basename(src)}\n{log}")
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = out + f".tmp{os.getpid()}"
     link = [cc, *ARCH, "-shared", "-cudart", "static", *objs, "-o", tmp]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
+    os.replace(tmp, out)
+    if checked:
+        return out
+    # the C timing harness, linked against the library it times
+    tmp = HOSTCOST_PATH + f".tmp{os.getpid()}"
+    cmd = [cc, *ARCH, *NVCC_FLAGS, "-shared", "-cudart", "static", HOSTCOST_SRC, "-o", tmp,
+           "-L", BUILD_DIR, "-lrmsnorm_gb300", "-Xlinker", "-rpath,$ORIGIN"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"host-cost harness failed to build:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, HOSTCOST_PATH)
     return LIB_PATH
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                checked="--checked" in sys.argv))

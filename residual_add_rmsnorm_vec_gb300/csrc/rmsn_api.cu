@@ -18,6 +18,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <unordered_map>
 #include <utility>
@@ -44,8 +45,9 @@ struct SelKey {
     int64_t T, H;
     uint32_t flags;
     int paths;  // bit 0: vector path, bit 1: ragged-row path
+    int fmt;    // block-scaled output format (0: the output dtype of `flags`)
     bool operator==(const SelKey& o) const {
-        return T == o.T && H == o.H && flags == o.flags && paths == o.paths;
+        return T == o.T && H == o.H && flags == o.flags && paths == o.paths && fmt == o.fmt;
     }
 };
 struct OccKey {
@@ -61,7 +63,8 @@ inline uint64_t mix(uint64_t h, uint64_t v) {
 }
 struct SelKeyHash {
     size_t operator()(const SelKey& k) const {
-        return (size_t)mix(mix(mix((uint64_t)k.T, (uint64_t)k.H), k.flags), (uint64_t)k.paths);
+        return (size_t)mix(mix(mix(mix((uint64_t)k.T, (uint64_t)k.H), k.flags), (uint64_t)k.paths),
+                           (uint64_t)k.fmt);
     }
 };
 struct OccKeyHash {
@@ -71,12 +74,23 @@ struct OccKeyHash {
     }
 };
 
+// A ring tensor map is a pure function of (base address, rows, row length,
+// element size): a cached map is reused whenever all four match.
+struct MapEntry {
+    const void* base = nullptr;
+    int64_t T = 0, H = 0;
+    int bytes = 0;
+    CUtensorMap map;  // the type carries its own alignment
+};
+constexpr int kMapCache = 32;
+
 struct DeviceInfo {
     std::once_flag once;
     int num_sms = 0;
     int max_smem = 0;              // opt-in dynamic shared memory per block
     int pageable_access = 0;       // device can read and write pageable host memory
     uint32_t* status = nullptr;    // device address of g_status on this device
+    std::atomic<int64_t> wait_cycles{kDefaultWaitCycles};  // ring wait bound (tests may lower it)
     cudaError_t err = cudaSuccess;
     std::mutex mu;
     std::vector<std::pair<const void*, int>> smem_set;  // kernel -> raised dynamic smem limit
@@ -84,6 +98,9 @@ struct DeviceInfo {
     std::unordered_map<OccKey, int, OccKeyHash> occ_cache;
     // selector results: (tokens, hidden, flags, vector path) -> configuration
     std::unordered_map<SelKey, std::pair<rmsn_config, const KernelEntry*>, SelKeyHash> sel_cache;
+    // tensor maps of the ring kernel's 2-D copies, replaced round-robin
+    MapEntry maps[kMapCache];
+    int map_next = 0;
 };
 
 DeviceInfo g_dev[kMaxDevices];
@@ -322,6 +339,22 @@ bool shape_config(const Problem& p, const KernelEntry& e, DeviceInfo* d, int gri
         c->warps_per_row = w;
         threads = w * 32;
         units = p.T;
+    } else if (e.variant == kCluster) {
+        // one row per cluster of K one-warp blocks; the row's vectors fill
+        // CH chunks of K * 32 lanes (and would not fit half as many)
+        const int K = e.max_warps;
+        if (p.nvec > 32 * K * e.chunks) return false;
+        if (e.chunks > 1 && p.nvec <= 32 * K * (e.chunks / 2)) return false;
+        if (p.T > (int64_t)(INT32_MAX / K)) return false;
+        c->vec_bytes = 32;
+        c->warps_per_block = 1;
+        c->warps_per_row = K;
+        c->cluster = K;
+        threads = 32;
+        units = p.T * K;
+        if (blocks_per_sm(d, e.fn, threads, 0) < 1) return false;
+        c->grid = (int32_t)units;  // every row its own cluster, not limited to one wave
+        return true;
     } else if (e.variant == kWarpRows) {
         if (p.nvec > 32 * e.chunks) return false;
         if (e.chunks > 1 && p.nvec <= 32 * (e.chunks / 2)) return false;  // a smaller CH fits
@@ -370,9 +403,21 @@ constexpr int kTableF16R32 = 8;
 
 #include "rmsn_selector_table.inc"
 
-// The selector (see the file comment): the measured table first, then the
-// decode rule (one warp per block while the whole problem needs no more warps
-// than there are SMs), then the fixed prefill rule (fewest warps with CH <= 2).
+bool select_rules(const Problem& p, DeviceInfo* d, rmsn_config* c);
+
+// Launch of a table row's shape for this problem, if it is built and fits.
+bool table_shape(const Problem& p, DeviceInfo* d, int variant, int ch, int wmax, int stages,
+                 rmsn_config* c) {
+    const KernelEntry* e = find_kernel(p, variant, ch, wmax);
+    return e && shape_config(p, *e, d, 0, stages, c);
+}
+
+// The selector (see the file comment): the measured table first (rows of this
+// hidden size; else of the nearest measured hidden size within a factor of
+// two, whose row lengths are of the same kind: a ring row only for rows its
+// swizzled copies can take), then the decode rule (one warp per block while
+// the whole problem needs no more warps than there are SMs), then the fixed
+// prefill rule (fewest warps with CH <= 2).
 bool select(const Problem& p, DeviceInfo* d, rmsn_config* c) {
     if (!p.vec_ok) {
         if (p.ragged_ok) {
@@ -385,20 +430,41 @@ bool select(const Problem& p, DeviceInfo* d, rmsn_config* c) {
         return e && shape_config(p, *e, d, 0, 0, c);
     }
     int variant = 0, ch = 0, wmax = 0, stages = 0;
-    int tin = p.res_f32 ? (p.in_dt == kF16 ? kTableF16R32 : kTableBF16R32) : p.in_dt;
-    int tout = p.out_dt;
-    bool found = table_lookup(tin, tout, p.H, p.T, &variant, &ch, &wmax, &stages);
-    if (!found && (tin == kF16 || tin == kTableF16R32)) {
-        // fp16 moves the same bytes through the same kernels as bf16: without
-        // rows of its own it takes the bf16 rows
-        tin = tin == kF16 ? kBF16 : kTableBF16R32;
-        if (tout == kF16) tout = kBF16;
-        found = table_lookup(tin, tout, p.H, p.T, &variant, &ch, &wmax, &stages);
+    const int res = p.res ? 1 : 0;
+    // table keys to try: the problem's own, then (fp16 moves the same bytes
+    // through the same kernels as bf16) the bf16 rows for fp16
+    int keys[2][2];
+    int nkeys = 0;
+    const int tin = p.res_f32 ? (p.in_dt == kF16 ? kTableF16R32 : kTableBF16R32) : p.in_dt;
+    keys[nkeys][0] = tin;
+    keys[nkeys++][1] = p.out_dt;
+    if (tin == kF16 || tin == kTableF16R32) {
+        keys[nkeys][0] = tin == kF16 ? kBF16 : kTableBF16R32;
+        keys[nkeys++][1] = p.out_dt == kF16 ? kBF16 : p.out_dt;
     }
-    if (found) {
-        const KernelEntry* e = find_kernel(p, variant, ch, wmax);
-        if (e && shape_config(p, *e, d, 0, stages, c)) return true;
+    for (int k = 0; k < nkeys; ++k) {
+        if (table_lookup(keys[k][0], keys[k][1], p.H, p.T, res, &variant, &ch, &wmax, &stages))
+            return table_shape(p, d, variant, ch, wmax, stages, c) ||
+                   select_rules(p, d, c);
     }
+    for (int k = 0; k < nkeys; ++k) {
+        int64_t near[16];
+        const int n = table_neighbours(keys[k][0], keys[k][1], p.H, near, 16);
+        for (int i = 0; i < n; ++i) {
+            if (!table_lookup(keys[k][0], keys[k][1], near[i], p.T, res, &variant, &ch, &wmax,
+                              &stages))
+                continue;
+            if (variant == kBulkRow && !bulk_swizzle_ok(p)) continue;
+            if (table_shape(p, d, variant, ch, wmax, stages, c)) return true;
+        }
+    }
+    return select_rules(p, d, c);
+}
+
+// The blog's decode rule, then the fixed prefill rule (shapes the table does
+// not cover).
+bool select_rules(const Problem& p, DeviceInfo* d, rmsn_config* c) {
+    int ch = 0;
     const int64_t warps_needed = (p.T * p.nvec + 31) / 32;
     if (warps_needed <= d->num_sms && p.nvec <= 32 * 8) {
         ch = 1;
@@ -506,6 +572,30 @@ bool encode_rows(CUtensorMap* m, const void* base, int64_t T, int64_t H, int byt
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// encode_rows through the device's map cache.
+bool cached_rows(DeviceInfo* d, CUtensorMap* m, const void* base, int64_t T, int64_t H,
+                 int bytes) {
+    {
+        std::lock_guard<std::mutex> lock(d->mu);
+        for (const MapEntry& e : d->maps) {
+            if (e.base == base && e.T == T && e.H == H && e.bytes == bytes) {
+                memcpy(m, &e.map, sizeof(*m));
+                return true;
+            }
+        }
+    }
+    if (!encode_rows(m, base, T, H, bytes)) return false;
+    std::lock_guard<std::mutex> lock(d->mu);
+    MapEntry& e = d->maps[d->map_next];
+    d->map_next = (d->map_next + 1) % kMapCache;
+    e.base = base;
+    e.T = T;
+    e.H = H;
+    e.bytes = bytes;
+    memcpy(&e.map, m, sizeof(*m));
+    return true;
+}
+
 int launch(const KernelEntry* e, const rmsn_config& c, DeviceInfo* d, const Problem& p,
            const void* x, const void* residual, const void* weight, const void* bias, void* out,
            void* residual_out, float* out_scale, float eps, float weight_offset,
@@ -529,6 +619,7 @@ int launch(const KernelEntry* e, const rmsn_config& c, DeviceInfo* d, const Prob
     a.pdl = p.pdl ? 1 : 0;
     a.early_params = p.early_params ? 1 : 0;
     a.status = d->status;
+    a.wait_cycles = d->wait_cycles.load(std::memory_order_relaxed);
     // the bulk kernel also takes the tensor-copy descriptors of x and the
     // residual (zero and unused when its stages take 1-D copies)
     alignas(64) CUtensorMap mx;
@@ -537,26 +628,36 @@ int launch(const KernelEntry* e, const rmsn_config& c, DeviceInfo* d, const Prob
     memset(&mr, 0, sizeof(mr));
     a.swz = 0;
     if (e->variant == kBulkRow && bulk_swizzle_ok(p) &&
-        encode_rows(&mx, x, p.T, p.H, p.in_bytes) &&
-        (!p.res || encode_rows(&mr, residual, p.T, p.H, p.res_bytes)))
+        cached_rows(d, &mx, x, p.T, p.H, p.in_bytes) &&
+        (!p.res || cached_rows(d, &mr, residual, p.T, p.H, p.res_bytes)))
         a.swz = 1;
     void* args_one[] = {&a};
     void* args_bulk[] = {&a, &mx, &mr};
     void** args = e->variant == kBulkRow ? args_bulk : args_one;
     cudaError_t err;
-    if (p.pdl) {
+    if (p.pdl || e->variant == kCluster) {
         // programmatic dependent launch: the kernel may start while the
-        // preceding kernel in `stream` runs; it waits for it before reading
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        // preceding kernel in `stream` runs; it waits for it before reading.
+        // The split-row kernel runs as clusters of c.cluster blocks.
+        cudaLaunchAttribute attr[2];
+        unsigned n = 0;
+        if (p.pdl) {
+            attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[n++].val.programmaticStreamSerializationAllowed = 1;
+        }
+        if (e->variant == kCluster) {
+            attr[n].id = cudaLaunchAttributeClusterDimension;
+            attr[n].val.clusterDim.x = (unsigned)c.cluster;
+            attr[n].val.clusterDim.y = 1;
+            attr[n++].val.clusterDim.z = 1;
+        }
         cudaLaunchConfig_t lc = {};
         lc.gridDim = dim3((unsigned)c.grid);
         lc.blockDim = dim3((unsigned)(c.warps_per_block * 32));
         lc.dynamicSmemBytes = (size_t)c.smem_bytes;
         lc.stream = stream;
         lc.attrs = attr;
-        lc.numAttrs = 1;
+        lc.numAttrs = n;
         err = cudaLaunchKernelExC(&lc, e->fn, args);
     } else {
         err = cudaLaunchKernel(e->fn, dim3((unsigned)c.grid),
@@ -566,11 +667,14 @@ int launch(const KernelEntry* e, const rmsn_config& c, DeviceInfo* d, const Prob
     return err == cudaSuccess ? RMSN_OK : RMSN_ECUDA;
 }
 
-// Device address at which the current device reaches `p`: device and managed
-// memory as is, page-locked host memory through its mapped address, other
-// host memory only where the device can access pageable memory.  Returns
-// false when the device cannot reach `p`.
-bool device_view(DeviceInfo* d, const void* p, const void** dev) {
+// Device address at which the current device reaches `p`: device memory of
+// this device and managed memory as is, page-locked host memory through its
+// mapped address, other host memory only where the device can access
+// pageable memory.  Device memory of another GPU is refused (without peer
+// access a kernel reading it would fault, and whether peer access is on is
+// not something the call can see without changing it).  Returns false when
+// the device cannot reach `p`.
+bool device_view(DeviceInfo* d, int dev_id, const void* p, const void** dev) {
     *dev = p;
     if (!p) return true;
     cudaPointerAttributes attr;
@@ -580,6 +684,7 @@ bool device_view(DeviceInfo* d, const void* p, const void** dev) {
     }
     switch (attr.type) {
         case cudaMemoryTypeDevice:
+            return attr.device == dev_id;
         case cudaMemoryTypeManaged:
             return true;
         case cudaMemoryTypeHost:
@@ -636,7 +741,7 @@ RMSN_API int rmsnorm_fwd_ex(const void* x, const void* residual, const void* wei
         e = find_kernel(p, cfg->variant, cfg->chunks, cfg->max_warps);
         if (!e || !shape_config(p, *e, d, cfg->grid, cfg->stages, &c)) return RMSN_EUNSUPPORTED;
     } else {
-        const SelKey key{p.T, p.H, flags, (p.vec_ok ? 1 : 0) | (p.ragged_ok ? 2 : 0)};
+        const SelKey key{p.T, p.H, flags, (p.vec_ok ? 1 : 0) | (p.ragged_ok ? 2 : 0), 0};
         bool hit = false;
         {
             std::lock_guard<std::mutex> lock(d->mu);
@@ -688,9 +793,25 @@ RMSN_API int rmsnorm_fwd_blockscaled(const void* x, const void* residual, const 
         e = find_kernel(p, cfg->variant, cfg->chunks, cfg->max_warps);
         if (!e || !shape_config(p, *e, d, cfg->grid, cfg->stages, &c)) return RMSN_EUNSUPPORTED;
     } else {
-        if (!select(p, d, &c)) return RMSN_EUNSUPPORTED;
-        e = find_kernel(p, c.variant, c.chunks, c.max_warps);
-        if (!e) return RMSN_EUNSUPPORTED;
+        const SelKey key{p.T, p.H, flags, 1, format};
+        bool hit = false;
+        {
+            std::lock_guard<std::mutex> lock(d->mu);
+            auto it = d->sel_cache.find(key);
+            if (it != d->sel_cache.end()) {
+                c = it->second.first;
+                e = it->second.second;
+                hit = true;
+            }
+        }
+        if (!hit) {
+            if (!select(p, d, &c)) return RMSN_EUNSUPPORTED;
+            e = find_kernel(p, c.variant, c.chunks, c.max_warps);
+            if (!e) return RMSN_EUNSUPPORTED;
+            std::lock_guard<std::mutex> lock(d->mu);
+            if (d->sel_cache.size() > 4096) d->sel_cache.clear();
+            d->sel_cache[key] = {c, e};
+        }
     }
     return launch(e, c, d, p, x, residual, weight, bias, out, residual_out, token_scale, eps,
                   weight_offset, stream, block_scale);
@@ -706,6 +827,8 @@ RMSN_API int rmsnorm_fwd_host(const void* x, const void* residual, const void* w
     if (st != RMSN_OK || n_tokens == 0) return st;
     DeviceInfo* d = device_info();
     if (!d) return RMSN_ECUDA;
+    int dev_id = 0;
+    if (cudaGetDevice(&dev_id) != cudaSuccess) return RMSN_ECUDA;
     const void* dx;
     const void* dr;
     const void* dw;
@@ -713,10 +836,10 @@ RMSN_API int rmsnorm_fwd_host(const void* x, const void* residual, const void* w
     const void* dout;
     const void* dres;
     const void* dscale;
-    if (!device_view(d, x, &dx) || !device_view(d, residual, &dr) ||
-        !device_view(d, weight, &dw) || !device_view(d, bias, &db) ||
-        !device_view(d, out, &dout) || !device_view(d, residual_out, &dres) ||
-        !device_view(d, out_scale, &dscale))
+    if (!device_view(d, dev_id, x, &dx) || !device_view(d, dev_id, residual, &dr) ||
+        !device_view(d, dev_id, weight, &dw) || !device_view(d, dev_id, bias, &db) ||
+        !device_view(d, dev_id, out, &dout) || !device_view(d, dev_id, residual_out, &dres) ||
+        !device_view(d, dev_id, out_scale, &dscale))
         return RMSN_EINVAL;
     // the mapped addresses decide the vector path
     p.vec_ok = vector_path_ok(p, dx, dr, dw, db, dres, dout);
@@ -803,6 +926,13 @@ RMSN_API int rmsnorm_read_status(uint32_t* status, int clear) {
     return RMSN_OK;
 }
 
+RMSN_API int rmsnorm_set_wait_limit(int64_t cycles) {
+    DeviceInfo* d = device_info();
+    if (!d) return RMSN_ECUDA;
+    d->wait_cycles.store(cycles == 0 ? kDefaultWaitCycles : cycles, std::memory_order_relaxed);
+    return RMSN_OK;
+}
+
 RMSN_API int rmsnorm_qk_fwd(void* q, void* k, const void* q_weight, const void* k_weight,
                             int64_t n_tokens, int64_t n_q_heads, int64_t n_k_heads,
                             int64_t head_dim, int64_t q_token_stride, int64_t k_token_stride,
@@ -865,6 +995,7 @@ RMSN_API int rmsnorm_qk_fwd(void* q, void* k, const void* q_weight, const void* 
     a.eps = eps;
     a.woff = weight_offset;
     a.pdl = (flags & RMSN_PDL) ? 1 : 0;
+    a.status = d->status;
     void* args[] = {&a};
     cudaError_t err;
     if (flags & RMSN_PDL) {

@@ -36,6 +36,12 @@ namespace rmsn {
     RMSN_BULK(CH, WMAX, false, false), RMSN_BULK(CH, WMAX, true, false),                     \
         RMSN_BULK(CH, WMAX, false, true), RMSN_BULK(CH, WMAX, true, true)
 #endif
+#define RMSN_CLU(CH, K, RES, BIAS)                                                          \
+    {RMSN_DTI, RMSN_DTO, kCluster, CH, K, 0, RES, BIAS, RMSN_RF32,                            \
+     (const void*)&rmsn_cluster_kernel<RMSN_TI, RMSN_TO, CH, RES, BIAS>}
+#define RMSN_CLU4(CH, K)                                                                     \
+    RMSN_CLU(CH, K, false, false), RMSN_CLU(CH, K, true, false), RMSN_CLU(CH, K, false, true), \
+        RMSN_CLU(CH, K, true, true)
 #define RMSN_GEN(RES)                                                                        \
     {RMSN_DTI, RMSN_DTO, kGeneric, 0, 8, 0, RES, -1, RMSN_RF32,                              \
      (const void*)&rmsn_generic_kernel<RMSN_TI, RMSN_TO, RES, RMSN_TX>}
@@ -53,6 +59,11 @@ static const KernelEntry kTable[] = {
     // prefill: rows streamed through shared memory by bulk async copies
     RMSN_BULK4(1, 8), RMSN_BULK4(2, 8), RMSN_BULK4(1, 16), RMSN_BULK4(2, 16),
     RMSN_BULK4(1, 32), RMSN_BULK4(2, 32),
+#endif
+#ifdef RMSN_WITH_CLUSTER
+    // decode: one row split over a cluster of K one-warp blocks
+    RMSN_CLU4(1, 2), RMSN_CLU4(1, 4), RMSN_CLU4(1, 8), RMSN_CLU4(2, 2), RMSN_CLU4(2, 4),
+    RMSN_CLU4(2, 8), RMSN_CLU4(4, 2), RMSN_CLU4(4, 4),
 #endif
 #ifndef RMSN_NO_GENERIC
     // any shape

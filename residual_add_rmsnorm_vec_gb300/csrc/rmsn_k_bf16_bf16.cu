@@ -4,4 +4,5 @@
 #define RMSN_DTI kBF16
 #define RMSN_DTO kBF16
 #define RMSN_TABLE_FN kernels_bf16_bf16
+#define RMSN_WITH_CLUSTER
 #include "rmsn_instances.cuh"

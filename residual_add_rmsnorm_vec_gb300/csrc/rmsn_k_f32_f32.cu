@@ -4,4 +4,5 @@
 #define RMSN_DTI kF32
 #define RMSN_DTO kF32
 #define RMSN_TABLE_FN kernels_f32_f32
+#define RMSN_WITH_CLUSTER
 #include "rmsn_instances.cuh"

@@ -270,6 +270,38 @@ __device__ __forceinline__ F2 add16x2_f32(uint32_t u, float c) {
     return f2(lo, hi);
 }
 
+// The products h * w of the two 16-bit lanes of h and w (type T), exact: the
+// product of two 8-bit (bf16) or 11-bit (fp16) significands fits fp32's 24
+// bits, so the FMA with a -0 addend rounds nothing (and keeps the sign of a
+// zero product).  Underflow below fp32's normal range is the only loss, at
+// |h w| < 2^-126.
+template <class T>
+__device__ __forceinline__ F2 mul16x2_exact(uint32_t h, uint32_t w) {
+    float lo, hi;
+    if constexpr (IsF16<T>::value)
+        asm("{\n\t.reg .b16 hl, hh, wl, wh;\n\tmov.b32 {hl, hh}, %2;\n\tmov.b32 {wl, wh}, %3;\n\t"
+            "fma.rn.f32.f16 %0, hl, wl, 0f80000000;\n\tfma.rn.f32.f16 %1, hh, wh, 0f80000000;\n\t}"
+            : "=f"(lo), "=f"(hi)
+            : "r"(h), "r"(w));
+    else
+        asm("{\n\t.reg .b16 hl, hh, wl, wh;\n\tmov.b32 {hl, hh}, %2;\n\tmov.b32 {wl, wh}, %3;\n\t"
+            "fma.rn.f32.bf16 %0, hl, wl, 0f80000000;\n\tfma.rn.f32.bf16 %1, hh, wh, 0f80000000;\n\t}"
+            : "=f"(lo), "=f"(hi)
+            : "r"(h), "r"(w));
+    return f2(lo, hi);
+}
+
+// Both lanes of two packed 16-bit words of T added: the exact sum rounded
+// once to T (nearest even), which is the residual's definition; the fp32 sum
+// rounded to T gives the same value.
+template <class T>
+__device__ __forceinline__ uint32_t add16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    if constexpr (IsF16<T>::value) asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    else asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // max(m, |a|, |b|) in one three-input maximum.
 __device__ __forceinline__ float absmax3(float m, float a, float b) {
     float r;
@@ -378,6 +410,35 @@ __device__ __forceinline__ void pdl_wait(int pdl) {
     if (pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- bounds-checked build
+// Built with -DRMSNORM_BOUNDS_CHECK, every global access and ring copy below is
+// first checked against the extent of its tensor; an access out of range is
+// skipped (loads leave zeros) and sets bit 1 of the status word, so a wrong
+// index shows up as a status bit instead of a fault.  In the normal build
+// every check is the constant true and compiles away.
+
+#ifdef RMSNORM_BOUNDS_CHECK
+__device__ __forceinline__ bool check_ok(uint32_t* status, bool ok) {
+    if (!ok) atomicOr(status, 2u);
+    return ok;
+}
+#define RMSN_CHECK(status, cond) ::rmsn::check_ok((status), (cond))
+#else
+#define RMSN_CHECK(status, cond) true
+#endif
+
+// Elements [e, e + n) inside the [T, H] row tensors of a.
+__device__ __forceinline__ bool rows_ok(const RmsnArgs& a, int64_t e, int64_t n) {
+    return RMSN_CHECK(a.status, e >= 0 && e + n <= a.T * (int64_t)a.H);
+}
+// Elements [j, j + n) inside the [H] weight and bias.
+__device__ __forceinline__ bool cols_ok(const RmsnArgs& a, int64_t j, int64_t n) {
+    return RMSN_CHECK(a.status, j >= 0 && j + n <= (int64_t)a.H);
+}
+__device__ __forceinline__ bool row_ok(const RmsnArgs& a, int64_t row) {
+    return RMSN_CHECK(a.status, row >= 0 && row < a.T);
+}
+
 // ---------------------------------------------------------------- reductions
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -469,6 +530,30 @@ __device__ __forceinline__ void scale_vec(const V8& h, const V8& w, const V8& b,
     }
 }
 
+// y for the quantised outputs, whose codes and scales are taken from fp32 y.
+// Without a weight offset (16-bit weights): y = RN(p * inv + b) with p = h w
+// formed exactly, one rounding in all; the weight and h are used as packed
+// 16-bit lanes, so nothing is unpacked but the bias.  With an offset (or an
+// fp32 stream) the rounding sequence of scale_vec.
+template <class TI, bool BIAS>
+__device__ __forceinline__ void scale_vec_q(const V8& h, const V8& w, const V8& b, float inv,
+                                            float woff, float (&y)[32 / TI::kBytes], float& m) {
+    if constexpr (TI::kBytes == 2) {
+        if (woff == 0.f) {
+            const F2 inv2 = f2(inv, inv);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const F2 p = mul16x2_exact<TI>(h.u[k], w.u[k]);
+                const F2 r = BIAS ? fma2(p, inv2, widen2<TI>(b.u[k])) : mul2(p, inv2);
+                f2split(r, y[2 * k], y[2 * k + 1]);
+                m = absmax3(m, y[2 * k], y[2 * k + 1]);
+            }
+            return;
+        }
+    }
+    scale_vec<TI, BIAS, true, true>(h, w, b, inv, woff, y, m);
+}
+
 // Store the VE outputs of one input vector at element offset `e`.
 template <class TI, class TO>
 __device__ __forceinline__ void store_out(void* out, int64_t e, const float (&y)[32 / TI::kBytes],
@@ -490,10 +575,15 @@ __device__ __forceinline__ void store_out(void* out, int64_t e, const float (&y)
         else st_stream16(o, u);
     } else {
         uint32_t u[VE / 4];
+        const F2 q2 = f2(qmul, qmul);
 #pragma unroll
-        for (int k = 0; k < VE / 4; ++k)
-            u[k] = pack_e4m3x4(__fmul_rn(y[4 * k], qmul), __fmul_rn(y[4 * k + 1], qmul),
-                               __fmul_rn(y[4 * k + 2], qmul), __fmul_rn(y[4 * k + 3], qmul));
+        for (int k = 0; k < VE / 4; ++k) {
+            // y * qmul two lanes at a time (each lane rounded once, as __fmul_rn)
+            float s0, s1, s2, s3;
+            f2split(mul2(f2(y[4 * k], y[4 * k + 1]), q2), s0, s1);
+            f2split(mul2(f2(y[4 * k + 2], y[4 * k + 3]), q2), s2, s3);
+            u[k] = pack_e4m3x4(s0, s1, s2, s3);
+        }
         uint8_t* o = reinterpret_cast<uint8_t*>(out) + e;
         if constexpr (VE == 16) st_stream16(o, u);
         else st_stream8(o, u);
@@ -528,7 +618,7 @@ __device__ __forceinline__ void load_params(const RmsnArgs& a, int G, int t, V8 
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
         const int v = c * G + t;
-        if (v < a.nvec) {
+        if (v < a.nvec && cols_ok(a, (int64_t)v * VE, VE)) {
             if (a.has_w) {
                 wv[c] = ld_vec<TX, TI, false>(a.w, (int64_t)v * VE);
             } else {
@@ -541,11 +631,12 @@ __device__ __forceinline__ void load_params(const RmsnArgs& a, int G, int t, V8 
 }
 
 // h = RN_in(x + r) (the sum formed in fp32), stored to residual_out; returns
-// this thread's fp32 sum of h^2.  A packed 16-bit add (add.rn.bf16x2) gives
-// the same h in fewer instructions, but measured on GB300 it made the
-// prefill ring ~15% slower, so the sum stays in fp32.  PACK: the squares take
-// the 16-bit lanes straight into the FMA.
-template <class TI, int CH, bool RES, bool PACK = true>
+// this thread's fp32 sum of h^2.  PADD: the packed 16-bit add (add.rn.bf16x2 /
+// f16x2), the same h in an eighth of the instructions; measured on GB300 it
+// made the 16-bit-output prefill ring ~15% slower, so only the quantised
+// outputs, whose ring is bound by instruction issue, take it.  PACK: the
+// squares take the 16-bit lanes straight into the FMA.
+template <class TI, int CH, bool RES, bool PACK = true, bool PADD = false>
 __device__ __forceinline__ float residual_sumsq(const RmsnArgs& a, int64_t rbase, int G, int t,
                                                 V8 (&hv)[CH], const V8* rv) {
     constexpr int VE = 32 / TI::kBytes;
@@ -555,7 +646,10 @@ __device__ __forceinline__ float residual_sumsq(const RmsnArgs& a, int64_t rbase
         const int v = c * G + t;
         if (v < a.nvec) {
             if constexpr (RES) {
-                if constexpr (TI::kBytes == 2) {
+                if constexpr (TI::kBytes == 2 && PADD) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) hv[c].u[k] = add16x2<TI>(hv[c].u[k], rv[c].u[k]);
+                } else if constexpr (TI::kBytes == 2) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         const float lo = __fadd_rn(lo2<TI>(hv[c].u[k]), lo2<TI>(rv[c].u[k]));
@@ -569,7 +663,8 @@ __device__ __forceinline__ float residual_sumsq(const RmsnArgs& a, int64_t rbase
                                                                __uint_as_float(rv[c].u[k])));
                 }
                 const int64_t off = (rbase + (int64_t)v * VE) * TI::kBytes;
-                st_stream32(static_cast<char*>(a.res_out) + off, hv[c].u);
+                if (rows_ok(a, rbase + (int64_t)v * VE, VE))
+                    st_stream32(static_cast<char*>(a.res_out) + off, hv[c].u);
             }
             if constexpr (TI::kBytes == 2 && PACK) {
 #pragma unroll
@@ -594,10 +689,10 @@ __device__ __forceinline__ float residual_sumsq(const RmsnArgs& a, int64_t rbase
 //          clamped to [-127, 127], stored as E8M0 (s + 127); codes y * 2^-s.
 //   NVFP4: per-token fp32 g = max|row| / (448 * 6) (the row max all-reduce),
 //          block scale E4M3(max|block| * (1 / (6 g))), codes
-//          E2M1(y * (1 / (scale * g))); 1 / (6 g) is correctly rounded, the
-//          per-block reciprocal is the hardware approximation.
+//          E2M1(y * r_b) with r_b the hardware approximation of
+//          1 / (scale * g); 1 / (6 g) is correctly rounded.
 // All conversions round to nearest even and saturate.
-template <class TI, class TO, int CH, bool BIAS, bool KEEP, class ReduceMax>
+template <class TI, class TO, int CH, bool BIAS, bool KEEP, bool QF, class ReduceMax>
 __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row, int64_t rbase,
                                                   int G, int t, float inv, const V8 (&hv)[CH],
                                                   V8 (&wv)[CH], V8* bv, ReduceMax reduce_max) {
@@ -619,7 +714,10 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
                 opaque(wv[c]);
                 if constexpr (BIAS) opaque(bv[c]);
                 float m = 0.f, y[VE];
-                scale_vec<TI, BIAS, true>(hv[c], wv[c], bv[BIAS ? c : 0], inv, a.woff, y, m);
+                if constexpr (QF)
+                    scale_vec_q<TI, BIAS>(hv[c], wv[c], bv[BIAS ? c : 0], inv, a.woff, y, m);
+                else
+                    scale_vec<TI, BIAS, true>(hv[c], wv[c], bv[BIAS ? c : 0], inv, a.woff, y, m);
                 if constexpr (HOLD) {
 #pragma unroll
                     for (int k = 0; k < VE; ++k) ys[c][k] = y[k];
@@ -630,7 +728,7 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
         }
         amax = reduce_max(amax);
         g = __fdiv_rn(amax, 2688.f);
-        if (t == 0) a.scale[row] = g;
+        if (t == 0 && row_ok(a, row)) a.scale[row] = g;
         rcp6g = g > 0.f ? __frcp_rn(__fmul_rn(6.f, g)) : 0.f;  // one reciprocal per row
     }
 #pragma unroll
@@ -647,7 +745,11 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
             } else {
                 opaque(wv[c]);
                 if constexpr (BIAS) opaque(bv[c]);
-                scale_vec<TI, BIAS, true>(hv[c], wv[c], bv[BIAS ? c : 0], inv, a.woff, y, bmax);
+                if constexpr (QF)
+                    scale_vec_q<TI, BIAS>(hv[c], wv[c], bv[BIAS ? c : 0], inv, a.woff, y, bmax);
+                else
+                    scale_vec<TI, BIAS, true>(hv[c], wv[c], bv[BIAS ? c : 0], inv, a.woff, y,
+                                              bmax);
             }
         }
         // every lane takes part; a block's lanes are all valid or all invalid
@@ -667,8 +769,10 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
                 sc = two & 0xFFu;
             }
             const float s = __fmul_rn(e4m3_value(sc), g);
-            // one reciprocal per block of 16: the hardware approximation
-            // (within 1 ulp) is far inside E2M1's half-step of 1/4 to 1/2
+            // one reciprocal per block of 16, the hardware approximation
+            // (within 1 ulp of 1/s): the codes are E2M1(RN(y * r)), which can
+            // differ by one step from E2M1(y / s) where y / s lies within a
+            // few fp32 ulp of a rounding midpoint of E2M1
             if (s > 0.f) asm("rcp.approx.f32 %0, %1;" : "=f"(mul) : "f"(s));
             else mul = 0.f;
             sbyte = (uint8_t)sc;
@@ -684,6 +788,7 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
         for (int k = 0; k < VE; k += 2)
             f2split(mul2(f2(y[k], y[k + 1]), f2(mul, mul)), y[k], y[k + 1]);
         const int64_t e = rbase + (int64_t)v * VE;  // element index of this vector
+        if (!rows_ok(a, e, VE)) continue;
         if constexpr (FP4) {
             uint32_t u[VE / 8];
 #pragma unroll
@@ -711,15 +816,18 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
 // `reduce_max` is the row-wide max all-reduce (only used for FP8 output).
 // KEEP: hold the row's y in registers between the FP8 max pass and the
 // quantising pass instead of recomputing it (for kernels with a large
-// register budget).  PACK: scale two lanes per instruction.
-template <class TI, class TO, int CH, bool BIAS, bool KEEP = false, bool PACK = true,
+// register budget).  QF: the quantised outputs take y from scale_vec_q (the
+// exact product h w; fewer instructions), else from scale_vec.  The
+// register kernels keep scale_vec: with two scale passes per row under a
+// 64-register bound the second form spills.
+template <class TI, class TO, int CH, bool BIAS, bool KEEP = false, bool QF = false,
           class ReduceMax>
 __device__ __forceinline__ void scale_store(const RmsnArgs& a, int64_t row, int64_t rbase, int G,
                                             int t, float inv, const V8 (&hv)[CH], V8 (&wv)[CH],
                                             V8* bv, ReduceMax reduce_max) {
     if constexpr (IsBlockFmt<TO>::value) {
-        scale_store_block<TI, TO, CH, BIAS, KEEP>(a, row, rbase, G, t, inv, hv, wv, bv,
-                                                  reduce_max);
+        scale_store_block<TI, TO, CH, BIAS, KEEP, QF>(a, row, rbase, G, t, inv, hv, wv, bv,
+                                                      reduce_max);
         return;
     }
     constexpr int VE = 32 / TI::kBytes;
@@ -735,8 +843,11 @@ __device__ __forceinline__ void scale_store(const RmsnArgs& a, int64_t row, int6
                 opaque(wv[c]);
                 if constexpr (BIAS) opaque(bv[c]);
                 float y[VE];
-                scale_vec<TI, BIAS, true, PACK>(hv[c], wv[c], bv[BIAS ? c : 0], inv, a.woff, y,
-                                                amax);
+                if constexpr (QF)
+                    scale_vec_q<TI, BIAS>(hv[c], wv[c], bv[BIAS ? c : 0], inv, a.woff, y, amax);
+                else
+                    scale_vec<TI, BIAS, true>(hv[c], wv[c], bv[BIAS ? c : 0], inv, a.woff, y,
+                                              amax);
                 if constexpr (HOLD) {
 #pragma unroll
                     for (int k = 0; k < VE; ++k) ys[c][k] = y[k];
@@ -745,20 +856,23 @@ __device__ __forceinline__ void scale_store(const RmsnArgs& a, int64_t row, int6
         }
         amax = reduce_max(amax);
         qmul = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
-        if (t == 0) a.scale[row] = __fdiv_rn(amax, 448.f);
+        if (t == 0 && row_ok(a, row)) a.scale[row] = __fdiv_rn(amax, 448.f);
     }
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
         const int v = c * G + t;
         if (v < a.nvec) {
+            if (!rows_ok(a, rbase + (int64_t)v * VE, VE)) continue;
             if constexpr (HOLD) {
                 store_out<TI, TO>(a.out, rbase + (int64_t)v * VE, ys[c], qmul);
             } else {
                 opaque(wv[c]);
                 if constexpr (BIAS) opaque(bv[c]);
                 float y[VE], m = 0.f;
-                scale_vec<TI, BIAS, false, PACK>(hv[c], wv[c], bv[BIAS ? c : 0], inv, a.woff, y,
-                                                 m);
+                if constexpr (QF && TO::kBytes == 1)
+                    scale_vec_q<TI, BIAS>(hv[c], wv[c], bv[BIAS ? c : 0], inv, a.woff, y, m);
+                else
+                    scale_vec<TI, BIAS>(hv[c], wv[c], bv[BIAS ? c : 0], inv, a.woff, y, m);
                 store_out<TI, TO>(a.out, rbase + (int64_t)v * VE, y, qmul);
             }
         }
@@ -794,8 +908,8 @@ __global__ void __launch_bounds__(Bounds<WMAX, CH, RES && BIAS>::kThreads,
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
             const int v = c * G + t;
-            if (v < a.nvec) {
-                const int64_t e = rw * (int64_t)a.H + (int64_t)v * VE;
+            const int64_t e = rw * (int64_t)a.H + (int64_t)v * VE;
+            if (v < a.nvec && rows_ok(a, e, VE)) {
                 hv[c] = ld_vec<TX, TI, true>(a.x, e);
                 if constexpr (RES) rv[c] = ld_stream32(static_cast<const char*>(a.r) + e * TI::kBytes);
             }
@@ -829,6 +943,106 @@ __global__ void __launch_bounds__(Bounds<WMAX, CH, RES && BIAS>::kThreads,
     }
 }
 
+// ---------------------------------------------------------------- split-row (cluster) kernel
+//
+// Decode-size rows split over a thread-block cluster (a split row for the
+// blog's decode case, section "Prefill and decode", where the batch has too
+// few rows to fill the SMs).  Each row goes to one cluster of K blocks of one
+// warp; thread t = rank * 32 + lane of the row's K * 32 threads holds vectors
+// v = c * 32K + t, c < CH, as in the register kernel.  The blocks exchange
+// their partial sums of squares through distributed shared memory: lane j of
+// each block stores the block's partial into slot `rank` of block j, a
+// cluster barrier (release / acquire) makes the slots visible, and every block
+// adds the K partials in rank order, so all get the same total.  A relaxed
+// arrive at entry, waited for before the first remote store, ensures every
+// block of the cluster has started before its shared memory is written; no
+// block touches another's shared memory after the second barrier, so blocks
+// may then exit in any order.  16-bit and fp32 outputs only (the quantised
+// outputs would need a second exchange for the row maximum).
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_index() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Store v at the shared-memory location `local` (an address of this block's
+// shared memory) of block `rank` of the cluster.
+__device__ __forceinline__ void st_cluster_f32(const void* local, uint32_t rank, float v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(remote)
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(local))), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
+constexpr int kMaxClusterBlocks = 8;
+
+template <class TI, class TO, int CH, bool RES, bool BIAS>
+__global__ void __launch_bounds__(32) rmsn_cluster_kernel(const RmsnArgs a) {
+    static_assert(TO::kBytes >= 2, "16-bit and fp32 outputs only");
+    __shared__ float part[kMaxClusterBlocks];
+    const uint32_t rank = cluster_rank();
+    const uint32_t K = cluster_size();
+    const int lane = threadIdx.x;
+    const int G = 32 * (int)K;
+    const int t = (int)rank * 32 + lane;
+    const int64_t row = cluster_index();
+    cluster_arrive_relaxed();
+    pdl_launch_dependents(a.pdl);
+    V8 wv[CH];
+    V8 bv[BIAS ? CH : 1];
+    if (a.early_params) load_params<TI, TI, CH>(a, G, t, wv, bv, BIAS);
+    pdl_wait(a.pdl);
+    V8 hv[CH];
+    V8 rv[RES ? CH : 1];
+    const int64_t rbase = row * (int64_t)a.H;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        const int v = c * G + t;
+        const int64_t e = rbase + (int64_t)v * (32 / TI::kBytes);
+        if (v < a.nvec && rows_ok(a, e, 32 / TI::kBytes)) {
+            hv[c] = ld_stream32(static_cast<const char*>(a.x) + e * TI::kBytes);
+            if constexpr (RES) rv[c] = ld_stream32(static_cast<const char*>(a.r) + e * TI::kBytes);
+        }
+    }
+    if (!a.early_params) load_params<TI, TI, CH>(a, G, t, wv, bv, BIAS);
+    const float acc = warp_sum(residual_sumsq<TI, CH, RES>(a, rbase, G, t, hv, rv));
+    cluster_wait();  // every block of the cluster has started
+    if (lane < (int)K) st_cluster_f32(&part[rank], (uint32_t)lane, acc);
+    cluster_arrive_release();
+    cluster_wait();
+    float sumsq = part[0];
+    for (uint32_t i = 1; i < K; ++i) sumsq = __fadd_rn(sumsq, part[i]);
+    const float inv = inv_rms(sumsq, a.H, a.eps);
+    scale_store<TI, TO, CH, BIAS>(a, row, rbase, G, t, inv, hv, wv, bv,
+                                  [](float m) { return m; });
+}
+
 // ---------------------------------------------------------------- bulk-copy kernel
 //
 // Persistent blocks (one row at a time, up to WMAX warps).  Whole rows of x
@@ -841,13 +1055,14 @@ __global__ void __launch_bounds__(Bounds<WMAX, CH, RES && BIAS>::kThreads,
 // refills it with the row `stages` ahead.  Bytes in flight per SM are set by
 // the ring size, not by the register file.
 //
-// Every mbarrier wait is bounded (about one second of clock cycles).  A wait
-// that runs out sets bit 0 of *a.status and a shared abort flag; the block
-// still takes part in the row's barrier so no thread is left waiting, then
-// stops, after thread 0 has waited (again bounded) for its copies in flight.
+// Every mbarrier wait is bounded (a.wait_cycles, by default about one second
+// of clock cycles).  A wait that runs out sets bit 0 of *a.status and a
+// shared abort flag; the block still takes part in the row's barrier so no
+// thread is left waiting, then stops, after thread 0 has waited (bounded by
+// the default, whatever a.wait_cycles says) for its copies in flight, so no
+// copy into the block's shared memory outlives the block.
 
 constexpr int kMaxStages = 8;
-constexpr long long kWaitCycles = 2000000000LL;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -869,12 +1084,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait for the phase with the given parity to complete, for at most `limit`
+// clock cycles; a negative limit tests the phase once and does not wait.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  long long limit) {
+    if (limit < 0) return mbar_test_wait(bar, parity);
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > kWaitCycles) return false;
+        if (clock64() - t0 > limit) return false;
     }
     return true;
 }
@@ -1009,11 +1239,14 @@ __global__ void __launch_bounds__(WMAX * 32, 1)
                      const __grid_constant__ CUtensorMap mr) {
     constexpr int VE = 32 / TI::kBytes;
     constexpr int XVB = VE * TX::kBytes;  // bytes of one x vector
-    // per-token FP8 rows take one element per instruction and the butterfly
-    // row max here: measured on GB300, the paired fp32 forms and the redux
-    // max made this kernel's long FP8 launches 1-5% slower (while they speed
-    // up every other output and the short rows)
-    constexpr bool PACK = !std::is_same<TO, FP8>::value;
+    // quantised outputs (per-token FP8, the block formats) are bound by
+    // instruction issue here, not by DRAM: they take the packed 16-bit
+    // residual add as well (the 16-bit outputs keep the fp32 add, measured
+    // faster in this kernel)
+    constexpr bool PADD = TO::kBytes == 1;
+    // a quantised row's y stays in registers between its two passes where
+    // the register budget allows it
+    constexpr bool HOLD = WMAX <= 16 && CH * VE <= 32;
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full[kMaxStages];
     __shared__ float red[4][32];
@@ -1038,18 +1271,25 @@ __global__ void __launch_bounds__(WMAX * 32, 1)
         for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    // thread 0: copy `row` into the stage at `dst`, completing on `bar` (a row
+    // outside the tensor, in the bounds-checked build, is not copied: the
+    // stage's phase completes on a plain arrival instead)
+    auto issue = [&](int64_t row, uint32_t dst, uint32_t bar) {
+        if (!row_ok(a, row)) {
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+            return;
+        }
+        if (a.swz)
+            issue_row_tensor<RES>(&mx, &mr, row, dst, bar, x_bytes, r_bytes);
+        else
+            issue_row<RES>(a, row, dst, bar, x_bytes, r_bytes);
+    };
     if (a.early_params) load_params<TX, TI, CH>(a, G, t, wv, bv, BIAS);
     pdl_wait(a.pdl);
     if (t == 0) {
-        for (int64_t k = 0; k < S && k < n_my; ++k) {
-            if (a.swz)
-                issue_row_tensor<RES>(&mx, &mr, blockIdx.x + k * gridDim.x,
-                                      ring0 + (uint32_t)k * stage_bytes, smem_u32(&full[k]),
-                                      x_bytes, r_bytes);
-            else
-                issue_row<RES>(a, blockIdx.x + k * gridDim.x, ring0 + (uint32_t)k * stage_bytes,
-                               smem_u32(&full[k]), x_bytes, r_bytes);
-        }
+        for (int64_t k = 0; k < S && k < n_my; ++k)
+            issue(blockIdx.x + k * gridDim.x, ring0 + (uint32_t)k * stage_bytes,
+                  smem_u32(&full[k]));
     }
     __syncthreads();
     if (!a.early_params) load_params<TX, TI, CH>(a, G, t, wv, bv, BIAS);
@@ -1062,7 +1302,7 @@ __global__ void __launch_bounds__(WMAX * 32, 1)
         k_abort = k;
         const int64_t row = blockIdx.x + k * gridDim.x;
         const int64_t rbase = row * (int64_t)a.H;
-        if (!mbar_wait_bounded(smem_u32(&full[s]), phase)) {
+        if (!mbar_wait_bounded(smem_u32(&full[s]), phase, a.wait_cycles)) {
             atomicOr(a.status, 1u);
             abort_flag = 1;
         }
@@ -1072,7 +1312,7 @@ __global__ void __launch_bounds__(WMAX * 32, 1)
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
             const int v = c * G + t;
-            if (v < a.nvec) {
+            if (v < a.nvec && RMSN_CHECK(a.status, (uint32_t)(v + 1) * XVB <= x_bytes)) {
                 if (a.swz) {
                     hv[c] = ld_shared_vec_swz<TX, TI>(base, (uint32_t)v);
                     if constexpr (RES) rv[c] = ld_shared32_swz(base + x_bytes, (uint32_t)v);
@@ -1082,31 +1322,27 @@ __global__ void __launch_bounds__(WMAX * 32, 1)
                 }
             }
         }
-        const float acc = residual_sumsq<TI, CH, RES, PACK>(a, rbase, G, t, hv, rv);
+        const float acc = residual_sumsq<TI, CH, RES, true, PADD>(a, rbase, G, t, hv, rv);
         const float sumsq = block_allreduce<false>(acc, red[parity]);
         // every thread has read buffer s: refill it with the row S ahead
         if (abort_flag) break;
         if (t == 0 && k + S < n_my) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            if (a.swz)
-                issue_row_tensor<RES>(&mx, &mr, blockIdx.x + (k + S) * gridDim.x, base,
-                                      smem_u32(&full[s]), x_bytes, r_bytes);
-            else
-                issue_row<RES>(a, blockIdx.x + (k + S) * gridDim.x, base, smem_u32(&full[s]),
-                               x_bytes, r_bytes);
+            issue(blockIdx.x + (k + S) * gridDim.x, base, smem_u32(&full[s]));
         }
         const float inv = inv_rms(sumsq, a.H, a.eps);
         float* slot = red[2 + parity];
-        scale_store<TI, TO, CH, BIAS, (WMAX <= 16 && CH * VE <= 32), PACK>(
+        scale_store<TI, TO, CH, BIAS, HOLD, PADD && HOLD>(
             a, row, rbase, G, t, inv, hv, wv, bv,
-            [&](float m) { return block_allreduce<true, PACK>(m, slot); });
+            [&](float m) { return block_allreduce<true>(m, slot); });
         parity ^= 1;
     }
     if (abort_flag && t == 0) {
         // drain: rows k_abort .. k_abort + S - 1 may still have copies in
         // flight; wait (bounded) for each before the block's memory is reused
         for (int64_t j = k_abort; j < k_abort + S && j < n_my; ++j)
-            mbar_wait_bounded(smem_u32(&full[j % S]), (uint32_t)((j / S) & 1));
+            mbar_wait_bounded(smem_u32(&full[j % S]), (uint32_t)((j / S) & 1),
+                              kDefaultWaitCycles);
     }
 }
 
@@ -1148,6 +1384,7 @@ __device__ __forceinline__ void st_elem(void* p, int64_t i, float v) {
 template <class TH, class TX>
 __device__ __forceinline__ float generic_y(const RmsnArgs& a, const void* hsrc, int64_t base,
                                            int j, float inv) {
+    if (!rows_ok(a, base + j, 1) || !cols_ok(a, j, 1)) return 0.f;
     const float h = ld_elem<TH>(hsrc, base + j);
     const float w = a.has_w ? ld_elem<TX>(a.w, j) : 1.f;
     if (a.b) return scale_elem<true>(h, inv, w, a.woff, ld_elem<TX>(a.b, j));
@@ -1166,6 +1403,7 @@ __global__ void __launch_bounds__(256) rmsn_generic_kernel(const RmsnArgs a) {
         const int64_t base = row * (int64_t)H;
         float acc = 0.f;
         for (int j = threadIdx.x; j < H; j += blockDim.x) {
+            if (!rows_ok(a, base + j, 1)) continue;
             float h = ld_elem<TX>(a.x, base + j);
             if constexpr (RES) {
                 h = round_to<TI>(__fadd_rn(h, ld_elem<TI>(a.r, base + j)));
@@ -1185,9 +1423,10 @@ __global__ void __launch_bounds__(256) rmsn_generic_kernel(const RmsnArgs a) {
             }
             amax = block_allreduce<true>(amax, red[2 + parity]);
             qmul = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
-            if (threadIdx.x == 0) a.scale[row] = __fdiv_rn(amax, 448.f);
+            if (threadIdx.x == 0 && row_ok(a, row)) a.scale[row] = __fdiv_rn(amax, 448.f);
         }
         for (int j = threadIdx.x; j < H; j += blockDim.x) {
+            if (!rows_ok(a, base + j, 1)) continue;
             const float y = generic_y<HSrc, TX>(a, hsrc, base, j, inv);
             if constexpr (TO::kBytes == 1) {
                 uint16_t q;
@@ -1249,6 +1488,7 @@ __global__ void __launch_bounds__(256, CH <= 2 ? 4 : (CH <= 4 ? 2 : 1))
     pdl_launch_dependents(a.pdl);
     pdl_wait(a.pdl);
     for (int j = t; j < H; j += G) {
+        if (!cols_ok(a, j, 1)) continue;
         wsm[ragged_slot(j)] = __fadd_rn(a.has_w ? ld_elem<TI>(a.w, j) : 1.f, a.woff);
         if constexpr (BIAS) bsm[ragged_slot(j)] = ld_elem<TI>(a.b, j);
     }
@@ -1269,8 +1509,8 @@ __global__ void __launch_bounds__(256, CH <= 2 ? 4 : (CH <= 4 ? 2 : 1))
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
             const int v = c * G + t;
-            if (v < nv) {
-                const int64_t off = e0 + head + (int64_t)v * VE;
+            const int64_t off = e0 + head + (int64_t)v * VE;
+            if (v < nv && rows_ok(a, off, VE)) {
                 const uint4 xw = ld_stream16(xb + off * S);
                 hu[c][0] = xw.x;
                 hu[c][1] = xw.y;
@@ -1298,7 +1538,7 @@ __global__ void __launch_bounds__(256, CH <= 2 ? 4 : (CH <= 4 ? 2 : 1))
                 }
             }
         }
-        if (t < ne) {
+        if (t < ne && rows_ok(a, e0 + je, 1)) {
             he = ld_elem<TI>(a.x, e0 + je);
             if constexpr (RES) {
                 he = round_to<TI>(__fadd_rn(he, ld_elem<TI>(a.r, e0 + je)));
@@ -1310,7 +1550,7 @@ __global__ void __launch_bounds__(256, CH <= 2 ? 4 : (CH <= 4 ? 2 : 1))
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
             const int v = c * G + t;
-            if (v < nv) {
+            if (v < nv && rows_ok(a, e0 + head + (int64_t)v * VE, VE)) {
                 const int col = head + v * VE;
                 float y[VE];
 #pragma unroll
@@ -1330,7 +1570,7 @@ __global__ void __launch_bounds__(256, CH <= 2 ? 4 : (CH <= 4 ? 2 : 1))
                 st_stream16(static_cast<char*>(a.out) + (e0 + col) * S, u);
             }
         }
-        if (t < ne) {
+        if (t < ne && rows_ok(a, e0 + je, 1)) {
             const float tk = __fmul_rn(he, inv);
             const int sl = ragged_slot(je);
             st_elem<TI>(a.out, e0 + je, BIAS ? __fmaf_rn(wsm[sl], tk, bsm[sl]) : __fmul_rn(wsm[sl], tk));

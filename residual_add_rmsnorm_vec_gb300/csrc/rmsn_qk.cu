@@ -37,8 +37,13 @@ __global__ void __launch_bounds__(256) rmsn_qk_kernel(const QkArgs a) {
         void* row = is_q ? a.q : a.k;
         const int64_t e0 = is_q ? tok * a.qs + (int64_t)hh * a.D
                                 : tok * a.ks + (int64_t)(hh - a.Hq) * a.D;
-        const bool act = valid && sub < a.nvec;
         const int64_t e = e0 + (int64_t)sub * VE;
+        // elements of q (k) the heads span: (T - 1) * stride + heads * head_dim
+        const int64_t ext = is_q ? (a.T - 1) * a.qs + (int64_t)a.Hq * a.D
+                                 : (a.T - 1) * a.ks + (int64_t)a.Hk * a.D;
+        const bool act = valid && sub < a.nvec &&
+                         RMSN_CHECK(a.status, e >= 0 && e + VE <= ext &&
+                                                  (sub + 1) * 32 <= a.D * TI::kBytes);
         V8 x;
         float acc = 0.f;
         if (act) {

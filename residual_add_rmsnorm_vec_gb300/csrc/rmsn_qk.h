@@ -19,6 +19,7 @@ struct QkArgs {
     float eps;
     float woff;
     int32_t pdl;   // launched as a programmatic dependent
+    uint32_t* status;  // device status word (bit 1: a bounds check failed, checked build)
 };
 
 struct QkEntry {

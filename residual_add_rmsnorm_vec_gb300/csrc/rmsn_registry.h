@@ -27,15 +27,23 @@ struct RmsnArgs {
     int32_t early_params;  // weight / bias may be read before the prerequisite grid ends
     int32_t swz;           // bulk kernel: stages filled by 128-byte-swizzled tensor copies
     uint32_t* status;    // device status word: bit 0 = a bounded wait ran out
+    int64_t wait_cycles;  // bound of the ring's row waits in clock cycles; < 0: probe the
+                          // barrier once without waiting (tests of the expiry path)
 };
+
+// Default bound of a ring wait: about one second of SM clock cycles.
+constexpr int64_t kDefaultWaitCycles = 2000000000LL;
 
 enum DType : int32_t {
     kF32 = 0, kBF16 = 1, kFP8 = 2, kMXFP8 = 3, kMXFP4 = 4, kNVFP4 = 5, kF16 = 6
 };
 
-enum Variant : int32_t { kWarpRows = 0, kBlockRow = 1, kBulkRow = 2, kGeneric = 3, kRagged = 4 };
+enum Variant : int32_t {
+    kWarpRows = 0, kBlockRow = 1, kBulkRow = 2, kGeneric = 3, kRagged = 4, kCluster = 5
+};
 
-// One compiled kernel.
+// One compiled kernel.  For kCluster, max_warps holds the cluster size (blocks
+// of one warp per row).
 struct KernelEntry {
     int32_t in_dt, out_dt, variant, chunks, max_warps, stages, res, bias;
     int32_t res_f32;  // fp32 residual stream under a bf16 / fp16 in_dt

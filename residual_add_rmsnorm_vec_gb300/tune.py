@@ -160,22 +160,34 @@ def sweep(pkg, shapes, in_dt, out_dt, res, bias, reps, l2_hot_below=0):
     return out
 
 
+ROW_RE = (r"\s*\{(-?\d+), (-?\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)"
+          r"(?:, (\d+), (\d+))?\},(?:\s*// ([\d.]+) us, ([\d.]+) GB/s)?")
+
+
 def merge_table(entries, path):
     """Replace, in the table at `path`, the rows of each (input dtype, output
-    dtype, hidden) measured in `entries` and keep every other row, so a sweep
-    of some hidden sizes leaves the rows of the others in place."""
+    dtype, hidden, residual setting) measured in `entries` and keep every
+    other row, so a sweep of some hidden sizes (or of one residual setting)
+    leaves the rows of the others in place.  Rows written before the table
+    recorded the residual setting are read as measured with a residual, but
+    the fp32 rows (measured without one)."""
     import re
 
-    measured = {(DTYPE_CODES[e["in"]], DTYPE_CODES[e["out"]], e["H"]) for e in entries}
+    measured = {(DTYPE_CODES[e["in"]], DTYPE_CODES[e["out"]], e["H"], int(bool(e["res"])))
+                for e in entries}
     kept = []
     for line in open(path):
-        m = re.match(r"\s*\{(-?\d+), (-?\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)\},"
-                     r"(?:\s*// ([\d.]+) us, ([\d.]+) GB/s)?", line)
-        key = m and (int(m.group(1)), int(m.group(2)), int(m.group(3)))
-        if m and key not in measured and int(m.group(1)) >= 0:
-            v = [int(m.group(i)) for i in range(1, 9)]
-            kept.append(tuple(v[:4]) + tuple(v[4:8]) + (None, None,
-                        float(m.group(9) or 0), float(m.group(10) or 0)))
+        m = re.match(ROW_RE, line)
+        if not m or int(m.group(1)) < 0:
+            continue
+        v = [int(m.group(i)) for i in range(1, 9)]
+        res = int(m.group(9)) if m.group(9) is not None else int(v[0] != DTYPE_CODES["f32"])
+        bias = int(m.group(10)) if m.group(10) is not None else int(v[1] != DTYPE_CODES["bf16"]
+                                                                  and v[0] != DTYPE_CODES["f32"]
+                                                                  and v[0] < 6)
+        if (v[0], v[1], v[2], res) in measured:
+            continue
+        kept.append(tuple(v) + (res, bias, float(m.group(11) or 0), float(m.group(12) or 0)))
     write_table(entries, path, extra_rows=kept)
 
 
@@ -192,44 +204,60 @@ def write_table(entries, path, extra_rows=()):
         pick = min(near, key=lambda d: (d["warps_per_block"], d["variant"] != 1, d["stages"],
                                         d["us"]))
         rows.append((DTYPE_CODES[e["in"]], DTYPE_CODES[e["out"]], e["H"], e["T"], pick["variant"],
-                     pick["chunks"], pick["max_warps"], pick["stages"], e["res"], e["bias"],
-                     pick["us"], pick["gbs"]))
+                     pick["chunks"], pick["max_warps"], pick["stages"], int(bool(e["res"])),
+                     int(bool(e["bias"])), pick["us"], pick["gbs"]))
     rows.extend(extra_rows)
-    rows.sort(key=lambda r: r[:4])
+    rows.sort(key=lambda r: (r[0], r[1], r[2], -r[8], r[3]))
     lines = [
         "// Launch shapes chosen from measured bandwidth on a GB300 by",
         "// residual_add_rmsnorm_vec_gb300/tune.py (CUDA-graph replay of back-to-back",
         "// launches; inputs rotated past the L2 size from 512 tokens up, L2-hot below).",
         "// For one (input dtype, output dtype, hidden) the row with the largest",
-        "// t_min <= n_tokens applies; other shapes fall back to the fixed rule in the",
-        "// selector.  Input keys are DType codes, or 7 / 8 for bf16 / fp16",
-        "// activations over an fp32 residual stream.",
+        "// t_min <= n_tokens applies, among the rows measured with the caller's",
+        "// residual setting where the table has any; hidden sizes without rows take",
+        "// the rows of the nearest measured hidden size (within a factor of two),",
+        "// else the fixed rule in the selector.  Input keys are DType codes, or 7 / 8",
+        "// for bf16 / fp16 activations over an fp32 residual stream.  res / bias: the",
+        "// operands the row was measured with.",
         "struct TableRow {",
         "    int in_dt, out_dt;",
         "    int64_t hidden, t_min;",
         "    int variant, chunks, max_warps, stages;",
+        "    int res, bias;",
         "};",
         "",
         "static const TableRow kSelectorTable[] = {",
     ]
     seen = set()
     for r in rows:
-        key = r[:4]
+        key = r[:4] + (r[8],)
         if key in seen:
             continue
         seen.add(key)
-        lines.append(f"    {{{r[0]}, {r[1]}, {r[2]}, {r[3]}, {r[4]}, {r[5]}, {r[6]}, {r[7]}}},"
-                     f"  // {r[10]:.2f} us, {r[11]:.0f} GB/s")
+        lines.append(f"    {{{r[0]}, {r[1]}, {r[2]}, {r[3]}, {r[4]}, {r[5]}, {r[6]}, {r[7]}, "
+                     f"{r[8]}, {r[9]}}},  // {r[10]:.2f} us, {r[11]:.0f} GB/s")
     if not seen:
-        lines.append("    {-1, -1, 0, 0, 0, 0, 0, 0},")
-    lines += [
+        lines.append("    {-1, -1, 0, 0, 0, 0, 0, 0, 0, 0},")
+    lines += LOOKUP_CPP
+    with open(path, "w") as f:
+        f.write("\n".join(lines) + "\n")
+
+
+LOOKUP_CPP = [
         "};",
         "",
-        "bool table_lookup(int in_dt, int out_dt, int64_t hidden, int64_t n_tokens, int* variant,",
-        "                  int* chunks, int* max_warps, int* stages) {",
+        "// The row for (in_dt, out_dt, hidden) and n_tokens: among the rows measured",
+        "// with the residual setting `res` if there are any, else among the others.",
+        "bool table_lookup(int in_dt, int out_dt, int64_t hidden, int64_t n_tokens, int res,",
+        "                  int* variant, int* chunks, int* max_warps, int* stages) {",
+        "    bool same = false;",
+        "    for (const TableRow& r : kSelectorTable)",
+        "        same = same || (r.in_dt == in_dt && r.out_dt == out_dt && r.hidden == hidden &&",
+        "                        r.res == res);",
         "    const TableRow* best = nullptr;",
         "    for (const TableRow& r : kSelectorTable) {",
         "        if (r.in_dt != in_dt || r.out_dt != out_dt || r.hidden != hidden) continue;",
+        "        if (same && r.res != res) continue;",
         "        if (r.t_min <= n_tokens && (!best || r.t_min > best->t_min)) best = &r;",
         "    }",
         "    if (!best) return false;",
@@ -239,10 +267,33 @@ def write_table(entries, path, extra_rows=()):
         "    *stages = best->stages;",
         "    return true;",
         "}",
-    ]
-    with open(path, "w") as f:
-        f.write("\n".join(lines) + "\n")
-
+        "",
+        "// Measured hidden sizes of (in_dt, out_dt) other than `hidden` and within a",
+        "// factor of two of it, nearest first by ratio (the smaller of two equally",
+        "// near first); writes at most `cap`, returns how many.",
+        "int table_neighbours(int in_dt, int out_dt, int64_t hidden, int64_t* out, int cap) {",
+        "    int n = 0;",
+        "    for (const TableRow& r : kSelectorTable) {",
+        "        if (r.in_dt != in_dt || r.out_dt != out_dt || r.hidden == hidden) continue;",
+        "        if (r.hidden > 2 * hidden || 2 * r.hidden < hidden) continue;",
+        "        bool seen = false;",
+        "        for (int i = 0; i < n; ++i) seen = seen || out[i] == r.hidden;",
+        "        if (seen || n >= cap) continue;",
+        "        // insert in order: a before b when max(a,h)/min(a,h) < max(b,h)/min(b,h)",
+        "        const int64_t a = r.hidden;",
+        "        int i = n++;",
+        "        for (; i > 0; --i) {",
+        "            const int64_t b = out[i - 1];",
+        "            const int64_t lhs = (a > hidden ? a : hidden) * (b < hidden ? b : hidden);",
+        "            const int64_t rhs = (b > hidden ? b : hidden) * (a < hidden ? a : hidden);",
+        "            if (lhs > rhs || (lhs == rhs && a > b)) break;",
+        "            out[i] = b;",
+        "        }",
+        "        out[i] = a;",
+        "    }",
+        "    return n;",
+        "}",
+]
 
 def main():
     import torch

@@ -30,7 +30,8 @@ def test_header_declares_the_boundary():
     assert names == sorted(["rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_fwd_blockscaled",
                             "rmsnorm_fwd_host",
                             "rmsnorm_qk_fwd", "rmsnorm_query_config", "rmsnorm_list_configs",
-                            "rmsnorm_read_status", "rmsnorm_status_string"]), names
+                            "rmsnorm_read_status", "rmsnorm_set_wait_limit",
+                            "rmsnorm_status_string"]), names
 
 
 def test_library_exports_every_declared_symbol(lib):

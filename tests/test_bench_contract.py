@@ -42,6 +42,14 @@ def test_reference_arm_line(extra, workload):
     assert workload in d["config"]["workload"]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
+    # the same config object as the repo's own arm prints (bench.step_config)
+    from residual_add_rmsnorm_vec_gb300 import synth
+
+    class A:
+        out = "fp8" if "--out" in extra else "bf16"
+        hidden = int(extra[extra.index("--hidden") + 1]) if "--hidden" in extra else 8192
+    tokens = int(extra[extra.index("--tokens") + 1]) if "--tokens" in extra else 16384
+    assert d["config"] == bench.step_config(bench.step_workload(synth, A, tokens), 1)
 
 
 def test_reference_arm_other_ranks_print_nothing():

@@ -174,3 +174,42 @@ def test_block_formats_zero_rows_and_rejections(pkg):
     # NVFP4 needs the per-token scale
     assert pkg.rmsnorm_fwd_blockscaled(p, None, None, None, p, p, None, None, 2, 64, 1e-6, flags,
                                        pkg.RMSN_FMT_NVFP4, 0.0, None, s) == pkg.RMSN_EINVAL
+
+
+E2M1_MIDPOINTS = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+
+
+def test_nvfp4_codes_differ_only_at_rounding_midpoints(pkg):
+    # The GPU forms NVFP4 codes as E2M1(y * r_b) with r_b within 1 fp32 ulp
+    # of 1 / (c_b g).  On the FP8-with-bias shape, every code that differs
+    # from E2M1 of the exact quotient (fp64 y over the GPU's own scales) must
+    # have that quotient within fp32 rounding of an E2M1 midpoint; the
+    # fraction of codes equal to the oracle's is printed.
+    wl = synth.Workload("nv_mid", 4096, 5120, 40, "bf16", "bf16", 1e-6, has_bias=True)
+    inp = synth.make_inputs(wl)
+    g = parity.to_device(inp, "cuda")
+    q, bs, ts, _ = pkg.fused_add_rmsnorm_blockscaled(g["x"], g["residual"], g["weight"],
+                                                     g["bias"], eps=wl.eps, fmt="nvfp4")
+    torch.cuda.synchronize()
+    ref = oracle.rmsnorm_block(inp["x"], inp["residual"], inp["weight"], inp["bias"],
+                               eps=float(np.float32(wl.eps)), in_dtype="bf16", fmt="nvfp4")
+    orc = oracle.default()
+    gq = unpack4(q.cpu().numpy())
+    bs, ts = bs.cpu().numpy(), ts.cpu().numpy()
+    dec = np.array([orc.e4m3_to_f64(c) for c in range(256)])
+    s = dec[bs].repeat(16, axis=1) * ts.astype(np.float64)[:, None]
+    quot = np.where(s > 0, ref["y64"] / np.where(s > 0, s, 1), 0.0)
+    e2m1 = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    mag = np.minimum(np.abs(quot), 6.0)
+    idx = np.abs(mag[..., None] - e2m1).argmin(axis=-1)  # nearest; ties resolved below
+    want = np.where(quot < 0, 8, 0) + idx
+    diff = np.abs(ordered4(gq) - ordered4(want.astype(np.uint8)))
+    off = diff != 0
+    near = np.min(np.abs(mag[..., None] - E2M1_MIDPOINTS), axis=-1)
+    assert diff.max() <= 1
+    assert np.all(near[off] <= 1e-5 * np.maximum(mag[off], 0.25)), \
+        "a code differs from E2M1 of the exact quotient away from a rounding midpoint"
+    exact = float((gq == unpack4(ref["q"])).mean())
+    print(f"\nNVFP4 4096x5120 with bias: {exact:.6f} of codes equal the oracle's; "
+          f"{int(off.sum())} differ from E2M1 of the exact quotient, all at midpoints")
+    assert exact > 0.999

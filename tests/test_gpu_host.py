@@ -96,3 +96,34 @@ def test_host_entry_validates_before_launch(pkg):
     assert pkg.rmsnorm_fwd_host(None, None, None, None, None, None, None, 0, 64, 1e-6,
                                 pkg.make_flags("bf16", "bf16", False, False, False), 0.0,
                                 None) == pkg.RMSN_OK
+
+
+def test_other_gpu_memory_refused_before_launch(pkg):
+    # device memory of another GPU cannot be read without peer access: the
+    # host entry refuses it on the host, before anything is launched
+    if torch.cuda.device_count() < 2:
+        pytest.skip("needs a second GPU to hold the foreign buffer")
+    T, H = 4, 256
+    x = torch.zeros((T, H), dtype=torch.bfloat16, device="cuda:1")
+    out = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    torch.cuda.set_device(0)
+    st = pkg.rmsnorm_fwd_host(x.data_ptr(), None, None, None, out.data_ptr(), None, None, T, H,
+                              1e-6, pkg.make_flags("bf16", "bf16", False, False, False), 0.0,
+                              torch.cuda.current_stream(0).cuda_stream)
+    assert st == pkg.RMSN_EINVAL
+
+
+def test_own_device_memory_accepted(pkg):
+    # the same call with the buffer on the current GPU runs and is correct
+    wl = synth.Workload("host_own_dev", 4, 256, 3, "bf16", "bf16", 1e-6, has_residual=False,
+                        has_weight=False)
+    inp = synth.make_inputs(wl)
+    x = inp["x"].to("cuda:0")
+    out = torch.empty((4, 256), dtype=torch.bfloat16).pin_memory()
+    st = pkg.rmsnorm_fwd_host(x.data_ptr(), None, None, None, out.data_ptr(), None, None, 4, 256,
+                              1e-6, pkg.make_flags("bf16", "bf16", False, False, False), 0.0,
+                              torch.cuda.current_stream(0).cuda_stream)
+    assert st == pkg.RMSN_OK
+    torch.cuda.synchronize()
+    parity.compare(wl, parity.gpu_outputs_to_host(wl, out, None, None),
+                   parity.oracle_run(wl, inp), "own device")

@@ -163,6 +163,25 @@ def test_every_config(pkg, fs, H):
     assert pkg.rmsnorm_read_status() == 0
 
 
+@pytest.mark.parametrize("T", synth.DECODE_TOKENS)
+def test_cluster_variant_decode(pkg, T):
+    # the split-row variant: each row over a cluster of one-warp blocks that
+    # exchange partial sums through distributed shared memory, every built
+    # cluster size, on the decode workload (and with a bias and an offset)
+    wl = synth.decode_workload(T)
+    flags = pkg.make_flags("bf16", "bf16", True, True, False)
+    cfgs = [c for c in pkg.rmsnorm_list_configs(T, 4096, flags)
+            if c.variant == pkg.VARIANT_CLUSTER]
+    assert {c.cluster for c in cfgs} == {2, 4, 8}
+    for c in cfgs:
+        assert c.grid == T * c.cluster and c.warps_per_block == 1
+        check(pkg, wl, config=c, where=f"cluster {c.as_dict()}")
+    wlb = synth.Workload(f"cluster_bias_T{T}", T, 4096, 83, "bf16", "bf16", 1e-6, has_bias=True)
+    for c in pkg.rmsnorm_list_configs(T, 4096, pkg.make_flags("bf16", "bf16", True, True, True)):
+        if c.variant == pkg.VARIANT_CLUSTER:
+            check(pkg, wlb, config=c, weight_offset=0.5, where=f"cluster bias {c.as_dict()}")
+
+
 @pytest.mark.parametrize("T,H", [(1, 4096), (256, 4096), (2048, 8192), (4096, 5120)])
 def test_fp16_io(pkg, T, H):
     wl = synth.Workload(f"f16_T{T}_H{H}", T, H, 80, "f16", "f16", 1e-6, has_bias=H == 5120,

@@ -29,7 +29,7 @@ def pkg():
     return p
 
 
-def chain(pkg, inp, eps, n, pdl, early, graph=False):
+def chain(pkg, inp, eps, n, pdl, early, graph=False, config=None):
     x0 = inp["x"].cuda()
     r0 = inp["residual"].cuda()
     w = inp["weight"].cuda()
@@ -40,7 +40,8 @@ def chain(pkg, inp, eps, n, pdl, early, graph=False):
     def run():
         for k in range(n):
             pkg.fused_add_rmsnorm(xs[k], rs[k], w, None, eps=eps, out=xs[k + 1],
-                                  residual_out=rs[k + 1], pdl=pdl, early_params=early)
+                                  residual_out=rs[k + 1], pdl=pdl, early_params=early,
+                                  config=config)
 
     if graph:
         run()  # warm the launch-shape caches before capture
@@ -78,6 +79,23 @@ def test_pdl_chain_matches_plain_chain(pkg, T, H, early):
     got = {"out": ref[0], "residual_out": ref[n], "out_scale": None}
     parity.compare(wl, got, o, "pdl chain first call")
     assert pkg.rmsnorm_read_status() == 0
+
+
+@pytest.mark.parametrize("T", [1, 32, 256])
+def test_pdl_chain_cluster_variant(pkg, T):
+    # the split-row cluster launches chained by PDL (both launch attributes)
+    # give the same bits as the plain chain, eagerly and in a graph
+    wl = synth.Workload(f"pdl_cluster_T{T}", T, 4096, 23, "bf16", "bf16", 1e-6)
+    inp = synth.make_inputs(wl)
+    flags = pkg.make_flags("bf16", "bf16", True, True, False)
+    for c in pkg.rmsnorm_list_configs(T, 4096, flags):
+        if c.variant != pkg.VARIANT_CLUSTER:
+            continue
+        ref = chain(pkg, inp, wl.eps, 4, pdl=False, early=False, config=c)
+        for graph in (False, True):
+            got = chain(pkg, inp, wl.eps, 4, pdl=True, early=True, graph=graph, config=c)
+            for k, (a, b) in enumerate(zip(got, ref)):
+                assert np.array_equal(a, b), (c.cluster, graph, k)
 
 
 def test_early_params_needs_pdl(pkg):

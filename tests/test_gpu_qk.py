@@ -71,6 +71,7 @@ def test_qk_norm_fused_qkv(pkg, T, Hq, Hk, D, dtype, pad):
     # value heads and padding untouched
     assert np.array_equal(got[:, (Hq + Hk) * D:], orig[:, (Hq + Hk) * D:])
     assert S == (Hq + 2 * Hk) * D + pad
+    assert pkg.rmsnorm_read_status() == 0
 
 
 def test_qk_norm_contiguous_heads_no_weights_and_pdl(pkg):

@@ -1,0 +1,87 @@
+"""The bulk-copy kernel's give-up path, run on a healthy GPU.
+
+Every wait of the ring kernel for a row to land in shared memory is bounded.
+rmsnorm_set_wait_limit(-1) makes each wait test its barrier once and not
+wait, so on rows whose copies are still in flight the wait runs out while
+the copies themselves complete normally.  The kernel must then return, set
+bit 0 of the status word, leave every row it did not finish unwritten, and
+have finished rows equal to the oracle's; the block drains its own copies
+with the default bound before it exits, so the device stays usable.
+"""
+import numpy as np
+import pytest
+import torch
+
+import parity
+from residual_add_rmsnorm_vec_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+CANARY = 0x7FC1  # a bf16 NaN pattern the kernel never writes for finite inputs
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from residual_add_rmsnorm_vec_gb300 import build
+
+    build.build()
+    import residual_add_rmsnorm_vec_gb300 as p
+
+    torch.cuda.set_device(0)
+    return p
+
+
+def ring_config(pkg, stages):
+    return pkg.RmsnConfig.from_dict({"variant": pkg.VARIANT_BULK_ROW, "chunks": 2,
+                                     "max_warps": 16, "stages": stages})
+
+
+def run(pkg, g, cfg, T, H):
+    out = torch.full((T, H), CANARY, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    res = torch.full((T, H), CANARY, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    pkg.fused_add_rmsnorm(g["x"], g["residual"], g["weight"], g["bias"], eps=1e-6, out=out,
+                          residual_out=res, config=cfg)
+    torch.cuda.synchronize()
+    return parity.bits16(out), parity.bits16(res)
+
+
+@pytest.mark.parametrize("stages", [2, 4])
+def test_wait_that_runs_out_stops_cleanly(pkg, stages):
+    T, H = 4096, 8192
+    wl = synth.Workload("wait_expiry", T, H, 95, "bf16", "bf16", 1e-6, has_bias=True)
+    inp = synth.make_inputs(wl)
+    ref = parity.oracle_run(wl, inp)
+    g = parity.to_device(inp, DEV)
+    cfg = ring_config(pkg, stages)
+    pkg.rmsnorm_read_status(clear=True)
+    hits, finished = 0, 0
+    try:
+        assert pkg.rmsnorm_set_wait_limit(-1) == pkg.RMSN_OK
+        for _ in range(4):
+            out, res = run(pkg, g, cfg, T, H)
+            status = pkg.rmsnorm_read_status(clear=True)
+            done = ~np.all(out == CANARY, axis=1)  # rows the kernel wrote an output for
+            # a row is written whole or not at all
+            assert np.all(np.all(out[done] != CANARY, axis=1))
+            # finished rows: exactly the oracle's residual, output within 1 ulp
+            assert np.array_equal(res[done], ref["residual_out"][done])
+            d = np.abs(parity.ordered16(out[done]) - parity.ordered16(ref["out"][done]))
+            assert d.size == 0 or d.max() <= parity.BF16_ULP
+            finished += int(done.sum())
+            if status & 1:
+                hits += 1
+                assert not done.all(), "the status says a wait ran out, yet every row finished"
+            else:
+                assert done.all(), "rows were left unwritten with no wait reported"
+    finally:
+        pkg.rmsnorm_set_wait_limit(0)
+        pkg.rmsnorm_read_status(clear=True)
+    assert hits >= 1, "no wait ran out although none was allowed to wait"
+    # the device is still usable: the default bound gives the full result
+    out, res = run(pkg, g, cfg, T, H)
+    assert pkg.rmsnorm_read_status() == 0
+    got = {"out": out, "residual_out": res, "out_scale": None}
+    parity.compare(wl, got, ref, "after the give-up path", bias=inp["bias"])

@@ -40,7 +40,8 @@ def codes():
 def rows():
     out = []
     for line in read("rmsn_selector_table.inc").splitlines():
-        m = re.match(r"\s*\{(-?\d+), (-?\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)\},", line)
+        m = re.match(r"\s*\{(-?\d+), (-?\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), "
+                     r"([01]), ([01])\},", line)
         if m:
             out.append(tuple(int(v) for v in m.groups()))
     assert out, "no rows parsed"
@@ -90,7 +91,7 @@ def test_tuner_writes_the_library_codes(codes):
 def test_every_row_names_a_built_kernel(rows, instantiated, codes):
     _, variants, _, max_stages = codes
     for r in rows:
-        tin, tout, hidden, t_min, variant, ch, wmax, stages = r
+        tin, tout, hidden, t_min, variant, ch, wmax, stages, res, bias = r
         assert (tin, tout) in instantiated, f"no translation unit for {r}"
         assert (variant, ch, wmax) in instantiated[(tin, tout)], f"kernel not built: {r}"
         if variant == variants["kBulkRow"]:
@@ -103,7 +104,7 @@ def test_every_row_names_a_built_kernel(rows, instantiated, codes):
 def test_rows_cover_every_token_count_in_order(rows):
     groups = {}
     for r in rows:
-        groups.setdefault(r[:3], []).append(r[3])
+        groups.setdefault(r[:3] + (r[8],), []).append(r[3])
     for key, t_mins in groups.items():
         assert t_mins[0] == 1, f"{key}: first row starts at {t_mins[0]} tokens"
         assert all(a < b for a, b in zip(t_mins, t_mins[1:])), f"{key}: {t_mins}"
@@ -117,3 +118,19 @@ def test_rows_are_whole_vector_shapes(rows, codes):
             r32["kTableBF16R32"]: 4, r32["kTableF16R32"]: 4}
     for r in rows:
         assert (r[2] * elem[r[0]]) % 32 == 0, r
+
+
+def test_rows_record_the_operands_they_were_measured_with(rows, codes):
+    """Each row says whether its sweep had a residual and a bias: the 16-bit
+    and fp32-stream rows were measured with a residual and no bias, the
+    quantised outputs with both, the fp32 rows with neither."""
+    dtypes, _, r32, _ = codes
+    quant = {dtypes[k] for k in ("kFP8", "kMXFP8", "kMXFP4", "kNVFP4")}
+    for r in rows:
+        tin, tout, res, bias = r[0], r[1], r[8], r[9]
+        if tin == dtypes["kF32"]:
+            assert (res, bias) == (0, 0), r
+        elif tout in quant:
+            assert (res, bias) == (1, 1), r
+        else:
+            assert bias == 0, r

@@ -12,7 +12,8 @@ import pytest
 
 from residual_add_rmsnorm_vec_gb300 import tune
 
-ROW = re.compile(r"\s*\{(-?\d+), (-?\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)\},")
+ROW = re.compile(r"\s*\{(-?\d+), (-?\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), "
+                 r"(\d+), (\d+)\},")
 
 
 def cand(variant, warps, us, chunks=2, max_warps=16, stages=0):
@@ -20,8 +21,8 @@ def cand(variant, warps, us, chunks=2, max_warps=16, stages=0):
             "max_warps": max_warps, "stages": stages, "us": us, "gbs": 1e3 / us}
 
 
-def entry(T, H, cands, i="bf16", o="bf16"):
-    return {"T": T, "H": H, "in": i, "out": o, "res": True, "bias": False,
+def entry(T, H, cands, i="bf16", o="bf16", res=True):
+    return {"T": T, "H": H, "in": i, "out": o, "res": res, "bias": False,
             "best": min(cands, key=lambda d: d["us"]), "all": cands}
 
 
@@ -45,7 +46,7 @@ def test_tie_break_prefers_fewer_warps_then_register_kernel_then_fewer_stages(tm
     ]
     path = tmp_path / "t.inc"
     tune.write_table(entries, str(path))
-    got = {r[3]: r[4:] for r in rows_of(path) if r[:3] == (bf, bf, 4096)}
+    got = {r[3]: r[4:8] for r in rows_of(path) if r[:3] == (bf, bf, 4096)}
     assert got[1] == (1, 2, 16, 0)
     assert got[16] == (2, 2, 16, 2)
     assert got[256] == (1, 2, 8, 0)
@@ -66,7 +67,12 @@ def test_merge_replaces_only_the_measured_hidden_sizes(tmp_path):
     assert [r for r in after if r[2] == 5120] == [r for r in before if r[2] == 5120]
     # the measured (pair, hidden) is replaced whole: its 4096-token row goes
     fp8 = [r for r in after if r[1] == c["fp8"] and r[2] == 4096]
-    assert fp8 == [(c["bf16"], c["fp8"], 4096, 1, 1, 2, 16, 0)]
+    assert fp8 == [(c["bf16"], c["fp8"], 4096, 1, 1, 2, 16, 0, 1, 0)]
+    # a sweep without a residual adds its own rows and keeps those with one
+    tune.merge_table([entry(1, 4096, [cand(1, 4, 2.0)], res=False)], str(path))
+    bf = [r for r in rows_of(path) if r[:3] == (c["bf16"], c["bf16"], 4096)]
+    assert sorted(r[8] for r in bf) == [0, 1] and (c["bf16"], c["bf16"], 4096, 1, 1, 2, 16, 0,
+                                                   0, 0) in bf
 
 
 HARNESS = r"""
@@ -79,7 +85,7 @@ int main() {
                               {1, 2, 4096, 64}};
     for (auto& x : q) {
         int v = -1, c = -1, w = -1, s = -1;
-        const bool f = table_lookup((int)x[0], (int)x[1], x[2], x[3], &v, &c, &w, &s);
+        const bool f = table_lookup((int)x[0], (int)x[1], x[2], x[3], 1, &v, &c, &w, &s);
         std::printf("%d %d %d %d %d\n", f ? 1 : 0, v, c, w, s);
     }
     return 0;
@@ -108,3 +114,54 @@ def test_generated_lookup_takes_the_largest_threshold_not_above_the_tokens(tmp_p
         (0, -1, -1, -1, -1),  # a hidden size without rows
         (0, -1, -1, -1, -1),  # a dtype pair without rows
     ]
+
+
+NEIGHBOURS = r"""
+#include <cstdint>
+#include <cstdio>
+#include "t.inc"
+int main() {
+    const long long q[] = {2560, 3584, 6656, 10240, 4096, 1024, 40000, 12288};
+    for (long long h : q) {
+        int64_t out[16];
+        const int n = table_neighbours(1, 1, h, out, 16);
+        std::printf("%lld:", h);
+        for (int i = 0; i < n; ++i) std::printf(" %lld", (long long)out[i]);
+        std::printf("\n");
+    }
+    // residual setting: rows measured without a residual win for res = 0 only
+    int v, c, w, s;
+    table_lookup(1, 1, 4096, 8, 0, &v, &c, &w, &s);
+    std::printf("res0 %d %d\n", c, w);
+    table_lookup(1, 1, 4096, 8, 1, &v, &c, &w, &s);
+    std::printf("res1 %d %d\n", c, w);
+    // only rows with a residual at 8192: a call without one takes them
+    const bool f = table_lookup(1, 1, 8192, 8, 0, &v, &c, &w, &s);
+    std::printf("fallback %d %d %d\n", f ? 1 : 0, c, w);
+    return 0;
+}
+"""
+
+
+@pytest.mark.skipif(shutil.which("g++") is None, reason="no host C++ compiler")
+def test_generated_neighbours_nearest_first_and_residual_rows(tmp_path):
+    rows = [entry(1, h, [cand(1, 8, 2.0, max_warps=8)]) for h in (2048, 3072, 4096, 5120, 8192,
+                                                                  16384)]
+    rows.append(entry(1, 4096, [cand(1, 4, 1.0, chunks=1, max_warps=4)], res=False))
+    tune.write_table(rows, str(tmp_path / "t.inc"))
+    (tmp_path / "h.cpp").write_text(NEIGHBOURS)
+    subprocess.run(["g++", "-std=c++17", "-O1", "-o", str(tmp_path / "h"), str(tmp_path / "h.cpp")],
+                   check=True, cwd=tmp_path)
+    out = subprocess.run([str(tmp_path / "h")], check=True, capture_output=True,
+                         text=True).stdout.splitlines()
+    assert out[:8] == [
+        "2560: 3072 2048 4096 5120",  # ratios 1.2, 1.25, 1.6, 2.0
+        "3584: 4096 3072 5120 2048",  # 1.143, 1.167, 1.429, 1.75 (8192 is beyond 2x)
+        "6656: 8192 5120 4096",       # 1.231, 1.3, 1.625
+        "10240: 8192 16384 5120",     # 1.25, 1.6, 2.0
+        "4096: 5120 3072 2048 8192",  # not itself; 2048 and 8192 tie at 2.0: smaller first
+        "1024: 2048",
+        "40000:",
+        "12288: 16384 8192",
+    ]
+    assert out[8:] == ["res0 1 4", "res1 2 8", "fallback 1 2 8"]
