@@ -638,7 +638,7 @@ def run_qk(pkg, synth, dev, stream):
     Hq, Hk, D = 32, 8, 128
     peak, _ = load_peaks()
     out = {"heads": f"{Hq} q + {Hk} k heads x {D}, bf16", "unit": "us/call"}
-    for T in (1, 64, 4096, 16384):
+    for T in (1, 64, 512, 1024, 4096, 16384):
         inp = synth.qk_inputs(T, Hq, Hk, D, "bf16")
         n_sets = 2 if T >= 16384 else 1
         wq, wk = inp["q_weight"].to(dev), inp["k_weight"].to(dev)
@@ -650,9 +650,9 @@ def run_qk(pkg, synth, dev, stream):
             sets.append((qkv, q, k, q.contiguous(), k.contiguous()))
         fl = pkg.make_flags("bf16", "bf16", False, True, False)
 
-        def qk_call(i):
+        def qk_call(i, variant=None):
             _, q, k, _, _ = sets[i % n_sets]
-            pkg.qk_norm_(q, k, wq, wk, head_dim=D, eps=1e-6)
+            pkg.qk_norm_(q, k, wq, wk, head_dim=D, eps=1e-6, variant=variant)
 
         def rows_call(i):
             _, _, _, qc, kc = sets[i % n_sets]
@@ -688,10 +688,14 @@ def run_qk(pkg, synth, dev, stream):
         nbytes = 2 * T * (Hq + Hk) * D * 2 + 2 * D * 2
         us_qk = graph_us(qk_call)
         us_rows = graph_us(rows_call)
+        # both QK kernels forced: the ring variant and the one-pass register kernel
+        us_ring = graph_us(lambda i: qk_call(i, "ring"))
+        us_direct = graph_us(lambda i: qk_call(i, "direct"))
         res = {"qk_us": round(us_qk, 3), "qk_gbs": round(nbytes / us_qk / 1e3, 1),
                "row_norm_us": round(us_rows, 3),
                "row_norm_gbs": round(nbytes / us_rows / 1e3, 1),
-               "speedup": round(us_rows / us_qk, 2)}
+               "speedup": round(us_rows / us_qk, 2),
+               "ring_us": round(us_ring, 3), "direct_us": round(us_direct, 3)}
         if n_sets > 1:
             res["qk_frac_of_peak"] = round(nbytes / us_qk / 1e3 / peak, 4)
             res["buffer_sets"] = n_sets

@@ -226,12 +226,21 @@ int rmsnorm_fwd_host(const void* x, const void* residual, const void* weight, co
  * are not touched.  The q buffer must span (n_tokens - 1) * q_token_stride +
  * n_q_heads * head_dim elements (likewise k).  flags: RMSN_IN_F32,
  * RMSN_IN_BF16 or RMSN_IN_F16 (q, k and weights share it), optionally
- * RMSN_PDL.  One launch
- * covers both q and k.  The fast path needs head_dim * element size to be a
+ * RMSN_PDL, and at most one of RMSN_QK_RING / RMSN_QK_DIRECT.  One launch
+ * covers both q and k.  Long batches (from 1024 tokens, where a head is 4 to
+ * 32 whole 32-byte vectors and a token's heads at most 2048 of them) take a
+ * ring variant: persistent blocks stream each token's query and key heads
+ * into shared memory with TMA bulk copies and hold the weights in registers;
+ * shorter ones a one-pass register kernel.  The fast path needs head_dim * element size to be a
  * multiple of 32 bytes and at most 1024 bytes (head_dim 64, 128, 256 in bf16
  * and fp32, 512 in bf16), 32-byte aligned pointers and token strides;
  * otherwise RMSN_EUNSUPPORTED.  Returns an rmsn_status.
  */
+#define RMSN_QK_RING 0x400u   /* rmsnorm_qk_fwd: take the ring variant whatever the batch
+                                 (RMSN_EUNSUPPORTED where it does not apply); for tests
+                                 and tuning */
+#define RMSN_QK_DIRECT 0x800u /* rmsnorm_qk_fwd: take the one-pass register kernel */
+
 int rmsnorm_qk_fwd(void* q, void* k, const void* q_weight, const void* k_weight,
                    int64_t n_tokens, int64_t n_q_heads, int64_t n_k_heads, int64_t head_dim,
                    int64_t q_token_stride, int64_t k_token_stride, float eps,

@@ -35,6 +35,8 @@ RMSN_HAS_BIAS = 0x40
 RMSN_PDL = 0x80
 RMSN_RESIDUAL_F32 = 0x200
 RMSN_PDL_EARLY_PARAMS = 0x100
+RMSN_QK_RING = 0x400
+RMSN_QK_DIRECT = 0x800
 
 VARIANT_WARP_ROWS = 0
 VARIANT_BLOCK_ROW = 1

@@ -174,12 +174,13 @@ def fused_add_rmsnorm_host(x: torch.Tensor, residual: torch.Tensor | None = None
 def qk_norm_(q: torch.Tensor | None, k: torch.Tensor | None, q_weight: torch.Tensor | None = None,
              k_weight: torch.Tensor | None = None, *, head_dim: int, eps: float,
              weight_offset: float = 0.0, stream: torch.cuda.Stream | None = None,
-             pdl: bool = False):
+             pdl: bool = False, variant: str | None = None):
     """Per-head QK norm of q and k IN PLACE (``rmsnorm_qk_fwd``).
 
     q is [T, Hq * head_dim] or [T, Hq, head_dim], or a column slice of a
     fused qkv matrix (its row stride is used as the token stride); likewise
-    k.  Either may be None.  Returns (q, k).
+    k.  Either may be None.  ``variant``: None (the library's choice), "ring"
+    or "direct" (force one kernel; for tests and tuning).  Returns (q, k).
     """
     def view2d(t):
         if t is None:
@@ -217,6 +218,7 @@ def qk_norm_(q: torch.Tensor | None, k: torch.Tensor | None, q_weight: torch.Ten
     _check("q_weight", q_weight, (head_dim,), (ref.dtype,), ref.device)
     _check("k_weight", k_weight, (head_dim,), (ref.dtype,), ref.device)
     flags = _IN[ref.dtype] | (_lib.RMSN_PDL if pdl else 0)
+    flags |= {None: 0, "ring": _lib.RMSN_QK_RING, "direct": _lib.RMSN_QK_DIRECT}[variant]
     s = stream if stream is not None else torch.cuda.current_stream(ref.device)
     st = _lib.rmsnorm_qk_fwd(_ptr(q2), _ptr(k2), _ptr(q_weight), _ptr(k_weight), ref.shape[0],
                              hq, hk, head_dim, qs, ks, eps, weight_offset, flags, s.cuda_stream)

@@ -34,6 +34,11 @@ namespace rmsn {
 namespace {
 
 constexpr int kMaxDevices = 64;
+// QK norm takes its ring variant from this many tokens up (measured on GB300:
+// below it the one-pass register kernel finishes sooner), with about this
+// many bytes of token buffers per block.
+constexpr int64_t kQkRingTokens = 1024;
+constexpr int64_t kQkRingBytes = 96 * 1024;
 constexpr int64_t kMaxHidden = int64_t(1) << 24;
 
 // Status word of the kernels on each device (bit 0: a bounded wait ran out).
@@ -937,7 +942,8 @@ RMSN_API int rmsnorm_qk_fwd(void* q, void* k, const void* q_weight, const void* 
                             int64_t n_tokens, int64_t n_q_heads, int64_t n_k_heads,
                             int64_t head_dim, int64_t q_token_stride, int64_t k_token_stride,
                             float eps, float weight_offset, uint32_t flags, cudaStream_t stream) {
-    if (flags & ~(RMSN_IN_MASK | RMSN_PDL)) return RMSN_EINVAL;
+    if (flags & ~(RMSN_IN_MASK | RMSN_PDL | RMSN_QK_RING | RMSN_QK_DIRECT)) return RMSN_EINVAL;
+    if ((flags & RMSN_QK_RING) && (flags & RMSN_QK_DIRECT)) return RMSN_EINVAL;
     const uint32_t in = flags & RMSN_IN_MASK;
     if (in != RMSN_IN_F32 && in != RMSN_IN_BF16 && in != RMSN_IN_F16) return RMSN_EINVAL;
     const int dt = in == RMSN_IN_F32 ? kF32 : (in == RMSN_IN_BF16 ? kBF16 : kF16);
@@ -967,18 +973,50 @@ RMSN_API int rmsnorm_qk_fwd(void* q, void* k, const void* q_weight, const void* 
     const int nvec = (int)(head_dim * bytes / 32);
     int tph = 1;
     while (tph < nvec) tph *= 2;
-    const QkEntry* e = nullptr;
+    const QkEntry* table = nullptr;
     int n = 0;
-    const QkEntry* table = qk_kernels(&n);
+    table = qk_kernels(&n);
+    // the ring variant: a token's heads are whole warps' worth of vectors
+    // (vectors per head a power of two from 4 up), at most 2048 vectors per
+    // token (two per thread), at least two token buffers in shared memory
+    const int64_t tok_vecs = (n_q_heads + n_k_heads) * nvec;
+    const int64_t tok_bytes = tok_vecs * 32;
+    const bool ring_ok = tph == nvec && nvec >= 4 && tok_vecs <= 2048 &&
+                         2 * tok_bytes <= d->max_smem - 1024;
+    bool ring = ring_ok && n_tokens >= kQkRingTokens;
+    if (flags & RMSN_QK_RING) {
+        if (!ring_ok) return RMSN_EUNSUPPORTED;
+        ring = true;
+    }
+    if (flags & RMSN_QK_DIRECT) ring = false;
+    const int ch = tok_vecs > 1024 ? 2 : 1;
+    const QkEntry* e = nullptr;
     for (int i = 0; i < n; ++i)
-        if (table[i].dt == dt && table[i].tph == tph) e = &table[i];
+        if (table[i].dt == dt && table[i].tph == tph && table[i].ring == (ring ? ch : 0))
+            e = &table[i];
     if (!e) return RMSN_EUNSUPPORTED;
-    const int threads = 256;
-    const int64_t heads = (n_q_heads + n_k_heads) * n_tokens;
-    const int64_t need = (heads * tph + threads - 1) / threads;
-    const int bps = blocks_per_sm(d, e->fn, threads, 0);
-    const int64_t resident = (int64_t)d->num_sms * (bps > 0 ? bps : 1);
-    const int64_t grid = need < resident ? need : resident;
+    int threads = 256, stages = 0;
+    size_t smem = 0;
+    int64_t grid = 0;
+    if (ring) {
+        threads = (int)(((tok_vecs + ch - 1) / ch + 31) / 32 * 32);
+        // about 96 KiB of token buffers per block (two blocks per SM), 2..8 of them
+        stages = (int)(kQkRingBytes / tok_bytes);
+        stages = stages < 2 ? 2 : (stages > kMaxStages ? kMaxStages : stages);
+        smem = (size_t)stages * (size_t)tok_bytes;
+        if ((int64_t)smem > 48 * 1024 && (int64_t)smem > enable_smem(d, e->fn))
+            return RMSN_EUNSUPPORTED;
+        const int bps = blocks_per_sm(d, e->fn, threads, (int)smem);
+        if (bps < 1) return RMSN_EUNSUPPORTED;
+        const int64_t resident = (int64_t)d->num_sms * bps;
+        grid = n_tokens < resident ? n_tokens : resident;
+    } else {
+        const int64_t heads = (n_q_heads + n_k_heads) * n_tokens;
+        const int64_t need = (heads * tph + threads - 1) / threads;
+        const int bps = blocks_per_sm(d, e->fn, threads, 0);
+        const int64_t resident = (int64_t)d->num_sms * (bps > 0 ? bps : 1);
+        grid = need < resident ? need : resident;
+    }
 
     QkArgs a;
     a.q = q;
@@ -996,6 +1034,8 @@ RMSN_API int rmsnorm_qk_fwd(void* q, void* k, const void* q_weight, const void* 
     a.woff = weight_offset;
     a.pdl = (flags & RMSN_PDL) ? 1 : 0;
     a.status = d->status;
+    a.stages = stages;
+    a.wait_cycles = d->wait_cycles.load(std::memory_order_relaxed);
     void* args[] = {&a};
     cudaError_t err;
     if (flags & RMSN_PDL) {
@@ -1005,12 +1045,13 @@ RMSN_API int rmsnorm_qk_fwd(void* q, void* k, const void* q_weight, const void* 
         cudaLaunchConfig_t lc = {};
         lc.gridDim = dim3((unsigned)grid);
         lc.blockDim = dim3(threads);
+        lc.dynamicSmemBytes = smem;
         lc.stream = stream;
         lc.attrs = attr;
         lc.numAttrs = 1;
         err = cudaLaunchKernelExC(&lc, e->fn, args);
     } else {
-        err = cudaLaunchKernel(e->fn, dim3((unsigned)grid), dim3(threads), args, 0, stream);
+        err = cudaLaunchKernel(e->fn, dim3((unsigned)grid), dim3(threads), args, smem, stream);
     }
     return err == cudaSuccess ? RMSN_OK : RMSN_ECUDA;
 }

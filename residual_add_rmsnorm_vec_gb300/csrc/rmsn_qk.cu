@@ -75,7 +75,150 @@ __global__ void __launch_bounds__(256) rmsn_qk_kernel(const QkArgs a) {
     }
 }
 
-#define RMSN_QK(TI, DT, TPH) {DT, TPH, (const void*)&rmsn_qk_kernel<TI, TPH>}
+// ---------------------------------------------------------------- ring variant
+//
+// For long batches: persistent blocks, each taking tokens blockIdx.x +
+// k * gridDim.x.  Thread 0 copies a token's query heads and key heads (two
+// 1-D bulk copies, TMA, completing on the stage's mbarrier) into a ring of
+// `stages` shared-memory buffers, up to `stages` tokens ahead; thread t holds
+// the 32-byte vectors v = c * G + t (c < CH) of every token, so its weight
+// vectors are the same for the whole launch and are loaded once into
+// registers.  A head's TPH vectors sit on TPH neighbouring lanes (G is a
+// multiple of 32 and TPH divides 32), so its sum of squares is a butterfly
+// over those lanes; the normalised vectors are stored straight back in
+// place.  One block barrier per token releases its buffer, which thread 0
+// then refills.  Waits are bounded as in the row kernel's ring: one that runs
+// out sets bit 0 of the status word, the block stops after the token's
+// barrier, and thread 0 drains its copies in flight (default bound) first.
+template <class TI, int TPH, int CH>
+__global__ void __launch_bounds__(1024, 1) rmsn_qk_ring_kernel(const QkArgs a) {
+    constexpr int VE = 32 / TI::kBytes;
+    extern __shared__ __align__(128) unsigned char qring[];
+    __shared__ __align__(8) uint64_t full[kMaxStages];
+    __shared__ int abort_flag;
+    const int t = threadIdx.x;
+    const int G = blockDim.x;
+    const int S = a.stages;
+    const int hv = a.nvec;                                // vectors per head
+    const uint32_t qbytes = (uint32_t)a.Hq * a.D * TI::kBytes;
+    const uint32_t kbytes = (uint32_t)a.Hk * a.D * TI::kBytes;
+    const uint32_t stage_bytes = qbytes + kbytes;
+    const int nvq = (int)(qbytes / 32), nv = (int)(stage_bytes / 32);
+    const uint32_t ring0 = smem_u32(qring);
+    const int64_t n_my = a.T > blockIdx.x ? (a.T - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    pdl_launch_dependents(a.pdl);
+    if (t == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // this thread's weight vectors (query or key weight, vector index in the head)
+    V8 wv[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        const int v = c * G + t;
+        const bool is_q = v < nvq;
+        const void* w = is_q ? a.qw : a.kw;
+        const int sub = (is_q ? v : v - nvq) % hv;
+        if (v < nv && w) {
+            wv[c] = ld_keep32(static_cast<const char*>(w) + (int64_t)sub * 32);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) wv[c].u[k] = ones_word<TI>();
+        }
+    }
+    // thread 0: copy token `tok`'s query and key heads into the stage at `dst`
+    auto issue = [&](int64_t tok, uint32_t dst, uint32_t bar) {
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                     "r"(stage_bytes)
+                     : "memory");
+        if (qbytes) {
+            const char* src = static_cast<const char*>(a.q) + tok * a.qs * TI::kBytes;
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], "
+                "%2, [%3];" ::"r"(dst), "l"(src), "r"(qbytes), "r"(bar)
+                : "memory");
+        }
+        if (kbytes) {
+            const char* src = static_cast<const char*>(a.k) + tok * a.ks * TI::kBytes;
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], "
+                "%2, [%3];" ::"r"(dst + qbytes), "l"(src), "r"(kbytes), "r"(bar)
+                : "memory");
+        }
+    };
+    pdl_wait(a.pdl);
+    if (t == 0)
+        for (int64_t k = 0; k < S && k < n_my; ++k)
+            issue(blockIdx.x + k * gridDim.x, ring0 + (uint32_t)k * stage_bytes,
+                  smem_u32(&full[k]));
+    __syncthreads();
+    int64_t k_abort = 0;
+    for (int64_t k = 0; k < n_my; ++k) {
+        const int s = (int)(k % S);
+        const uint32_t phase = (uint32_t)((k / S) & 1);
+        k_abort = k;
+        const int64_t tok = blockIdx.x + k * gridDim.x;
+        if (!mbar_wait_bounded(smem_u32(&full[s]), phase, a.wait_cycles)) {
+            atomicOr(a.status, 1u);
+            abort_flag = 1;
+        }
+        const uint32_t base = ring0 + (uint32_t)s * stage_bytes;
+        V8 x[CH];
+        float acc[CH];
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int v = c * G + t;
+            acc[c] = 0.f;
+            if (v < nv) {
+                x[c] = ld_shared32(base + (uint32_t)v * 32u);
+#pragma unroll
+                for (int k2 = 0; k2 < 8; ++k2) {
+                    if constexpr (TI::kBytes == 2) {
+                        acc[c] = sumsq16x2<TI>(x[c].u[k2], acc[c]);
+                    } else {
+                        const float h = __uint_as_float(x[c].u[k2]);
+                        acc[c] = __fmaf_rn(h, h, acc[c]);
+                    }
+                }
+            }
+        }
+        // every thread has read the stage: it may be refilled after this barrier
+        __syncthreads();
+        if (abort_flag) break;
+        if (t == 0 && k + S < n_my) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(blockIdx.x + (k + S) * gridDim.x, base, smem_u32(&full[s]));
+        }
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+#pragma unroll
+            for (int o = TPH / 2; o > 0; o >>= 1)
+                acc[c] += __shfl_xor_sync(0xFFFFFFFFu, acc[c], o);
+            const int v = c * G + t;
+            if (v >= nv) continue;
+            const float inv = inv_rms(acc[c], a.D, a.eps);
+            const bool is_q = v < nvq;
+            void* row = is_q ? a.q : a.k;
+            const int64_t e = is_q ? tok * a.qs + (int64_t)v * VE
+                                   : tok * a.ks + (int64_t)(v - nvq) * VE;
+            const int64_t ext = is_q ? (a.T - 1) * a.qs + (int64_t)a.Hq * a.D
+                                     : (a.T - 1) * a.ks + (int64_t)a.Hk * a.D;
+            if (!RMSN_CHECK(a.status, e >= 0 && e + VE <= ext)) continue;
+            float y[VE], m = 0.f;
+            scale_vec<TI, false>(x[c], wv[c], wv[c], inv, a.woff, y, m);
+            store_out<TI, TI>(row, e, y, 0.f);
+        }
+    }
+    if (abort_flag && t == 0) {
+        for (int64_t j = k_abort; j < k_abort + S && j < n_my; ++j)
+            mbar_wait_bounded(smem_u32(&full[j % S]), (uint32_t)((j / S) & 1),
+                              kDefaultWaitCycles);
+    }
+}
+
+#define RMSN_QK(TI, DT, TPH) {DT, TPH, 0, (const void*)&rmsn_qk_kernel<TI, TPH>}
+#define RMSN_QKR(TI, DT, TPH, CH) {DT, TPH, CH, (const void*)&rmsn_qk_ring_kernel<TI, TPH, CH>}
 
 static const QkEntry kQkTable[] = {
     RMSN_QK(BF16, kBF16, 1), RMSN_QK(BF16, kBF16, 2),  RMSN_QK(BF16, kBF16, 4),
@@ -84,6 +227,16 @@ static const QkEntry kQkTable[] = {
     RMSN_QK(F32, kF32, 8),   RMSN_QK(F32, kF32, 16),   RMSN_QK(F32, kF32, 32),
     RMSN_QK(F16, kF16, 1),   RMSN_QK(F16, kF16, 2),    RMSN_QK(F16, kF16, 4),
     RMSN_QK(F16, kF16, 8),   RMSN_QK(F16, kF16, 16),   RMSN_QK(F16, kF16, 32),
+    // ring variant: head_dim 64 / 128 / 256 / 512 in 16-bit types, 32 .. 256 in fp32
+    RMSN_QKR(BF16, kBF16, 4, 1),  RMSN_QKR(BF16, kBF16, 8, 1),  RMSN_QKR(BF16, kBF16, 16, 1),
+    RMSN_QKR(BF16, kBF16, 32, 1), RMSN_QKR(BF16, kBF16, 4, 2),  RMSN_QKR(BF16, kBF16, 8, 2),
+    RMSN_QKR(BF16, kBF16, 16, 2), RMSN_QKR(BF16, kBF16, 32, 2),
+    RMSN_QKR(F16, kF16, 4, 1),    RMSN_QKR(F16, kF16, 8, 1),    RMSN_QKR(F16, kF16, 16, 1),
+    RMSN_QKR(F16, kF16, 32, 1),   RMSN_QKR(F16, kF16, 4, 2),    RMSN_QKR(F16, kF16, 8, 2),
+    RMSN_QKR(F16, kF16, 16, 2),   RMSN_QKR(F16, kF16, 32, 2),
+    RMSN_QKR(F32, kF32, 4, 1),    RMSN_QKR(F32, kF32, 8, 1),    RMSN_QKR(F32, kF32, 16, 1),
+    RMSN_QKR(F32, kF32, 32, 1),   RMSN_QKR(F32, kF32, 4, 2),    RMSN_QKR(F32, kF32, 8, 2),
+    RMSN_QKR(F32, kF32, 16, 2),   RMSN_QKR(F32, kF32, 32, 2),
 };
 
 const QkEntry* qk_kernels(int* n) {

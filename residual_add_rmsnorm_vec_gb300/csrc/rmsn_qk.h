@@ -19,12 +19,16 @@ struct QkArgs {
     float eps;
     float woff;
     int32_t pdl;   // launched as a programmatic dependent
-    uint32_t* status;  // device status word (bit 1: a bounds check failed, checked build)
+    uint32_t* status;  // device status word (bit 0: a bounded wait ran out; bit 1: a
+                       // bounds check failed, checked build)
+    int32_t stages;       // ring kernel: shared-memory token buffers
+    int64_t wait_cycles;  // ring kernel: bound of a token wait (< 0: test once)
 };
 
 struct QkEntry {
-    int32_t dt;   // DType of q, k and the weights
-    int32_t tph;  // lanes per head
+    int32_t dt;    // DType of q, k and the weights
+    int32_t tph;   // lanes per head
+    int32_t ring;  // 0: register kernel; else the ring kernel with `ring` vectors per thread
     const void* fn;
 };
 

@@ -48,10 +48,20 @@ def compare(dtype, got, ref, where):
     (5, 4, 4, 128, "f32"), (65, 6, 2, 64, "f32"), (9, 3, 1, 256, "f32"), (2, 1, 1, 16, "bf16"),
     (17, 32, 8, 128, "f16"), (3, 4, 2, 64, "f16"), (5, 2, 2, 256, "f16"),
 ])
+def ring_applies(Hq, Hk, D, dtype):
+    """The ring variant's shapes: 4..32 whole 32-byte vectors per head (a power
+    of two), at most 2048 per token."""
+    nvec = D * (4 if dtype == "f32" else 2) // 32
+    return nvec >= 4 and nvec & (nvec - 1) == 0 and nvec <= 32 and (Hq + Hk) * nvec <= 2048
+
+
 @pytest.mark.parametrize("pad", [0, 16])
-def test_qk_norm_fused_qkv(pkg, T, Hq, Hk, D, dtype, pad):
+@pytest.mark.parametrize("variant", [None, "ring", "direct"])
+def test_qk_norm_fused_qkv(pkg, T, Hq, Hk, D, dtype, pad, variant):
     if pad and dtype == "f32":
         pad = 8  # keep the row stride a multiple of 32 bytes
+    if variant == "ring" and not ring_applies(Hq, Hk, D, dtype):
+        pytest.skip("the ring variant does not take this head shape")
     inp = synth.qk_inputs(T, Hq, Hk, D, dtype, pad=pad)
     qkv = inp["qkv"]
     S = qkv.shape[1]
@@ -62,7 +72,8 @@ def test_qk_norm_fused_qkv(pkg, T, Hq, Hk, D, dtype, pad):
                               weight_offset=0.25)
     g = qkv.cuda()
     pkg.qk_norm_(g[:, :Hq * D], g[:, Hq * D:(Hq + Hk) * D], inp["q_weight"].cuda(),
-                 inp["k_weight"].cuda(), head_dim=D, eps=1e-6, weight_offset=0.25)
+                 inp["k_weight"].cuda(), head_dim=D, eps=1e-6, weight_offset=0.25,
+                 variant=variant)
     torch.cuda.synchronize()
     got = bits(g, dtype)
     orig = bits(qkv, dtype)
@@ -88,20 +99,40 @@ def test_qk_norm_contiguous_heads_no_weights_and_pdl(pkg):
     compare("bf16", bits(gk, "bf16").reshape(T, -1), rk, "k")
 
 
+def test_qk_ring_rejects_shapes_it_does_not_take(pkg):
+    # head_dim 96 bf16 is 6 vectors per head (not a power of two): the ring
+    # variant cannot be forced, the default launch still runs
+    T, Hq, Hk, D = 1100, 4, 2, 96
+    x = torch.zeros((T, (Hq + Hk) * D), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(pkg.RmsnError) as e:
+        pkg.qk_norm_(x[:, :Hq * D], x[:, Hq * D:], None, None, head_dim=D, eps=1e-6,
+                     variant="ring")
+    assert e.value.status == pkg.RMSN_EUNSUPPORTED
+    pkg.qk_norm_(x[:, :Hq * D], x[:, Hq * D:], None, None, head_dim=D, eps=1e-6)
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream().cuda_stream
+    assert pkg.rmsnorm_qk_fwd(x.data_ptr(), None, None, None, T, Hq, 0, D, (Hq + Hk) * D, 0,
+                              1e-6, 0.0, pkg.RMSN_IN_BF16 | pkg.RMSN_QK_RING |
+                              pkg.RMSN_QK_DIRECT, s) == pkg.RMSN_EINVAL
+
+
 def test_qk_norm_only_q_or_only_k(pkg):
     T, H, D = 16, 4, 64
     inp = synth.qk_inputs(T, H, H, D, "bf16")
     x = inp["qkv"][:, :H * D].contiguous()
     rq, _ = oracle.qk_norm(x, None, inp["q_weight"], None, n_q_heads=H, n_k_heads=0,
                            head_dim=D, eps=1e-6, dtype="bf16")
-    g = x.cuda()
-    pkg.qk_norm_(g, None, inp["q_weight"].cuda(), None, head_dim=D, eps=1e-6)
-    torch.cuda.synchronize()
-    compare("bf16", bits(g, "bf16"), rq, "q only")
-    g = x.cuda()
-    pkg.qk_norm_(None, g, None, inp["q_weight"].cuda(), head_dim=D, eps=1e-6)
-    torch.cuda.synchronize()
-    compare("bf16", bits(g, "bf16"), rq, "k only")
+    for variant in (None, "ring"):
+        g = x.cuda()
+        pkg.qk_norm_(g, None, inp["q_weight"].cuda(), None, head_dim=D, eps=1e-6,
+                     variant=variant)
+        torch.cuda.synchronize()
+        compare("bf16", bits(g, "bf16"), rq, f"q only {variant}")
+        g = x.cuda()
+        pkg.qk_norm_(None, g, None, inp["q_weight"].cuda(), head_dim=D, eps=1e-6,
+                     variant=variant)
+        torch.cuda.synchronize()
+        compare("bf16", bits(g, "bf16"), rq, f"k only {variant}")
 
 
 def test_qk_norm_rejections(pkg):

@@ -85,3 +85,41 @@ def test_wait_that_runs_out_stops_cleanly(pkg, stages):
     assert pkg.rmsnorm_read_status() == 0
     got = {"out": out, "residual_out": res, "out_scale": None}
     parity.compare(wl, got, ref, "after the give-up path", bias=inp["bias"])
+
+
+def test_qk_ring_wait_that_runs_out_stops_cleanly(pkg):
+    # the QK norm's ring variant under the same limit: every token's heads are
+    # either normalised exactly as the oracle does or left as they were
+    import oracle
+
+    T, Hq, Hk, D = 8192, 32, 8, 128
+    inp = synth.qk_inputs(T, Hq, Hk, D, "bf16")
+    qkv = inp["qkv"]
+    ref_q, ref_k = oracle.qk_norm(qkv[:, :Hq * D].contiguous(),
+                                  qkv[:, Hq * D:(Hq + Hk) * D].contiguous(), inp["q_weight"],
+                                  inp["k_weight"], n_q_heads=Hq, n_k_heads=Hk, head_dim=D,
+                                  eps=1e-6, dtype="bf16")
+    orig = parity.bits16(qkv[:, :(Hq + Hk) * D])
+    want = np.concatenate([ref_q, ref_k], axis=1)
+    pkg.rmsnorm_read_status(clear=True)
+    hits = 0
+    try:
+        pkg.rmsnorm_set_wait_limit(-1)
+        for _ in range(4):
+            g = qkv.cuda()
+            pkg.qk_norm_(g[:, :Hq * D], g[:, Hq * D:(Hq + Hk) * D], inp["q_weight"].cuda(),
+                         inp["k_weight"].cuda(), head_dim=D, eps=1e-6, variant="ring")
+            torch.cuda.synchronize()
+            got = parity.bits16(g[:, :(Hq + Hk) * D])
+            status = pkg.rmsnorm_read_status(clear=True)
+            same_as_input = np.all(got == orig, axis=1)
+            d = np.abs(parity.ordered16(got) - parity.ordered16(want)).max(axis=1)
+            assert np.all(same_as_input | (d <= 1)), "a token half written or wrong"
+            if status & 1:
+                hits += 1
+            else:
+                assert np.all(d <= 1)
+    finally:
+        pkg.rmsnorm_set_wait_limit(0)
+        pkg.rmsnorm_read_status(clear=True)
+    assert hits >= 1, "no wait ran out although none was allowed to wait"
