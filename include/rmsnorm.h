@@ -93,10 +93,13 @@ typedef enum {
     RMSN_VARIANT_RAGGED = 4,    /* rows off the 32-byte grid, same dtype in and out, all row
                                    pointers equally aligned mod 16 bytes: 16-byte vectors for
                                    the row's interior, single elements for head and tail */
-    RMSN_VARIANT_CLUSTER = 5    /* decode: each row split over a thread-block cluster of
+    RMSN_VARIANT_CLUSTER = 5,   /* decode: each row split over a thread-block cluster of
                                    `cluster` one-warp blocks that exchange partial sums of
                                    squares through distributed shared memory (bf16 / fp16 /
                                    fp32 in with the same dtype out, not FP8) */
+    RMSN_VARIANT_BULK_PIPE = 6  /* the bulk-copy ring with a two-row pipeline: one block
+                                   barrier carries a row's sum of squares and the previous
+                                   row's maximum (bf16 / fp16 in, per-token FP8 or NVFP4 out) */
 } rmsn_variant;
 
 /* One launch configuration. */
@@ -107,7 +110,7 @@ typedef struct {
     int32_t warps_per_row;   /* warps that share one row */
     int32_t chunks;          /* vectors per thread per row (template) */
     int32_t max_warps;       /* template block-size bound (register budget) */
-    int32_t stages;          /* shared-memory row buffers (bulk variant) */
+    int32_t stages;          /* shared-memory row buffers (bulk variants) */
     int32_t grid;            /* blocks launched */
     int32_t smem_bytes;      /* dynamic shared memory per block */
     int32_t num_sms;         /* SMs of the device the config was made for */

@@ -17,7 +17,7 @@ from ._lib import (  # noqa: F401
     RMSN_HAS_RESIDUAL, RMSN_HAS_WEIGHT, RMSN_IN_BF16, RMSN_IN_F16, RMSN_IN_F32, RMSN_OK,
     RMSN_OUT_BF16, RMSN_OUT_F16,
     RMSN_PDL, RMSN_PDL_EARLY_PARAMS, RMSN_QK_DIRECT, RMSN_QK_RING, RMSN_RESIDUAL_F32, RMSN_FMT_MXFP8, RMSN_FMT_MXFP4, RMSN_FMT_NVFP4, BLOCK_FORMATS,
-    RMSN_OUT_F32, RMSN_OUT_FP8E4M3, VARIANT_BLOCK_ROW, VARIANT_BULK_ROW, VARIANT_CLUSTER, VARIANT_GENERIC, VARIANT_RAGGED,
+    RMSN_OUT_F32, RMSN_OUT_FP8E4M3, VARIANT_BLOCK_ROW, VARIANT_BULK_PIPE, VARIANT_BULK_ROW, VARIANT_CLUSTER, VARIANT_GENERIC, VARIANT_RAGGED,
     VARIANT_NAMES, VARIANT_WARP_ROWS, RmsnConfig, RmsnError, library_path, load,
     rmsnorm_fwd, rmsnorm_fwd_ex, rmsnorm_fwd_blockscaled, rmsnorm_fwd_host, rmsnorm_list_configs, rmsnorm_qk_fwd,
     rmsnorm_query_config,

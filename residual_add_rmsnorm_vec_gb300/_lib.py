@@ -44,8 +44,9 @@ VARIANT_BULK_ROW = 2
 VARIANT_GENERIC = 3
 VARIANT_RAGGED = 4
 VARIANT_CLUSTER = 5
+VARIANT_BULK_PIPE = 6
 VARIANT_NAMES = {0: "warp_rows", 1: "block_row", 2: "bulk_row", 3: "generic", 4: "ragged",
-                 5: "cluster"}
+                 5: "cluster", 6: "bulk_pipe"}
 
 RMSN_FMT_MXFP8 = 1
 RMSN_FMT_MXFP4 = 2

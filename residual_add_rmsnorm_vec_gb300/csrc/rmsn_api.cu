@@ -376,7 +376,7 @@ bool shape_config(const Problem& p, const KernelEntry& e, DeviceInfo* d, int gri
         c->warps_per_row = w;
         threads = w * 32;
         units = p.T;
-        if (e.variant == kBulkRow) {
+        if (e.variant == kBulkRow || e.variant == kBulkPipe) {
             const int sb = bulk_stage_bytes(p);
             int st = stages_req > 0 ? stages_req : kBulkSmemTarget / sb;
             if (st > kMaxStages) st = kMaxStages;
@@ -459,7 +459,7 @@ bool select(const Problem& p, DeviceInfo* d, rmsn_config* c) {
             if (!table_lookup(keys[k][0], keys[k][1], near[i], p.T, res, &variant, &ch, &wmax,
                               &stages))
                 continue;
-            if (variant == kBulkRow && !bulk_swizzle_ok(p)) continue;
+            if ((variant == kBulkRow || variant == kBulkPipe) && !bulk_swizzle_ok(p)) continue;
             if (table_shape(p, d, variant, ch, wmax, stages, c)) return true;
         }
     }
@@ -632,13 +632,14 @@ int launch(const KernelEntry* e, const rmsn_config& c, DeviceInfo* d, const Prob
     memset(&mx, 0, sizeof(mx));
     memset(&mr, 0, sizeof(mr));
     a.swz = 0;
-    if (e->variant == kBulkRow && bulk_swizzle_ok(p) &&
+    const bool ring = e->variant == kBulkRow || e->variant == kBulkPipe;
+    if (ring && bulk_swizzle_ok(p) &&
         cached_rows(d, &mx, x, p.T, p.H, p.in_bytes) &&
         (!p.res || cached_rows(d, &mr, residual, p.T, p.H, p.res_bytes)))
         a.swz = 1;
     void* args_one[] = {&a};
     void* args_bulk[] = {&a, &mx, &mr};
-    void** args = e->variant == kBulkRow ? args_bulk : args_one;
+    void** args = ring ? args_bulk : args_one;
     cudaError_t err;
     if (p.pdl || e->variant == kCluster) {
         // programmatic dependent launch: the kernel may start while the
@@ -907,9 +908,10 @@ RMSN_API int rmsnorm_list_configs(int64_t n_tokens, int64_t hidden, uint32_t fla
         }
         // the bulk kernel is listed once per ring depth
         const int stage_opts[] = {0, 2, 3, 4, 6, 8};
-        const int n_opts = e.variant == kBulkRow ? 6 : 1;
+        const bool ring = e.variant == kBulkRow || e.variant == kBulkPipe;
+        const int n_opts = ring ? 6 : 1;
         for (int i = 0; i < n_opts; ++i) {
-            if (e.variant == kBulkRow && i == 0) continue;
+            if (ring && i == 0) continue;
             rmsn_config c;
             if (!shape_config(p, e, d, 0, stage_opts[i], &c)) continue;
             if (count < capacity) out[count] = c;

@@ -42,6 +42,12 @@ namespace rmsn {
 #define RMSN_CLU4(CH, K)                                                                     \
     RMSN_CLU(CH, K, false, false), RMSN_CLU(CH, K, true, false), RMSN_CLU(CH, K, false, true), \
         RMSN_CLU(CH, K, true, true)
+#define RMSN_PIPE(CH, WMAX, RES, BIAS)                                                      \
+    {RMSN_DTI, RMSN_DTO, kBulkPipe, CH, WMAX, 0, RES, BIAS, RMSN_RF32,                        \
+     (const void*)&rmsn_bulk_kernel<RMSN_TI, RMSN_TO, CH, WMAX, RES, BIAS, RMSN_TX, true>}
+#define RMSN_PIPE4(CH, WMAX)                                                                 \
+    RMSN_PIPE(CH, WMAX, false, false), RMSN_PIPE(CH, WMAX, true, false),                     \
+        RMSN_PIPE(CH, WMAX, false, true), RMSN_PIPE(CH, WMAX, true, true)
 #define RMSN_GEN(RES)                                                                        \
     {RMSN_DTI, RMSN_DTO, kGeneric, 0, 8, 0, RES, -1, RMSN_RF32,                              \
      (const void*)&rmsn_generic_kernel<RMSN_TI, RMSN_TO, RES, RMSN_TX>}
@@ -59,6 +65,10 @@ static const KernelEntry kTable[] = {
     // prefill: rows streamed through shared memory by bulk async copies
     RMSN_BULK4(1, 8), RMSN_BULK4(2, 8), RMSN_BULK4(1, 16), RMSN_BULK4(2, 16),
     RMSN_BULK4(1, 32), RMSN_BULK4(2, 32),
+#endif
+#ifdef RMSN_WITH_PIPE
+    // prefill, per-token FP8 / NVFP4: the ring with two rows in flight per barrier
+    RMSN_PIPE4(1, 8), RMSN_PIPE4(2, 8), RMSN_PIPE4(1, 16), RMSN_PIPE4(2, 16),
 #endif
 #ifdef RMSN_WITH_CLUSTER
     // decode: one row split over a cluster of K one-warp blocks

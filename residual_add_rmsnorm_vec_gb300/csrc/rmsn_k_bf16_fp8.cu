@@ -4,4 +4,5 @@
 #define RMSN_DTI kBF16
 #define RMSN_DTO kFP8
 #define RMSN_TABLE_FN kernels_bf16_fp8
+#define RMSN_WITH_PIPE
 #include "rmsn_instances.cuh"

@@ -6,4 +6,5 @@
 #define RMSN_DTO kNVFP4
 #define RMSN_TABLE_FN kernels_bf16_nvfp4
 #define RMSN_NO_GENERIC
+#define RMSN_WITH_PIPE
 #include "rmsn_instances.cuh"

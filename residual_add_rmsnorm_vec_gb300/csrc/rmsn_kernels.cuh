@@ -541,13 +541,16 @@ __device__ __forceinline__ void scale_vec_q(const V8& h, const V8& w, const V8& 
     if constexpr (TI::kBytes == 2) {
         if (woff == 0.f) {
             const F2 inv2 = f2(inv, inv);
+            float m2 = 0.f;  // a second maximum chain (the maximum is order-free)
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const F2 p = mul16x2_exact<TI>(h.u[k], w.u[k]);
                 const F2 r = BIAS ? fma2(p, inv2, widen2<TI>(b.u[k])) : mul2(p, inv2);
                 f2split(r, y[2 * k], y[2 * k + 1]);
-                m = absmax3(m, y[2 * k], y[2 * k + 1]);
+                if (k & 1) m2 = absmax3(m2, y[2 * k], y[2 * k + 1]);
+                else m = absmax3(m, y[2 * k], y[2 * k + 1]);
             }
+            m = fmaxf(m, m2);
             return;
         }
     }
@@ -666,7 +669,17 @@ __device__ __forceinline__ float residual_sumsq(const RmsnArgs& a, int64_t rbase
                 if (rows_ok(a, rbase + (int64_t)v * VE, VE))
                     st_stream32(static_cast<char*>(a.res_out) + off, hv[c].u);
             }
-            if constexpr (TI::kBytes == 2 && PACK) {
+            if constexpr (TI::kBytes == 2 && PACK && PADD) {
+                // two interleaved chains, added at the end: half the dependent
+                // latency for the quantised ring, whose rows are latency-bound
+                float acc2 = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; k += 2) {
+                    acc = sumsq16x2<TI>(hv[c].u[k], acc);
+                    acc2 = sumsq16x2<TI>(hv[c].u[k + 1], acc2);
+                }
+                acc = __fadd_rn(acc, acc2);
+            } else if constexpr (TI::kBytes == 2 && PACK) {
 #pragma unroll
                 for (int k = 0; k < 8; ++k) acc = sumsq16x2<TI>(hv[c].u[k], acc);
             } else {
@@ -692,6 +705,79 @@ __device__ __forceinline__ float residual_sumsq(const RmsnArgs& a, int64_t rbase
 //          E2M1(y * r_b) with r_b the hardware approximation of
 //          1 / (scale * g); 1 / (6 g) is correctly rounded.
 // All conversions round to nearest even and saturate.
+// NVFP4's per-token scale g = max|row| / (448 * 6), stored for the row, and
+// the correctly rounded 1 / (6 g) its block scales are formed with.
+template <class TO>
+__device__ __forceinline__ void nv_row_scale(const RmsnArgs& a, int64_t row, int t, float amax,
+                                             float& g, float& rcp6g) {
+    g = __fdiv_rn(amax, 2688.f);
+    if (t == 0 && row_ok(a, row)) a.scale[row] = g;
+    rcp6g = g > 0.f ? __frcp_rn(__fmul_rn(6.f, g)) : 0.f;  // one reciprocal per row
+}
+
+// One vector of y (element index e, vector v of the row) in a block format:
+// its block scale from the block maximum bmax (NVFP4: with g and 1 / (6 g)),
+// the codes of y under it, stored with the block scale (by the block's first
+// lane).
+template <class TI, class TO>
+__device__ __forceinline__ void store_block_vec(const RmsnArgs& a, int64_t e, int v,
+                                                float (&y)[32 / TI::kBytes], float bmax, float g,
+                                                float rcp6g) {
+    constexpr int VE = 32 / TI::kBytes;
+    constexpr int LPB = TO::kBlock / VE;
+    constexpr bool NV = TO::kBlock == 16;
+    constexpr bool FP4 = !std::is_same<TO, MXFP8>::value;
+    float mul;      // code = convert(y * mul)
+    uint8_t sbyte;  // block scale code
+    if constexpr (NV) {
+        uint32_t sc = 0;
+        if (g > 0.f) {
+            uint16_t two;
+            asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+                : "=h"(two)
+                : "f"(0.f), "f"(__fmul_rn(bmax, rcp6g)));
+            sc = two & 0xFFu;
+        }
+        const float s = __fmul_rn(e4m3_value(sc), g);
+        // one reciprocal per block of 16, the hardware approximation (within
+        // 1 ulp of 1/s): the codes are E2M1(RN(y * r)), which can differ by
+        // one step from E2M1(y / s) where y / s lies within a few fp32 ulp of
+        // a rounding midpoint of E2M1
+        if (s > 0.f) asm("rcp.approx.f32 %0, %1;" : "=f"(mul) : "f"(s));
+        else mul = 0.f;
+        sbyte = (uint8_t)sc;
+    } else {
+        constexpr int emax = FP4 ? 2 : 8;
+        const int ef = (int)((__float_as_uint(bmax) >> 23) & 0xFFu);
+        int sx = ef == 0 ? -127 : ef - 127 - emax;  // zero / subnormal maxima clamp
+        sx = sx < -127 ? -127 : (sx > 126 ? 126 : sx);
+        mul = __uint_as_float((uint32_t)(127 - sx) << 23);  // 2^-s, exact
+        sbyte = (uint8_t)(sx + 127);
+    }
+#pragma unroll
+    for (int k = 0; k < VE; k += 2) f2split(mul2(f2(y[k], y[k + 1]), f2(mul, mul)), y[k], y[k + 1]);
+    if (!rows_ok(a, e, VE)) return;
+    if constexpr (FP4) {
+        uint32_t u[VE / 8];
+#pragma unroll
+        for (int k = 0; k < VE / 8; ++k)
+            u[k] = pack_e2m1x8(y[8 * k], y[8 * k + 1], y[8 * k + 2], y[8 * k + 3], y[8 * k + 4],
+                               y[8 * k + 5], y[8 * k + 6], y[8 * k + 7]);
+        uint8_t* o = reinterpret_cast<uint8_t*>(a.out) + e / 2;
+        if constexpr (VE == 16) st_stream8(o, u);
+        else asm volatile("st.global.b32 [%0], %1;" ::"l"(o), "r"(u[0]) : "memory");
+    } else {
+        uint32_t u[VE / 4];
+#pragma unroll
+        for (int k = 0; k < VE / 4; ++k)
+            u[k] = pack_e4m3x4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
+        uint8_t* o = reinterpret_cast<uint8_t*>(a.out) + e;
+        if constexpr (VE == 16) st_stream16(o, u);
+        else st_stream8(o, u);
+    }
+    if (v % LPB == 0) static_cast<uint8_t*>(a.bscale)[e / TO::kBlock] = sbyte;
+}
+
 template <class TI, class TO, int CH, bool BIAS, bool KEEP, bool QF, class ReduceMax>
 __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row, int64_t rbase,
                                                   int G, int t, float inv, const V8 (&hv)[CH],
@@ -726,10 +812,7 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
                 amax = fmaxf(amax, m);
             }
         }
-        amax = reduce_max(amax);
-        g = __fdiv_rn(amax, 2688.f);
-        if (t == 0 && row_ok(a, row)) a.scale[row] = g;
-        rcp6g = g > 0.f ? __frcp_rn(__fmul_rn(6.f, g)) : 0.f;  // one reciprocal per row
+        nv_row_scale<TO>(a, row, t, reduce_max(amax), g, rcp6g);
     }
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
@@ -757,58 +840,23 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
         for (int o = LPB / 2; o > 0; o >>= 1)
             bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, o));
         if (!valid) continue;
-        float mul;     // code = convert(y * mul)
-        uint8_t sbyte;  // block scale code
-        if constexpr (NV) {
-            uint32_t sc = 0;
-            if (g > 0.f) {
-                uint16_t two;
-                asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
-                    : "=h"(two)
-                    : "f"(0.f), "f"(__fmul_rn(bmax, rcp6g)));
-                sc = two & 0xFFu;
-            }
-            const float s = __fmul_rn(e4m3_value(sc), g);
-            // one reciprocal per block of 16, the hardware approximation
-            // (within 1 ulp of 1/s): the codes are E2M1(RN(y * r)), which can
-            // differ by one step from E2M1(y / s) where y / s lies within a
-            // few fp32 ulp of a rounding midpoint of E2M1
-            if (s > 0.f) asm("rcp.approx.f32 %0, %1;" : "=f"(mul) : "f"(s));
-            else mul = 0.f;
-            sbyte = (uint8_t)sc;
-        } else {
-            constexpr int emax = FP4 ? 2 : 8;
-            const int ef = (int)((__float_as_uint(bmax) >> 23) & 0xFFu);
-            int sx = ef == 0 ? -127 : ef - 127 - emax;  // zero / subnormal maxima clamp
-            sx = sx < -127 ? -127 : (sx > 126 ? 126 : sx);
-            mul = __uint_as_float((uint32_t)(127 - sx) << 23);  // 2^-s, exact
-            sbyte = (uint8_t)(sx + 127);
-        }
+        store_block_vec<TI, TO>(a, rbase + (int64_t)v * VE, v, y, bmax, g, rcp6g);
+    }
+}
+
+// Per-token FP8 of a held row of y: scale max|y| / 448, codes y * 448 / max|y|.
+template <class TI, int CH>
+__device__ __forceinline__ void store_fp8_held(const RmsnArgs& a, int64_t row, int64_t rbase,
+                                               int G, int t, const float (&ys)[CH][32 / TI::kBytes],
+                                               float amax) {
+    constexpr int VE = 32 / TI::kBytes;
+    const float qmul = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
+    if (t == 0 && row_ok(a, row)) a.scale[row] = __fdiv_rn(amax, 448.f);
 #pragma unroll
-        for (int k = 0; k < VE; k += 2)
-            f2split(mul2(f2(y[k], y[k + 1]), f2(mul, mul)), y[k], y[k + 1]);
-        const int64_t e = rbase + (int64_t)v * VE;  // element index of this vector
-        if (!rows_ok(a, e, VE)) continue;
-        if constexpr (FP4) {
-            uint32_t u[VE / 8];
-#pragma unroll
-            for (int k = 0; k < VE / 8; ++k)
-                u[k] = pack_e2m1x8(y[8 * k], y[8 * k + 1], y[8 * k + 2], y[8 * k + 3],
-                                   y[8 * k + 4], y[8 * k + 5], y[8 * k + 6], y[8 * k + 7]);
-            uint8_t* o = reinterpret_cast<uint8_t*>(a.out) + e / 2;
-            if constexpr (VE == 16) st_stream8(o, u);
-            else asm volatile("st.global.b32 [%0], %1;" ::"l"(o), "r"(u[0]) : "memory");
-        } else {
-            uint32_t u[VE / 4];
-#pragma unroll
-            for (int k = 0; k < VE / 4; ++k)
-                u[k] = pack_e4m3x4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
-            uint8_t* o = reinterpret_cast<uint8_t*>(a.out) + e;
-            if constexpr (VE == 16) st_stream16(o, u);
-            else st_stream8(o, u);
-        }
-        if (v % LPB == 0)
-            static_cast<uint8_t*>(a.bscale)[e / TO::kBlock] = sbyte;
+    for (int c = 0; c < CH; ++c) {
+        const int v = c * G + t;
+        if (v < a.nvec && rows_ok(a, rbase + (int64_t)v * VE, VE))
+            store_out<TI, FP8>(a.out, rbase + (int64_t)v * VE, ys[c], qmul);
     }
 }
 
@@ -1233,7 +1281,36 @@ __device__ __forceinline__ V8 ld_shared_vec_swz(uint32_t base, uint32_t v) {
 // the row of x followed by the row of the residual (TI).  With a.swz the
 // stages are filled by swizzled 2-D tensor copies described by mx / mr (and
 // start on 1024-byte boundaries), else by 1-D bulk copies.
-template <class TI, class TO, int CH, int WMAX, bool RES, bool BIAS, class TX = TI>
+// Sum and maximum over the warps of a block with one barrier: `slot` holds
+// [64] floats (sums, then maxima) and alternates between calls.
+__device__ __forceinline__ void block_allreduce_sum_max(float s, float m, float* slot, float& sum,
+                                                        float& mx) {
+    s = warp_sum(s);
+    m = warp_max(m);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+        slot[warp] = s;
+        slot[32 + warp] = m;
+    }
+    __syncthreads();
+    const int nw = blockDim.x >> 5;
+    sum = slot[0];
+    mx = slot[32];
+    for (int i = 1; i < nw; ++i) {
+        sum = __fadd_rn(sum, slot[i]);
+        mx = fmaxf(mx, slot[32 + i]);
+    }
+}
+
+// PIPE (per-token FP8 and NVFP4 outputs, whose rows need a second block
+// reduction for the row maximum): a two-row software pipeline.  Iteration k
+// takes row k - 1 through the scale pass and its maxima and row k through the
+// residual add and its sum of squares; one barrier then reduces both (row k's
+// sum, row k - 1's maximum), after which row k - 1 is quantised and stored.
+// One barrier per row instead of two, and two independent dependency chains
+// between barriers.
+template <class TI, class TO, int CH, int WMAX, bool RES, bool BIAS, class TX = TI,
+          bool PIPE = false>
 __global__ void __launch_bounds__(WMAX * 32, 1)
     rmsn_bulk_kernel(const RmsnArgs a, const __grid_constant__ CUtensorMap mx,
                      const __grid_constant__ CUtensorMap mr) {
@@ -1249,7 +1326,7 @@ __global__ void __launch_bounds__(WMAX * 32, 1)
     constexpr bool HOLD = WMAX <= 16 && CH * VE <= 32;
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full[kMaxStages];
-    __shared__ float red[4][32];
+    __shared__ float red[PIPE ? 2 : 4][PIPE ? 64 : 32];
     __shared__ int abort_flag;
 
     const int G = blockDim.x;
@@ -1266,10 +1343,18 @@ __global__ void __launch_bounds__(WMAX * 32, 1)
     V8 wv[CH];
     V8 bv[BIAS ? CH : 1];
     if (t == 0) {
-        // shared memory only: done before waiting for the prerequisite grid
+        // shared memory and the copy descriptors only: done before waiting for
+        // the prerequisite grid
         abort_flag = 0;
         for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (a.swz) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mx))
+                         : "memory");
+            if (RES)
+                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mr))
+                             : "memory");
+        }
     }
     // thread 0: copy `row` into the stage at `dst`, completing on `bar` (a row
     // outside the tensor, in the bounds-checked build, is not copied: the
@@ -1296,6 +1381,100 @@ __global__ void __launch_bounds__(WMAX * 32, 1)
 
     int parity = 0;
     int64_t k_abort = 0;
+    // the row of iteration k: x, residual -> registers (h), residual_out, and
+    // this thread's sum of squares of h
+    auto take_row = [&](int64_t k, V8 (&hv)[CH]) -> float {
+        const int s = (int)(k % S);
+        const uint32_t phase = (uint32_t)((k / S) & 1);
+        const int64_t row = blockIdx.x + k * gridDim.x;
+        if (!mbar_wait_bounded(smem_u32(&full[s]), phase, a.wait_cycles)) {
+            atomicOr(a.status, 1u);
+            abort_flag = 1;
+        }
+        const uint32_t base = ring0 + (uint32_t)s * stage_bytes;
+        V8 rv[RES ? CH : 1];
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int v = c * G + t;
+            if (v < a.nvec && RMSN_CHECK(a.status, (uint32_t)(v + 1) * XVB <= x_bytes)) {
+                if (a.swz) {
+                    hv[c] = ld_shared_vec_swz<TX, TI>(base, (uint32_t)v);
+                    if constexpr (RES) rv[c] = ld_shared32_swz(base + x_bytes, (uint32_t)v);
+                } else {
+                    hv[c] = ld_shared_vec<TX, TI>(base + (uint32_t)v * XVB);
+                    if constexpr (RES) rv[c] = ld_shared32(base + x_bytes + (uint32_t)v * 32);
+                }
+            }
+        }
+        return residual_sumsq<TI, CH, RES, true, PADD>(a, row * (int64_t)a.H, G, t, hv, rv);
+    };
+    if constexpr (PIPE) {
+        static_assert((std::is_same<TO, FP8>::value || std::is_same<TO, NVFP4>::value) &&
+                          TX::kBytes == TI::kBytes,
+                      "the two-row pipeline is built for per-token FP8 and NVFP4");
+        constexpr bool NV = IsBlockFmt<TO>::value;
+        V8 hp[CH];                // h of the previous row
+        float ys[CH][VE];         // its y, held across the barrier
+        float bms[NV ? CH : 1];   // NVFP4: the lane's maximum of each of its vectors
+        float inv_p = 0.f;
+        for (int64_t k = 0; k <= n_my; ++k) {
+            const bool cur = k < n_my;
+            V8 hv[CH];
+            float acc = 0.f, amax = 0.f;
+            if (k > 0) {
+#pragma unroll
+                for (int c = 0; c < CH; ++c) {
+                    const int v = c * G + t;
+                    if (v < a.nvec) {
+                        opaque(wv[c]);
+                        if constexpr (BIAS) opaque(bv[c]);
+                        float m = 0.f;
+                        scale_vec_q<TI, BIAS>(hp[c], wv[c], bv[BIAS ? c : 0], inv_p, a.woff,
+                                              ys[c], m);
+                        if constexpr (NV) bms[c] = m;
+                        amax = fmaxf(amax, m);
+                    }
+                }
+            }
+            // row k after row k - 1's scale pass: the two h are not live together
+            if (cur) {
+                k_abort = k;
+                acc = take_row(k, hv);
+            }
+            // one barrier: row k's sum of squares, row k - 1's maximum
+            float sumsq, rmax;
+            block_allreduce_sum_max(acc, amax, red[parity], sumsq, rmax);
+            if (abort_flag) break;
+            if (cur && t == 0 && k + S < n_my) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(blockIdx.x + (k + S) * gridDim.x, ring0 + (uint32_t)(k % S) * stage_bytes,
+                      smem_u32(&full[k % S]));
+            }
+            if (k > 0) {
+                const int64_t row_p = blockIdx.x + (k - 1) * gridDim.x;
+                const int64_t rbase_p = row_p * (int64_t)a.H;
+                if constexpr (NV) {
+                    float g, rcp6g;
+                    nv_row_scale<TO>(a, row_p, t, rmax, g, rcp6g);
+#pragma unroll
+                    for (int c = 0; c < CH; ++c) {
+                        const int v = c * G + t;
+                        if (v < a.nvec)
+                            store_block_vec<TI, TO>(a, rbase_p + (int64_t)v * VE, v, ys[c],
+                                                    bms[c], g, rcp6g);
+                    }
+                } else {
+                    store_fp8_held<TI, CH>(a, row_p, rbase_p, G, t, ys, rmax);
+                }
+            }
+            if (cur) {
+                inv_p = inv_rms(sumsq, a.H, a.eps);
+#pragma unroll
+                for (int c = 0; c < CH; ++c) hp[c] = hv[c];
+            }
+            parity ^= 1;
+        }
+    } else
     for (int64_t k = 0; k < n_my; ++k) {
         const int s = (int)(k % S);
         const uint32_t phase = (uint32_t)((k / S) & 1);

@@ -39,7 +39,8 @@ enum DType : int32_t {
 };
 
 enum Variant : int32_t {
-    kWarpRows = 0, kBlockRow = 1, kBulkRow = 2, kGeneric = 3, kRagged = 4, kCluster = 5
+    kWarpRows = 0, kBlockRow = 1, kBulkRow = 2, kGeneric = 3, kRagged = 4, kCluster = 5,
+    kBulkPipe = 6  // the ring kernel with its two-row pipeline (per-token FP8, NVFP4)
 };
 
 // One compiled kernel.  For kCluster, max_warps holds the cluster size (blocks

@@ -11,10 +11,13 @@ Cases:
                      decode workload), the selector's launch
   cluster_T<T>_K<K>  the same rows on the split-row cluster variant, K blocks
   qk_T<T>            QK norm, 32 query + 8 key heads x 128 bf16 in a fused
-                     qkv buffer (value heads skipped), one launch
+                     qkv buffer (value heads skipped), one launch; qkring_T<T> /
+                     qkdirect_T<T> force the ring / the register kernel
   ragged_T<T>_H<H>   bf16 rows off the 32-byte grid (ragged-row kernel), bias
   fp8_T<T>_H<H>      bf16 in, per-token FP8 out, bias (the quantised workload)
   nvfp4_T<T>_H<H>    bf16 in, NVFP4 out, bias
+  fp8pipe_T<T>_H<H>, nvfp4pipe_T<T>_H<H>
+                     the same on the two-row pipelined ring (2 vectors a thread)
   prefill_T<T>_H<H>  the prefill workload (outlier channels, eps 1e-5)
 """
 from __future__ import annotations
@@ -37,16 +40,17 @@ def run_case(name: str, reps: int) -> str:
     kind, T = m.group(1), int(m.group(2))
     H = int(m.group(3)) if m.group(3) else 4096
     s = torch.cuda.current_stream(dev).cuda_stream
-    if kind == "qk":
+    if kind in ("qk", "qkring", "qkdirect"):
         Hq, Hk, D = 32, 8, 128
         inp = synth.qk_inputs(T, Hq, Hk, D, "bf16")
         qkv = inp["qkv"].to(dev)
         q, k = qkv[:, :Hq * D], qkv[:, Hq * D:(Hq + Hk) * D]
         wq, wk = inp["q_weight"].to(dev), inp["k_weight"].to(dev)
+        variant = {"qk": None, "qkring": "ring", "qkdirect": "direct"}[kind]
         for _ in range(reps):
-            pkg.qk_norm_(q, k, wq, wk, head_dim=D, eps=1e-6)
+            pkg.qk_norm_(q, k, wq, wk, head_dim=D, eps=1e-6, variant=variant)
         torch.cuda.synchronize(dev)
-        return f"qk T={T} heads {Hq}+{Hk} x {D}"
+        return f"{kind} T={T} heads {Hq}+{Hk} x {D}"
     if kind in ("decode", "cluster"):
         wl = synth.decode_workload(T) if H == 4096 else synth.Workload(
             f"decode_T{T}_H{H}", T, H, 10 + T, "bf16", "bf16", 1e-6)
@@ -55,7 +59,7 @@ def run_case(name: str, reps: int) -> str:
     elif kind == "ragged":
         wl = synth.Workload(f"ragged_T{T}_H{H}", T, H, 80, "bf16", "bf16", 1e-5, has_bias=True,
                             r_std=2.0)
-    elif kind in ("fp8", "nvfp4"):
+    elif kind in ("fp8", "nvfp4", "fp8pipe", "nvfp4pipe"):
         wl = synth.fp8_workload(H, n_tokens=T)
     else:
         raise SystemExit(f"unknown case {name}")
@@ -70,17 +74,24 @@ def run_case(name: str, reps: int) -> str:
         if not cands:
             raise SystemExit(f"no cluster configuration with K={K} for {T}x{H}")
         cfg = cands[0]
+    if kind.endswith("pipe"):
+        flags = pkg.make_flags("bf16", "fp8", True, True, True)
+        cands = [c for c in pkg.rmsnorm_list_configs(T, H, flags)
+                 if c.variant == pkg.VARIANT_BULK_PIPE and c.chunks == 2]
+        if not cands:
+            raise SystemExit(f"no pipelined ring configuration for {T}x{H}")
+        cfg = cands[0]
     for _ in range(reps):
-        if kind == "nvfp4":
+        if kind.startswith("nvfp4"):
             out = pkg.fused_add_rmsnorm_blockscaled(g["x"], g["residual"], g["weight"], g["bias"],
-                                                    eps=wl.eps, fmt="nvfp4")
+                                                    eps=wl.eps, fmt="nvfp4", config=cfg)
         else:
             out = pkg.fused_add_rmsnorm(g["x"], g["residual"], g["weight"], g["bias"], eps=wl.eps,
                                         out_dtype=wl.out_dtype, config=cfg)
     torch.cuda.synchronize(dev)
     del out
     if cfg is None:
-        flags = pkg.make_flags("bf16", "fp8" if kind == "nvfp4" else wl.out_dtype,
+        flags = pkg.make_flags("bf16", "fp8" if kind.startswith("nvfp4") else wl.out_dtype,
                                wl.has_residual, True, wl.has_bias)
         cfg = pkg.rmsnorm_query_config(T, H, flags)
     return f"{name}: {cfg.as_dict()}"

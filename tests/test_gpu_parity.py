@@ -441,12 +441,19 @@ def _same_shape(a, b):
 def test_selector_decode_vs_prefill(pkg):
     flags = pkg.make_flags("bf16", "bf16", True, True, False)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    # a hidden size without measured rows: the decode rule (one warp per block
-    # while the problem needs fewer warps than there are SMs), else multi-warp
-    c = pkg.rmsnorm_query_config(8, 2560, flags)
-    assert c.variant == pkg.VARIANT_WARP_ROWS and c.warps_per_block == 1 and c.num_sms == sms
-    c = pkg.rmsnorm_query_config(4096, 2560, flags)
-    assert c.variant == pkg.VARIANT_BLOCK_ROW and c.warps_per_block > 1
+    # a hidden size without measured rows but a measured neighbour within 2x
+    # (2560: 3072 is nearest) takes the neighbour's launch shape
+    for T in (8, 4096):
+        c = pkg.rmsnorm_query_config(T, 2560, flags)
+        n = pkg.rmsnorm_query_config(T, 3072, flags)
+        assert _same_shape(c, n) and c.num_sms == sms, (T, c.as_dict(), n.as_dict())
+    # no measured hidden size within 2x (bf16 512: the nearest, 2048, is 4x
+    # away): the decode rule (one warp per block while the problem needs
+    # fewer warps than there are SMs), else one block per row
+    c = pkg.rmsnorm_query_config(8, 512, flags)
+    assert c.variant == pkg.VARIANT_WARP_ROWS and c.warps_per_block == 1
+    c = pkg.rmsnorm_query_config(16384, 512, flags)
+    assert c.variant == pkg.VARIANT_BLOCK_ROW
     # measured shapes: whatever the table picked is a valid built configuration
     for T, H in ((1, 4096), (8, 4096), (256, 4096), (16384, 8192), (4096, 16384), (8, 3072),
                  (4096, 6144), (16384, 7168)):
@@ -470,8 +477,9 @@ def test_ring_copy_mode(pkg):
     rings = [c for c in pkg.rmsnorm_list_configs(37, 256, flags)
              if c.variant == pkg.VARIANT_BULK_ROW]
     assert rings and all(c.ring_copy == 1 for c in rings)
+    rings = (pkg.VARIANT_BULK_ROW, pkg.VARIANT_BULK_PIPE)
     assert all(c.ring_copy == 0 for c in pkg.rmsnorm_list_configs(37, 256, flags)
-               if c.variant != pkg.VARIANT_BULK_ROW)
+               if c.variant not in rings)
 
 
 def test_selection_cache_keeps_colliding_problems_apart(pkg):

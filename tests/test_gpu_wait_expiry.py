@@ -87,6 +87,68 @@ def test_wait_that_runs_out_stops_cleanly(pkg, stages):
     parity.compare(wl, got, ref, "after the give-up path", bias=inp["bias"])
 
 
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_pipelined_ring_wait_that_runs_out_stops_cleanly(pkg, fmt):
+    # the two-row pipelined ring (quantised outputs): every row is either
+    # written exactly as a launch with the default bound writes it, or not
+    # written at all (its canaries intact: FP8 code 0xFF and E4M3 block scale
+    # 0xFF are NaN, which the saturating conversions never produce)
+    T, H = 4096, 5120
+    wl = synth.fp8_workload(H, n_tokens=T)
+    g = parity.to_device(synth.make_inputs(wl), DEV)
+    flags = pkg.make_flags("bf16", "fp8", True, True, True)
+    cfg = [c for c in pkg.rmsnorm_list_configs(T, H, flags)
+           if c.variant == pkg.VARIANT_BULK_PIPE and c.chunks == 2][0]
+    s = torch.cuda.current_stream().cuda_stream
+    code, blk, per_byte = pkg.BLOCK_FORMATS["nvfp4"]
+
+    def launch():
+        q = torch.full((T, H if fmt == "fp8" else H // 2), 0xFF, dtype=torch.uint8, device=DEV)
+        bs = torch.full((T, H // blk), 0xFF, dtype=torch.uint8, device=DEV)
+        sc = torch.zeros((T,), dtype=torch.float32, device=DEV)
+        res = torch.full((T, H), CANARY, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+        ptr = [g["x"].data_ptr(), g["residual"].data_ptr(), g["weight"].data_ptr(),
+               g["bias"].data_ptr()]
+        if fmt == "fp8":
+            st = pkg.rmsnorm_fwd_ex(*ptr, q.data_ptr(), res.data_ptr(), sc.data_ptr(), T, H,
+                                    wl.eps, flags, 0.0, cfg, s)
+        else:
+            st = pkg.rmsnorm_fwd_blockscaled(*ptr, q.data_ptr(), bs.data_ptr(), sc.data_ptr(),
+                                             res.data_ptr(), T, H, wl.eps,
+                                             pkg.make_flags("bf16", "f32", True, True, True),
+                                             code, 0.0, cfg, s)
+        assert st == pkg.RMSN_OK
+        torch.cuda.synchronize()
+        return (q.cpu().numpy(), bs.cpu().numpy(), sc.cpu().numpy(), parity.bits16(res))
+
+    want = launch()
+    assert pkg.rmsnorm_read_status() == 0
+    pkg.rmsnorm_read_status(clear=True)
+    hits = 0
+    try:
+        pkg.rmsnorm_set_wait_limit(-1)
+        for _ in range(4):
+            q, bs, sc, res = launch()
+            status = pkg.rmsnorm_read_status(clear=True)
+            mark = q if fmt == "fp8" else bs
+            done = ~np.all(mark == 0xFF, axis=1)
+            assert np.all(mark[~done] == 0xFF) and np.all(q[~done] == 0xFF)
+            assert np.all(mark[done] != 0xFF), "a row's output half written"
+            assert np.array_equal(q[done], want[0][done]) and np.array_equal(sc[done], want[2][done])
+            assert np.array_equal(res[done], want[3][done])
+            if fmt == "nvfp4":
+                assert np.array_equal(bs[done], want[1][done])
+            if status & 1:
+                hits += 1
+                assert not done.all()
+            else:
+                assert done.all()
+    finally:
+        pkg.rmsnorm_set_wait_limit(0)
+        pkg.rmsnorm_read_status(clear=True)
+    assert hits >= 1, "no wait ran out although none was allowed to wait"
+
+
 def test_qk_ring_wait_that_runs_out_stops_cleanly(pkg):
     # the QK norm's ring variant under the same limit: every token's heads are
     # either normalised exactly as the oracle does or left as they were

@@ -56,7 +56,9 @@ def instantiated(codes):
     body = inst[inst.index("static const KernelEntry kTable[]"):]
     vec = re.findall(r"RMSN_VEC4\((\d+), (\d+), (true|false)\)", body)
     bulk = re.findall(r"RMSN_BULK4\((\d+), (\d+)\)", body)
-    assert vec and bulk
+    pipe = re.findall(r"RMSN_PIPE4\((\d+), (\d+)\)", body)
+    clu = re.findall(r"RMSN_CLU4\((\d+), (\d+)\)", body)
+    assert vec and bulk and pipe and clu
     built = {}
     for tu in glob.glob(os.path.join(CSRC, "rmsn_k_*.cu")):
         with open(tu) as f:
@@ -72,6 +74,10 @@ def instantiated(codes):
                    int(w)) for ch, w, wr in vec}
         if "#define RMSN_NO_BULK" not in src:
             shapes |= {(variants["kBulkRow"], int(ch), int(w)) for ch, w in bulk}
+        if "#define RMSN_WITH_PIPE" in src:
+            shapes |= {(variants["kBulkPipe"], int(ch), int(w)) for ch, w in pipe}
+        if "#define RMSN_WITH_CLUSTER" in src:
+            shapes |= {(variants["kCluster"], int(ch), int(k)) for ch, k in clu}
         built[(tin, dtypes[m_out.group(1)])] = shapes
     return built
 
@@ -94,7 +100,7 @@ def test_every_row_names_a_built_kernel(rows, instantiated, codes):
         tin, tout, hidden, t_min, variant, ch, wmax, stages, res, bias = r
         assert (tin, tout) in instantiated, f"no translation unit for {r}"
         assert (variant, ch, wmax) in instantiated[(tin, tout)], f"kernel not built: {r}"
-        if variant == variants["kBulkRow"]:
+        if variant in (variants["kBulkRow"], variants["kBulkPipe"]):
             assert 2 <= stages <= max_stages, r
         else:
             assert stages == 0, r
