@@ -991,106 +991,6 @@ __global__ void __launch_bounds__(Bounds<WMAX, CH, RES && BIAS>::kThreads,
     }
 }
 
-// ---------------------------------------------------------------- split-row (cluster) kernel
-//
-// Decode-size rows split over a thread-block cluster (a split row for the
-// blog's decode case, section "Prefill and decode", where the batch has too
-// few rows to fill the SMs).  Each row goes to one cluster of K blocks of one
-// warp; thread t = rank * 32 + lane of the row's K * 32 threads holds vectors
-// v = c * 32K + t, c < CH, as in the register kernel.  The blocks exchange
-// their partial sums of squares through distributed shared memory: lane j of
-// each block stores the block's partial into slot `rank` of block j, a
-// cluster barrier (release / acquire) makes the slots visible, and every block
-// adds the K partials in rank order, so all get the same total.  A relaxed
-// arrive at entry, waited for before the first remote store, ensures every
-// block of the cluster has started before its shared memory is written; no
-// block touches another's shared memory after the second barrier, so blocks
-// may then exit in any order.  16-bit and fp32 outputs only (the quantised
-// outputs would need a second exchange for the row maximum).
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_size() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_index() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_arrive_release() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Store v at the shared-memory location `local` (an address of this block's
-// shared memory) of block `rank` of the cluster.
-__device__ __forceinline__ void st_cluster_f32(const void* local, uint32_t rank, float v) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-                 : "=r"(remote)
-                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(local))), "r"(rank));
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
-}
-
-constexpr int kMaxClusterBlocks = 8;
-
-template <class TI, class TO, int CH, bool RES, bool BIAS>
-__global__ void __launch_bounds__(32) rmsn_cluster_kernel(const RmsnArgs a) {
-    static_assert(TO::kBytes >= 2, "16-bit and fp32 outputs only");
-    __shared__ float part[kMaxClusterBlocks];
-    const uint32_t rank = cluster_rank();
-    const uint32_t K = cluster_size();
-    const int lane = threadIdx.x;
-    const int G = 32 * (int)K;
-    const int t = (int)rank * 32 + lane;
-    const int64_t row = cluster_index();
-    cluster_arrive_relaxed();
-    pdl_launch_dependents(a.pdl);
-    V8 wv[CH];
-    V8 bv[BIAS ? CH : 1];
-    if (a.early_params) load_params<TI, TI, CH>(a, G, t, wv, bv, BIAS);
-    pdl_wait(a.pdl);
-    V8 hv[CH];
-    V8 rv[RES ? CH : 1];
-    const int64_t rbase = row * (int64_t)a.H;
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-        const int v = c * G + t;
-        const int64_t e = rbase + (int64_t)v * (32 / TI::kBytes);
-        if (v < a.nvec && rows_ok(a, e, 32 / TI::kBytes)) {
-            hv[c] = ld_stream32(static_cast<const char*>(a.x) + e * TI::kBytes);
-            if constexpr (RES) rv[c] = ld_stream32(static_cast<const char*>(a.r) + e * TI::kBytes);
-        }
-    }
-    if (!a.early_params) load_params<TI, TI, CH>(a, G, t, wv, bv, BIAS);
-    const float acc = warp_sum(residual_sumsq<TI, CH, RES>(a, rbase, G, t, hv, rv));
-    cluster_wait();  // every block of the cluster has started
-    if (lane < (int)K) st_cluster_f32(&part[rank], (uint32_t)lane, acc);
-    cluster_arrive_release();
-    cluster_wait();
-    float sumsq = part[0];
-    for (uint32_t i = 1; i < K; ++i) sumsq = __fadd_rn(sumsq, part[i]);
-    const float inv = inv_rms(sumsq, a.H, a.eps);
-    scale_store<TI, TO, CH, BIAS>(a, row, rbase, G, t, inv, hv, wv, bv,
-                                  [](float m) { return m; });
-}
-
 // ---------------------------------------------------------------- bulk-copy kernel
 //
 // Persistent blocks (one row at a time, up to WMAX warps).  Whole rows of x
@@ -1523,6 +1423,132 @@ __global__ void __launch_bounds__(WMAX * 32, 1)
             mbar_wait_bounded(smem_u32(&full[j % S]), (uint32_t)((j / S) & 1),
                               kDefaultWaitCycles);
     }
+}
+
+// ---------------------------------------------------------------- split-row (cluster) kernel
+//
+// Decode-size rows split over a thread-block cluster (a split row for the
+// blog's decode case, section "Prefill and decode", where the batch has too
+// few rows to fill the SMs).  Each row goes to one cluster of K blocks of one
+// warp; thread t = rank * 32 + lane of the row's K * 32 threads holds vectors
+// v = c * 32K + t, c < CH, as in the register kernel.  The blocks exchange
+// their partial sums of squares through distributed shared memory: lane j of
+// each block sends the block's partial with an asynchronous store
+// (st.async) into slot `rank` of block j, completing on block j's mbarrier,
+// which expects 4 K bytes; each block waits (bounded) on its own mbarrier and
+// adds the K partials in rank order, so all get the same total.  A relaxed
+// cluster arrive at entry (after the mbarrier is initialised), waited for
+// before the first remote store, ensures every block of the cluster has
+// started and set up its mbarrier.  A block leaves only after all K partials
+// have landed in its own shared memory, so no store into a block outlives it.
+// 16-bit and fp32 outputs only (the quantised outputs would need a second
+// exchange for the row maximum).
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_index() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Asynchronous store of v at the shared-memory location `local` (an address
+// of this block's shared memory) in block `rank` of the cluster, completing 4
+// transaction bytes on the mbarrier at `bar` (likewise this block's address)
+// in that block.
+__device__ __forceinline__ void st_async_cluster_f32(const void* local, const void* bar,
+                                                     uint32_t rank, float v) {
+    uint32_t rdst, rbar;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(rdst)
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(local))), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(rbar)
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar))), "r"(rank));
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(rdst),
+        "r"(__float_as_uint(v)), "r"(rbar)
+        : "memory");
+}
+
+constexpr int kMaxClusterBlocks = 8;
+
+template <class TI, class TO, int CH, bool RES, bool BIAS>
+__global__ void __launch_bounds__(32) rmsn_cluster_kernel(const RmsnArgs a) {
+    static_assert(TO::kBytes >= 2, "16-bit and fp32 outputs only");
+    __shared__ float part[kMaxClusterBlocks];
+    __shared__ __align__(8) uint64_t got;  // completes when all K partials have landed
+    const uint32_t rank = cluster_rank();
+    const uint32_t K = cluster_size();
+    const int lane = threadIdx.x;
+    const int G = 32 * (int)K;
+    const int t = (int)rank * 32 + lane;
+    const int64_t row = cluster_index();
+    if (lane == 0) {
+        mbar_init(smem_u32(&got), 1);
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                         smem_u32(&got)),
+                     "r"(4u * K)
+                     : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    cluster_arrive_relaxed();
+    pdl_launch_dependents(a.pdl);
+    V8 wv[CH];
+    V8 bv[BIAS ? CH : 1];
+    if (a.early_params) load_params<TI, TI, CH>(a, G, t, wv, bv, BIAS);
+    pdl_wait(a.pdl);
+    V8 hv[CH];
+    V8 rv[RES ? CH : 1];
+    const int64_t rbase = row * (int64_t)a.H;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        const int v = c * G + t;
+        const int64_t e = rbase + (int64_t)v * (32 / TI::kBytes);
+        if (v < a.nvec && rows_ok(a, e, 32 / TI::kBytes)) {
+            hv[c] = ld_stream32(static_cast<const char*>(a.x) + e * TI::kBytes);
+            if constexpr (RES) rv[c] = ld_stream32(static_cast<const char*>(a.r) + e * TI::kBytes);
+        }
+    }
+    if (!a.early_params) load_params<TI, TI, CH>(a, G, t, wv, bv, BIAS);
+    const float acc = warp_sum(residual_sumsq<TI, CH, RES>(a, rbase, G, t, hv, rv));
+    cluster_wait();  // every block of the cluster has started and set up `got`
+    if (lane < (int)K) st_async_cluster_f32(&part[rank], &got, (uint32_t)lane, acc);
+    if (!mbar_wait_bounded(smem_u32(&got), 0, kDefaultWaitCycles)) {
+        // a partial did not arrive: report it, and wait for the stores into
+        // this block once more before leaving (bounded again)
+        atomicOr(a.status, 1u);
+        mbar_wait_bounded(smem_u32(&got), 0, kDefaultWaitCycles);
+        return;
+    }
+    float sumsq = part[0];
+    for (uint32_t i = 1; i < K; ++i) sumsq = __fadd_rn(sumsq, part[i]);
+    const float inv = inv_rms(sumsq, a.H, a.eps);
+    scale_store<TI, TO, CH, BIAS>(a, row, rbase, G, t, inv, hv, wv, bv,
+                                  [](float m) { return m; });
 }
 
 // ---------------------------------------------------------------- generic kernel
