@@ -230,11 +230,12 @@ int rmsnorm_fwd_host(const void* x, const void* residual, const void* weight, co
  * n_q_heads * head_dim elements (likewise k).  flags: RMSN_IN_F32,
  * RMSN_IN_BF16 or RMSN_IN_F16 (q, k and weights share it), optionally
  * RMSN_PDL, and at most one of RMSN_QK_RING / RMSN_QK_DIRECT.  One launch
- * covers both q and k.  Long batches (from 1024 tokens, where a head is 4 to
- * 32 whole 32-byte vectors and a token's heads at most 2048 of them) take a
- * ring variant: persistent blocks stream each token's query and key heads
- * into shared memory with TMA bulk copies and hold the weights in registers;
- * shorter ones a one-pass register kernel.  The fast path needs head_dim * element size to be a
+ * covers both q and k, by a one-pass register kernel; RMSN_QK_RING asks for a
+ * ring variant instead (heads of 4 to 32 whole 32-byte vectors, a power of
+ * two, at most 2048 per token), in which persistent blocks stream each
+ * token's query and key heads into shared memory with TMA bulk copies and hold
+ * the weights in registers.  Without a weight offset the 16-bit kernels form
+ * x * w exactly and round once more, for (x * w) * inv.  The fast path needs head_dim * element size to be a
  * multiple of 32 bytes and at most 1024 bytes (head_dim 64, 128, 256 in bf16
  * and fp32, 512 in bf16), 32-byte aligned pointers and token strides;
  * otherwise RMSN_EUNSUPPORTED.  Returns an rmsn_status.

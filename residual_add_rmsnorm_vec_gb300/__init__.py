@@ -22,5 +22,5 @@ from ._lib import (  # noqa: F401
     rmsnorm_fwd, rmsnorm_fwd_ex, rmsnorm_fwd_blockscaled, rmsnorm_fwd_host, rmsnorm_list_configs, rmsnorm_qk_fwd,
     rmsnorm_query_config,
     rmsnorm_read_status, rmsnorm_set_wait_limit, status_string)
-from .api import (check_row_args, fused_add_rmsnorm, fused_add_rmsnorm_blockscaled,  # noqa: F401
+from .api import (block_format_configs, check_row_args, fused_add_rmsnorm, fused_add_rmsnorm_blockscaled,  # noqa: F401
                   fused_add_rmsnorm_host, make_flags, qk_norm_)

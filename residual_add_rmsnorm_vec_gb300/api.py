@@ -270,3 +270,19 @@ def fused_add_rmsnorm_blockscaled(x: torch.Tensor, residual: torch.Tensor | None
     if st != _lib.RMSN_OK:
         raise _lib.RmsnError(st, "rmsnorm_fwd_blockscaled")
     return q, bs, ts, residual_out
+
+
+def block_format_configs(n_tokens: int, hidden: int, fmt: str, residual: bool = True,
+                         bias: bool = True) -> list:
+    """Launch configurations a block-scaled output can be forced to: the
+    vector kernels listed for the per-token FP8 output of the same shape
+    (the block formats are built on the same launch shapes), less the
+    element-wise kernels and, for the MX formats, the two-row pipelined ring
+    (built for per-token FP8 and NVFP4 only)."""
+    if fmt not in _lib.BLOCK_FORMATS:
+        raise ValueError(f"unknown block format {fmt!r}")
+    flags = make_flags("bf16", "fp8", residual, True, bias)
+    skip = {_lib.VARIANT_GENERIC, _lib.VARIANT_RAGGED}
+    if fmt != "nvfp4":
+        skip.add(_lib.VARIANT_BULK_PIPE)
+    return [c for c in _lib.rmsnorm_list_configs(n_tokens, hidden, flags) if c.variant not in skip]

@@ -34,10 +34,10 @@ namespace rmsn {
 namespace {
 
 constexpr int kMaxDevices = 64;
-// QK norm takes its ring variant from this many tokens up (measured on GB300:
-// below it the one-pass register kernel finishes sooner), with about this
-// many bytes of token buffers per block.
-constexpr int64_t kQkRingTokens = 1024;
+// QK norm's ring variant is taken only when asked for (RMSN_QK_RING): measured
+// on GB300 the one-pass register kernel finished sooner at every batch size.
+// About this many bytes of token buffers per ring block.
+constexpr int64_t kQkRingTokens = INT64_MAX;
 constexpr int64_t kQkRingBytes = 96 * 1024;
 constexpr int64_t kMaxHidden = int64_t(1) << 24;
 
@@ -1036,6 +1036,7 @@ RMSN_API int rmsnorm_qk_fwd(void* q, void* k, const void* q_weight, const void* 
     a.woff = weight_offset;
     a.pdl = (flags & RMSN_PDL) ? 1 : 0;
     a.status = d->status;
+    a.rcp_d = (head_dim & (head_dim - 1)) == 0 ? 1.0f / (float)head_dim : 0.f;  // exact
     a.stages = stages;
     a.wait_cycles = d->wait_cycles.load(std::memory_order_relaxed);
     void* args[] = {&a};

@@ -15,6 +15,50 @@
 
 namespace rmsn {
 
+// rsqrt(sum / D + eps), the mean square correctly rounded.  For a power-of-two
+// D, sum * (1 / D) is that same correctly rounded quotient (scaling by a power
+// of two is exact), one multiply instead of a division.
+__device__ __forceinline__ float qk_inv(float acc, const QkArgs& a) {
+    const float ms = a.rcp_d > 0.f ? __fmul_rn(acc, a.rcp_d) : __fdiv_rn(acc, (float)a.D);
+    return __frsqrt_rn(__fadd_rn(ms, a.eps));
+}
+
+// y = (w + woff) * (x * inv) for one vector.  Without an offset, 16-bit x and
+// w: y = RN(p * inv) with p = x w formed exactly (one rounding, and the 16-bit
+// lanes go straight into the FMAs); else the roundings of the listing, two
+// lanes per instruction.
+template <class TI>
+__device__ __forceinline__ void qk_scale(const V8& x, const V8& w, float inv, float woff,
+                                         float (&y)[32 / TI::kBytes]) {
+    if constexpr (TI::kBytes == 2) {
+        if (woff == 0.f) {
+            const F2 inv2 = f2(inv, inv);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                f2split(mul2(mul16x2_exact<TI>(x.u[k], w.u[k]), inv2), y[2 * k], y[2 * k + 1]);
+            return;
+        }
+    }
+    float m = 0.f;
+    scale_vec<TI, false>(x, w, w, inv, woff, y, m);
+}
+
+// This lane's sum of squares of one vector (fp32, in element order).
+template <class TI>
+__device__ __forceinline__ float qk_sumsq(const V8& x) {
+    float acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        if constexpr (TI::kBytes == 2) {
+            acc = sumsq16x2<TI>(x.u[k], acc);
+        } else {
+            const float h = __uint_as_float(x.u[k]);
+            acc = __fmaf_rn(h, h, acc);
+        }
+    }
+    return acc;
+}
+
 template <class TI, int TPH>
 __global__ void __launch_bounds__(256) rmsn_qk_kernel(const QkArgs a) {
     constexpr int VE = 32 / TI::kBytes;
@@ -48,15 +92,11 @@ __global__ void __launch_bounds__(256) rmsn_qk_kernel(const QkArgs a) {
         float acc = 0.f;
         if (act) {
             x = ld_stream32(static_cast<const char*>(row) + e * TI::kBytes);
-#pragma unroll
-            for (int k = 0; k < VE; ++k) {
-                const float h = elem<TI>(x, k);
-                acc = __fmaf_rn(h, h, acc);
-            }
+            acc = qk_sumsq<TI>(x);
         }
 #pragma unroll
         for (int o = TPH / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-        const float inv = inv_rms(acc, a.D, a.eps);
+        const float inv = qk_inv(acc, a);
         if (act) {
             const void* w = is_q ? a.qw : a.kw;
             V8 wv;
@@ -67,9 +107,7 @@ __global__ void __launch_bounds__(256) rmsn_qk_kernel(const QkArgs a) {
                 for (int k = 0; k < 8; ++k) wv.u[k] = ones_word<TI>();
             }
             float y[VE];
-#pragma unroll
-            for (int k = 0; k < VE; ++k)
-                y[k] = scale_elem<false>(elem<TI>(x, k), inv, elem<TI>(wv, k), a.woff, 0.f);
+            qk_scale<TI>(x, wv, inv, a.woff, y);
             store_out<TI, TI>(row, e, y, 0.f);
         }
     }
@@ -172,15 +210,7 @@ __global__ void __launch_bounds__(1024, 1) rmsn_qk_ring_kernel(const QkArgs a) {
             acc[c] = 0.f;
             if (v < nv) {
                 x[c] = ld_shared32(base + (uint32_t)v * 32u);
-#pragma unroll
-                for (int k2 = 0; k2 < 8; ++k2) {
-                    if constexpr (TI::kBytes == 2) {
-                        acc[c] = sumsq16x2<TI>(x[c].u[k2], acc[c]);
-                    } else {
-                        const float h = __uint_as_float(x[c].u[k2]);
-                        acc[c] = __fmaf_rn(h, h, acc[c]);
-                    }
-                }
+                acc[c] = qk_sumsq<TI>(x[c]);
             }
         }
         // every thread has read the stage: it may be refilled after this barrier
@@ -197,7 +227,7 @@ __global__ void __launch_bounds__(1024, 1) rmsn_qk_ring_kernel(const QkArgs a) {
                 acc[c] += __shfl_xor_sync(0xFFFFFFFFu, acc[c], o);
             const int v = c * G + t;
             if (v >= nv) continue;
-            const float inv = inv_rms(acc[c], a.D, a.eps);
+            const float inv = qk_inv(acc[c], a);
             const bool is_q = v < nvq;
             void* row = is_q ? a.q : a.k;
             const int64_t e = is_q ? tok * a.qs + (int64_t)v * VE
@@ -205,8 +235,8 @@ __global__ void __launch_bounds__(1024, 1) rmsn_qk_ring_kernel(const QkArgs a) {
             const int64_t ext = is_q ? (a.T - 1) * a.qs + (int64_t)a.Hq * a.D
                                      : (a.T - 1) * a.ks + (int64_t)a.Hk * a.D;
             if (!RMSN_CHECK(a.status, e >= 0 && e + VE <= ext)) continue;
-            float y[VE], m = 0.f;
-            scale_vec<TI, false>(x[c], wv[c], wv[c], inv, a.woff, y, m);
+            float y[VE];
+            qk_scale<TI>(x[c], wv[c], inv, a.woff, y);
             store_out<TI, TI>(row, e, y, 0.f);
         }
     }

@@ -21,6 +21,7 @@ struct QkArgs {
     int32_t pdl;   // launched as a programmatic dependent
     uint32_t* status;  // device status word (bit 0: a bounded wait ran out; bit 1: a
                        // bounds check failed, checked build)
+    float rcp_d;          // 1 / head_dim when head_dim is a power of two (exact), else 0
     int32_t stages;       // ring kernel: shared-memory token buffers
     int64_t wait_cycles;  // ring kernel: bound of a token wait (< 0: test once)
 };

@@ -17,7 +17,8 @@ Cases:
   fp8_T<T>_H<H>      bf16 in, per-token FP8 out, bias (the quantised workload)
   nvfp4_T<T>_H<H>    bf16 in, NVFP4 out, bias
   fp8pipe_T<T>_H<H>, nvfp4pipe_T<T>_H<H>
-                     the same on the two-row pipelined ring (2 vectors a thread)
+                     the same on the two-row pipelined ring (2 vectors a thread,
+                     the 16-warp-bound instance)
   prefill_T<T>_H<H>  the prefill workload (outlier channels, eps 1e-5)
 """
 from __future__ import annotations
@@ -78,6 +79,7 @@ def run_case(name: str, reps: int) -> str:
         flags = pkg.make_flags("bf16", "fp8", True, True, True)
         cands = [c for c in pkg.rmsnorm_list_configs(T, H, flags)
                  if c.variant == pkg.VARIANT_BULK_PIPE and c.chunks == 2]
+        cands.sort(key=lambda c: -c.max_warps)  # the 16-warp-bound instance first
         if not cands:
             raise SystemExit(f"no pipelined ring configuration for {T}x{H}")
         cfg = cands[0]

@@ -88,9 +88,8 @@ def measure(pkg, T, H, in_dt="bf16", out_dt="bf16", res=True, bias=False, reps=3
     b = (0.01 * torch.randn(H, device=dev)).to(tin) if bias else None
     stream = torch.cuda.current_stream()
     if configs is None:
-        configs = pkg.rmsnorm_list_configs(T, H, flags)
-        if block:
-            configs = [c for c in configs if c.variant != pkg.VARIANT_GENERIC]
+        configs = (pkg.block_format_configs(T, H, out_dt, res, bias) if block
+                   else pkg.rmsnorm_list_configs(T, H, flags))
     algo = _algorithmic_bytes(T, H, in_b, out_b, res, bias, out_dt == "fp8", out_dt, res_b)
     results = []
     for cfg in configs:
@@ -162,6 +161,52 @@ def sweep(pkg, shapes, in_dt, out_dt, res, bias, reps, l2_hot_below=0):
 
 ROW_RE = (r"\s*\{(-?\d+), (-?\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)"
           r"(?:, (\d+), (\d+))?\},(?:\s*// ([\d.]+) us, ([\d.]+) GB/s)?")
+
+
+def fixed_rule_shape(T, H, sms, in_bytes=2):
+    """(variant, chunks, max_warps) of the selector's fixed rules for a
+    shape without table rows (the blog's decode rule, else one block per row
+    with two vectors per thread): the fallback the nearest-measured-hidden
+    lookup sits in front of, for comparison."""
+    nvec = H * in_bytes // 32
+    if (T * nvec + 31) // 32 <= sms and nvec <= 256:
+        ch = 1
+        while 32 * ch < nvec:
+            ch *= 2
+        return (0, ch, 1)
+    for ch, wm in ((2, 4), (2, 8), (2, 16), (2, 32), (4, 16)):
+        if (nvec + 32 * ch - 1) // (32 * ch) <= wm:
+            return (1, ch, wm)
+    return (3, 0, 8)
+
+
+def check_selector(pkg, shapes, reps=30, l2_hot_below=512):
+    """For each (T, H) (bf16 with a residual and a weight): every built launch
+    timed, against the selector's pick and the fixed rules' pick."""
+    import torch
+
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    flags = pkg.make_flags("bf16", "bf16", True, True, False)
+    key = lambda d: (d["variant"], d["chunks"], d["max_warps"], d["stages"])
+    out = []
+    for T, H in shapes:
+        rs = measure(pkg, T, H, "bf16", "bf16", True, False, reps, l2_hot=T < l2_hot_below)
+        best = min(rs, key=lambda d: d["us"])
+        sel = pkg.rmsnorm_query_config(T, H, flags).as_dict()
+        sel_us = min((d["us"] for d in rs if key(d) == key(sel)), default=None)
+        rule = fixed_rule_shape(T, H, sms)
+        rule_us = min((d["us"] for d in rs if (d["variant"], d["chunks"], d["max_warps"]) == rule),
+                      default=None)
+        name = lambda d: (f"{d['variant_name']} ch{d['chunks']} w{d['warps_per_block']}"
+                          f"/{d['max_warps']} st{d['stages']}")
+        row = {"T": T, "H": H, "best": name(best), "best_us": best["us"], "selector": name(sel),
+               "selector_us": sel_us, "rule": f"{pkg.VARIANT_NAMES[rule[0]]} ch{rule[1]}/{rule[2]}",
+               "rule_us": rule_us,
+               "selector_over_best": round(sel_us / best["us"], 3) if sel_us else None,
+               "rule_over_best": round(rule_us / best["us"], 3) if rule_us else None}
+        print(json.dumps(row), flush=True)
+        out.append(row)
+    return out
 
 
 def merge_table(entries, path):
@@ -319,6 +364,10 @@ def main():
     ap.add_argument("--pairs", default="",
                     help="comma list of input:output pairs (e.g. f16:f16,bf16+r32:bf16) to sweep "
                          "on the hidden sizes 2048..16384; rows merged into the table")
+    ap.add_argument("--check-selector", default="",
+                    help="comma list of TxH shapes (bf16, residual, weight): time every built "
+                         "launch and report the selector's and the fixed rules' picks against "
+                         "the fastest (e.g. for hidden sizes without table rows)")
     ap.add_argument("--outs", default="",
                     help="comma list of quantised outputs (fp8, mxfp8, mxfp4, nvfp4) to sweep on "
                          "the quantised shapes; rows merged into the table")
@@ -329,6 +378,14 @@ def main():
     if args.quick:
         grid = [(1, 4096), (256, 4096), (16384, 8192)]
     hot = args.l2_hot_below
+    if args.check_selector:
+        shapes = [tuple(int(v) for v in sh.split("x")) for sh in args.check_selector.split(",")]
+        rows = check_selector(pkg, shapes, args.reps, hot)
+        with open(args.out, "w") as f:
+            json.dump({"meta": {"gpu": torch.cuda.get_device_name(0), "reps": args.reps,
+                                "l2_hot_below": hot, "timing": "cuda graph replay"},
+                       "rows": rows}, f, indent=1)
+        return
     if args.pairs or args.shapes:
         shapes = [(T, H) for H in HIDDEN for T in (1, 16, 256, 1024, 4096, 16384)]
         if args.shapes:

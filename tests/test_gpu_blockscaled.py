@@ -132,10 +132,9 @@ def test_block_formats_parity(pkg, fmt, wl):
 @pytest.mark.parametrize("fmt", FORMATS)
 def test_block_formats_every_config(pkg, fmt):
     wl = synth.Workload("bs_cfg", 37, 2048, 75, "bf16", "bf16", 1e-6, has_bias=True)
-    flags = pkg.make_flags("bf16", "fp8", True, True, True)
-    cfgs = [c for c in pkg.rmsnorm_list_configs(37, 2048, flags)
-            if c.variant != pkg.VARIANT_GENERIC]
+    cfgs = pkg.block_format_configs(37, 2048, fmt)
     assert cfgs
+    assert (pkg.VARIANT_BULK_PIPE in {c.variant for c in cfgs}) == (fmt == "nvfp4")
     for c in cfgs:
         run(pkg, fmt, wl, config=c)
 

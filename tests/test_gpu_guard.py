@@ -127,9 +127,7 @@ def test_block_formats_write_only_their_outputs(pkg, fmt, T, H):
     x, r, w, b = (inp[k].cuda() for k in ("x", "residual", "weight", "bias"))
     code, blk, per_byte = pkg.BLOCK_FORMATS[fmt]
     flags = pkg.make_flags("bf16", "f32", True, True, True)
-    cfgs = [c for c in pkg.rmsnorm_list_configs(T, H, pkg.make_flags("bf16", "fp8", True, True,
-                                                                      True))
-            if c.variant != pkg.VARIANT_GENERIC]
+    cfgs = pkg.block_format_configs(T, H, fmt)
     s = torch.cuda.current_stream().cuda_stream
     for c in [None] + cfgs:
         q = Guarded((T, H // per_byte), torch.uint8)

@@ -443,10 +443,12 @@ def test_selector_decode_vs_prefill(pkg):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     # a hidden size without measured rows but a measured neighbour within 2x
     # (2560: 3072 is nearest) takes the neighbour's launch shape
+    keys = ("variant", "chunks", "max_warps", "stages")
     for T in (8, 4096):
         c = pkg.rmsnorm_query_config(T, 2560, flags)
         n = pkg.rmsnorm_query_config(T, 3072, flags)
-        assert _same_shape(c, n) and c.num_sms == sms, (T, c.as_dict(), n.as_dict())
+        assert all(getattr(c, k) == getattr(n, k) for k in keys) and c.num_sms == sms, \
+            (T, c.as_dict(), n.as_dict())
     # no measured hidden size within 2x (bf16 512: the nearest, 2048, is 4x
     # away): the decode rule (one warp per block while the problem needs
     # fewer warps than there are SMs), else one block per row

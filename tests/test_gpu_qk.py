@@ -41,13 +41,6 @@ def compare(dtype, got, ref, where):
     return 1.0
 
 
-@pytest.mark.parametrize("T,Hq,Hk,D,dtype", [
-    (1, 32, 8, 128, "bf16"), (7, 16, 4, 64, "bf16"), (512, 32, 8, 128, "bf16"),
-    (4096, 32, 8, 128, "bf16"), (16384, 32, 8, 128, "bf16"), (33, 8, 2, 256, "bf16"),
-    (3, 2, 1, 512, "bf16"),
-    (5, 4, 4, 128, "f32"), (65, 6, 2, 64, "f32"), (9, 3, 1, 256, "f32"), (2, 1, 1, 16, "bf16"),
-    (17, 32, 8, 128, "f16"), (3, 4, 2, 64, "f16"), (5, 2, 2, 256, "f16"),
-])
 def ring_applies(Hq, Hk, D, dtype):
     """The ring variant's shapes: 4..32 whole 32-byte vectors per head (a power
     of two), at most 2048 per token."""
@@ -55,9 +48,17 @@ def ring_applies(Hq, Hk, D, dtype):
     return nvec >= 4 and nvec & (nvec - 1) == 0 and nvec <= 32 and (Hq + Hk) * nvec <= 2048
 
 
+@pytest.mark.parametrize("T,Hq,Hk,D,dtype", [
+    (1, 32, 8, 128, "bf16"), (7, 16, 4, 64, "bf16"), (512, 32, 8, 128, "bf16"),
+    (4096, 32, 8, 128, "bf16"), (16384, 32, 8, 128, "bf16"), (33, 8, 2, 256, "bf16"),
+    (3, 2, 1, 512, "bf16"),
+    (5, 4, 4, 128, "f32"), (65, 6, 2, 64, "f32"), (9, 3, 1, 256, "f32"), (2, 1, 1, 16, "bf16"),
+    (17, 32, 8, 128, "f16"), (3, 4, 2, 64, "f16"), (5, 2, 2, 256, "f16"),
+])
 @pytest.mark.parametrize("pad", [0, 16])
 @pytest.mark.parametrize("variant", [None, "ring", "direct"])
-def test_qk_norm_fused_qkv(pkg, T, Hq, Hk, D, dtype, pad, variant):
+@pytest.mark.parametrize("woff", [0.25, 0.0])
+def test_qk_norm_fused_qkv(pkg, T, Hq, Hk, D, dtype, pad, variant, woff):
     if pad and dtype == "f32":
         pad = 8  # keep the row stride a multiple of 32 bytes
     if variant == "ring" and not ring_applies(Hq, Hk, D, dtype):
@@ -66,13 +67,13 @@ def test_qk_norm_fused_qkv(pkg, T, Hq, Hk, D, dtype, pad, variant):
     qkv = inp["qkv"]
     S = qkv.shape[1]
     ref_q, _ = oracle.qk_norm(qkv, None, inp["q_weight"], None, n_q_heads=Hq, n_k_heads=0,
-                              head_dim=D, eps=1e-6, dtype=dtype, weight_offset=0.25)
+                              head_dim=D, eps=1e-6, dtype=dtype, weight_offset=woff)
     _, ref_k = oracle.qk_norm(None, qkv[:, Hq * D:].contiguous(), None, inp["k_weight"],
                               n_q_heads=0, n_k_heads=Hk, head_dim=D, eps=1e-6, dtype=dtype,
-                              weight_offset=0.25)
+                              weight_offset=woff)
     g = qkv.cuda()
     pkg.qk_norm_(g[:, :Hq * D], g[:, Hq * D:(Hq + Hk) * D], inp["q_weight"].cuda(),
-                 inp["k_weight"].cuda(), head_dim=D, eps=1e-6, weight_offset=0.25,
+                 inp["k_weight"].cuda(), head_dim=D, eps=1e-6, weight_offset=woff,
                  variant=variant)
     torch.cuda.synchronize()
     got = bits(g, dtype)
