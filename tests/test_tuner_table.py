@@ -165,3 +165,17 @@ def test_generated_neighbours_nearest_first_and_residual_rows(tmp_path):
         "12288: 16384 8192",
     ]
     assert out[8:] == ["res0 1 4", "res1 2 8", "fallback 1 2 8"]
+
+
+def test_fixed_rule_mirror_follows_the_documented_rules():
+    # the tuner's copy of the selector's fixed rules (used to report how far
+    # they were from the fastest launch): one warp per row while the problem
+    # needs no more warps than SMs and a row fits 8 vectors a lane, else the
+    # fewest of 4 / 8 / 16 / 32 warps with two vectors per thread
+    assert tune.fixed_rule_shape(8, 2560, 152) == (0, 8, 1)     # 160 vectors: CH 8 covers
+    assert tune.fixed_rule_shape(1, 4096, 152) == (0, 8, 1)
+    assert tune.fixed_rule_shape(2, 512, 152) == (0, 1, 1)      # 32 vectors: one chunk
+    assert tune.fixed_rule_shape(4096, 2560, 152) == (1, 2, 4)  # 4096 warps > 152 SMs
+    assert tune.fixed_rule_shape(1, 10240, 152) == (1, 2, 16)   # 640 vectors > 8 per lane
+    assert tune.fixed_rule_shape(16384, 6656, 152) == (1, 2, 8)
+    assert tune.fixed_rule_shape(1, 65536, 152) == (3, 0, 8)    # nothing fits: generic
