@@ -59,57 +59,86 @@ __device__ __forceinline__ float qk_sumsq(const V8& x) {
     return acc;
 }
 
+// Elements [e, e + n) inside the span of q (is_q) or k: (T - 1) * stride +
+// heads * head_dim elements (the bounds-checked build's test).
+__device__ __forceinline__ bool qk_in_span(const QkArgs& a, bool is_q, int64_t e, int n) {
+    const int64_t ext = is_q ? (a.T - 1) * a.qs + (int64_t)a.Hq * a.D
+                             : (a.T - 1) * a.ks + (int64_t)a.Hk * a.D;
+    return e >= 0 && e + n <= ext;
+}
+
+// One head's vector of this lane: where it lives, and whether the lane has one.
+struct QkSlot {
+    void* row;
+    int64_t e;  // element index in q (k)
+    bool is_q, act;
+};
+
 template <class TI, int TPH>
-__global__ void __launch_bounds__(256) rmsn_qk_kernel(const QkArgs a) {
+__device__ __forceinline__ QkSlot qk_slot(const QkArgs& a, int64_t head, int sub) {
     constexpr int VE = 32 / TI::kBytes;
+    const int64_t heads = a.Hq + a.Hk;
+    const bool valid = head < a.T * heads;
+    const int64_t tok = valid ? head / heads : 0;
+    const int hh = valid ? (int)(head % heads) : 0;
+    QkSlot sl;
+    sl.is_q = hh < a.Hq;
+    sl.row = sl.is_q ? a.q : a.k;
+    const int64_t e0 = sl.is_q ? tok * a.qs + (int64_t)hh * a.D
+                               : tok * a.ks + (int64_t)(hh - a.Hq) * a.D;
+    sl.e = e0 + (int64_t)sub * VE;
+    sl.act = valid && sub < a.nvec &&
+             RMSN_CHECK(a.status, qk_in_span(a, sl.is_q, sl.e, VE) &&
+                                      (sub + 1) * 32 <= a.D * TI::kBytes);
+    return sl;
+}
+
+// Normalise and store one head's vector (x loaded, acc its lane's sum of squares).
+template <class TI, int TPH>
+__device__ __forceinline__ void qk_finish(const QkArgs& a, const QkSlot& sl, const V8& x,
+                                          float acc, int sub) {
+    constexpr int VE = 32 / TI::kBytes;
+#pragma unroll
+    for (int o = TPH / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+    const float inv = qk_inv(acc, a);
+    if (sl.act) {
+        const void* w = sl.is_q ? a.qw : a.kw;
+        V8 wv;
+        if (w) {
+            wv = ld_keep32(static_cast<const char*>(w) + (int64_t)sub * 32);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) wv.u[k] = ones_word<TI>();
+        }
+        float y[VE];
+        qk_scale<TI>(x, wv, inv, a.woff, y);
+        store_out<TI, TI>(sl.row, sl.e, y, 0.f);
+    }
+}
+
+// One pass: a head per TPH lanes, each warp taking 32 / TPH heads at a time,
+// grid-stride; every lane loads the vectors of two heads (this step's and the
+// next's) before it works on either, so two 32-byte requests per lane are in
+// flight while the butterflies and the scaling run.
+template <class TI, int TPH>
+__global__ void __launch_bounds__(256, 5) rmsn_qk_kernel(const QkArgs a) {
     pdl_launch_dependents(a.pdl);
     pdl_wait(a.pdl);
     const int lane = threadIdx.x & 31;
     const int sub = lane % TPH;  // this lane's vector within its head
-    const int64_t heads = a.Hq + a.Hk;
-    const int64_t nh = a.T * heads;
+    const int64_t nh = a.T * (int64_t)(a.Hq + a.Hk);
     const int64_t step = (int64_t)gridDim.x * blockDim.x / TPH;
     // the warp's first head: the loop bound is uniform across the warp, so
     // every lane reaches every shuffle
     for (int64_t base = ((int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31)) / TPH;
-         base < nh; base += step) {
-        const int64_t head = base + lane / TPH;
-        const bool valid = head < nh;
-        const int64_t tok = valid ? head / heads : 0;
-        const int hh = valid ? (int)(head % heads) : 0;
-        const bool is_q = hh < a.Hq;
-        void* row = is_q ? a.q : a.k;
-        const int64_t e0 = is_q ? tok * a.qs + (int64_t)hh * a.D
-                                : tok * a.ks + (int64_t)(hh - a.Hq) * a.D;
-        const int64_t e = e0 + (int64_t)sub * VE;
-        // elements of q (k) the heads span: (T - 1) * stride + heads * head_dim
-        const int64_t ext = is_q ? (a.T - 1) * a.qs + (int64_t)a.Hq * a.D
-                                 : (a.T - 1) * a.ks + (int64_t)a.Hk * a.D;
-        const bool act = valid && sub < a.nvec &&
-                         RMSN_CHECK(a.status, e >= 0 && e + VE <= ext &&
-                                                  (sub + 1) * 32 <= a.D * TI::kBytes);
-        V8 x;
-        float acc = 0.f;
-        if (act) {
-            x = ld_stream32(static_cast<const char*>(row) + e * TI::kBytes);
-            acc = qk_sumsq<TI>(x);
-        }
-#pragma unroll
-        for (int o = TPH / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-        const float inv = qk_inv(acc, a);
-        if (act) {
-            const void* w = is_q ? a.qw : a.kw;
-            V8 wv;
-            if (w) {
-                wv = ld_keep32(static_cast<const char*>(w) + (int64_t)sub * 32);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) wv.u[k] = ones_word<TI>();
-            }
-            float y[VE];
-            qk_scale<TI>(x, wv, inv, a.woff, y);
-            store_out<TI, TI>(row, e, y, 0.f);
-        }
+         base < nh; base += 2 * step) {
+        const QkSlot s0 = qk_slot<TI, TPH>(a, base + lane / TPH, sub);
+        const QkSlot s1 = qk_slot<TI, TPH>(a, base + step + lane / TPH, sub);
+        V8 x0, x1;
+        if (s0.act) x0 = ld_stream32(static_cast<const char*>(s0.row) + s0.e * TI::kBytes);
+        if (s1.act) x1 = ld_stream32(static_cast<const char*>(s1.row) + s1.e * TI::kBytes);
+        qk_finish<TI, TPH>(a, s0, x0, s0.act ? qk_sumsq<TI>(x0) : 0.f, sub);
+        qk_finish<TI, TPH>(a, s1, x1, s1.act ? qk_sumsq<TI>(x1) : 0.f, sub);
     }
 }
 
@@ -232,9 +261,7 @@ __global__ void __launch_bounds__(1024, 1) rmsn_qk_ring_kernel(const QkArgs a) {
             void* row = is_q ? a.q : a.k;
             const int64_t e = is_q ? tok * a.qs + (int64_t)v * VE
                                    : tok * a.ks + (int64_t)(v - nvq) * VE;
-            const int64_t ext = is_q ? (a.T - 1) * a.qs + (int64_t)a.Hq * a.D
-                                     : (a.T - 1) * a.ks + (int64_t)a.Hk * a.D;
-            if (!RMSN_CHECK(a.status, e >= 0 && e + VE <= ext)) continue;
+            if (!RMSN_CHECK(a.status, qk_in_span(a, is_q, e, VE))) continue;
             float y[VE];
             qk_scale<TI>(x[c], wv[c], inv, a.woff, y);
             store_out<TI, TI>(row, e, y, 0.f);
