@@ -67,79 +67,91 @@ __device__ __forceinline__ bool qk_in_span(const QkArgs& a, bool is_q, int64_t e
     return e >= 0 && e + n <= ext;
 }
 
-// One head's vector of this lane: where it lives, and whether the lane has one.
-struct QkSlot {
-    void* row;
-    int64_t e;  // element index in q (k)
-    bool is_q, act;
-};
-
-template <class TI, int TPH>
-__device__ __forceinline__ QkSlot qk_slot(const QkArgs& a, int64_t head, int sub) {
-    constexpr int VE = 32 / TI::kBytes;
-    const int64_t heads = a.Hq + a.Hk;
-    const bool valid = head < a.T * heads;
-    const int64_t tok = valid ? head / heads : 0;
-    const int hh = valid ? (int)(head % heads) : 0;
-    QkSlot sl;
-    sl.is_q = hh < a.Hq;
-    sl.row = sl.is_q ? a.q : a.k;
-    const int64_t e0 = sl.is_q ? tok * a.qs + (int64_t)hh * a.D
-                               : tok * a.ks + (int64_t)(hh - a.Hq) * a.D;
-    sl.e = e0 + (int64_t)sub * VE;
-    sl.act = valid && sub < a.nvec &&
-             RMSN_CHECK(a.status, qk_in_span(a, sl.is_q, sl.e, VE) &&
-                                      (sub + 1) * 32 <= a.D * TI::kBytes);
-    return sl;
+// 16 bytes from global to shared memory, asynchronously (cp.async, L2 only).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
-// Normalise and store one head's vector (x loaded, acc its lane's sum of squares).
-template <class TI, int TPH>
-__device__ __forceinline__ void qk_finish(const QkArgs& a, const QkSlot& sl, const V8& x,
-                                          float acc, int sub) {
-    constexpr int VE = 32 / TI::kBytes;
-#pragma unroll
-    for (int o = TPH / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-    const float inv = qk_inv(acc, a);
-    if (sl.act) {
-        const void* w = sl.is_q ? a.qw : a.kw;
-        V8 wv;
-        if (w) {
-            wv = ld_keep32(static_cast<const char*>(w) + (int64_t)sub * 32);
-        } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) wv.u[k] = ones_word<TI>();
-        }
-        float y[VE];
-        qk_scale<TI>(x, wv, inv, a.woff, y);
-        store_out<TI, TI>(sl.row, sl.e, y, 0.f);
-    }
-}
-
-// One pass: a head per TPH lanes, each warp taking 32 / TPH heads at a time,
-// grid-stride; every lane loads the vectors of two heads (this step's and the
-// next's) before it works on either, so two 32-byte requests per lane are in
-// flight while the butterflies and the scaling run.
 template <class TI, int TPH>
 __global__ void __launch_bounds__(256, 5) rmsn_qk_kernel(const QkArgs a) {
+    constexpr int VE = 32 / TI::kBytes;
+    // each thread's next vector, prefetched while it works on the current
+    // one: two 16-byte halves per buffer, laid out so that a warp's 16-byte
+    // reads of one half are contiguous (conflict-free)
+    __shared__ __align__(16) uint4 pre[2][2][256];
     pdl_launch_dependents(a.pdl);
     pdl_wait(a.pdl);
     const int lane = threadIdx.x & 31;
     const int sub = lane % TPH;  // this lane's vector within its head
-    const int64_t nh = a.T * (int64_t)(a.Hq + a.Hk);
+    const int64_t heads = a.Hq + a.Hk;
+    const int64_t nh = a.T * heads;
     const int64_t step = (int64_t)gridDim.x * blockDim.x / TPH;
+    // where this lane's vector of the head `head` lives, and whether it has one
+    auto slot = [&](int64_t head, void*& row, int64_t& e, bool& is_q) -> bool {
+        const bool valid = head < nh;
+        const int64_t tok = valid ? head / heads : 0;
+        const int hh = valid ? (int)(head % heads) : 0;
+        is_q = hh < a.Hq;
+        row = is_q ? a.q : a.k;
+        e = (is_q ? tok * a.qs + (int64_t)hh * a.D : tok * a.ks + (int64_t)(hh - a.Hq) * a.D) +
+            (int64_t)sub * VE;
+        return valid && sub < a.nvec &&
+               RMSN_CHECK(a.status, qk_in_span(a, is_q, e, VE) &&
+                                        (sub + 1) * 32 <= a.D * TI::kBytes);
+    };
+    auto fetch = [&](int buf, const void* row, int64_t e) {
+        const char* src = static_cast<const char*>(row) + e * TI::kBytes;
+        cp_async16(smem_u32(&pre[buf][0][threadIdx.x]), src);
+        cp_async16(smem_u32(&pre[buf][1][threadIdx.x]), src + 16);
+    };
     // the warp's first head: the loop bound is uniform across the warp, so
     // every lane reaches every shuffle
-    for (int64_t base = ((int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31)) / TPH;
-         base < nh; base += 2 * step) {
-        const QkSlot s0 = qk_slot<TI, TPH>(a, base + lane / TPH, sub);
-        const QkSlot s1 = qk_slot<TI, TPH>(a, base + step + lane / TPH, sub);
-        V8 x0, x1;
-        if (s0.act) x0 = ld_stream32(static_cast<const char*>(s0.row) + s0.e * TI::kBytes);
-        if (s1.act) x1 = ld_stream32(static_cast<const char*>(s1.row) + s1.e * TI::kBytes);
-        qk_finish<TI, TPH>(a, s0, x0, s0.act ? qk_sumsq<TI>(x0) : 0.f, sub);
-        qk_finish<TI, TPH>(a, s1, x1, s1.act ? qk_sumsq<TI>(x1) : 0.f, sub);
+    int64_t base = ((int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31)) / TPH;
+    void* row;
+    int64_t e;
+    bool is_q;
+    bool act = slot(base + lane / TPH, row, e, is_q);
+    if (act) fetch(0, row, e);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    for (int buf = 0; base < nh; base += step, buf ^= 1) {
+        // request the next step's vector, then wait for this one's
+        void* nrow;
+        int64_t ne;
+        bool nis_q;
+        const bool nact = slot(base + step + lane / TPH, nrow, ne, nis_q);
+        if (nact) fetch(buf ^ 1, nrow, ne);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+        V8 x;
+        float acc = 0.f;
+        if (act) {
+            const uint4 lo = pre[buf][0][threadIdx.x], hi = pre[buf][1][threadIdx.x];
+            x.u[0] = lo.x; x.u[1] = lo.y; x.u[2] = lo.z; x.u[3] = lo.w;
+            x.u[4] = hi.x; x.u[5] = hi.y; x.u[6] = hi.z; x.u[7] = hi.w;
+            acc = qk_sumsq<TI>(x);
+        }
+#pragma unroll
+        for (int o = TPH / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+        const float inv = qk_inv(acc, a);
+        if (act) {
+            const void* w = is_q ? a.qw : a.kw;
+            V8 wv;
+            if (w) {
+                wv = ld_keep32(static_cast<const char*>(w) + (int64_t)sub * 32);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) wv.u[k] = ones_word<TI>();
+            }
+            float y[VE];
+            qk_scale<TI>(x, wv, inv, a.woff, y);
+            store_out<TI, TI>(row, e, y, 0.f);
+        }
+        row = nrow;
+        e = ne;
+        is_q = nis_q;
+        act = nact;
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- ring variant
