@@ -67,18 +67,9 @@ __device__ __forceinline__ bool qk_in_span(const QkArgs& a, bool is_q, int64_t e
     return e >= 0 && e + n <= ext;
 }
 
-// 16 bytes from global to shared memory, asynchronously (cp.async, L2 only).
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-
 template <class TI, int TPH>
-__global__ void __launch_bounds__(256, 5) rmsn_qk_kernel(const QkArgs a) {
+__global__ void __launch_bounds__(256) rmsn_qk_kernel(const QkArgs a) {
     constexpr int VE = 32 / TI::kBytes;
-    // each thread's next vector, prefetched while it works on the current
-    // one: two 16-byte halves per buffer, laid out so that a warp's 16-byte
-    // reads of one half are contiguous (conflict-free)
-    __shared__ __align__(16) uint4 pre[2][2][256];
     pdl_launch_dependents(a.pdl);
     pdl_wait(a.pdl);
     const int lane = threadIdx.x & 31;
@@ -99,37 +90,27 @@ __global__ void __launch_bounds__(256, 5) rmsn_qk_kernel(const QkArgs a) {
                RMSN_CHECK(a.status, qk_in_span(a, is_q, e, VE) &&
                                         (sub + 1) * 32 <= a.D * TI::kBytes);
     };
-    auto fetch = [&](int buf, const void* row, int64_t e) {
-        const char* src = static_cast<const char*>(row) + e * TI::kBytes;
-        cp_async16(smem_u32(&pre[buf][0][threadIdx.x]), src);
-        cp_async16(smem_u32(&pre[buf][1][threadIdx.x]), src + 16);
-    };
     // the warp's first head: the loop bound is uniform across the warp, so
     // every lane reaches every shuffle
-    int64_t base = ((int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31)) / TPH;
-    void* row;
-    int64_t e;
-    bool is_q;
-    bool act = slot(base + lane / TPH, row, e, is_q);
-    if (act) fetch(0, row, e);
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    for (int buf = 0; base < nh; base += step, buf ^= 1) {
-        // request the next step's vector, then wait for this one's
-        void* nrow;
-        int64_t ne;
-        bool nis_q;
-        const bool nact = slot(base + step + lane / TPH, nrow, ne, nis_q);
-        if (nact) fetch(buf ^ 1, nrow, ne);
-        asm volatile("cp.async.commit_group;" ::: "memory");
-        asm volatile("cp.async.wait_group 1;" ::: "memory");
+    for (int64_t base = ((int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31)) / TPH;
+         base < nh; base += step) {
+        void* row;
+        int64_t e;
+        bool is_q;
+        const bool act = slot(base + lane / TPH, row, e, is_q);
         V8 x;
         float acc = 0.f;
-        if (act) {
-            const uint4 lo = pre[buf][0][threadIdx.x], hi = pre[buf][1][threadIdx.x];
-            x.u[0] = lo.x; x.u[1] = lo.y; x.u[2] = lo.z; x.u[3] = lo.w;
-            x.u[4] = hi.x; x.u[5] = hi.y; x.u[6] = hi.z; x.u[7] = hi.w;
-            acc = qk_sumsq<TI>(x);
+        if (act) x = ld_stream32(static_cast<const char*>(row) + e * TI::kBytes);
+        {
+            // ask L2 for the next step's vector while this one is worked on
+            void* nrow;
+            int64_t ne;
+            bool nq;
+            if (slot(base + step + lane / TPH, nrow, ne, nq))
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char*>(nrow) +
+                                                            ne * TI::kBytes));
         }
+        if (act) acc = qk_sumsq<TI>(x);
 #pragma unroll
         for (int o = TPH / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
         const float inv = qk_inv(acc, a);
@@ -146,12 +127,7 @@ __global__ void __launch_bounds__(256, 5) rmsn_qk_kernel(const QkArgs a) {
             qk_scale<TI>(x, wv, inv, a.woff, y);
             store_out<TI, TI>(row, e, y, 0.f);
         }
-        row = nrow;
-        e = ne;
-        is_q = nis_q;
-        act = nact;
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- ring variant
