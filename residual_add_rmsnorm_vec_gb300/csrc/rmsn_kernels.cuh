@@ -785,7 +785,6 @@ __device__ __forceinline__ void scale_store_block(const RmsnArgs& a, int64_t row
     constexpr int VE = 32 / TI::kBytes;
     constexpr int LPB = TO::kBlock / VE;
     constexpr bool NV = TO::kBlock == 16;
-    constexpr bool FP4 = !std::is_same<TO, MXFP8>::value;
     constexpr bool HOLD = KEEP && NV;  // keep y between NVFP4's row-max and block passes
     static_assert(LPB >= 1 && LPB <= 4, "block spans 1..4 lanes");
     float ys[HOLD ? CH : 1][HOLD ? VE : 1];

@@ -77,40 +77,28 @@ __global__ void __launch_bounds__(256) rmsn_qk_kernel(const QkArgs a) {
     const int64_t heads = a.Hq + a.Hk;
     const int64_t nh = a.T * heads;
     const int64_t step = (int64_t)gridDim.x * blockDim.x / TPH;
-    // where this lane's vector of the head `head` lives, and whether it has one
-    auto slot = [&](int64_t head, void*& row, int64_t& e, bool& is_q) -> bool {
-        const bool valid = head < nh;
-        const int64_t tok = valid ? head / heads : 0;
-        const int hh = valid ? (int)(head % heads) : 0;
-        is_q = hh < a.Hq;
-        row = is_q ? a.q : a.k;
-        e = (is_q ? tok * a.qs + (int64_t)hh * a.D : tok * a.ks + (int64_t)(hh - a.Hq) * a.D) +
-            (int64_t)sub * VE;
-        return valid && sub < a.nvec &&
-               RMSN_CHECK(a.status, qk_in_span(a, is_q, e, VE) &&
-                                        (sub + 1) * 32 <= a.D * TI::kBytes);
-    };
     // the warp's first head: the loop bound is uniform across the warp, so
     // every lane reaches every shuffle
     for (int64_t base = ((int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31)) / TPH;
          base < nh; base += step) {
-        void* row;
-        int64_t e;
-        bool is_q;
-        const bool act = slot(base + lane / TPH, row, e, is_q);
+        const int64_t head = base + lane / TPH;
+        const bool valid = head < nh;
+        const int64_t tok = valid ? head / heads : 0;
+        const int hh = valid ? (int)(head % heads) : 0;
+        const bool is_q = hh < a.Hq;
+        void* row = is_q ? a.q : a.k;
+        const int64_t e0 = is_q ? tok * a.qs + (int64_t)hh * a.D
+                                : tok * a.ks + (int64_t)(hh - a.Hq) * a.D;
+        const int64_t e = e0 + (int64_t)sub * VE;
+        const bool act = valid && sub < a.nvec &&
+                         RMSN_CHECK(a.status, qk_in_span(a, is_q, e, VE) &&
+                                                  (sub + 1) * 32 <= a.D * TI::kBytes);
         V8 x;
         float acc = 0.f;
-        if (act) x = ld_stream32(static_cast<const char*>(row) + e * TI::kBytes);
-        {
-            // ask L2 for the next step's vector while this one is worked on
-            void* nrow;
-            int64_t ne;
-            bool nq;
-            if (slot(base + step + lane / TPH, nrow, ne, nq))
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char*>(nrow) +
-                                                            ne * TI::kBytes));
+        if (act) {
+            x = ld_stream32(static_cast<const char*>(row) + e * TI::kBytes);
+            acc = qk_sumsq<TI>(x);
         }
-        if (act) acc = qk_sumsq<TI>(x);
 #pragma unroll
         for (int o = TPH / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
         const float inv = qk_inv(acc, a);
