@@ -983,8 +983,10 @@ RMSN_API int rmsnorm_qk_fwd(void* q, void* k, const void* q_weight, const void* 
     // token (two per thread), at least two token buffers in shared memory
     const int64_t tok_vecs = (n_q_heads + n_k_heads) * nvec;
     const int64_t tok_bytes = tok_vecs * 32;
+    // a ring buffer holds two tokens with one vector per thread, else one
+    const int64_t buf_bytes = (tok_vecs > 1024 ? 1 : 2) * tok_bytes;
     const bool ring_ok = tph == nvec && nvec >= 4 && tok_vecs <= 2048 &&
-                         2 * tok_bytes <= d->max_smem - 1024;
+                         2 * buf_bytes <= d->max_smem - 1024;
     bool ring = ring_ok && n_tokens >= kQkRingTokens;
     if (flags & RMSN_QK_RING) {
         if (!ring_ok) return RMSN_EUNSUPPORTED;
@@ -1003,9 +1005,9 @@ RMSN_API int rmsnorm_qk_fwd(void* q, void* k, const void* q_weight, const void* 
     if (ring) {
         threads = (int)(((tok_vecs + ch - 1) / ch + 31) / 32 * 32);
         // about 96 KiB of token buffers per block (two blocks per SM), 2..8 of them
-        stages = (int)(kQkRingBytes / tok_bytes);
+        stages = (int)(kQkRingBytes / buf_bytes);
         stages = stages < 2 ? 2 : (stages > kMaxStages ? kMaxStages : stages);
-        smem = (size_t)stages * (size_t)tok_bytes;
+        smem = (size_t)stages * (size_t)buf_bytes;
         if ((int64_t)smem > 48 * 1024 && (int64_t)smem > enable_smem(d, e->fn))
             return RMSN_EUNSUPPORTED;
         const int bps = blocks_per_sm(d, e->fn, threads, (int)smem);

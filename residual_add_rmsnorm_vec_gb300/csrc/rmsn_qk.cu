@@ -120,22 +120,48 @@ __global__ void __launch_bounds__(256) rmsn_qk_kernel(const QkArgs a) {
 
 // ---------------------------------------------------------------- ring variant
 //
-// For long batches: persistent blocks, each taking tokens blockIdx.x +
-// k * gridDim.x.  Thread 0 copies a token's query heads and key heads (two
-// 1-D bulk copies, TMA, completing on the stage's mbarrier) into a ring of
-// `stages` shared-memory buffers, up to `stages` tokens ahead; thread t holds
-// the 32-byte vectors v = c * G + t (c < CH) of every token, so its weight
-// vectors are the same for the whole launch and are loaded once into
-// registers.  A head's TPH vectors sit on TPH neighbouring lanes (G is a
+// For long batches (opt-in, RMSN_QK_RING): persistent blocks, each taking
+// tokens blockIdx.x + k * gridDim.x.  Thread 0 copies the query heads and
+// the key heads of TPS consecutive tokens of the block (two 1-D bulk copies
+// per token, TMA, completing on the stage's mbarrier) into one buffer of a
+// ring of `stages` shared-memory buffers, up to `stages` buffers ahead;
+// thread t holds the 32-byte vectors v = c * G + t (c < CH) of every token,
+// so its weight vectors are the same for the whole launch and are loaded once
+// into registers.  A head's TPH vectors sit on TPH neighbouring lanes (G is a
 // multiple of 32 and TPH divides 32), so its sum of squares is a butterfly
 // over those lanes; the normalised vectors are stored straight back in
-// place.  One block barrier per token releases its buffer, which thread 0
-// then refills.  Waits are bounded as in the row kernel's ring: one that runs
-// out sets bit 0 of the status word, the block stops after the token's
-// barrier, and thread 0 drains its copies in flight (default bound) first.
+// place.  Each lane reads its vector's two 16-byte halves in a lane-dependent
+// order, so the 8 lanes of a quarter warp meet 32 different banks.  One block
+// barrier per buffer (TPS = 2 tokens with one vector per thread) releases it,
+// and thread 0 refills it.  Waits are bounded as in the row kernel's ring:
+// one that runs out sets bit 0 of the status word, the block stops after the
+// buffer's barrier, and thread 0 drains its copies in flight (default bound).
+
+// A 32-byte vector from shared memory, its halves read in the order that
+// keeps a quarter warp's 16-byte loads on distinct banks (lanes 4-7 of each
+// 8 start with the upper half).
+__device__ __forceinline__ V8 ld_shared32_lanes(uint32_t addr) {
+    const uint32_t sw = (threadIdx.x & 4u) << 2;  // 16 or 0
+    uint32_t p[4], q[4];
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(p[0]), "=r"(p[1]), "=r"(p[2]), "=r"(p[3])
+                 : "r"(addr + sw));
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3])
+                 : "r"(addr + (sw ^ 16u)));
+    V8 v;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        v.u[k] = sw ? q[k] : p[k];
+        v.u[4 + k] = sw ? p[k] : q[k];
+    }
+    return v;
+}
+
 template <class TI, int TPH, int CH>
 __global__ void __launch_bounds__(1024, 1) rmsn_qk_ring_kernel(const QkArgs a) {
     constexpr int VE = 32 / TI::kBytes;
+    constexpr int TPS = CH == 1 ? 2 : 1;  // tokens per buffer
     extern __shared__ __align__(128) unsigned char qring[];
     __shared__ __align__(8) uint64_t full[kMaxStages];
     __shared__ int abort_flag;
@@ -145,10 +171,12 @@ __global__ void __launch_bounds__(1024, 1) rmsn_qk_ring_kernel(const QkArgs a) {
     const int hv = a.nvec;                                // vectors per head
     const uint32_t qbytes = (uint32_t)a.Hq * a.D * TI::kBytes;
     const uint32_t kbytes = (uint32_t)a.Hk * a.D * TI::kBytes;
-    const uint32_t stage_bytes = qbytes + kbytes;
-    const int nvq = (int)(qbytes / 32), nv = (int)(stage_bytes / 32);
+    const uint32_t tok_bytes = qbytes + kbytes;
+    const uint32_t stage_bytes = TPS * tok_bytes;
+    const int nvq = (int)(qbytes / 32), nv = (int)(tok_bytes / 32);
     const uint32_t ring0 = smem_u32(qring);
     const int64_t n_my = a.T > blockIdx.x ? (a.T - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int64_t n_buf = (n_my + TPS - 1) / TPS;  // buffers this block fills
     pdl_launch_dependents(a.pdl);
     if (t == 0) {
         abort_flag = 0;
@@ -170,81 +198,94 @@ __global__ void __launch_bounds__(1024, 1) rmsn_qk_ring_kernel(const QkArgs a) {
             for (int k = 0; k < 8; ++k) wv[c].u[k] = ones_word<TI>();
         }
     }
-    // thread 0: copy token `tok`'s query and key heads into the stage at `dst`
-    auto issue = [&](int64_t tok, uint32_t dst, uint32_t bar) {
+    // thread 0: copy the tokens of buffer b (the block's tokens b * TPS ..)
+    // into the stage at `dst`
+    auto issue = [&](int64_t b, uint32_t dst, uint32_t bar) {
+        const int64_t first = b * TPS;
+        const int ntok = (int)(n_my - first < TPS ? n_my - first : TPS);
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                     "r"(stage_bytes)
+                     "r"((uint32_t)ntok * tok_bytes)
                      : "memory");
-        if (qbytes) {
-            const char* src = static_cast<const char*>(a.q) + tok * a.qs * TI::kBytes;
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], "
-                "%2, [%3];" ::"r"(dst), "l"(src), "r"(qbytes), "r"(bar)
-                : "memory");
-        }
-        if (kbytes) {
-            const char* src = static_cast<const char*>(a.k) + tok * a.ks * TI::kBytes;
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], "
-                "%2, [%3];" ::"r"(dst + qbytes), "l"(src), "r"(kbytes), "r"(bar)
-                : "memory");
+        for (int j = 0; j < ntok; ++j) {
+            const int64_t tok = blockIdx.x + (first + j) * gridDim.x;
+            const uint32_t d = dst + (uint32_t)j * tok_bytes;
+            if (qbytes) {
+                const char* src = static_cast<const char*>(a.q) + tok * a.qs * TI::kBytes;
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], "
+                    "[%1], %2, [%3];" ::"r"(d), "l"(src), "r"(qbytes), "r"(bar)
+                    : "memory");
+            }
+            if (kbytes) {
+                const char* src = static_cast<const char*>(a.k) + tok * a.ks * TI::kBytes;
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], "
+                    "[%1], %2, [%3];" ::"r"(d + qbytes), "l"(src), "r"(kbytes), "r"(bar)
+                    : "memory");
+            }
         }
     };
     pdl_wait(a.pdl);
     if (t == 0)
-        for (int64_t k = 0; k < S && k < n_my; ++k)
-            issue(blockIdx.x + k * gridDim.x, ring0 + (uint32_t)k * stage_bytes,
-                  smem_u32(&full[k]));
+        for (int64_t b = 0; b < S && b < n_buf; ++b)
+            issue(b, ring0 + (uint32_t)b * stage_bytes, smem_u32(&full[b]));
     __syncthreads();
-    int64_t k_abort = 0;
-    for (int64_t k = 0; k < n_my; ++k) {
-        const int s = (int)(k % S);
-        const uint32_t phase = (uint32_t)((k / S) & 1);
-        k_abort = k;
-        const int64_t tok = blockIdx.x + k * gridDim.x;
+    int64_t b_abort = 0;
+    for (int64_t b = 0; b < n_buf; ++b) {
+        const int s = (int)(b % S);
+        const uint32_t phase = (uint32_t)((b / S) & 1);
+        b_abort = b;
         if (!mbar_wait_bounded(smem_u32(&full[s]), phase, a.wait_cycles)) {
             atomicOr(a.status, 1u);
             abort_flag = 1;
         }
         const uint32_t base = ring0 + (uint32_t)s * stage_bytes;
-        V8 x[CH];
-        float acc[CH];
+        const int ntok = (int)(n_my - b * TPS < TPS ? n_my - b * TPS : TPS);
+        V8 x[TPS][CH];
+        float acc[TPS][CH];
 #pragma unroll
-        for (int c = 0; c < CH; ++c) {
-            const int v = c * G + t;
-            acc[c] = 0.f;
-            if (v < nv) {
-                x[c] = ld_shared32(base + (uint32_t)v * 32u);
-                acc[c] = qk_sumsq<TI>(x[c]);
+        for (int j = 0; j < TPS; ++j) {
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                const int v = c * G + t;
+                acc[j][c] = 0.f;
+                if (v < nv && j < ntok) {
+                    x[j][c] = ld_shared32_lanes(base + (uint32_t)j * tok_bytes + (uint32_t)v * 32u);
+                    acc[j][c] = qk_sumsq<TI>(x[j][c]);
+                }
             }
         }
-        // every thread has read the stage: it may be refilled after this barrier
+        // every thread has read the buffer: it may be refilled after this barrier
         __syncthreads();
         if (abort_flag) break;
-        if (t == 0 && k + S < n_my) {
+        if (t == 0 && b + S < n_buf) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue(blockIdx.x + (k + S) * gridDim.x, base, smem_u32(&full[s]));
+            issue(b + S, base, smem_u32(&full[s]));
         }
 #pragma unroll
-        for (int c = 0; c < CH; ++c) {
+        for (int j = 0; j < TPS; ++j) {
+            const int64_t tok = blockIdx.x + (b * TPS + j) * gridDim.x;
 #pragma unroll
-            for (int o = TPH / 2; o > 0; o >>= 1)
-                acc[c] += __shfl_xor_sync(0xFFFFFFFFu, acc[c], o);
-            const int v = c * G + t;
-            if (v >= nv) continue;
-            const float inv = qk_inv(acc[c], a);
-            const bool is_q = v < nvq;
-            void* row = is_q ? a.q : a.k;
-            const int64_t e = is_q ? tok * a.qs + (int64_t)v * VE
-                                   : tok * a.ks + (int64_t)(v - nvq) * VE;
-            if (!RMSN_CHECK(a.status, qk_in_span(a, is_q, e, VE))) continue;
-            float y[VE];
-            qk_scale<TI>(x[c], wv[c], inv, a.woff, y);
-            store_out<TI, TI>(row, e, y, 0.f);
+            for (int c = 0; c < CH; ++c) {
+#pragma unroll
+                for (int o = TPH / 2; o > 0; o >>= 1)
+                    acc[j][c] += __shfl_xor_sync(0xFFFFFFFFu, acc[j][c], o);
+                const int v = c * G + t;
+                if (v >= nv || j >= ntok) continue;
+                const float inv = qk_inv(acc[j][c], a);
+                const bool is_q = v < nvq;
+                void* row = is_q ? a.q : a.k;
+                const int64_t e = is_q ? tok * a.qs + (int64_t)v * VE
+                                       : tok * a.ks + (int64_t)(v - nvq) * VE;
+                if (!RMSN_CHECK(a.status, qk_in_span(a, is_q, e, VE))) continue;
+                float y[VE];
+                qk_scale<TI>(x[j][c], wv[c], inv, a.woff, y);
+                store_out<TI, TI>(row, e, y, 0.f);
+            }
         }
     }
     if (abort_flag && t == 0) {
-        for (int64_t j = k_abort; j < k_abort + S && j < n_my; ++j)
+        for (int64_t j = b_abort; j < b_abort + S && j < n_buf; ++j)
             mbar_wait_bounded(smem_u32(&full[j % S]), (uint32_t)((j / S) & 1),
                               kDefaultWaitCycles);
     }
