@@ -1008,8 +1008,8 @@ RMSN_API int rmsnorm_qk_fwd(void* q, void* k, const void* q_weight, const void* 
         stages = (int)(kQkRingBytes / buf_bytes);
         stages = stages < 2 ? 2 : (stages > kMaxStages ? kMaxStages : stages);
         smem = (size_t)stages * (size_t)buf_bytes;
-        if ((int64_t)smem > 48 * 1024 && (int64_t)smem > enable_smem(d, e->fn))
-            return RMSN_EUNSUPPORTED;
+        // the opt-in limit, always: the kernel's static shared memory counts too
+        if ((int64_t)smem > enable_smem(d, e->fn)) return RMSN_EUNSUPPORTED;
         const int bps = blocks_per_sm(d, e->fn, threads, (int)smem);
         if (bps < 1) return RMSN_EUNSUPPORTED;
         const int64_t resident = (int64_t)d->num_sms * bps;
