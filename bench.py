@@ -650,9 +650,9 @@ def run_qk(pkg, synth, dev, stream):
             sets.append((qkv, q, k, q.contiguous(), k.contiguous()))
         fl = pkg.make_flags("bf16", "bf16", False, True, False)
 
-        def qk_call(i, variant=None):
+        def qk_call(i, variant=None, pdl=False):
             _, q, k, _, _ = sets[i % n_sets]
-            pkg.qk_norm_(q, k, wq, wk, head_dim=D, eps=1e-6, variant=variant)
+            pkg.qk_norm_(q, k, wq, wk, head_dim=D, eps=1e-6, variant=variant, pdl=pdl)
 
         def rows_call(i):
             _, _, _, qc, kc = sets[i % n_sets]
@@ -691,14 +691,29 @@ def run_qk(pkg, synth, dev, stream):
         # both QK kernels forced: the ring variant and the one-pass register kernel
         us_ring = graph_us(lambda i: qk_call(i, "ring"))
         us_direct = graph_us(lambda i: qk_call(i, "direct"))
+        # consecutive launches chained by programmatic dependent launch
+        us_pdl = graph_us(lambda i: qk_call(i, pdl=True))
         res = {"qk_us": round(us_qk, 3), "qk_gbs": round(nbytes / us_qk / 1e3, 1),
                "row_norm_us": round(us_rows, 3),
                "row_norm_gbs": round(nbytes / us_rows / 1e3, 1),
                "speedup": round(us_rows / us_qk, 2),
-               "ring_us": round(us_ring, 3), "direct_us": round(us_direct, 3)}
+               "ring_us": round(us_ring, 3), "direct_us": round(us_direct, 3),
+               "pdl_us": round(us_pdl, 3)}
         if n_sets > 1:
             res["qk_frac_of_peak"] = round(nbytes / us_qk / 1e3 / peak, 4)
+            res["qk_pdl_frac_of_peak"] = round(nbytes / us_pdl / 1e3 / peak, 4)
             res["buffer_sets"] = n_sets
+            # torch's elementwise y = x * 1 over the same bytes (the q and k
+            # heads' worth, read once and written once) in the same graph
+            # method: the rate one launch of this size reaches, launch and
+            # drain included
+            n_el = T * (Hq + Hk) * D
+            els = [(torch.empty(n_el, dtype=torch.bfloat16, device=dev).fill_(1.0),
+                    torch.empty(n_el, dtype=torch.bfloat16, device=dev)) for _ in range(n_sets)]
+            us_el = graph_us(lambda i: torch.mul(els[i % n_sets][0], 1.0, out=els[i % n_sets][1]))
+            del els
+            res["elementwise_same_bytes_us"] = round(us_el, 3)
+            res["qk_vs_elementwise_same_bytes"] = round(us_el / us_qk, 4)
         out[f"T{T}"] = res
         del sets
     torch.cuda.empty_cache()
@@ -787,6 +802,16 @@ def run_quantized(pkg, synth, dev, stream):
             us_pdl = graph_us(lambda i, call=call: call(i, pdl=True))
             res[fmt] = {"us": round(us, 2), "gbs": round(nbytes / us / 1e3, 1),
                         "us_pdl": round(us_pdl, 2), "gbs_pdl": round(nbytes / us_pdl / 1e3, 1)}
+        # torch's elementwise y = x * 1 moving the per-token FP8 step's bytes
+        # (half read, half written), two rotating sets, the same graph
+        # method: the rate one launch of this size reaches, launch and drain
+        # included
+        nb = wl.algorithmic_bytes()
+        els = [(torch.empty(nb // 4, dtype=torch.bfloat16, device=dev).fill_(1.0),
+                torch.empty(nb // 4, dtype=torch.bfloat16, device=dev)) for _ in range(2)]
+        us_el = graph_us(lambda i: torch.mul(els[i % 2][0], 1.0, out=els[i % 2][1]))
+        res["elementwise_same_bytes"] = {"us": round(us_el, 2), "gbs": round(nb / us_el / 1e3, 1)}
+        del els
         out[f"T{T}_H{H}"] = res
         del sets, inp
         torch.cuda.empty_cache()

@@ -39,6 +39,8 @@ constexpr int kMaxDevices = 64;
 // About this many bytes of token buffers per ring block.
 constexpr int64_t kQkRingTokens = INT64_MAX;
 constexpr int64_t kQkRingBytes = 96 * 1024;
+// x extent of the one-pass QK grid (token groups); more tokens loop
+constexpr int64_t kQkMaxGridX = int64_t(1) << 30;
 constexpr int64_t kMaxHidden = int64_t(1) << 24;
 
 // Status word of the kernels on each device (bit 0: a bounded wait ran out).
@@ -394,7 +396,18 @@ bool shape_config(const Problem& p, const KernelEntry& e, DeviceInfo* d, int gri
     const int bps = blocks_per_sm(d, e.fn, threads, c->smem_bytes);
     if (bps < 1) return false;
     const int64_t resident = (int64_t)sms * bps;
-    int64_t grid = units < resident ? units : resident;
+    // the register kernels take one unit per block where a unit moves at
+    // least 4 KiB of x: the block scheduler refills SMs as blocks finish,
+    // which keeps more rows in flight than resident blocks looping over rows
+    // (measured on GB300: 16384 x 16384 bf16 in 304 against 344 us, 16384 x
+    // 8192 in 155 against 164 us); smaller units stay on a resident grid
+    // (rows of 128 bf16 took twice as long as blocks of their own), and so
+    // do the ring kernels (their copies run ahead of the rows)
+    const int64_t unit_rows = e.variant == kWarpRows ? e.max_warps : 1;
+    const bool one_pass = (e.variant == kBlockRow || e.variant == kWarpRows) &&
+                          unit_rows * p.H * p.in_bytes >= 4096;
+    const int64_t cap = one_pass ? (int64_t)INT32_MAX : resident;
+    int64_t grid = units < cap ? units : cap;
     if (grid_req > 0) grid = grid_req < units ? grid_req : units;
     if (grid < 1) grid = 1;
     c->grid = (int32_t)grid;
@@ -993,15 +1006,20 @@ RMSN_API int rmsnorm_qk_fwd(void* q, void* k, const void* q_weight, const void* 
         ring = true;
     }
     if (flags & RMSN_QK_DIRECT) ring = false;
-    const int ch = tok_vecs > 1024 ? 2 : 1;
+    const int kind = ring ? kQkBlockRing : kQkDirect;
+    // block ring: vectors per thread; one-pass kernel: tokens per block
+    // (two tokens per block once there are at least two blocks per SM: more
+    // bytes in flight per lane; measured on GB300 from 512 tokens on)
+    const int ch = ring ? (tok_vecs > 1024 ? 2 : 1) : (n_tokens >= 2 * (int64_t)d->num_sms ? 2 : 1);
     const QkEntry* e = nullptr;
     for (int i = 0; i < n; ++i)
-        if (table[i].dt == dt && table[i].tph == tph && table[i].ring == (ring ? ch : 0))
+        if (table[i].dt == dt && table[i].tph == tph && table[i].kind == kind && table[i].ch == ch)
             e = &table[i];
     if (!e) return RMSN_EUNSUPPORTED;
     int threads = 256, stages = 0;
     size_t smem = 0;
     int64_t grid = 0;
+    unsigned grid_y = 1;
     if (ring) {
         threads = (int)(((tok_vecs + ch - 1) / ch + 31) / 32 * 32);
         // about 96 KiB of token buffers per block (two blocks per SM), 2..8 of them
@@ -1015,11 +1033,15 @@ RMSN_API int rmsnorm_qk_fwd(void* q, void* k, const void* q_weight, const void* 
         const int64_t resident = (int64_t)d->num_sms * bps;
         grid = n_tokens < resident ? n_tokens : resident;
     } else {
-        const int64_t heads = (n_q_heads + n_k_heads) * n_tokens;
-        const int64_t need = (heads * tph + threads - 1) / threads;
-        const int bps = blocks_per_sm(d, e->fn, threads, 0);
-        const int64_t resident = (int64_t)d->num_sms * (bps > 0 ? bps : 1);
-        grid = need < resident ? need : resident;
+        // one block per token and group of heads: W warps of 32 / tph heads,
+        // W <= 16 chosen so the groups split evenly over the blocks
+        const int64_t nh = 32 / tph;
+        const int64_t warps = (n_q_heads + n_k_heads + nh - 1) / nh;
+        const int64_t gy = (warps + 15) / 16;
+        threads = (int)((warps + gy - 1) / gy) * 32;
+        const int64_t blocks = (n_tokens + ch - 1) / ch;
+        grid = blocks < kQkMaxGridX ? blocks : kQkMaxGridX;
+        grid_y = (unsigned)gy;
     }
 
     QkArgs a;
@@ -1048,7 +1070,7 @@ RMSN_API int rmsnorm_qk_fwd(void* q, void* k, const void* q_weight, const void* 
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cudaLaunchConfig_t lc = {};
-        lc.gridDim = dim3((unsigned)grid);
+        lc.gridDim = dim3((unsigned)grid, grid_y);
         lc.blockDim = dim3(threads);
         lc.dynamicSmemBytes = smem;
         lc.stream = stream;
@@ -1056,7 +1078,8 @@ RMSN_API int rmsnorm_qk_fwd(void* q, void* k, const void* q_weight, const void* 
         lc.numAttrs = 1;
         err = cudaLaunchKernelExC(&lc, e->fn, args);
     } else {
-        err = cudaLaunchKernel(e->fn, dim3((unsigned)grid), dim3(threads), args, smem, stream);
+        err = cudaLaunchKernel(e->fn, dim3((unsigned)grid, grid_y), dim3(threads), args, smem,
+                               stream);
     }
     return err == cudaSuccess ? RMSN_OK : RMSN_ECUDA;
 }

@@ -14,7 +14,9 @@
 // Kernels:
 //   rmsn_vec_kernel     one row per warp (WARP_ROWS) or per block; each thread
 //                       holds CH 32-byte vectors of the row in registers
-//                       between the load and the store.
+//                       between the load and the store.  Launched with one
+//                       unit (row, or WARP_ROWS rows) per block; a smaller
+//                       grid loops over the rows.
 //   rmsn_bulk_kernel    persistent blocks streaming whole rows into a ring of
 //                       shared-memory buffers with TMA copies (swizzled 2-D
 //                       tensor copies, or 1-D bulk copies).

@@ -26,10 +26,13 @@ struct QkArgs {
     int64_t wait_cycles;  // ring kernel: bound of a token wait (< 0: test once)
 };
 
+enum QkKind : int32_t { kQkDirect = 0, kQkBlockRing = 1 };
+
 struct QkEntry {
     int32_t dt;    // DType of q, k and the weights
     int32_t tph;   // lanes per head
-    int32_t ring;  // 0: register kernel; else the ring kernel with `ring` vectors per thread
+    int32_t kind;  // QkKind
+    int32_t ch;    // block ring: vectors per thread; one-pass kernel: tokens per block
     const void* fn;
 };
 

@@ -54,6 +54,8 @@ def ring_applies(Hq, Hk, D, dtype):
     (3, 2, 1, 512, "bf16"),
     (5, 4, 4, 128, "f32"), (65, 6, 2, 64, "f32"), (9, 3, 1, 256, "f32"), (2, 1, 1, 16, "bf16"),
     (17, 32, 8, 128, "f16"), (3, 4, 2, 64, "f16"), (5, 2, 2, 256, "f16"),
+    (1100, 4, 2, 96, "bf16"), (37, 5, 3, 96, "bf16"), (29, 7, 5, 64, "f32"),
+    (305, 6, 2, 64, "bf16"), (333, 3, 1, 128, "f32"), (641, 64, 8, 128, "bf16"),
 ])
 @pytest.mark.parametrize("pad", [0, 16])
 @pytest.mark.parametrize("variant", [None, "ring", "direct"])

@@ -150,8 +150,8 @@ def test_pipelined_ring_wait_that_runs_out_stops_cleanly(pkg, fmt):
 
 
 def test_qk_ring_wait_that_runs_out_stops_cleanly(pkg):
-    # the QK norm's ring variant under the same limit: every token's heads are
-    # either normalised exactly as the oracle does or left as they were
+    # the QK norm's ring variant under the same limit: every head is either
+    # normalised as the oracle does or left as it was
     import oracle
 
     T, Hq, Hk, D = 8192, 32, 8, 128
@@ -172,11 +172,12 @@ def test_qk_ring_wait_that_runs_out_stops_cleanly(pkg):
             pkg.qk_norm_(g[:, :Hq * D], g[:, Hq * D:(Hq + Hk) * D], inp["q_weight"].cuda(),
                          inp["k_weight"].cuda(), head_dim=D, eps=1e-6, variant="ring")
             torch.cuda.synchronize()
-            got = parity.bits16(g[:, :(Hq + Hk) * D])
+            got = parity.bits16(g[:, :(Hq + Hk) * D]).reshape(T, Hq + Hk, D)
             status = pkg.rmsnorm_read_status(clear=True)
-            same_as_input = np.all(got == orig, axis=1)
-            d = np.abs(parity.ordered16(got) - parity.ordered16(want)).max(axis=1)
-            assert np.all(same_as_input | (d <= 1)), "a token half written or wrong"
+            same_as_input = np.all(got == orig.reshape(T, Hq + Hk, D), axis=2)
+            d = np.abs(parity.ordered16(got) -
+                       parity.ordered16(want.reshape(T, Hq + Hk, D))).max(axis=2)
+            assert np.all(same_as_input | (d <= 1)), "a head half written or wrong"
             if status & 1:
                 hits += 1
             else:
