@@ -470,6 +470,30 @@ def test_selector_decode_vs_prefill(pkg):
     assert c.variant == pkg.VARIANT_GENERIC
 
 
+def test_register_launch_grid(pkg):
+    # the register kernels take one unit per block where a unit moves at
+    # least 4 KiB of x (grid = rows, or row groups for one warp per row);
+    # smaller units, and the rings, stay on a grid of resident blocks
+    flags = pkg.make_flags("bf16", "bf16", True, True, False)
+    for c in pkg.rmsnorm_list_configs(16384, 8192, flags):
+        if c.variant == pkg.VARIANT_BLOCK_ROW:
+            assert c.grid == 16384, c.as_dict()
+        elif c.variant in (pkg.VARIANT_BULK_ROW, pkg.VARIANT_BULK_PIPE):
+            assert c.grid <= 8 * c.num_sms, c.as_dict()
+    for c in pkg.rmsnorm_list_configs(65536, 2048, flags):
+        if c.variant == pkg.VARIANT_WARP_ROWS:
+            assert c.grid == -(-65536 // c.warps_per_block), c.as_dict()
+    small = [c for c in pkg.rmsnorm_list_configs(65536, 128, flags)
+             if c.variant in (pkg.VARIANT_BLOCK_ROW, pkg.VARIANT_WARP_ROWS)]
+    assert small and all(c.grid < 65536 // c.warps_per_block for c in small
+                         if c.variant == pkg.VARIANT_WARP_ROWS)
+    assert all(c.grid < 65536 for c in small if c.variant == pkg.VARIANT_BLOCK_ROW)
+    # the selected bench launch is the one-row register launch, and its
+    # parity at full size is covered by test_prefill_full_size
+    c = pkg.rmsnorm_query_config(16384, 8192, flags)
+    assert c.variant == pkg.VARIANT_BLOCK_ROW and c.grid == 16384
+
+
 def test_ring_copy_mode(pkg):
     # the ring launches of the bench shape fill their stages with swizzled
     # tensor copies; rows that are not whole 1 KiB units fall back to 1-D
