@@ -136,7 +136,11 @@ typedef struct {
  * size is a multiple of 32 bytes and every pointer is 32-byte aligned;
  * otherwise rows with the same dtype in and out whose row pointers are all
  * equally aligned modulo 16 bytes take the ragged-row kernel (16-byte
- * vectors plus single-element row ends), and the rest the generic kernel.  residual_out may be the same buffer as
+ * vectors plus single-element row ends), as do rows with a per-token FP8
+ * output whose out pointer is offset from a (16 / input element size)-byte
+ * boundary by as many elements as x is from a 16-byte one (x, residual and
+ * residual_out equally aligned), and the rest the generic kernel.
+ * residual_out may be the same buffer as
  * residual, or as x when both have the same dtype; out may be the same
  * buffer as x or residual when their dtypes are equal; any other overlap is
  * undefined.  n_tokens == 0

@@ -162,7 +162,7 @@ const std::vector<KernelEntry>& registry() {
             kernels_bf16_f32, kernels_bf16_bf16, kernels_bf16_fp8,   kernels_f16_f16,
             kernels_f16_f32,  kernels_f16_fp8,   kernels_bf16_mxfp8, kernels_bf16_mxfp4,
             kernels_bf16_nvfp4, kernels_bf16r32_bf16, kernels_bf16r32_fp8, kernels_f16r32_f16,
-            kernels_f16r32_fp8, kernels_ragged};
+            kernels_f16r32_fp8, kernels_ragged, kernels_ragged_fp8};
         for (auto fn : fns) {
             int n = 0;
             const KernelEntry* t = fn(&n);
@@ -243,17 +243,25 @@ bool vector_path_ok(const Problem& p, const void* x, const void* r, const void* 
 // stream, and every row pointer equally aligned modulo 16 bytes (so a row's
 // 16-byte vectors sit at the same columns in all of them).
 bool ragged_dtypes_ok(const Problem& p) {
-    return p.in_dt == p.out_dt && (p.in_dt == kBF16 || p.in_dt == kF16 || p.in_dt == kF32) &&
-           !p.res_f32;
+    return (p.in_dt == p.out_dt || p.out_dt == kFP8) &&
+           (p.in_dt == kBF16 || p.in_dt == kF16 || p.in_dt == kF32) && !p.res_f32;
 }
 
+// x, residual and residual_out (and an out of the same dtype) equally aligned
+// modulo 16 bytes; an FP8 out offset from its 16 / size-byte boundary by as
+// many elements as x from its 16-byte boundary.
 bool ragged_path_ok(const Problem& p, const void* x, const void* r, const void* ro,
                     const void* out) {
     if (!ragged_dtypes_ok(p)) return false;
     const uintptr_t m = reinterpret_cast<uintptr_t>(x) & 15u;
-    const void* others[] = {r, ro, out};
-    for (const void* q : others)
-        if (q && (reinterpret_cast<uintptr_t>(q) & 15u) != m) return false;
+    const bool q = p.out_dt == kFP8;
+    const void* others[] = {r, ro, q ? nullptr : out};
+    for (const void* o : others)
+        if (o && (reinterpret_cast<uintptr_t>(o) & 15u) != m) return false;
+    if (q) {
+        const uintptr_t s = (uintptr_t)p.in_bytes;
+        if (reinterpret_cast<uintptr_t>(out) % (16u / s) != m / s) return false;
+    }
     return true;
 }
 

@@ -7,7 +7,7 @@
 namespace rmsn {
 
 #define RMSN_RAG(TI, DT, CH, RES, BIAS) \
-    {DT, DT, kRagged, CH, 8, 0, RES, BIAS, 0, (const void*)&rmsn_ragged_kernel<TI, CH, RES, BIAS>}
+    {DT, DT, kRagged, CH, 8, 0, RES, BIAS, 0, (const void*)&rmsn_ragged_kernel<TI, TI, CH, RES, BIAS>}
 #define RMSN_RAG4(TI, DT, CH)                                                        \
     RMSN_RAG(TI, DT, CH, false, false), RMSN_RAG(TI, DT, CH, true, false),           \
         RMSN_RAG(TI, DT, CH, false, true), RMSN_RAG(TI, DT, CH, true, true)

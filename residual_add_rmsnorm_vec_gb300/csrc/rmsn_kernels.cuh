@@ -1652,18 +1652,23 @@ __global__ void __launch_bounds__(256) rmsn_generic_kernel(const RmsnArgs a) {
 //
 // Rows whose 32-byte vectors do not line up with the row (hidden not a
 // multiple of the vector, or every pointer offset from a 32-byte boundary by
-// the same amount) in the same dtype in and out.  x, residual, residual_out
-// and out share one alignment modulo 16 bytes, so each row splits the same
-// way in all four: a head (the elements before the row's first 16-byte
-// boundary), an interior of 16-byte vectors, CH per thread, held in
-// registers between the load and the store, and a tail.  Head and tail
-// together hold at most 2 (16 / size - 1) elements, one per thread.  Weight
+// the same amount), with the same dtype in and out or a per-token FP8
+// output.  x, residual, residual_out (and a same-dtype out) share one
+// alignment modulo 16 bytes, so each row splits the same way in all of them:
+// a head (the elements before the row's first 16-byte boundary), an interior
+// of 16-byte vectors, CH per thread, held in registers between the load and
+// the store, and a tail.  Head and tail together hold at most
+// 2 (16 / size - 1) elements, one per thread.  An FP8 out is offset from its
+// boundary by the same number of elements as x (its interior codes are then
+// 16 / size byte groups on their own boundaries); its row takes a second
+// pass over the registers for max|y| and a second block reduction.  Weight
 // (plus the scalar offset) and bias are staged once per block in shared
 // memory as fp32: their alignment relative to a row's vectors changes from
 // row to row.  One block of 256 threads per row, rows grid-stride; the
 // arithmetic (fp32 add rounded to the stream type, fp32 sum of squares,
-// correctly rounded mean, reciprocal square root, scale) is that of the
-// vector kernels.
+// correctly rounded mean, reciprocal square root, scale; the FP8 scale
+// max|y| / 448 and codes RN_E4M3(y * (448 / max|y|))) is that of the vector
+// kernels.
 
 template <class TI>
 __device__ __forceinline__ float elem4(const uint32_t (&u)[4], int k) {
@@ -1679,14 +1684,23 @@ __device__ __forceinline__ float elem4(const uint32_t (&u)[4], int k) {
 // 16 bytes of the row apart, read from 32 different banks.
 __device__ __forceinline__ int ragged_slot(int j) { return j + (j >> 5); }
 
-template <class TI, int CH, bool RES, bool BIAS>
+// One float as an E4M3 code (nearest-even, saturating).
+__device__ __forceinline__ uint32_t e4m3_code(float v) {
+    uint16_t q;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q) : "f"(0.f), "f"(v));
+    return q & 0xFFu;
+}
+
+template <class TI, class TO, int CH, bool RES, bool BIAS>
 __global__ void __launch_bounds__(256, CH <= 2 ? 4 : (CH <= 4 ? 2 : 1))
     rmsn_ragged_kernel(const RmsnArgs a) {
     constexpr int S = TI::kBytes;
     constexpr int VE = 16 / S;  // elements per 16-byte vector
+    constexpr bool Q = std::is_same<TO, FP8>::value;
+    static_assert(Q || std::is_same<TO, TI>::value, "same dtype in and out, or per-token FP8");
     // weight + offset, then bias, as fp32 in padded slots (ragged_slot)
     extern __shared__ __align__(16) float wsm[];
-    __shared__ float red[2][32];
+    __shared__ float red[4][32];
     const int H = a.H;
     const int t = threadIdx.x;
     const int G = blockDim.x;
@@ -1753,6 +1767,36 @@ __global__ void __launch_bounds__(256, CH <= 2 ? 4 : (CH <= 4 ? 2 : 1))
             acc = __fmaf_rn(he, he, acc);
         }
         const float inv = inv_rms(block_allreduce<false>(acc, red[parity]), H, a.eps);
+        // y of interior element k of chunk c (column col + k), and of the
+        // edge element
+        auto y_of = [&](int c, int col, int k) {
+            const float tk = __fmul_rn(elem4<TI>(hu[c], k), inv);
+            const int sl = ragged_slot(col + k);
+            return BIAS ? __fmaf_rn(wsm[sl], tk, bsm[sl]) : __fmul_rn(wsm[sl], tk);
+        };
+        float ye = 0.f;
+        if (t < ne && rows_ok(a, e0 + je, 1)) {
+            const float tk = __fmul_rn(he, inv);
+            const int sl = ragged_slot(je);
+            ye = BIAS ? __fmaf_rn(wsm[sl], tk, bsm[sl]) : __fmul_rn(wsm[sl], tk);
+        }
+        float qmul = 0.f;
+        if constexpr (Q) {
+            // max|y| over the row: the interior recomputed from the registers
+            float amax = fabsf(ye);
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                const int v = c * G + t;
+                if (v < nv && rows_ok(a, e0 + head + (int64_t)v * VE, VE)) {
+#pragma unroll
+                    for (int k = 0; k < VE; ++k)
+                        amax = fmaxf(amax, fabsf(y_of(c, head + v * VE, k)));
+                }
+            }
+            amax = block_allreduce<true>(amax, red[2 + parity]);
+            qmul = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
+            if (t == 0 && row_ok(a, row)) a.scale[row] = __fdiv_rn(amax, 448.f);
+        }
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
             const int v = c * G + t;
@@ -1760,26 +1804,36 @@ __global__ void __launch_bounds__(256, CH <= 2 ? 4 : (CH <= 4 ? 2 : 1))
                 const int col = head + v * VE;
                 float y[VE];
 #pragma unroll
-                for (int k = 0; k < VE; ++k) {
-                    const float tk = __fmul_rn(elem4<TI>(hu[c], k), inv);
-                    const int sl = ragged_slot(col + k);
-                    y[k] = BIAS ? __fmaf_rn(wsm[sl], tk, bsm[sl]) : __fmul_rn(wsm[sl], tk);
-                }
-                uint32_t u[4];
-                if constexpr (S == 2) {
+                for (int k = 0; k < VE; ++k) y[k] = y_of(c, col, k);
+                if constexpr (Q) {
+                    // VE codes on a VE-byte boundary: y * qmul, then E4M3
+                    uint32_t u[VE / 4];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) u[k] = pack2<TI>(y[2 * k], y[2 * k + 1]);
+                    for (int k = 0; k < VE / 4; ++k)
+                        u[k] = pack_e4m3x4(__fmul_rn(y[4 * k], qmul), __fmul_rn(y[4 * k + 1], qmul),
+                                           __fmul_rn(y[4 * k + 2], qmul),
+                                           __fmul_rn(y[4 * k + 3], qmul));
+                    uint8_t* o = static_cast<uint8_t*>(a.out) + e0 + col;
+                    if constexpr (VE == 8) st_stream8(o, u);
+                    else asm volatile("st.global.b32 [%0], %1;" ::"l"(o), "r"(u[0]) : "memory");
                 } else {
+                    uint32_t u[4];
+                    if constexpr (S == 2) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) u[k] = __float_as_uint(y[k]);
+                        for (int k = 0; k < 4; ++k) u[k] = pack2<TI>(y[2 * k], y[2 * k + 1]);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) u[k] = __float_as_uint(y[k]);
+                    }
+                    st_stream16(static_cast<char*>(a.out) + (e0 + col) * S, u);
                 }
-                st_stream16(static_cast<char*>(a.out) + (e0 + col) * S, u);
             }
         }
         if (t < ne && rows_ok(a, e0 + je, 1)) {
-            const float tk = __fmul_rn(he, inv);
-            const int sl = ragged_slot(je);
-            st_elem<TI>(a.out, e0 + je, BIAS ? __fmaf_rn(wsm[sl], tk, bsm[sl]) : __fmul_rn(wsm[sl], tk));
+            if constexpr (Q)
+                static_cast<uint8_t*>(a.out)[e0 + je] = (uint8_t)e4m3_code(__fmul_rn(ye, qmul));
+            else
+                st_elem<TI>(a.out, e0 + je, ye);
         }
         parity ^= 1;
     }

@@ -70,5 +70,6 @@ const KernelEntry* kernels_bf16_mxfp8(int* n);
 const KernelEntry* kernels_bf16_mxfp4(int* n);
 const KernelEntry* kernels_bf16_nvfp4(int* n);
 const KernelEntry* kernels_ragged(int* n);
+const KernelEntry* kernels_ragged_fp8(int* n);
 
 }  // namespace rmsn

@@ -245,7 +245,9 @@ def test_weight_offset(pkg):
 
 @pytest.mark.parametrize("H", [1, 3, 7, 8, 15, 17, 100, 1000, 4095, 4097, 6000])
 @pytest.mark.parametrize("out_dt", ["bf16", "fp8", "f32"])
-def test_ragged_hidden_generic_path(pkg, H, out_dt):
+def test_ragged_hidden_out_dtypes(pkg, H, out_dt):
+    # odd hidden sizes with a bias: the ragged-row kernel (bf16, FP8 out) or
+    # the generic one (fp32 out)
     wl = synth.Workload(f"ragged_H{H}", 33, H, 9, "bf16", out_dt, 1e-6, has_bias=True)
     check(pkg, wl)
 
@@ -306,18 +308,20 @@ RAGGED_H = [1, 7, 9, 100, 1000, 4097, 8190]
 
 
 @pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("out", ["same", "fp8"])
 @pytest.mark.parametrize("res,bias", [(True, True), (True, False), (False, True), (False, False)])
 @pytest.mark.parametrize("H", RAGGED_H)
-def test_ragged_kernel_every_config(pkg, dt, res, bias, H):
+def test_ragged_kernel_every_config(pkg, dt, out, res, bias, H):
     # rows off the 32-byte grid: the selector takes the ragged-row kernel, and
     # every listed shape of it (and a 3-block grid looping over rows) matches
-    # the oracle
+    # the oracle, for the input's dtype out and for a per-token FP8 output
     T = 37
     if H * (4 if dt == "f32" else 2) % 32 == 0:
         pytest.skip("rows on the 32-byte grid take the vector kernels")
-    wl = synth.Workload(f"rag_{dt}_H{H}", T, H, 79, dt, dt, 1e-6, has_residual=res,
+    odt = dt if out == "same" else "fp8"
+    wl = synth.Workload(f"rag_{dt}_{odt}_H{H}", T, H, 79, dt, odt, 1e-6, has_residual=res,
                         has_bias=bias)
-    flags = pkg.make_flags(dt, dt, res, True, bias)
+    flags = pkg.make_flags(dt, odt, res, True, bias)
     assert pkg.rmsnorm_query_config(T, H, flags).variant == pkg.VARIANT_RAGGED
     cfgs = [c for c in pkg.rmsnorm_list_configs(T, H, flags) if c.variant == pkg.VARIANT_RAGGED]
     assert cfgs
@@ -331,12 +335,44 @@ def test_ragged_kernel_every_config(pkg, dt, res, bias, H):
     assert pkg.rmsnorm_read_status() == 0
 
 
-@pytest.mark.parametrize("T,H,dt", [(3000, 4097, "bf16"), (2048, 8190, "bf16"),
-                                    (16384, 8190, "bf16"), (1000, 6001, "f32")])
-def test_ragged_kernel_large(pkg, T, H, dt):
+@pytest.mark.parametrize("T,H,dt,odt", [(3000, 4097, "bf16", "bf16"), (2048, 8190, "bf16", "bf16"),
+                                        (16384, 8190, "bf16", "bf16"), (1000, 6001, "f32", "f32"),
+                                        (4096, 5118, "bf16", "fp8"), (16384, 8190, "bf16", "fp8"),
+                                        (999, 7167, "f16", "fp8"), (777, 3001, "f32", "fp8")])
+def test_ragged_kernel_large(pkg, T, H, dt, odt):
     rows = synth.sample_rows(T, 1024) if T > 4096 else None
-    check(pkg, synth.Workload(f"rag_large_T{T}_H{H}", T, H, 80, dt, dt, 1e-5, has_bias=True,
-                              r_std=2.0), rows=rows)
+    check(pkg, synth.Workload(f"rag_large_T{T}_H{H}_{odt}", T, H, 80, dt, odt, 1e-5,
+                              has_bias=True, r_std=2.0), rows=rows)
+
+
+def test_ragged_fp8_output_alignment(pkg):
+    # views offset by one element: x, residual and the FP8 out one element
+    # off their boundaries take the ragged-row kernel; an FP8 out offset
+    # differently falls back to the generic kernel; both match the oracle
+    wl = synth.Workload("rag_fp8_views", 24, 2048, 13, "bf16", "fp8", 1e-6, has_bias=True)
+    inp = synth.make_inputs(wl)
+    ref = parity.oracle_run(wl, inp)
+    T, H = wl.n_tokens, wl.hidden
+    w, b = inp["weight"].to(DEV), inp["bias"].to(DEV)  # alive until the kernels ran
+    for q_off in (1, 2):
+        xb = torch.zeros(T * H + 8, dtype=torch.bfloat16, device=DEV)
+        rb = torch.zeros(T * H + 8, dtype=torch.bfloat16, device=DEV)
+        rob = torch.zeros(T * H + 8, dtype=torch.bfloat16, device=DEV)
+        qb = torch.zeros(T * H + 8, dtype=torch.uint8, device=DEV)
+        x, r = xb[1:1 + T * H].view(T, H), rb[1:1 + T * H].view(T, H)
+        ro, q = rob[1:1 + T * H].view(T, H), qb[q_off:q_off + T * H].view(T, H)
+        x.copy_(inp["x"])
+        r.copy_(inp["residual"])
+        scale = torch.zeros(T, dtype=torch.float32, device=DEV)
+        s = torch.cuda.current_stream().cuda_stream
+        st = pkg.rmsnorm_fwd(x.data_ptr(), r.data_ptr(), w.data_ptr(), b.data_ptr(),
+                             q.data_ptr(), ro.data_ptr(),
+                             scale.data_ptr(), T, H, wl.eps,
+                             pkg.make_flags("bf16", "fp8", True, True, True), s)
+        assert st == pkg.RMSN_OK
+        torch.cuda.synchronize()
+        parity.compare(wl, parity.gpu_outputs_to_host(wl, q, ro, scale), ref,
+                       f"fp8 out offset {q_off}", bias=inp["bias"])
 
 
 @pytest.mark.parametrize("alias", ["residual_out=residual", "out=x", "out=residual"])
@@ -463,10 +499,13 @@ def test_selector_decode_vs_prefill(pkg):
         assert any(_same_shape(c, o) for o in pkg.rmsnorm_list_configs(T, H, flags)), (T, H)
         assert 1 <= c.grid <= max(T, 1)
     # rows off the 32-byte grid: the ragged-row kernel for the same dtype in
-    # and out, the generic one otherwise (here: an FP8 output)
+    # and out and for a per-token FP8 output, the generic one otherwise (here:
+    # an fp32 output from bf16 rows)
     c = pkg.rmsnorm_query_config(16, 1000, flags)
     assert c.variant == pkg.VARIANT_RAGGED
     c = pkg.rmsnorm_query_config(16, 1000, pkg.make_flags("bf16", "fp8", True, True, False))
+    assert c.variant == pkg.VARIANT_RAGGED
+    c = pkg.rmsnorm_query_config(16, 1000, pkg.make_flags("bf16", "f32", True, True, False))
     assert c.variant == pkg.VARIANT_GENERIC
 
 
