@@ -134,12 +134,13 @@ typedef struct {
  * rmsnorm_fwd_host.  Each pointer must be aligned to its
  * element size; the 256-bit vector kernels are used when hidden * element
  * size is a multiple of 32 bytes and every pointer is 32-byte aligned;
- * otherwise rows with the same dtype in and out whose row pointers are all
- * equally aligned modulo 16 bytes take the ragged-row kernel (16-byte
- * vectors plus single-element row ends), as do rows with a per-token FP8
- * output whose out pointer is offset from a (16 / input element size)-byte
- * boundary by as many elements as x is from a 16-byte one (x, residual and
- * residual_out equally aligned), and the rest the generic kernel.
+ * otherwise rows of bf16 / fp16 / fp32 (not over an fp32 residual stream)
+ * take the ragged-row kernel (16-byte vectors plus single-element row ends)
+ * when x, residual and residual_out are equally aligned modulo 16 bytes and
+ * out, of the same dtype, per-token FP8, fp32 (16-bit rows) or 16-bit (fp32
+ * rows), is offset from a (16 / input element size) x (output element
+ * size)-byte boundary by as many elements as x is from a 16-byte one; the
+ * rest take the generic kernel.
  * residual_out may be the same buffer as
  * residual, or as x when both have the same dtype; out may be the same
  * buffer as x or residual when their dtypes are equal; any other overlap is

@@ -162,7 +162,7 @@ const std::vector<KernelEntry>& registry() {
             kernels_bf16_f32, kernels_bf16_bf16, kernels_bf16_fp8,   kernels_f16_f16,
             kernels_f16_f32,  kernels_f16_fp8,   kernels_bf16_mxfp8, kernels_bf16_mxfp4,
             kernels_bf16_nvfp4, kernels_bf16r32_bf16, kernels_bf16r32_fp8, kernels_f16r32_f16,
-            kernels_f16r32_fp8, kernels_ragged, kernels_ragged_fp8};
+            kernels_f16r32_fp8, kernels_ragged, kernels_ragged_fp8, kernels_ragged_mixed};
         for (auto fn : fns) {
             int n = 0;
             const KernelEntry* t = fn(&n);
@@ -242,27 +242,29 @@ bool vector_path_ok(const Problem& p, const void* x, const void* r, const void* 
 // The ragged-row kernel: the same 2- or 4-byte dtype in and out, no fp32
 // stream, and every row pointer equally aligned modulo 16 bytes (so a row's
 // 16-byte vectors sit at the same columns in all of them).
+// The ragged-row kernel's dtype pairs: bf16 / fp16 / fp32 in; out in the
+// same dtype, as per-token FP8, in fp32 from 16-bit rows or in a 16-bit type
+// from fp32 rows.
 bool ragged_dtypes_ok(const Problem& p) {
-    return (p.in_dt == p.out_dt || p.out_dt == kFP8) &&
-           (p.in_dt == kBF16 || p.in_dt == kF16 || p.in_dt == kF32) && !p.res_f32;
+    const bool in16 = p.in_dt == kBF16 || p.in_dt == kF16;
+    if (!(in16 || p.in_dt == kF32) || p.res_f32) return false;
+    if (p.out_dt == p.in_dt || p.out_dt == kFP8) return true;
+    return in16 ? p.out_dt == kF32 : (p.out_dt == kBF16 || p.out_dt == kF16);
 }
 
-// x, residual and residual_out (and an out of the same dtype) equally aligned
-// modulo 16 bytes; an FP8 out offset from its 16 / size-byte boundary by as
-// many elements as x from its 16-byte boundary.
+// x, residual and residual_out equally aligned modulo 16 bytes; out offset
+// from a (16 / in size) x (out size)-byte boundary by as many elements as x
+// from its 16-byte boundary.
 bool ragged_path_ok(const Problem& p, const void* x, const void* r, const void* ro,
                     const void* out) {
     if (!ragged_dtypes_ok(p)) return false;
     const uintptr_t m = reinterpret_cast<uintptr_t>(x) & 15u;
-    const bool q = p.out_dt == kFP8;
-    const void* others[] = {r, ro, q ? nullptr : out};
+    const void* others[] = {r, ro};
     for (const void* o : others)
         if (o && (reinterpret_cast<uintptr_t>(o) & 15u) != m) return false;
-    if (q) {
-        const uintptr_t s = (uintptr_t)p.in_bytes;
-        if (reinterpret_cast<uintptr_t>(out) % (16u / s) != m / s) return false;
-    }
-    return true;
+    const uintptr_t si = (uintptr_t)p.in_bytes, so = (uintptr_t)p.out_bytes, ve = 16u / si;
+    const uintptr_t ob = reinterpret_cast<uintptr_t>(out);
+    return ob % so == 0 && (ob / so) % ve == m / si;
 }
 
 const KernelEntry* find_kernel(const Problem& p, int variant, int ch, int wmax) {

@@ -1652,16 +1652,17 @@ __global__ void __launch_bounds__(256) rmsn_generic_kernel(const RmsnArgs a) {
 //
 // Rows whose 32-byte vectors do not line up with the row (hidden not a
 // multiple of the vector, or every pointer offset from a 32-byte boundary by
-// the same amount), with the same dtype in and out or a per-token FP8
-// output.  x, residual, residual_out (and a same-dtype out) share one
-// alignment modulo 16 bytes, so each row splits the same way in all of them:
-// a head (the elements before the row's first 16-byte boundary), an interior
-// of 16-byte vectors, CH per thread, held in registers between the load and
-// the store, and a tail.  Head and tail together hold at most
-// 2 (16 / size - 1) elements, one per thread.  An FP8 out is offset from its
-// boundary by the same number of elements as x (its interior codes are then
-// 16 / size byte groups on their own boundaries); its row takes a second
-// pass over the registers for max|y| and a second block reduction.  Weight
+// the same amount): bf16, fp16 or fp32 in, and out in the same dtype, in
+// fp32 / a 16-bit type (fp32 in), or as per-token FP8.  x, residual and
+// residual_out share one alignment modulo 16 bytes, so each row splits the
+// same way in all of them: a head (the elements before the row's first
+// 16-byte boundary), an interior of 16-byte vectors, CH per thread, held in
+// registers between the load and the store, and a tail.  Head and tail
+// together hold at most 2 (16 / size - 1) elements, one per thread.  out is
+// offset from a (16 / size) x (out size)-byte boundary by as many elements as
+// x is from a 16-byte one, so each interior vector's outputs are one group on
+// its own boundary.  An FP8 row takes a second pass over the registers for
+// max|y| and a second block reduction.  Weight
 // (plus the scalar offset) and bias are staged once per block in shared
 // memory as fp32: their alignment relative to a row's vectors changes from
 // row to row.  One block of 256 threads per row, rows grid-stride; the
@@ -1697,7 +1698,7 @@ __global__ void __launch_bounds__(256, CH <= 2 ? 4 : (CH <= 4 ? 2 : 1))
     constexpr int S = TI::kBytes;
     constexpr int VE = 16 / S;  // elements per 16-byte vector
     constexpr bool Q = std::is_same<TO, FP8>::value;
-    static_assert(Q || std::is_same<TO, TI>::value, "same dtype in and out, or per-token FP8");
+    static_assert(Q || TO::kBytes == 2 || TO::kBytes == 4, "16-bit, fp32 or per-token FP8 out");
     // weight + offset, then bias, as fp32 in padded slots (ragged_slot)
     extern __shared__ __align__(16) float wsm[];
     __shared__ float red[4][32];
@@ -1817,15 +1818,22 @@ __global__ void __launch_bounds__(256, CH <= 2 ? 4 : (CH <= 4 ? 2 : 1))
                     if constexpr (VE == 8) st_stream8(o, u);
                     else asm volatile("st.global.b32 [%0], %1;" ::"l"(o), "r"(u[0]) : "memory");
                 } else {
-                    uint32_t u[4];
-                    if constexpr (S == 2) {
+                    // VE outputs of TO: a VE * size-byte group on its own boundary
+                    constexpr int OB = TO::kBytes;
+                    char* o = static_cast<char*>(a.out) + (e0 + col) * OB;
+                    if constexpr (OB == 2) {
+                        uint32_t u[VE / 2];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) u[k] = pack2<TI>(y[2 * k], y[2 * k + 1]);
+                        for (int k = 0; k < VE / 2; ++k) u[k] = pack2<TO>(y[2 * k], y[2 * k + 1]);
+                        if constexpr (VE == 8) st_stream16(o, u);
+                        else st_stream8(o, u);
                     } else {
+                        uint32_t u[VE];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) u[k] = __float_as_uint(y[k]);
+                        for (int k = 0; k < VE; ++k) u[k] = __float_as_uint(y[k]);
+                        if constexpr (VE == 8) st_stream32(o, u);
+                        else st_stream16(o, u);
                     }
-                    st_stream16(static_cast<char*>(a.out) + (e0 + col) * S, u);
                 }
             }
         }
@@ -1833,7 +1841,7 @@ __global__ void __launch_bounds__(256, CH <= 2 ? 4 : (CH <= 4 ? 2 : 1))
             if constexpr (Q)
                 static_cast<uint8_t*>(a.out)[e0 + je] = (uint8_t)e4m3_code(__fmul_rn(ye, qmul));
             else
-                st_elem<TI>(a.out, e0 + je, ye);
+                st_elem<TO>(a.out, e0 + je, ye);
         }
         parity ^= 1;
     }

@@ -71,5 +71,6 @@ const KernelEntry* kernels_bf16_mxfp4(int* n);
 const KernelEntry* kernels_bf16_nvfp4(int* n);
 const KernelEntry* kernels_ragged(int* n);
 const KernelEntry* kernels_ragged_fp8(int* n);
+const KernelEntry* kernels_ragged_mixed(int* n);
 
 }  // namespace rmsn

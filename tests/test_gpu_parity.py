@@ -246,8 +246,7 @@ def test_weight_offset(pkg):
 @pytest.mark.parametrize("H", [1, 3, 7, 8, 15, 17, 100, 1000, 4095, 4097, 6000])
 @pytest.mark.parametrize("out_dt", ["bf16", "fp8", "f32"])
 def test_ragged_hidden_out_dtypes(pkg, H, out_dt):
-    # odd hidden sizes with a bias: the ragged-row kernel (bf16, FP8 out) or
-    # the generic one (fp32 out)
+    # odd hidden sizes with a bias: the ragged-row kernel for each output
     wl = synth.Workload(f"ragged_H{H}", 33, H, 9, "bf16", out_dt, 1e-6, has_bias=True)
     check(pkg, wl)
 
@@ -308,17 +307,18 @@ RAGGED_H = [1, 7, 9, 100, 1000, 4097, 8190]
 
 
 @pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
-@pytest.mark.parametrize("out", ["same", "fp8"])
+@pytest.mark.parametrize("out", ["same", "fp8", "mixed"])
 @pytest.mark.parametrize("res,bias", [(True, True), (True, False), (False, True), (False, False)])
 @pytest.mark.parametrize("H", RAGGED_H)
 def test_ragged_kernel_every_config(pkg, dt, out, res, bias, H):
     # rows off the 32-byte grid: the selector takes the ragged-row kernel, and
     # every listed shape of it (and a 3-block grid looping over rows) matches
-    # the oracle, for the input's dtype out and for a per-token FP8 output
+    # the oracle, for the input's dtype out, a per-token FP8 output, and fp32
+    # out of 16-bit rows / bf16 out of fp32 rows
     T = 37
     if H * (4 if dt == "f32" else 2) % 32 == 0:
         pytest.skip("rows on the 32-byte grid take the vector kernels")
-    odt = dt if out == "same" else "fp8"
+    odt = {"same": dt, "fp8": "fp8", "mixed": "bf16" if dt == "f32" else "f32"}[out]
     wl = synth.Workload(f"rag_{dt}_{odt}_H{H}", T, H, 79, dt, odt, 1e-6, has_residual=res,
                         has_bias=bias)
     flags = pkg.make_flags(dt, odt, res, True, bias)
@@ -338,7 +338,8 @@ def test_ragged_kernel_every_config(pkg, dt, out, res, bias, H):
 @pytest.mark.parametrize("T,H,dt,odt", [(3000, 4097, "bf16", "bf16"), (2048, 8190, "bf16", "bf16"),
                                         (16384, 8190, "bf16", "bf16"), (1000, 6001, "f32", "f32"),
                                         (4096, 5118, "bf16", "fp8"), (16384, 8190, "bf16", "fp8"),
-                                        (999, 7167, "f16", "fp8"), (777, 3001, "f32", "fp8")])
+                                        (999, 7167, "f16", "fp8"), (777, 3001, "f32", "fp8"),
+                                        (16384, 8190, "bf16", "f32"), (555, 4097, "f32", "f16")])
 def test_ragged_kernel_large(pkg, T, H, dt, odt):
     rows = synth.sample_rows(T, 1024) if T > 4096 else None
     check(pkg, synth.Workload(f"rag_large_T{T}_H{H}_{odt}", T, H, 80, dt, odt, 1e-5,
@@ -499,13 +500,12 @@ def test_selector_decode_vs_prefill(pkg):
         assert any(_same_shape(c, o) for o in pkg.rmsnorm_list_configs(T, H, flags)), (T, H)
         assert 1 <= c.grid <= max(T, 1)
     # rows off the 32-byte grid: the ragged-row kernel for the same dtype in
-    # and out and for a per-token FP8 output, the generic one otherwise (here:
-    # an fp32 output from bf16 rows)
-    c = pkg.rmsnorm_query_config(16, 1000, flags)
-    assert c.variant == pkg.VARIANT_RAGGED
-    c = pkg.rmsnorm_query_config(16, 1000, pkg.make_flags("bf16", "fp8", True, True, False))
-    assert c.variant == pkg.VARIANT_RAGGED
-    c = pkg.rmsnorm_query_config(16, 1000, pkg.make_flags("bf16", "f32", True, True, False))
+    # and out, a per-token FP8 output and fp32 out of 16-bit rows; the generic
+    # one otherwise (here: bf16 activations over an fp32 residual stream)
+    for out in ("bf16", "fp8", "f32"):
+        c = pkg.rmsnorm_query_config(16, 1000, pkg.make_flags("bf16", out, True, True, False))
+        assert c.variant == pkg.VARIANT_RAGGED, out
+    c = pkg.rmsnorm_query_config(16, 1001, flags | pkg.RMSN_RESIDUAL_F32)
     assert c.variant == pkg.VARIANT_GENERIC
 
 
