@@ -101,7 +101,7 @@ def compare(wl, got: dict, ref: dict, where: str = "", bias=None) -> dict:
             # only elements where the bias cancels may be further off: the
             # fp32 bound on |y| + |b_j| applies to them
             far = d > BF16_ULP
-            assert "y64" in ref, f"{where}: the oracle's fp64 y is needed to judge cancellation"
+            assert "y64" in ref, f"{where}: the oracle's fp64 y is needed to decide cancellation"
             bs = np.broadcast_to(bias.double().numpy()[None, :], d.shape)[far]
             y64 = ref["y64"][far]
             cancels = np.abs(y64) <= CANCEL * (np.abs(y64 - bs) + np.abs(bs))
