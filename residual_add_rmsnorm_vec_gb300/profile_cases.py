@@ -13,7 +13,8 @@ Cases:
   qk_T<T>            QK norm, 32 query + 8 key heads x 128 bf16 in a fused
                      qkv buffer (value heads skipped), one launch; qkring_T<T> /
                      qkdirect_T<T> force the ring / the register kernel
-  ragged_T<T>_H<H>   bf16 rows off the 32-byte grid (ragged-row kernel), bias
+  ragged_T<T>_H<H>   bf16 rows off the 32-byte grid (ragged-row kernel), bias;
+                     raggedfp8_T<T>_H<H>: the same with a per-token FP8 output
   fp8_T<T>_H<H>      bf16 in, per-token FP8 out, bias (the quantised workload)
   nvfp4_T<T>_H<H>    bf16 in, NVFP4 out, bias
   fp8pipe_T<T>_H<H>, nvfp4pipe_T<T>_H<H>
@@ -57,8 +58,9 @@ def run_case(name: str, reps: int) -> str:
             f"decode_T{T}_H{H}", T, H, 10 + T, "bf16", "bf16", 1e-6)
     elif kind == "prefill":
         wl = synth.prefill_workload(T, H)
-    elif kind == "ragged":
-        wl = synth.Workload(f"ragged_T{T}_H{H}", T, H, 80, "bf16", "bf16", 1e-5, has_bias=True,
+    elif kind in ("ragged", "raggedfp8"):
+        wl = synth.Workload(f"{kind}_T{T}_H{H}", T, H, 80, "bf16",
+                            "fp8" if kind == "raggedfp8" else "bf16", 1e-5, has_bias=True,
                             r_std=2.0)
     elif kind in ("fp8", "nvfp4", "fp8pipe", "nvfp4pipe"):
         wl = synth.fp8_workload(H, n_tokens=T)
