@@ -242,8 +242,10 @@ int rmsnorm_fwd_host(const void* x, const void* residual, const void* weight, co
  * the weights in registers.  Without a weight offset the 16-bit kernels form
  * x * w exactly and round once more, for (x * w) * inv.  The fast path needs head_dim * element size to be a
  * multiple of 32 bytes and at most 1024 bytes (head_dim 64, 128, 256 in bf16
- * and fp32, 512 in bf16), 32-byte aligned pointers and token strides;
- * otherwise RMSN_EUNSUPPORTED.  Returns an rmsn_status.
+ * and fp32, 512 in bf16), 32-byte aligned pointers and token strides, and at
+ * most 65535 x 16 warps' worth of heads per token (32 / lanes-per-head heads
+ * a warp: over a million heads at head_dim 512 bf16); otherwise
+ * RMSN_EUNSUPPORTED.  Returns an rmsn_status.
  */
 #define RMSN_QK_RING 0x400u   /* rmsnorm_qk_fwd: take the ring variant whatever the batch
                                  (RMSN_EUNSUPPORTED where it does not apply); for tests

@@ -1048,6 +1048,7 @@ RMSN_API int rmsnorm_qk_fwd(void* q, void* k, const void* q_weight, const void* 
         const int64_t nh = 32 / tph;
         const int64_t warps = (n_q_heads + n_k_heads + nh - 1) / nh;
         const int64_t gy = (warps + 15) / 16;
+        if (gy > 65535) return RMSN_EUNSUPPORTED;  // the grid's y extent
         threads = (int)((warps + gy - 1) / gy) * 32;
         const int64_t blocks = (n_tokens + ch - 1) / ch;
         grid = blocks < kQkMaxGridX ? blocks : kQkMaxGridX;

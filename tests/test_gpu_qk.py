@@ -158,3 +158,12 @@ def test_qk_norm_rejections(pkg):
                               bf, s) == pkg.RMSN_EALIGN
     assert pkg.rmsnorm_qk_fwd(None, None, None, None, 0, 4, 0, 64, 256, 0, 1e-6, 0.0, bf,
                               s) == pkg.RMSN_OK
+    # more head groups per token than the grid's y extent holds (head_dim 512
+    # bf16, one head per warp: 2^20 + 16 heads); the buffers are the full
+    # size, so even a launch would stay inside them
+    Hq, Hk, D = 1 << 20, 16, 512
+    q = torch.zeros((1, Hq * D), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((1, Hk * D), dtype=torch.bfloat16, device="cuda")
+    assert pkg.rmsnorm_qk_fwd(q.data_ptr(), k.data_ptr(), None, None, 1, Hq, Hk, D, Hq * D,
+                              Hk * D, 1e-6, 0.0, bf, s) == pkg.RMSN_EUNSUPPORTED
+    del q, k
