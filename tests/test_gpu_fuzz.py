@@ -14,7 +14,7 @@ from residual_add_rmsnorm_vec_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 300
+N_CASES = 500
 HIDDEN = [1, 3, 12, 64, 100, 256, 511, 1000, 1024, 2048, 2050, 4095, 4096, 5120, 7168, 8190, 8192,
           12288, 16384]
 TOKENS = [1, 2, 7, 31, 64, 152, 300, 1024, 2500]
