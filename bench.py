@@ -274,7 +274,7 @@ def run_ours(args):
     forced = None
     if args.config:
         forced = pkg.RmsnConfig.from_dict(json.loads(args.config))
-    cfg = forced if forced is not None else pkg.rmsnorm_query_config(T, H, flags)
+    cfg = forced if forced is not None else pkg.rmsnorm_query_config(T, H, step_flags)
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
     def step(i):
@@ -603,6 +603,7 @@ def run_decode(pkg, synth, dev, stream):
         # (reads both, writes one tensor; no reduction), in a graph likewise
         gus_add = graph_time(lambda: torch.add(x, r, out=out))
         cfg = pkg.rmsnorm_query_config(T, 4096, flags)
+        cfg_pdl = pkg.rmsnorm_query_config(T, 4096, flags | pkg.RMSN_PDL)
         per_t[str(T)] = {"us": round(us, 3), "graph_us": round(gus, 3),
                          "graph_pdl_us": round(gus_pdl, 3),
                          "torch_add_graph_us": round(gus_add, 3),
@@ -610,7 +611,10 @@ def run_decode(pkg, synth, dev, stream):
                          "cluster": clusters,
                          "gbs_l2_hot": round(wl.algorithmic_bytes() / (us * 1e-6) / 1e9, 1),
                          "launch": f"{pkg.VARIANT_NAMES[cfg.variant]} ch{cfg.chunks} "
-                                   f"w{cfg.warps_per_block} grid{cfg.grid}"}
+                                   f"w{cfg.warps_per_block} grid{cfg.grid}",
+                         "launch_pdl": f"{pkg.VARIANT_NAMES[cfg_pdl.variant]} ch{cfg_pdl.chunks} "
+                                       f"w{cfg_pdl.warps_per_block} st{cfg_pdl.stages} "
+                                       f"grid{cfg_pdl.grid}"}
     res["tokens"] = per_t
     # an empty kernel launched from the same C loop (host cost, GPU time per launch)
     hc = host_cost_c(1, 4096)

@@ -425,9 +425,12 @@ bool shape_config(const Problem& p, const KernelEntry& e, DeviceInfo* d, int gri
 }
 
 // Table keys of the input side: the DType of x, or one of these two for
-// bf16 / fp16 activations over an fp32 residual stream.
+// bf16 / fp16 activations over an fp32 residual stream, or the third for bf16
+// rows measured as launches chained by programmatic dependent launch
+// (RMSN_PDL; tried before the plain bf16 rows for calls with that flag).
 constexpr int kTableBF16R32 = 7;
 constexpr int kTableF16R32 = 8;
+constexpr int kTableBF16PDL = 9;
 
 #include "rmsn_selector_table.inc"
 
@@ -459,11 +462,16 @@ bool select(const Problem& p, DeviceInfo* d, rmsn_config* c) {
     }
     int variant = 0, ch = 0, wmax = 0, stages = 0;
     const int res = p.res ? 1 : 0;
-    // table keys to try: the problem's own, then (fp16 moves the same bytes
-    // through the same kernels as bf16) the bf16 rows for fp16
-    int keys[2][2];
+    // table keys to try: the rows measured with PDL for a PDL call, the
+    // problem's own, then (fp16 moves the same bytes through the same kernels
+    // as bf16) the bf16 rows for fp16
+    int keys[3][2];
     int nkeys = 0;
     const int tin = p.res_f32 ? (p.in_dt == kF16 ? kTableF16R32 : kTableBF16R32) : p.in_dt;
+    if (p.pdl && tin == kBF16) {
+        keys[nkeys][0] = kTableBF16PDL;
+        keys[nkeys++][1] = p.out_dt;
+    }
     keys[nkeys][0] = tin;
     keys[nkeys++][1] = p.out_dt;
     if (tin == kF16 || tin == kTableF16R32) {
@@ -476,6 +484,8 @@ bool select(const Problem& p, DeviceInfo* d, rmsn_config* c) {
                    select_rules(p, d, c);
     }
     for (int k = 0; k < nkeys; ++k) {
+        // the PDL rows stand for their own hidden sizes only
+        if (keys[k][0] == kTableBF16PDL) continue;
         int64_t near[16];
         const int n = table_neighbours(keys[k][0], keys[k][1], p.H, near, 16);
         for (int i = 0; i < n; ++i) {

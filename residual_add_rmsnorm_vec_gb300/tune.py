@@ -30,7 +30,7 @@ TOKENS = (1, 4, 16, 64, 256, 1024, 4096, 16384, 65536)
 HIDDEN = (2048, 4096, 8192, 16384)
 # table keys; "+r32": bf16 / fp16 activations over an fp32 residual stream
 DTYPE_CODES = {"f32": 0, "bf16": 1, "fp8": 2, "mxfp8": 3, "mxfp4": 4, "nvfp4": 5, "f16": 6,
-               "bf16+r32": 7, "f16+r32": 8}
+               "bf16+r32": 7, "f16+r32": 8, "bf16+pdl": 9}
 BLOCK_FMTS = ("mxfp8", "mxfp4", "nvfp4")
 
 
@@ -56,6 +56,7 @@ def measure(pkg, T, H, in_dt="bf16", out_dt="bf16", res=True, bias=False, reps=3
 
     dev = torch.device("cuda")
     r32 = in_dt.endswith("+r32")
+    pdl = in_dt.endswith("+pdl")  # launches chained by programmatic dependent launch
     in_dt = in_dt.split("+")[0]
     tin = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[in_dt]
     tres = torch.float32 if r32 else tin
@@ -67,6 +68,7 @@ def measure(pkg, T, H, in_dt="bf16", out_dt="bf16", res=True, bias=False, reps=3
         out_dt, torch.uint8)
     # block formats share the launch shapes of the per-token FP8 output
     rflag = pkg.RMSN_RESIDUAL_F32 if r32 else 0
+    rflag |= pkg.RMSN_PDL if pdl else 0
     flags = pkg.make_flags(in_dt, "fp8" if block else out_dt, res, True, bias) | rflag
     call_flags = pkg.make_flags(in_dt, "f32", res, True, bias) | rflag if block else flags
     set_bytes = T * H * (in_b + (2 * res_b if res else 0) + out_b)
@@ -262,8 +264,10 @@ def write_table(entries, path, extra_rows=()):
         "// residual setting where the table has any; hidden sizes without rows take",
         "// the rows of the nearest measured hidden size (within a factor of two),",
         "// else the fixed rule in the selector.  Input keys are DType codes, or 7 / 8",
-        "// for bf16 / fp16 activations over an fp32 residual stream.  res / bias: the",
-        "// operands the row was measured with.",
+        "// for bf16 / fp16 activations over an fp32 residual stream, or 9 for bf16",
+        "// rows measured as launches chained by programmatic dependent launch (taken",
+        "// first for calls with RMSN_PDL).  res / bias: the operands the row was",
+        "// measured with.",
         "struct TableRow {",
         "    int in_dt, out_dt;",
         "    int64_t hidden, t_min;",

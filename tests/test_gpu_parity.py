@@ -499,6 +499,14 @@ def test_selector_decode_vs_prefill(pkg):
         c = pkg.rmsnorm_query_config(T, H, flags)
         assert any(_same_shape(c, o) for o in pkg.rmsnorm_list_configs(T, H, flags)), (T, H)
         assert 1 <= c.grid <= max(T, 1)
+        # PDL calls take the rows measured with PDL where the hidden size has
+        # them, else the plain rows: a built shape either way
+        cp = pkg.rmsnorm_query_config(T, H, flags | pkg.RMSN_PDL)
+        assert any(_same_shape(cp, o) for o in pkg.rmsnorm_list_configs(T, H, flags)), (T, H)
+    # hidden 3072 has no PDL rows: a PDL call takes its plain rows, not a
+    # PDL neighbour's
+    c, cp = (pkg.rmsnorm_query_config(256, 3072, flags | f) for f in (0, pkg.RMSN_PDL))
+    assert _same_shape(c, cp)
     # rows off the 32-byte grid: the ragged-row kernel for the same dtype in
     # and out, a per-token FP8 output and fp32 out of 16-bit rows; the generic
     # one otherwise (here: bf16 activations over an fp32 residual stream)

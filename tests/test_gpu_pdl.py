@@ -66,10 +66,14 @@ def chain(pkg, inp, eps, n, pdl, early, graph=False, config=None):
                                  (16384, 8192)])
 @pytest.mark.parametrize("early", [False, True])
 def test_pdl_chain_matches_plain_chain(pkg, T, H, early):
+    # both chains take the launch the selector picks for PDL calls (the table
+    # has rows measured with PDL), so only the launch attribute differs
     wl = synth.Workload(f"pdl_T{T}_H{H}", T, H, 21, "bf16", "bf16", 1e-6)
     inp = synth.make_inputs(wl)
     n = 6
-    ref = chain(pkg, inp, wl.eps, n, pdl=False, early=False)
+    cfg = pkg.rmsnorm_query_config(T, H, pkg.make_flags("bf16", "bf16", True, True, False) |
+                                   pkg.RMSN_PDL)
+    ref = chain(pkg, inp, wl.eps, n, pdl=False, early=False, config=cfg)
     for graph in (False, True):
         got = chain(pkg, inp, wl.eps, n, pdl=True, early=early, graph=graph)
         for k, (a, b) in enumerate(zip(got, ref)):

@@ -31,7 +31,8 @@ def codes():
     dtypes = enum_values(reg, "DType")
     variants = enum_values(reg, "Variant")
     api = read("rmsn_api.cu")
-    r32 = {k: int(v) for k, v in re.findall(r"constexpr int (kTable\w+R32) = (\d+);", api)}
+    r32 = {k: int(v) for k, v in re.findall(r"constexpr int (kTable\w+(?:R32|PDL)) = (\d+);",
+                                             api)}
     stages = int(re.search(r"constexpr int kMaxStages = (\d+);", api).group(1))
     return dtypes, variants, r32, stages
 
@@ -79,6 +80,8 @@ def instantiated(codes):
         if "#define RMSN_WITH_CLUSTER" in src:
             shapes |= {(variants["kCluster"], int(ch), int(k)) for ch, k in clu}
         built[(tin, dtypes[m_out.group(1)])] = shapes
+        if tin == dtypes["kBF16"]:  # rows measured with PDL take the same kernels
+            built[(r32["kTableBF16PDL"], dtypes[m_out.group(1)])] = shapes
     return built
 
 
@@ -92,6 +95,7 @@ def test_tuner_writes_the_library_codes(codes):
         assert tune.DTYPE_CODES[name] == dtypes[enum], name
     assert tune.DTYPE_CODES["bf16+r32"] == r32["kTableBF16R32"]
     assert tune.DTYPE_CODES["f16+r32"] == r32["kTableF16R32"]
+    assert tune.DTYPE_CODES["bf16+pdl"] == r32["kTableBF16PDL"]
 
 
 def test_every_row_names_a_built_kernel(rows, instantiated, codes):
@@ -121,7 +125,7 @@ def test_rows_are_whole_vector_shapes(rows, codes):
     size is a whole number of 32-byte vectors of the input type."""
     dtypes, _, r32, _ = codes
     elem = {dtypes["kF32"]: 4, dtypes["kBF16"]: 2, dtypes["kF16"]: 2,
-            r32["kTableBF16R32"]: 4, r32["kTableF16R32"]: 4}
+            r32["kTableBF16R32"]: 4, r32["kTableF16R32"]: 4, r32["kTableBF16PDL"]: 2}
     for r in rows:
         assert (r[2] * elem[r[0]]) % 32 == 0, r
 
