@@ -375,6 +375,9 @@ def main():
     ap.add_argument("--outs", default="",
                     help="comma list of quantised outputs (fp8, mxfp8, mxfp4, nvfp4) to sweep on "
                          "the quantised shapes; rows merged into the table")
+    ap.add_argument("--pdl", action="store_true",
+                    help="with --outs / --block-formats: time launches chained by programmatic "
+                         "dependent launch (the rows go to the PDL key)")
     args = ap.parse_args()
     build.build()
     torch.cuda.set_device(0)
@@ -410,7 +413,7 @@ def main():
         for fmt in (args.outs.split(",") if args.outs else BLOCK_FMTS):
             entries += sweep(pkg, [(T, H) for H in (4096, 5120, 7168, 8192)
                                    for T in (1, 64, 1024, 4096, 16384)],
-                             "bf16", fmt, True, True, args.reps, hot)
+                             "bf16+pdl" if args.pdl else "bf16", fmt, True, True, args.reps, hot)
         with open(args.out, "w") as f:
             json.dump({"meta": {"gpu": torch.cuda.get_device_name(0), "reps": args.reps,
                                 "l2_hot_below": hot, "timing": "cuda graph replay"},

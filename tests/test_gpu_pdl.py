@@ -110,9 +110,10 @@ def test_early_params_needs_pdl(pkg):
     assert st == pkg.RMSN_EINVAL
 
 
-def quant_chain(pkg, inp, eps, n, fmt, pdl):
+def quant_chain(pkg, inp, eps, n, fmt, pdl, config=None):
     """n calls where call k takes the residual_out of call k - 1 as its
-    residual (x, weight and bias fixed); returns every call's outputs."""
+    residual (x, weight and bias fixed); returns every call's outputs, then
+    the residual stream."""
     x = inp["x"].cuda()
     w, b = inp["weight"].cuda(), inp["bias"].cuda()
     rs = [inp["residual"].cuda()] + [torch.empty_like(x) for _ in range(n)]
@@ -120,11 +121,12 @@ def quant_chain(pkg, inp, eps, n, fmt, pdl):
     for k in range(n):
         if fmt == "fp8":
             q, ro, sc = pkg.fused_add_rmsnorm(x, rs[k], w, b, eps=eps, out_dtype="fp8",
-                                              residual_out=rs[k + 1], pdl=pdl)
+                                              residual_out=rs[k + 1], pdl=pdl, config=config)
             outs.append((q, sc))
         else:
             q, bs, ts, ro = pkg.fused_add_rmsnorm_blockscaled(x, rs[k], w, b, eps=eps, fmt=fmt,
-                                                              residual_out=rs[k + 1], pdl=pdl)
+                                                              residual_out=rs[k + 1], pdl=pdl,
+                                                              config=config)
             outs.append((q, bs) if ts is None else (q, bs, ts))
     torch.cuda.synchronize()
     return [[t.cpu() for t in o] for o in outs] + [[r.cpu()] for r in rs[1:]]
@@ -133,13 +135,24 @@ def quant_chain(pkg, inp, eps, n, fmt, pdl):
 @pytest.mark.parametrize("fmt", ["fp8", "mxfp8", "mxfp4", "nvfp4"])
 @pytest.mark.parametrize("T,H", [(4096, 5120), (33, 2048)])
 def test_pdl_chain_quantised_outputs(pkg, fmt, T, H):
-    # the quantised launches that bench.py times with RMSN_PDL: a chain over
-    # the residual stream is bit-identical with and without PDL
+    # the quantised launches chained by RMSN_PDL, as bench.py times them:
+    # with one launch shape forced on both chains, every output is
+    # bit-identical with and without PDL; with the selector's picks (the
+    # table has rows measured with PDL, so the shapes may differ) the
+    # residual stream, which no launch shape changes, still is
     wl = synth.Workload(f"pdlq_{fmt}_T{T}_H{H}", T, H, 22, "bf16", "bf16", 1e-6, has_bias=True)
     inp = synth.make_inputs(wl)
-    ref = quant_chain(pkg, inp, wl.eps, 4, fmt, pdl=False)
-    got = quant_chain(pkg, inp, wl.eps, 4, fmt, pdl=True)
+    cfgs = (pkg.rmsnorm_list_configs(T, H, pkg.make_flags("bf16", "fp8", True, True, True))
+            if fmt == "fp8" else pkg.block_format_configs(T, H, fmt))
+    rings = [c for c in cfgs if c.variant in (pkg.VARIANT_BULK_ROW, pkg.VARIANT_BULK_PIPE)]
+    cfg = rings[0] if rings else cfgs[0]
+    ref = quant_chain(pkg, inp, wl.eps, 4, fmt, pdl=False, config=cfg)
+    got = quant_chain(pkg, inp, wl.eps, 4, fmt, pdl=True, config=cfg)
     for k, (a, b) in enumerate(zip(got, ref)):
         for ta, tb in zip(a, b):
-            assert torch.equal(ta, tb), (fmt, k)
+            assert torch.equal(ta, tb), (fmt, k, cfg.as_dict())
+    ref = quant_chain(pkg, inp, wl.eps, 4, fmt, pdl=False)
+    got = quant_chain(pkg, inp, wl.eps, 4, fmt, pdl=True)
+    for k in range(4):
+        assert torch.equal(got[4 + k][0], ref[4 + k][0]), (fmt, "residual", k)
     assert pkg.rmsnorm_read_status() == 0
